@@ -1,0 +1,322 @@
+/*
+ * CPU oracle for the MoE decode routing path.  TEST INFRASTRUCTURE ONLY:
+ * only the tests, the package smoke check and the benchmark's CPU-baseline
+ * leg may load it.  It shares no code, header, table or constant generator
+ * with the CUDA library; the two meet only through the seeded inputs.
+ *
+ * Plain, slow and single-threaded on purpose: every function is the written
+ * definition of its step, with no blocking, fusion or reordering.  Floating
+ * point is fp64 except where the method itself fixes fp32 (the sigmoid score
+ * and the selection key of the sigmoid gate, see oracle_sigmoid_f32).
+ *
+ * Sources (GitHub PR pages about MoE decode routing):
+ *  - sglang #36557 "MiniMax-M3: Triton split-K router GEMV with in-kernel
+ *    fixup", description: the router GEMV [M,K] bf16 x [N,K] bf16 -> [M,N]
+ *    fp32 at N ~ 128, M <= 64.
+ *  - sglang #46691 (MiniMax-M3.1 MoE/GEMM kernels), Summary: gate (top-k),
+ *    aiter's sort into per-expert blocks, stage-1 activation quant.
+ *  - sglang #46652 (Kimi-K3 fused routing/sort/quant), Modifications and the
+ *    review diff of the sort kernel: stable rank = number of earlier
+ *    (token, slot) pairs on the same expert; MXFP8 stage-1 activations;
+ *    896 experts, top-16, hidden 3584.
+ * Where the pages are silent (sort layout, MX scale rule, sigmoid recipe,
+ * tie order) the readings are stated at each function.
+ *
+ * Compile with -ffp-contract=off: a fused multiply-add may appear only where
+ * it is written as fma()/fmaf().
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* bf16 storage                                                        */
+/* ------------------------------------------------------------------ */
+
+static double bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------ */
+/* a1 + a2: router GEMV (split-K is an implementation detail; the      */
+/* oracle computes the plain dot products).                            */
+/* sglang #36557, description: logits[m, n] = sum_k x[m, k] * W[n, k]. */
+/* Products of two bf16 values are exact in fp64; the sum runs in k    */
+/* order in fp64 and is rounded once to fp32.                          */
+/* ------------------------------------------------------------------ */
+void oracle_router_gemv(const uint16_t *x, int64_t ldx, const uint16_t *w,
+                        float *logits, int M, int N, int K)
+{
+    for (int m = 0; m < M; ++m) {
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k)
+                acc += bf16_value(x[(int64_t)m * ldx + k]) * bf16_value(w[(int64_t)n * K + k]);
+            logits[(int64_t)m * N + n] = (float)acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* a3: top-k gating.                                                   */
+/* ------------------------------------------------------------------ */
+
+/* Order used by every selection: larger key first; equal keys (including
+ * +0 and -0, which compare equal) go to the lower expert id. */
+typedef struct { float key; int id; } keyed;
+
+static int keyed_cmp(const void *pa, const void *pb)
+{
+    const keyed *a = (const keyed *)pa, *b = (const keyed *)pb;
+    if (a->key > b->key) return -1;
+    if (a->key < b->key) return 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id);
+}
+
+/* Full sort of all N experts by (key desc, id asc); the first k win. */
+static void select_topk(const float *key, int N, int k, int32_t *ids_out, keyed *work)
+{
+    for (int n = 0; n < N; ++n) { work[n].key = key[n]; work[n].id = n; }
+    qsort(work, (size_t)N, sizeof(keyed), keyed_cmp);
+    for (int j = 0; j < k; ++j) ids_out[j] = work[j].id;
+}
+
+/*
+ * Softmax gate (MiniMax-style routing: softmax, top-k, renormalise).
+ * READING: softmax is monotone, so the top-k of the probabilities is the
+ * top-k of the logits; the selection key is the fp32 logit itself, which
+ * keeps exp rounding out of the ids.  Weights: the softmax probabilities of
+ * the selected experts (fp64), divided by their sum when renormalize != 0.
+ */
+void oracle_topk_softmax(const float *logits, int M, int N, int k, int renormalize,
+                         int32_t *topk_ids, float *topk_weights)
+{
+    keyed *work = (keyed *)malloc(sizeof(keyed) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    for (int m = 0; m < M; ++m) {
+        const float *l = logits + (int64_t)m * N;
+        int32_t *ids = topk_ids + (int64_t)m * k;
+        select_topk(l, N, k, ids, work);
+        double lmax = -INFINITY;
+        for (int n = 0; n < N; ++n) if ((double)l[n] > lmax) lmax = l[n];
+        double z = 0.0;
+        for (int n = 0; n < N; ++n) { p[n] = exp((double)l[n] - lmax); z += p[n]; }
+        for (int n = 0; n < N; ++n) p[n] /= z;
+        double s = 0.0;
+        for (int j = 0; j < k; ++j) s += p[ids[j]];
+        for (int j = 0; j < k; ++j)
+            topk_weights[(int64_t)m * k + j] = (float)(renormalize ? p[ids[j]] / s : p[ids[j]]);
+    }
+    free(p);
+    free(work);
+}
+
+/*
+ * fp32 sigmoid score.  The routing pages fix "fp32 sigmoid scores" for the
+ * Kimi-K3-style gate but not how sigma is evaluated, and an fp32 sigma that
+ * differs by one ulp between two libraries can swap two experts whose biased
+ * scores are one ulp apart.  READING: the score is defined by one fully
+ * specified fp32 recipe, so any implementation that follows it gets the same
+ * bits:
+ *   y  = clamp(-l, -87, 88)
+ *   n  = rint(y * log2(e))                     (fp32 multiply, ties to even)
+ *   r  = fma(-n, ln2_hi, y); r = fma(-n, ln2_lo, r)
+ *        (Cody and Waite's argument reduction, "Software Manual for the
+ *         Elementary Functions", 1980, with a two-part ln 2)
+ *   p  = sum_{j=0..7} r^j / j!   by Horner's rule with fp32 fma
+ *        (degree-7 Taylor polynomial of e^r on |r| <= ln2/2)
+ *   e  = p * 2^n ;  s = 1 / (1 + e)            (fp32, round to nearest)
+ * The tests pin s to within a few fp32 ulps of the exact sigma.
+ */
+float oracle_sigmoid_f32(float l)
+{
+    const float log2e = 0x1.715476p+0f;
+    const float ln2_hi = 0x1.62e430p-1f;
+    const float ln2_lo = -0x1.05c610p-29f;
+    const float c[8] = {0x1p+0f, 0x1p+0f, 0x1p-1f, 0x1.555556p-3f,
+                        0x1.555556p-5f, 0x1.111112p-7f, 0x1.6c16c2p-10f, 0x1.a01a02p-13f};
+    float y = -l;
+    if (y < -87.0f) y = -87.0f;
+    if (y > 88.0f) y = 88.0f;
+    float t = y * log2e;
+    float n = rintf(t);
+    float r = fmaf(-n, ln2_hi, y);
+    r = fmaf(-n, ln2_lo, r);
+    float p = c[7];
+    for (int j = 6; j >= 0; --j) p = fmaf(p, r, c[j]);
+    int ni = (int)n;
+    uint32_t two_n_bits = (uint32_t)(ni + 127) << 23;
+    float two_n;
+    memcpy(&two_n, &two_n_bits, sizeof two_n);
+    float e = p * two_n;
+    float d = 1.0f + e;
+    return 1.0f / d;
+}
+
+/*
+ * Sigmoid + bias gate (Kimi-K3-style routing).  s_n = sigmoid_f32(l_n); the
+ * selection key is t_n = s_n + bias_n in fp32 (bias used for selection only);
+ * weights are the unbiased s of the selected experts, divided by their fp64
+ * sum when renormalize != 0.  bias may be NULL (treated as zero).
+ */
+void oracle_topk_sigmoid(const float *logits, const float *bias, int M, int N, int k,
+                         int renormalize, int32_t *topk_ids, float *topk_weights)
+{
+    keyed *work = (keyed *)malloc(sizeof(keyed) * (size_t)N);
+    float *s = (float *)malloc(sizeof(float) * (size_t)N);
+    float *t = (float *)malloc(sizeof(float) * (size_t)N);
+    for (int m = 0; m < M; ++m) {
+        const float *l = logits + (int64_t)m * N;
+        int32_t *ids = topk_ids + (int64_t)m * k;
+        for (int n = 0; n < N; ++n) {
+            s[n] = oracle_sigmoid_f32(l[n]);
+            t[n] = s[n] + (bias ? bias[n] : 0.0f);
+        }
+        select_topk(t, N, k, ids, work);
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) sum += (double)s[ids[j]];
+        for (int j = 0; j < k; ++j)
+            topk_weights[(int64_t)m * k + j] =
+                (float)(renormalize ? (double)s[ids[j]] / sum : (double)s[ids[j]]);
+    }
+    free(t);
+    free(s);
+    free(work);
+}
+
+/* ------------------------------------------------------------------ */
+/* a4: sort of the (token, slot) assignments into per-expert blocks.   */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Entries of sorted_token_ids / expert_ids the sort must write, in entries:
+ * the worst case of sum_e ceil(c_e / B) * B over all routings, rounded up to
+ * a multiple of B: M*k + min(N, M*k) * (B - 1), rounded up to B.
+ */
+int64_t oracle_sort_capacity(int M, int k, int N, int B)
+{
+    int64_t mk = (int64_t)M * k;
+    int64_t used = mk < N ? mk : N;
+    int64_t cap = mk + used * (B - 1);
+    return (cap + B - 1) / B * B;
+}
+
+/*
+ * READING of the sorted layout (the pages name aiter's multi-phase sort but
+ * print no layout; the Kimi-K3 sort kernel's review diff gives the stable
+ * rank): an assignment is its flat index f = m*k + j.  Experts are laid out
+ * in ascending id; within an expert the flat indices ascend (stable); each
+ * expert's run is padded to ceil(c_e/B)*B entries with the sentinel M*k, and
+ * experts with no assignment get no block.  expert_ids[b] is the expert that
+ * owns block b.  Everything past num_tokens_post_padded is filled: sentinel
+ * M*k in sorted_token_ids, -1 in expert_ids.  Ids outside [0, N) are not
+ * placed (masked experts).  A stable counting sort.
+ */
+void oracle_moe_sort(const int32_t *topk_ids, int M, int k, int N, int B,
+                     int32_t *sorted_token_ids, int32_t *expert_ids,
+                     int32_t *num_tokens_post_padded, int64_t capacity)
+{
+    int64_t mk = (int64_t)M * k;
+    int64_t *count = (int64_t *)calloc((size_t)N, sizeof(int64_t));
+    int64_t *start = (int64_t *)calloc((size_t)N, sizeof(int64_t));
+    int64_t *cursor = (int64_t *)calloc((size_t)N, sizeof(int64_t));
+    for (int64_t f = 0; f < mk; ++f) {
+        int32_t e = topk_ids[f];
+        if (e >= 0 && e < N) count[e]++;
+    }
+    int64_t pos = 0;
+    for (int e = 0; e < N; ++e) {
+        start[e] = pos;
+        pos += (count[e] + B - 1) / B * B;
+    }
+    for (int64_t i = 0; i < capacity; ++i) sorted_token_ids[i] = (int32_t)mk;
+    for (int64_t b = 0; b < capacity / B; ++b) expert_ids[b] = -1;
+    for (int64_t f = 0; f < mk; ++f) {
+        int32_t e = topk_ids[f];
+        if (e < 0 || e >= N) continue;
+        sorted_token_ids[start[e] + cursor[e]] = (int32_t)f;
+        cursor[e]++;
+    }
+    for (int e = 0; e < N; ++e)
+        for (int64_t b = start[e] / B; b < (start[e] + (count[e] + B - 1) / B * B) / B; ++b)
+            expert_ids[b] = e;
+    *num_tokens_post_padded = (int32_t)pos;
+    free(cursor);
+    free(start);
+    free(count);
+}
+
+/* ------------------------------------------------------------------ */
+/* a5: MXFP8 quantisation (OCP Microscaling Formats v1.0): blocks of   */
+/* 32 elements along K share one E8M0 scale; elements are E4M3.        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * E4M3 (OCP FP8: bias 7, no infinities, max finite 448, smallest subnormal
+ * 2^-9) of an exact value v, rounded to nearest with ties to the even code.
+ * READING: magnitudes above 448 saturate to +-448 (the MX spec leaves
+ * overflow to the implementation; the pages' fp8 producers clamp then round).
+ * The sign is kept, so values that round to zero from below give 0x80.
+ */
+uint8_t oracle_e4m3_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < 0x1p-6) {                       /* subnormal range, quantum 2^-9 */
+        double q = rint(a * 0x1p9);         /* 0..8; 8 is the smallest normal */
+        return sign | (uint8_t)q;
+    }
+    int e2;
+    frexp(a, &e2);                          /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;                         /* floor(log2 a), in [-6, 8] */
+    double q = rint(ldexp(a, 3 - e));       /* significand in eighths: 8..16 */
+    if (q == 16.0) { q = 8.0; e += 1; }
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)q - 8));
+}
+
+/* Element-wise e4m3 of an array of exact values (same rounding as above). */
+void oracle_e4m3_encode_array(const double *v, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+/*
+ * Shared scale of one block: X = floor(log2(amax)) - 8 (8 = emax of E4M3),
+ * clamped to [-127, 127]; stored as the E8M0 byte X + 127.  READING: an
+ * all-zero block has amax = 0 and takes the lowest scale, X = -127 (byte 0).
+ * Elements: e4m3(x * 2^-X).  Output layout: q [M, K] and scale [M, K/32],
+ * both row-major in token order.
+ */
+void oracle_mxfp8_quant(const uint16_t *x, int64_t ldx, int M, int K,
+                        uint8_t *q, uint8_t *scale)
+{
+    for (int m = 0; m < M; ++m) {
+        for (int b = 0; b < K / 32; ++b) {
+            const uint16_t *blk = x + (int64_t)m * ldx + (int64_t)b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs(bf16_value(blk[i]));
+                if (a > amax) amax = a;
+            }
+            int X;
+            if (amax == 0.0) {
+                X = -127;
+            } else {
+                int e2;
+                frexp(amax, &e2);
+                X = (e2 - 1) - 8;
+                if (X < -127) X = -127;
+                if (X > 127) X = 127;
+            }
+            scale[(int64_t)m * (K / 32) + b] = (uint8_t)(X + 127);
+            for (int i = 0; i < 32; ++i)
+                q[(int64_t)m * K + (int64_t)b * 32 + i] = oracle_e4m3_encode(ldexp(bf16_value(blk[i]), -X));
+        }
+    }
+}
