@@ -1,1 +1,293 @@
-"""GB300-native MoE decode routing: router GEMV, top-k gate, sort, MXFP8 quant."""
+"""GB300-native MoE decode routing: router GEMV, top-k gate, sort, MXFP8 quant.
+
+Thin Python binding over the C ABI of libmoe_route.so (include/moe_route.h):
+the functions below have the ABI's names without the ``mr_`` prefix, check
+dtypes/devices/contiguity, allocate outputs with torch when none are given,
+and pass raw pointers plus torch's current CUDA stream.  Every step of the
+path runs in the library's CUDA kernels; there is no other implementation
+behind these calls.  If the library is missing or fails to load, every call
+raises.
+
+bf16 tensors are torch.bfloat16; MXFP8 codes and E8M0 scales are uint8.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "MoeRouteError", "MoeRouteUnsupported", "Scratch", "library_path", "load_library",
+    "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
+    "moe_sort", "mxfp8_quant", "moe_route_sort_quant",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libmoe_route.so")
+_lib = None
+
+MR_OK, MR_ERR_UNSUPPORTED, MR_ERR_INVALID_ARG, MR_ERR_SCRATCH_TOO_SMALL, MR_ERR_CUDA = range(5)
+SCORING = {"softmax": 0, "sigmoid": 1}
+SCRATCH_COUNTER_BYTES = 32768
+
+
+class MoeRouteError(RuntimeError):
+    """The library rejected the call or CUDA reported an error."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_load().mr_status_string(status).decode()}")
+
+
+class MoeRouteUnsupported(MoeRouteError):
+    """The shape is outside what the kernels cover (MR_ERR_UNSUPPORTED)."""
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+# (name, restype, argtypes) of every exported symbol; the ABI test checks this
+# list against include/moe_route.h.
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "mr_status_string": (ctypes.c_char_p, [_I]),
+    "mr_abi_version": (_I, []),
+    "mr_router_gemv_supported": (_I, [_I, _I, _I, _I64]),
+    "mr_scratch_bytes": (_SZ, [_I, _I, _I, _I]),
+    "mr_scratch_reset": (_I, [_P, _SZ, _P]),
+    "mr_router_gemv": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "mr_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "mr_sort_capacity": (_I64, [_I, _I, _I, _I]),
+    "mr_moe_sort": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _I64, _P, _SZ, _P]),
+    "mr_mxfp8_quant": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
+    "mr_moe_route_sort_quant": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P,
+                                     _P, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
+}
+
+
+def load_library(path: str | None = None):
+    """Load libmoe_route.so (built by decode_expert_routing_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"libmoe_route.so not found at {p}: build it with "
+            "`python -m decode_expert_routing_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+_load = load_library
+
+
+def _check(status: int, what: str):
+    if status == MR_OK:
+        return
+    if status == MR_ERR_UNSUPPORTED:
+        raise MoeRouteUnsupported(status, what)
+    raise MoeRouteError(status, what)
+
+
+# ---------------------------------------------------------------- helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_ptr(t, name, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _row_major_2d(x, name):
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with a contiguous last dimension")
+    return x.stride(0)
+
+
+def router_gemv_supported(M: int, N: int, K: int, ldx: int | None = None) -> bool:
+    return bool(_load().mr_router_gemv_supported(M, N, K, K if ldx is None else ldx))
+
+
+def scratch_bytes(M_max: int, N: int, K: int, topk: int) -> int:
+    return int(_load().mr_scratch_bytes(M_max, N, K, topk))
+
+
+def sort_capacity(M: int, topk: int, N: int, block: int) -> int:
+    return int(_load().mr_sort_capacity(M, topk, N, block))
+
+
+class Scratch:
+    """A caller-owned scratch buffer (torch uint8 on a CUDA device), zeroed
+    once at creation; every call of the library leaves it reusable."""
+
+    def __init__(self, M_max: int, N: int, K: int, topk: int, device=None):
+        torch = _torch()
+        self.nbytes = scratch_bytes(M_max, N, K, topk)
+        if self.nbytes == 0:
+            raise ValueError("scratch size query rejected the arguments")
+        self.tensor = torch.empty(self.nbytes, dtype=torch.uint8,
+                                  device=device if device is not None else "cuda")
+        self.reset()
+
+    def reset(self, stream=None):
+        _check(_load().mr_scratch_reset(ctypes.c_void_p(self.tensor.data_ptr()), self.nbytes,
+                                        _stream_ptr(stream)), "mr_scratch_reset")
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.tensor.data_ptr())
+
+    def counters(self):
+        """The counter prefix as int32 (all zero between calls)."""
+        return self.tensor[:SCRATCH_COUNTER_BYTES].view(_torch().int32)
+
+
+# ---------------------------------------------------------------- the path
+
+def router_gemv(x, w, out=None, scratch: Scratch | None = None, stream=None):
+    """fp32 logits [M, N] = x [M, K] (bf16) @ w [N, K]^T (bf16)."""
+    torch = _torch()
+    ldx = _row_major_2d(x, "x")
+    M, K = x.shape
+    N = w.shape[0]
+    if not w.is_contiguous() or w.shape[1] != K:
+        raise ValueError("w must be contiguous [N, K]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if scratch is None:
+        scratch = Scratch(M, N, K, 1, device=x.device)
+    _check(_load().mr_router_gemv(_dev_ptr(x, "x", torch.bfloat16), ldx, _dev_ptr(w, "w", torch.bfloat16),
+                                  _dev_ptr(out, "out", torch.float32), M, N, K, scratch.ptr,
+                                  scratch.nbytes, _stream_ptr(stream)), "mr_router_gemv")
+    return out
+
+
+def route_topk(logits, topk: int, scoring: str = "softmax", bias=None, renormalize: bool = True,
+               ids=None, weights=None, stream=None):
+    """(topk_ids int32 [M, k], topk_weights fp32 [M, k])."""
+    torch = _torch()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be contiguous [M, N]")
+    M, N = logits.shape
+    if ids is None:
+        ids = torch.empty((M, topk), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((M, topk), dtype=torch.float32, device=logits.device)
+    _check(_load().mr_route_topk(_dev_ptr(logits, "logits", torch.float32), M, N, topk, SCORING[scoring],
+                                 _dev_ptr(bias, "bias", torch.float32, allow_none=True), int(renormalize),
+                                 _dev_ptr(ids, "ids", torch.int32), _dev_ptr(weights, "weights", torch.float32),
+                                 _stream_ptr(stream)), "mr_route_topk")
+    return ids, weights
+
+
+def moe_sort(topk_ids, num_experts: int, block: int, out=None, scratch: Scratch | None = None,
+             stream=None):
+    """(sorted_token_ids [cap], expert_ids [cap/block], num_tokens_post_padded [1]) int32."""
+    torch = _torch()
+    if topk_ids.dim() != 2 or not topk_ids.is_contiguous():
+        raise ValueError("topk_ids must be contiguous [M, k]")
+    M, k = topk_ids.shape
+    cap = sort_capacity(M, k, num_experts, block)
+    if cap < 0:
+        raise MoeRouteUnsupported(MR_ERR_UNSUPPORTED, "mr_sort_capacity")
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(cap, dtype=torch.int32, device=dev),
+               torch.empty(cap // block, dtype=torch.int32, device=dev),
+               torch.empty(1, dtype=torch.int32, device=dev))
+    st, ex, nt = out
+    sp, sb = (scratch.ptr, scratch.nbytes) if scratch is not None else (None, 0)
+    if scratch is None and M * k > 2048:
+        scratch = Scratch(M, num_experts, 512, k, device=dev)
+        sp, sb = scratch.ptr, scratch.nbytes
+    _check(_load().mr_moe_sort(_dev_ptr(topk_ids, "topk_ids", torch.int32), M, k, num_experts, block,
+                               _dev_ptr(st, "sorted_token_ids", torch.int32),
+                               _dev_ptr(ex, "expert_ids", torch.int32),
+                               _dev_ptr(nt, "num_tokens_post_padded", torch.int32), st.numel(), sp, sb,
+                               _stream_ptr(stream)), "mr_moe_sort")
+    return st, ex, nt
+
+
+def mxfp8_quant(x, out=None, stream=None):
+    """(q uint8 [M, K] e4m3 codes, scale uint8 [M, K/32] e8m0)."""
+    torch = _torch()
+    ldx = _row_major_2d(x, "x")
+    M, K = x.shape
+    if out is None:
+        out = (torch.empty((M, K), dtype=torch.uint8, device=x.device),
+               torch.empty((M, K // 32), dtype=torch.uint8, device=x.device))
+    q, s = out
+    _check(_load().mr_mxfp8_quant(_dev_ptr(x, "x", torch.bfloat16), ldx, M, K, _dev_ptr(q, "q", torch.uint8),
+                                  _dev_ptr(s, "scale", torch.uint8), _stream_ptr(stream)), "mr_mxfp8_quant")
+    return q, s
+
+
+def alloc_route_outputs(M: int, N: int, K: int, topk: int, block: int, device, quant: bool = True):
+    """Output tensors of moe_route_sort_quant (a dict)."""
+    torch = _torch()
+    cap = sort_capacity(M, topk, N, block)
+    out = dict(
+        logits=torch.empty((M, N), dtype=torch.float32, device=device),
+        topk_ids=torch.empty((M, topk), dtype=torch.int32, device=device),
+        topk_weights=torch.empty((M, topk), dtype=torch.float32, device=device),
+        sorted_token_ids=torch.empty(cap, dtype=torch.int32, device=device),
+        expert_ids=torch.empty(cap // block, dtype=torch.int32, device=device),
+        num_tokens_post_padded=torch.empty(1, dtype=torch.int32, device=device),
+    )
+    if quant:
+        out["q"] = torch.empty((M, K), dtype=torch.uint8, device=device)
+        out["scale"] = torch.empty((M, K // 32), dtype=torch.uint8, device=device)
+    return out
+
+
+def moe_route_sort_quant(x, w, topk: int, block: int, scoring: str = "softmax", bias=None,
+                         renormalize: bool = True, quant: bool = True, out=None,
+                         scratch: Scratch | None = None, stream=None):
+    """The whole path for M <= 16 tokens in one launch; returns a dict of outputs."""
+    torch = _torch()
+    ldx = _row_major_2d(x, "x")
+    M, K = x.shape
+    N = w.shape[0]
+    if not w.is_contiguous() or w.shape[1] != K:
+        raise ValueError("w must be contiguous [N, K]")
+    if out is None:
+        out = alloc_route_outputs(M, N, K, topk, block, x.device, quant)
+    if scratch is None:
+        scratch = Scratch(M, N, K, topk, device=x.device)
+    q = out.get("q") if quant else None
+    s = out.get("scale") if quant else None
+    _check(_load().mr_moe_route_sort_quant(
+        _dev_ptr(x, "x", torch.bfloat16), ldx, _dev_ptr(w, "w", torch.bfloat16), M, N, K, topk,
+        SCORING[scoring], _dev_ptr(bias, "bias", torch.float32, allow_none=True), int(renormalize), block,
+        _dev_ptr(out["logits"], "logits", torch.float32), _dev_ptr(out["topk_ids"], "topk_ids", torch.int32),
+        _dev_ptr(out["topk_weights"], "topk_weights", torch.float32),
+        _dev_ptr(out["sorted_token_ids"], "sorted_token_ids", torch.int32),
+        _dev_ptr(out["expert_ids"], "expert_ids", torch.int32),
+        _dev_ptr(out["num_tokens_post_padded"], "num_tokens_post_padded", torch.int32),
+        out["sorted_token_ids"].numel(), _dev_ptr(q, "q", torch.uint8, allow_none=True),
+        _dev_ptr(s, "scale", torch.uint8, allow_none=True), scratch.ptr, scratch.nbytes,
+        _stream_ptr(stream)), "mr_moe_route_sort_quant")
+    return out

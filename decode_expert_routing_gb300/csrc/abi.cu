@@ -1,0 +1,180 @@
+// C ABI entry points: host-side validation, then one launcher call each.
+// Nothing here allocates device memory.
+#include <stdint.h>
+
+#include "../../include/moe_route.h"
+#include "internal.h"
+
+namespace {
+
+using mr::GemvPlan;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MR_OK : MR_ERR_CUDA; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Common checks of an x operand.
+int check_x(const void* x, int64_t ldx, int M, int K) {
+    if (x == nullptr || !aligned(x, 16)) return MR_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || ldx < K || ldx % 8 != 0) return MR_ERR_INVALID_ARG;
+    return MR_OK;
+}
+
+int check_gate_args(int M, int N, int topk, int scoring) {
+    if (M < 1 || N < 1) return MR_ERR_INVALID_ARG;
+    if (scoring != MR_SCORE_SOFTMAX && scoring != MR_SCORE_SIGMOID) return MR_ERR_INVALID_ARG;
+    if (topk < 1 || topk > N) return MR_ERR_INVALID_ARG;
+    if (N > MR_MAX_EXPERTS || topk > MR_MAX_TOPK) return MR_ERR_UNSUPPORTED;
+    return MR_OK;
+}
+
+int check_sort_args(int M, int topk, int N, int block, int64_t capacity) {
+    if (M < 1 || topk < 1 || N < 1 || block < 1) return MR_ERR_INVALID_ARG;
+    if (N > MR_MAX_EXPERTS || topk > MR_MAX_TOPK || block > 1024) return MR_ERR_UNSUPPORTED;
+    const int64_t need = mr_sort_capacity(M, topk, N, block);
+    if (need < 0) return MR_ERR_UNSUPPORTED;
+    if (capacity < need) return MR_ERR_INVALID_ARG;
+    return MR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mr_status_string(int status) {
+    switch (status) {
+        case MR_OK: return "MR_OK";
+        case MR_ERR_UNSUPPORTED: return "MR_ERR_UNSUPPORTED: shape or layout outside the kernels' cover";
+        case MR_ERR_INVALID_ARG: return "MR_ERR_INVALID_ARG: null or misaligned pointer, or bad size";
+        case MR_ERR_SCRATCH_TOO_SMALL: return "MR_ERR_SCRATCH_TOO_SMALL: scratch_bytes below what the call needs";
+        case MR_ERR_CUDA: return "MR_ERR_CUDA: the CUDA runtime reported an error";
+        default: return "unknown mr_status";
+    }
+}
+
+int mr_abi_version(void) { return MR_ABI_VERSION; }
+
+int mr_router_gemv_supported(int M, int N, int K, int64_t ldx) {
+    GemvPlan p;
+    if (ldx < K || ldx % 8 != 0) return 0;
+    return mr::gemv_plan(M, N, K, &p) ? 1 : 0;
+}
+
+int64_t mr_sort_capacity(int M, int topk, int N, int block) {
+    if (M < 1 || topk < 1 || N < 1 || block < 1) return -1;
+    const int64_t mk = (int64_t)M * topk;
+    const int64_t used = mk < N ? mk : N;
+    const int64_t cap = (mk + used * (block - 1) + block - 1) / block * block;
+    if (cap >= ((int64_t)1 << 31)) return -1;  // positions are stored as int32
+    return cap;
+}
+
+size_t mr_scratch_bytes(int M_max, int N, int K, int topk) {
+    if (M_max < 1 || N < 1 || K < 1 || topk < 1) return 0;
+    size_t work = 0;
+    const int Mg = M_max < MR_MAX_GEMV_ROWS ? M_max : MR_MAX_GEMV_ROWS;
+    for (int M = 1; M <= Mg; ++M) {
+        GemvPlan p;
+        if (mr::gemv_plan(M, N, K, &p)) {
+            const size_t b = mr::gemv_work_bytes(p, M, N);
+            if (b > work) work = b;
+        }
+    }
+    const int64_t n_assign = (int64_t)M_max * topk;
+    if (n_assign > mr::kSortChunk && n_assign < ((int64_t)1 << 30)) {
+        const size_t b = mr::sort_work_bytes((int)n_assign, N);
+        if (b > work) work = b;
+    }
+    return mr::kWorkOffset + ((work + 255) / 256) * 256;
+}
+
+int mr_scratch_reset(void* scratch, size_t scratch_bytes, void* stream) {
+    if (scratch == nullptr || scratch_bytes < MR_SCRATCH_COUNTER_BYTES) return MR_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(scratch, 0, scratch_bytes, as_stream(stream)));
+}
+
+int mr_router_gemv(const void* x, int64_t ldx, const void* w, float* logits, int M, int N, int K,
+                   void* scratch, size_t scratch_bytes, void* stream) {
+    int s = check_x(x, ldx, M, K);
+    if (s != MR_OK) return s;
+    if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) ||
+        scratch == nullptr || !aligned(scratch, 256) || N < 1)
+        return MR_ERR_INVALID_ARG;
+    GemvPlan p;
+    if (!mr::gemv_plan(M, N, K, &p)) return MR_ERR_UNSUPPORTED;
+    if (scratch_bytes < mr::kWorkOffset + mr::gemv_work_bytes(p, M, N)) return MR_ERR_SCRATCH_TOO_SMALL;
+    return cuda_status(mr::launch_router_gemv(p, x, ldx, w, logits, M, N, K, scratch, as_stream(stream)));
+}
+
+int mr_route_topk(const float* logits, int M, int N, int topk, int scoring, const float* sel_bias,
+                  int renormalize, int32_t* topk_ids, float* topk_weights, void* stream) {
+    int s = check_gate_args(M, N, topk, scoring);
+    if (s != MR_OK) return s;
+    if (logits == nullptr || !aligned(logits, 4) || topk_ids == nullptr || !aligned(topk_ids, 4) ||
+        topk_weights == nullptr || !aligned(topk_weights, 4) || (sel_bias && !aligned(sel_bias, 4)))
+        return MR_ERR_INVALID_ARG;
+    return cuda_status(mr::launch_topk(logits, M, N, topk, scoring, scoring == MR_SCORE_SIGMOID ? sel_bias : nullptr,
+                                       renormalize ? 1 : 0, topk_ids, topk_weights, as_stream(stream)));
+}
+
+int mr_moe_sort(const int32_t* topk_ids, int M, int topk, int N, int block, int32_t* sorted_token_ids,
+                int32_t* expert_ids, int32_t* num_tokens_post_padded, int64_t capacity, void* scratch,
+                size_t scratch_bytes, void* stream) {
+    int s = check_sort_args(M, topk, N, block, capacity);
+    if (s != MR_OK) return s;
+    if (topk_ids == nullptr || !aligned(topk_ids, 4) || sorted_token_ids == nullptr ||
+        !aligned(sorted_token_ids, 4) || expert_ids == nullptr || !aligned(expert_ids, 4) ||
+        num_tokens_post_padded == nullptr || !aligned(num_tokens_post_padded, 4))
+        return MR_ERR_INVALID_ARG;
+    const int64_t n_assign = (int64_t)M * topk;
+    if (n_assign > mr::kSortChunk) {
+        if (n_assign >= ((int64_t)1 << 30)) return MR_ERR_UNSUPPORTED;
+        if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;
+        if (scratch_bytes < mr::kWorkOffset + mr::sort_work_bytes((int)n_assign, N))
+            return MR_ERR_SCRATCH_TOO_SMALL;
+    }
+    return cuda_status(mr::launch_sort(topk_ids, M, topk, N, block, sorted_token_ids, expert_ids,
+                                       num_tokens_post_padded, capacity, scratch, as_stream(stream)));
+}
+
+int mr_mxfp8_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, void* stream) {
+    int s = check_x(x, ldx, M, K);
+    if (s != MR_OK) return s;
+    if (K % 32 != 0) return MR_ERR_UNSUPPORTED;
+    if (q == nullptr || !aligned(q, 8) || scale == nullptr) return MR_ERR_INVALID_ARG;
+    return cuda_status(mr::launch_quant(x, ldx, M, K, q, scale, as_stream(stream)));
+}
+
+int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, int N, int K, int topk,
+                            int scoring, const float* sel_bias, int renormalize, int block,
+                            float* logits, int32_t* topk_ids, float* topk_weights,
+                            int32_t* sorted_token_ids, int32_t* expert_ids,
+                            int32_t* num_tokens_post_padded, int64_t capacity, uint8_t* q,
+                            uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
+    int s = check_x(x, ldx, M, K);
+    if (s != MR_OK) return s;
+    if ((s = check_gate_args(M, N, topk, scoring)) != MR_OK) return s;
+    if ((s = check_sort_args(M, topk, N, block, capacity)) != MR_OK) return s;
+    if (M > MR_MAX_FUSED_ROWS) return MR_ERR_UNSUPPORTED;
+    if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) ||
+        topk_ids == nullptr || !aligned(topk_ids, 4) || topk_weights == nullptr ||
+        !aligned(topk_weights, 4) || sorted_token_ids == nullptr || !aligned(sorted_token_ids, 4) ||
+        expert_ids == nullptr || !aligned(expert_ids, 4) || num_tokens_post_padded == nullptr ||
+        !aligned(num_tokens_post_padded, 4) || scratch == nullptr || !aligned(scratch, 256) ||
+        (sel_bias && !aligned(sel_bias, 4)))
+        return MR_ERR_INVALID_ARG;
+    if ((q == nullptr) != (scale == nullptr)) return MR_ERR_INVALID_ARG;
+    if (q != nullptr && !aligned(q, 8)) return MR_ERR_INVALID_ARG;
+    GemvPlan p;
+    if (!mr::gemv_plan(M, N, K, &p)) return MR_ERR_UNSUPPORTED;
+    if (scratch_bytes < mr::kWorkOffset + mr::gemv_work_bytes(p, M, N)) return MR_ERR_SCRATCH_TOO_SMALL;
+    return cuda_status(mr::launch_fused(p, x, ldx, w, M, N, K, topk, scoring,
+                                        scoring == MR_SCORE_SIGMOID ? sel_bias : nullptr,
+                                        renormalize ? 1 : 0, block, logits, topk_ids, topk_weights,
+                                        sorted_token_ids, expert_ids, num_tokens_post_padded, capacity,
+                                        q, scale, scratch, as_stream(stream)));
+}
+
+}  // extern "C"

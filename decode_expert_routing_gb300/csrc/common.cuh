@@ -1,0 +1,150 @@
+// Device helpers shared by the routing kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace mr {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// 16-byte streaming load of data read once per launch (the gate weight):
+// read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// 16-byte read-only load that may be served from L1 (activations reused by
+// the warps of one CTA).
+__device__ __forceinline__ uint4 ld_ro_v4(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_m16n8k16(float (&c)[4], uint32_t a0, uint32_t a1,
+                                                  uint32_t a2, uint32_t a3, uint32_t b0,
+                                                  uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Last-arriver ticket: returns the counter value before this CTA's increment.
+// Every thread must have written what it publishes before the call; the
+// whole CTA calls it.  acq_rel at gpu scope plus the fences make the other
+// CTAs' published writes visible to the CTA that draws the last ticket.
+__device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_slot) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+        *s_slot = old;
+    }
+    __syncthreads();
+    unsigned t = *s_slot;
+    __threadfence();
+    return t;
+}
+
+// Orderable image of an fp32 key: larger float -> larger unsigned.  The key
+// is first canonicalised (-0 -> +0) so that the two zeros tie.
+__device__ __forceinline__ unsigned ordered_key(float v) {
+    unsigned u = __float_as_uint(__fadd_rn(v, 0.0f));
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float warp_sum_fixed(float v) {
+    // butterfly: same tree on every call, so the sum is deterministic
+    v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 16));
+    v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 8));
+    v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 4));
+    v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 2));
+    v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 1));
+    return v;
+}
+
+// ---------------------------------------------------------------- MXFP8
+
+// E8M0 exponent X of a 32-block from the largest |x| as a bf16 magnitude
+// pattern (sign cleared): X = floor(log2(amax)) - 8, clamped to [-127, 127];
+// amax == 0 gives -127.  Integer-exact: normal bf16 -> exponent field - 127,
+// subnormal bf16 (value = mant * 2^-133) -> msb(mant) - 133.
+__device__ __forceinline__ int mx_scale_exponent(unsigned amax16) {
+    if (amax16 == 0u) return -127;
+    unsigned e = amax16 >> 7;
+    int fl = (e != 0u) ? (int)e - 127 : (31 - __clz((int)(amax16 & 0x7Fu))) - 133;
+    int X = fl - 8;
+    return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+__device__ __forceinline__ unsigned max_mag16(uint32_t v) {
+    unsigned lo = v & 0x7FFFu, hi = (v >> 16) & 0x7FFFu;
+    return lo > hi ? lo : hi;
+}
+
+// Quantise the 8 consecutive bf16 values of v (k = 8t .. 8t+7 of a 32-block
+// spread over the 4 lanes t = lane & 3 of a lane quad).  All 32 lanes of the
+// warp must call it together.  Returns the 8 e4m3 codes (lowest k in the
+// lowest byte) and writes the block's E8M0 byte to *scale_byte.
+__device__ __forceinline__ uint2 mx_quant_quad(uint4 v, unsigned* scale_byte) {
+    unsigned m = max_mag16(v.x);
+    m = max(m, max_mag16(v.y));
+    m = max(m, max_mag16(v.z));
+    m = max(m, max_mag16(v.w));
+    m = max(m, __shfl_xor_sync(kFull, m, 1));
+    m = max(m, __shfl_xor_sync(kFull, m, 2));
+    int X = mx_scale_exponent(m);
+    *scale_byte = (unsigned)(X + 127);
+    // 2^-X is a normal fp32 for every X reachable from bf16 input (X <= 119).
+    float inv = __uint_as_float((unsigned)(127 - X) << 23);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float lo = __fmul_rn(__uint_as_float(w[i] << 16), inv);
+        float hi = __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv);
+        __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+        if (i & 1)
+            out[i >> 1] |= (uint32_t)p << 16;
+        else
+            out[i >> 1] = (uint32_t)p;
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+// ---------------------------------------------------------------- sigmoid
+
+// fp32 sigmoid score by a fixed recipe (every step correctly rounded, no
+// contraction), so that any implementation of the same steps gives the same
+// bits: y = clamp(-l, -87, 88); n = rint(y * log2 e); Cody-Waite reduction
+// r = y - n*ln2 with a two-part ln 2 (fused multiply-adds); e^r by the
+// degree-7 Taylor polynomial in Horner form; e = p * 2^n; s = 1 / (1 + e).
+__device__ __forceinline__ float sigmoid_score(float l) {
+    float y = -l;
+    y = y < -87.0f ? -87.0f : y;
+    y = y > 88.0f ? 88.0f : y;
+    float n = rintf(__fmul_rn(y, 0x1.715476p+0f));
+    float r = __fmaf_rn(-n, 0x1.62e430p-1f, y);
+    r = __fmaf_rn(-n, -0x1.05c610p-29f, r);
+    float p = 0x1.a01a02p-13f;
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);
+    p = __fmaf_rn(p, r, 0x1p-1f);
+    p = __fmaf_rn(p, r, 0x1p+0f);
+    p = __fmaf_rn(p, r, 0x1p+0f);
+    float two_n = __uint_as_float((unsigned)((int)n + 127) << 23);
+    float e = __fmul_rn(p, two_n);
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+}
+
+}  // namespace mr

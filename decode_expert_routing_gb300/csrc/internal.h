@@ -1,0 +1,61 @@
+// Host-side plan and launchers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mr {
+
+// Counter slots inside the scratch prefix (MR_SCRATCH_COUNTER_BYTES = 32 KiB).
+constexpr int kCounterSlots = 8192;
+constexpr int kGemvCounterSlots = 4096;   // [row_tile * nblocks + nblk]
+constexpr int kFusedCounterSlot = 4096;   // fused route: completed n-blocks
+constexpr int kSortCounterSlot = 4097;    // multi-CTA sort: completed chunks
+constexpr size_t kWorkOffset = 32768;     // work area (partials or sort tables)
+
+// Assignments one sort CTA handles.
+constexpr int kSortChunk = 2048;
+constexpr int kSortThreads = 256;
+
+// One row of the per-M-bucket tiling table (the kernels are instantiated for
+// exactly these rows; see gemv_configs.h).
+struct GemvPlan {
+    int cfg;          // index into the table
+    int nthr;         // threads per CTA
+    int block_n;      // experts per CTA
+    int rows;         // token rows per CTA (row tile)
+    int kchunk;       // K per CTA
+    int split_k;      // CTAs along K
+    int nblocks;      // N / block_n
+    int row_tiles;    // ceil(M / rows)
+};
+
+bool gemv_plan(int M, int N, int K, GemvPlan* p);
+size_t gemv_work_bytes(const GemvPlan& p, int M, int N);
+size_t sort_work_bytes(int n_assign, int N);
+int topk_npl(int N);  // keys per lane of the gate: 4, 8, 16 or 32
+
+cudaError_t launch_router_gemv(const GemvPlan& p, const void* x, int64_t ldx, const void* w,
+                               float* logits, int M, int N, int K, void* scratch,
+                               cudaStream_t st);
+cudaError_t launch_topk(const float* logits, int M, int N, int topk, int scoring,
+                        const float* bias, int renormalize, int32_t* ids, float* weights,
+                        cudaStream_t st);
+cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, int32_t* sorted,
+                        int32_t* expert_ids, int32_t* ntpp, int64_t capacity, void* scratch,
+                        cudaStream_t st);
+cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale,
+                         cudaStream_t st);
+cudaError_t launch_fused(const GemvPlan& p, const void* x, int64_t ldx, const void* w, int M,
+                         int N, int K, int topk, int scoring, const float* bias,
+                         int renormalize, int block, float* logits, int32_t* ids,
+                         float* weights, int32_t* sorted, int32_t* expert_ids, int32_t* ntpp,
+                         int64_t capacity, uint8_t* q, uint8_t* scale, void* scratch,
+                         cudaStream_t st);
+
+// Opt a kernel into more than 48 KiB of dynamic shared memory, once per
+// device.
+cudaError_t ensure_smem(const void* func, int bytes, int* done_per_device);
+
+}  // namespace mr

@@ -1,0 +1,241 @@
+// Gate (a3), sort (a4) and MXFP8 quant (a5) launches.
+#include "internal.h"
+#include "sort.cuh"
+#include "topk.cuh"
+
+namespace mr {
+
+// ------------------------------------------------------------------ gate
+
+constexpr int kTopkWarps = 4;
+
+template <int NPL>
+__global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(TopkArgs a) {
+    const int m = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    if (m < a.M) warp_topk_row<NPL>(a, m, nullptr);
+}
+
+int topk_npl(int N) { return N <= 128 ? 4 : N <= 256 ? 8 : N <= 512 ? 16 : 32; }
+
+cudaError_t launch_topk(const float* logits, int M, int N, int topk, int scoring,
+                        const float* bias, int renormalize, int32_t* ids, float* weights,
+                        cudaStream_t st) {
+    TopkArgs a{logits, bias, ids, weights, M, N, topk, scoring, renormalize};
+    dim3 grid((M + kTopkWarps - 1) / kTopkWarps);
+    switch (topk_npl(N)) {
+        case 4: topk_kernel<4><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
+        case 8: topk_kernel<8><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
+        case 16: topk_kernel<16><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
+        default: topk_kernel<32><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ sort
+
+cudaError_t ensure_smem(const void* func, int bytes, int* done_per_device) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (__atomic_load_n(&done_per_device[dev], __ATOMIC_ACQUIRE) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (e == cudaSuccess) __atomic_store_n(&done_per_device[dev], 160 * 1024, __ATOMIC_RELEASE);
+    return e;
+}
+
+// Whole sort of <= kSortChunk assignments by one CTA.
+__global__ void __launch_bounds__(kSortThreads) sort_cta_kernel(SortArgs a) {
+    extern __shared__ __align__(16) int sm[];
+    const int nw = blockDim.x >> 5;
+    RankSmem rs{sm, sm + nw * a.N, sm + nw * a.N + a.N};
+    int* start = rs.lrank + a.n_assign;
+    int* warp_tot = start + a.N;
+    cta_sort(a, a.ids, rs, start, warp_tot);
+}
+
+struct SortWork {
+    int* chunk_cnt;   // [C][N]
+    int* chunk_off;   // [C][N]
+    int* lrank;       // [n_assign]
+    int* start;       // [N] padded start of each expert's run
+    int* cnt;         // [N] assignments per expert
+    int* total;       // [1]
+};
+
+__host__ __device__ inline SortWork sort_work(void* scratch, int n_assign, int N) {
+    const int C = (n_assign + kSortChunk - 1) / kSortChunk;
+    int* base = reinterpret_cast<int*>(static_cast<char*>(scratch) + kWorkOffset);
+    SortWork w;
+    w.chunk_cnt = base;
+    w.chunk_off = w.chunk_cnt + (size_t)C * N;
+    w.lrank = w.chunk_off + (size_t)C * N;
+    w.start = w.lrank + n_assign;
+    w.cnt = w.start + N;
+    w.total = w.cnt + N;
+    return w;
+}
+
+size_t sort_work_bytes(int n_assign, int N) {
+    const size_t C = (n_assign + kSortChunk - 1) / kSortChunk;
+    return sizeof(int) * (2 * C * N + (size_t)n_assign + 2 * (size_t)N + 4);
+}
+
+// Pass 1 of the multi-CTA sort: per-chunk counts and chunk-local stable
+// ranks; the last chunk to finish turns the counts into chunk offsets and
+// the padded expert starts.
+__global__ void __launch_bounds__(kSortThreads) sort_count_kernel(SortArgs a, SortWork w,
+                                                                  unsigned* counter) {
+    extern __shared__ __align__(16) int sm[];
+    __shared__ unsigned s_ticket;
+    const int nw = blockDim.x >> 5, tid = threadIdx.x, nthr = blockDim.x;
+    const int C = gridDim.x, c = blockIdx.x, N = a.N;
+    const int beg = c * kSortChunk, n = min(kSortChunk, a.n_assign - beg);
+    RankSmem rs{sm, sm + nw * N, sm + nw * N + N};
+    const int seg = cta_rank(a.ids + beg, n, N, rs);
+    for (int i = tid; i < n; i += nthr) {
+        const int e = a.ids[beg + i];
+        if (e >= 0 && e < N) w.lrank[beg + i] = rs.wcnt[(i / seg) * N + e] + rs.lrank[i];
+    }
+    for (int e = tid; e < N; e += nthr) w.chunk_cnt[(size_t)c * N + e] = rs.cnt[e];
+    const unsigned t = cta_ticket(counter, &s_ticket);
+    if (t != (unsigned)(C - 1)) return;
+    int* start = rs.lrank;  // reuse
+    int* warp_tot = start + N;
+    const int B = a.block;
+    for (int e = tid; e < N; e += nthr) {
+        int run = 0;
+        for (int cc = 0; cc < C; ++cc) {
+            const int v = __ldcg(w.chunk_cnt + (size_t)cc * N + e);
+            w.chunk_off[(size_t)cc * N + e] = run;
+            run += v;
+        }
+        rs.cnt[e] = run;
+        start[e] = (run + B - 1) / B * B;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan(start, N, warp_tot);
+    for (int e = tid; e < N; e += nthr) {
+        w.start[e] = start[e];
+        w.cnt[e] = rs.cnt[e];
+    }
+    // expert_ids of the real blocks, written here while the counts are at hand
+    for (int e = tid; e < N; e += nthr) {
+        const int st = start[e], p = (rs.cnt[e] + B - 1) / B * B;
+        for (int b = st / B; b < (st + p) / B; ++b) a.expert_ids[b] = e;
+    }
+    if (tid == 0) {
+        *w.total = total;
+        *a.ntpp = total;
+        *counter = 0u;
+    }
+}
+
+// Pass 2: place every assignment, fill the padding and the tail.
+__global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(SortArgs a, SortWork w) {
+    const int tid = threadIdx.x, nthr = blockDim.x, c = blockIdx.x, N = a.N, B = a.block;
+    const int beg = c * kSortChunk, n = min(kSortChunk, a.n_assign - beg);
+    for (int i = tid; i < n; i += nthr) {
+        const int e = a.ids[beg + i];
+        if (e < 0 || e >= N) continue;
+        a.sorted[w.start[e] + w.chunk_off[(size_t)c * N + e] + w.lrank[beg + i]] = beg + i;
+    }
+    const int64_t gt = (int64_t)c * nthr + tid, T = (int64_t)gridDim.x * nthr;
+    const int total = *w.total, sentinel = a.n_assign;
+    for (int64_t e = gt; e < N; e += T) {
+        const int cnt = w.cnt[e];
+        const int st = w.start[e], p = (cnt + B - 1) / B * B;
+        for (int i = cnt; i < p; ++i) a.sorted[st + i] = sentinel;
+    }
+    for (int64_t i = total + gt; i < a.capacity; i += T) a.sorted[i] = sentinel;
+    for (int64_t b = total / B + gt; b < a.capacity / B; b += T) a.expert_ids[b] = -1;
+}
+
+static int g_sort_cta_smem[64];
+static int g_sort_count_smem[64];
+
+cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, int32_t* sorted,
+                        int32_t* expert_ids, int32_t* ntpp, int64_t capacity, void* scratch,
+                        cudaStream_t st) {
+    SortArgs a{ids, M * topk, N, block, sorted, expert_ids, ntpp, capacity};
+    const int nw = kSortThreads / 32;
+    if (a.n_assign <= kSortChunk) {
+        const int smem = 4 * cta_sort_smem_ints(nw, N, a.n_assign);
+        cudaError_t e = ensure_smem((const void*)sort_cta_kernel, smem, g_sort_cta_smem);
+        if (e != cudaSuccess) return e;
+        sort_cta_kernel<<<1, kSortThreads, smem, st>>>(a);
+        return cudaGetLastError();
+    }
+    const int C = (a.n_assign + kSortChunk - 1) / kSortChunk;
+    SortWork w = sort_work(scratch, a.n_assign, N);
+    const int smem = 4 * (nw * N + N + kSortChunk);
+    cudaError_t e = ensure_smem((const void*)sort_count_kernel, smem, g_sort_count_smem);
+    if (e != cudaSuccess) return e;
+    unsigned* counter = static_cast<unsigned*>(scratch) + kSortCounterSlot;
+    sort_count_kernel<<<C, kSortThreads, smem, st>>>(a, w, counter);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    sort_scatter_kernel<<<C, kSortThreads, 0, st>>>(a, w);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ quant
+
+// One lane quantises 8 consecutive elements; a lane quad is one 32-block.
+// Each warp takes 32 consecutive 16-byte vectors per step (4 rows' worth of
+// blocks never straddle: K % 32 == 0), UNROLL steps in flight.
+constexpr int kQuantThreads = 256;
+constexpr int kQuantUnroll = 4;
+
+__global__ void __launch_bounds__(kQuantThreads) mxfp8_quant_kernel(const uint16_t* x, int64_t ldx,
+                                                                    int M, int K, uint8_t* q,
+                                                                    uint8_t* scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t vpr = K / 8;                   // vectors per row
+    const int64_t total = (int64_t)M * vpr;
+    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t K32 = K / 32;
+    for (int64_t base = warp_id * 32 * kQuantUnroll; base < total; base += nwarps * 32 * kQuantUnroll) {
+        uint4 v[kQuantUnroll];
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int64_t i = base + u * 32 + lane;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < total) {
+                const int64_t r = i / vpr, c = i - r * vpr;
+                v[u] = ld_stream_v4(x + r * ldx + c * 8);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int64_t i = base + u * 32 + lane;
+            unsigned sb;
+            const uint2 q8 = mx_quant_quad(v[u], &sb);
+            if (i < total) {
+                const int64_t r = i / vpr, c = i - r * vpr;
+                *reinterpret_cast<uint2*>(q + r * K + c * 8) = q8;
+                if ((lane & 3) == 0) scale[r * K32 + c / 4] = (uint8_t)sb;
+            }
+        }
+    }
+}
+
+cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale,
+                         cudaStream_t st) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t vectors = (int64_t)M * (K / 8);
+    const int64_t per_cta = (int64_t)kQuantThreads * kQuantUnroll;
+    int64_t ctas = (vectors + per_cta - 1) / per_cta;
+    const int64_t cap = (int64_t)sms * 8;  // 8 resident CTAs per SM, grid-stride beyond
+    if (ctas > cap) ctas = cap;
+    mxfp8_quant_kernel<<<(unsigned)ctas, kQuantThreads, 0, st>>>(static_cast<const uint16_t*>(x), ldx, M,
+                                                                 K, q, scale);
+    return cudaGetLastError();
+}
+
+}  // namespace mr

@@ -1,0 +1,110 @@
+// Warp-per-token top-k gate.
+//
+// The gate (sglang #46691 Summary; sglang #46652 Modifications): per token,
+// pick the k experts with the largest selection key and weight them.
+//   softmax: key = logit; weights = softmax of the selected logits
+//            (renormalised) or the full softmax probabilities.
+//   sigmoid: s = sigmoid(logit) (fixed fp32 recipe), key = s + bias;
+//            weights = s of the selected, renormalised or not.
+// Ties go to the lower expert id.
+//
+// GB300 design: one warp per token.  Lane l holds the keys of experts
+// l, l+32, l+64, ... as order-preserving 32-bit images, so the loads of a
+// row are coalesced.  Each of the k rounds takes the warp maximum with one
+// redux.sync (max) and breaks ties with a second (min over the candidate
+// ids), then only the winning lane rescans its NPL keys.  Slot j lives in
+// lane j, which then forms the weight; sums use a fixed butterfly, so the
+// result is deterministic.
+#pragma once
+
+#include "common.cuh"
+
+namespace mr {
+
+struct TopkArgs {
+    const float* logits;   // [M, N]
+    const float* bias;     // [N] or nullptr (sigmoid only)
+    int32_t* ids;          // [M, k]
+    float* weights;        // [M, k]
+    int M, N, k;
+    int scoring;           // 0 softmax, 1 sigmoid
+    int renormalize;
+};
+
+// Gate of one token (row m) by one warp.  If ids_smem != nullptr the chosen
+// ids are also written there (slot order).  Reads the logits through L2 so
+// that rows written by other CTAs of the same launch are seen.
+template <int NPL>
+__device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids_smem) {
+    const int lane = threadIdx.x & 31;
+    const float* row = a.logits + (int64_t)m * a.N;
+    unsigned key[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+        const int id = lane + 32 * j;
+        unsigned kv = 0u;  // below every real key: never selected while real keys remain
+        if (id < a.N) {
+            const float l = __ldcg(row + id);
+            float sel = l;
+            if (a.scoring == 1) sel = __fadd_rn(sigmoid_score(l), a.bias ? __ldg(a.bias + id) : 0.0f);
+            kv = ordered_key(sel);
+        }
+        key[j] = kv;
+    }
+    unsigned best = 0u;
+    int bestj = 0;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+        if (key[j] > best) { best = key[j]; bestj = j; }
+
+    int my_id = 0;
+    for (int r = 0; r < a.k; ++r) {
+        const unsigned kmax = __reduce_max_sync(kFull, best);
+        const unsigned cand = (best == kmax) ? (unsigned)(lane + 32 * bestj) : 0xFFFFFFFFu;
+        const unsigned win = __reduce_min_sync(kFull, cand);
+        if (lane == r) my_id = (int)win;
+        if (lane == (int)(win & 31u)) {
+            const int wj = (int)(win >> 5);
+            best = 0u;
+            bestj = 0;
+#pragma unroll
+            for (int j = 0; j < NPL; ++j) {
+                if (j == wj) key[j] = 0u;
+                if (key[j] > best) { best = key[j]; bestj = j; }
+            }
+        }
+    }
+
+    // weights: lane r < k owns slot r
+    const bool live = lane < a.k;
+    const float lsel = live ? __ldcg(row + my_id) : 0.0f;
+    float num = 0.0f, den;
+    if (a.scoring == 1) {
+        num = live ? sigmoid_score(lsel) : 0.0f;
+        den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
+    } else {
+        const float lmax = __shfl_sync(kFull, lsel, 0);  // slot 0 holds the largest logit
+        num = live ? expf(__fadd_rn(lsel, -lmax)) : 0.0f;
+        if (a.renormalize) {
+            den = warp_sum_fixed(num);
+        } else {
+            float part = 0.0f;
+            for (int id = lane; id < a.N; id += 32) part = __fadd_rn(part, expf(__fadd_rn(__ldcg(row + id), -lmax)));
+            den = warp_sum_fixed(part);
+        }
+    }
+    if (live) {
+        a.ids[(int64_t)m * a.k + lane] = my_id;
+        a.weights[(int64_t)m * a.k + lane] = (a.scoring == 1 && !a.renormalize) ? num : __fdiv_rn(num, den);
+        if (ids_smem) ids_smem[m * a.k + lane] = my_id;
+    }
+}
+
+template <int NPL>
+__device__ __forceinline__ void cta_topk_rows(const TopkArgs& a, int row_begin, int row_end,
+                                              int* ids_smem) {
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int m = row_begin + warp; m < row_end; m += nwarps) warp_topk_row<NPL>(a, m, ids_smem);
+}
+
+}  // namespace mr

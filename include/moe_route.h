@@ -1,0 +1,207 @@
+/*
+ * moe_route.h -- C ABI of the GB300 (sm_103a) MoE decode routing library.
+ *
+ * The path: a skinny router GEMV (bf16 activations x [M,K] times the bf16 gate
+ * W [N,K] -> fp32 logits [M,N]), top-k gating, the sort of the (token, slot)
+ * assignments into padded per-expert blocks, and MXFP8 quantisation of the
+ * stage-1 activations.  The method follows these GitHub PR pages:
+ *   [#36557] sglang "MiniMax-M3: Triton split-K router GEMV with in-kernel
+ *            fixup" (description): the GEMV shape, the per-M-bucket split-K
+ *            tiling, the in-kernel split-K fixup (the last CTA to finish a
+ *            (n-block, row-tile) pair reduces the partials and re-zeroes its
+ *            counter slot), and the shape predicate with fall-through.
+ *   [#46691] sglang MiniMax-M3.1 MoE/GEMM kernels (Summary; "Changes to
+ *            existing kernels"): GEMV up to 512 rows, the gate, aiter's sort
+ *            into per-expert blocks, sort + stage-1 quant in one launch for
+ *            decode batches, a one-launch decode router for 1-16 tokens that
+ *            is bitwise equal to the unfused chain, the int32 offset limit.
+ *   [#46652] sglang Kimi-K3 fused MoE routing, sort, quant (Modifications;
+ *            Accuracy Tests; review diff of the sort kernel): 896 experts,
+ *            top-16, hidden 3584, MXFP8 stage-1 activations, stable ranks.
+ *
+ * Conventions (all entry points):
+ *  - Pointers named x, w, logits, topk_*, sorted_*, expert_ids,
+ *    num_tokens_post_padded, q, scale, sel_bias and scratch are DEVICE
+ *    pointers owned by the caller.  The library never allocates or frees.
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every call is asynchronous on that stream; none synchronises
+ *    the host.  The returned status covers argument validation and the launch
+ *    (cudaGetLastError) only; a fault inside a kernel surfaces at the
+ *    caller's next synchronisation, as for any CUDA call.
+ *  - bf16 tensors are row-major with a contiguous last dimension; ldx is the
+ *    row stride of x in ELEMENTS.  x, w must be 16-byte aligned and ldx a
+ *    multiple of 8; other pointers need their natural alignment.
+ *  - All element offsets are computed in 64-bit (no int32 offset limit).
+ *  - Validation happens on the host before any launch: a status other than
+ *    MR_OK means nothing was launched.  MR_ERR_UNSUPPORTED means the shape is
+ *    outside what the kernels cover (the caller may use another path);
+ *    MR_ERR_INVALID_ARG means the call itself is wrong.
+ *  - Scratch: one caller-owned device buffer per stream, sized by
+ *    mr_scratch_bytes() and zeroed ONCE by mr_scratch_reset() (or any
+ *    memset) after allocation.  Every successful call leaves its counters
+ *    at zero again, so the buffer is reused across launches with no memset.
+ *    Two calls that may run concurrently must not share a scratch buffer.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MR_ABI_VERSION 1
+
+/* Bytes at the start of every scratch buffer that hold the launch counters. */
+#define MR_SCRATCH_COUNTER_BYTES 32768
+
+/* Limits of the kernels (MR_ERR_UNSUPPORTED beyond them). */
+#define MR_MAX_EXPERTS 1024
+#define MR_MAX_TOPK 32
+#define MR_MAX_GEMV_ROWS 512
+#define MR_MAX_FUSED_ROWS 16
+#define MR_GEMV_K_MULTIPLE 512
+
+typedef enum mr_status {
+    MR_OK = 0,
+    MR_ERR_UNSUPPORTED = 1,      /* shape / layout outside the kernels' cover  */
+    MR_ERR_INVALID_ARG = 2,      /* null or misaligned pointer, bad size       */
+    MR_ERR_SCRATCH_TOO_SMALL = 3,/* scratch_bytes below what the call needs    */
+    MR_ERR_CUDA = 4              /* the CUDA runtime reported an error         */
+} mr_status;
+
+typedef enum mr_scoring {
+    MR_SCORE_SOFTMAX = 0,        /* select by logit; weights = softmax         */
+    MR_SCORE_SIGMOID = 1         /* select by sigmoid + bias; weights = sigmoid */
+} mr_scoring;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mr_status_string(int status);
+
+/* MR_ABI_VERSION of the loaded library. */
+int mr_abi_version(void);
+
+/*
+ * Shape predicate of the router GEMV [#36557 description: "router_gemv_
+ * supported()": dtype, contiguous last dim, N % BLOCK_N, K % BLOCK_K, M].
+ * Returns 1 when mr_router_gemv covers (M, N, K, ldx), else 0.  Pure host
+ * function.  Covered: 1 <= M <= 512, 8 <= N <= 1024 with N divisible by the
+ * bucket's n-block, K a positive multiple of 512, ldx >= K and ldx % 8 == 0.
+ */
+int mr_router_gemv_supported(int M, int N, int K, int64_t ldx);
+
+/*
+ * Scratch bytes sufficient for every call of this library with M <= M_max
+ * tokens, N experts, hidden K and top-k (router GEMV split-K partials, the
+ * fused route, the multi-CTA sort of large batches).  The first
+ * MR_SCRATCH_COUNTER_BYTES hold counters.  Returns 0 for out-of-range
+ * arguments.  Pure host function.
+ */
+size_t mr_scratch_bytes(int M_max, int N, int K, int topk);
+
+/* Zeroes scratch[0, scratch_bytes) on stream (one cudaMemsetAsync). */
+int mr_scratch_reset(void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * a1 + a2. Router GEMV with in-kernel split-K fixup [#36557 description;
+ * #46691 Summary: up to 512 rows].
+ *   logits[m, n] = sum_k x[m, k] * w[n, k]   (fp32 accumulation)
+ * x: bf16 [M, ldx]; w: bf16 [N, K] contiguous; logits: fp32 [M, N].
+ * One launch.  The K range is split over CTAs; the last CTA to finish each
+ * (n-block, row-tile) sums the fp32 partials in split order (deterministic)
+ * and re-zeroes its counter.  Deterministic: the same inputs give the same
+ * bits on every call.
+ */
+int mr_router_gemv(const void *x, int64_t ldx, const void *w, float *logits,
+                   int M, int N, int K, void *scratch, size_t scratch_bytes,
+                   void *stream);
+
+/*
+ * a3. Top-k gating [#46691 Summary: the gate; #46652: sigmoid gate with a
+ * selection bias, top-16 of 896].  One warp per token.
+ *   MR_SCORE_SOFTMAX: selection key = the logit; weights = softmax
+ *     probabilities of the selected experts (divided by their sum when
+ *     renormalize != 0).
+ *   MR_SCORE_SIGMOID: s = sigmoid(logit) by a fixed fp32 recipe (Cody-Waite
+ *     reduction + degree-7 Taylor polynomial, fp32 fma; within 3 ulp of the
+ *     exact sigmoid); key = s + sel_bias[n] in fp32; weights = the unbiased
+ *     s of the selected (divided by their sum when renormalize != 0).
+ * Ties: the lower expert id wins; -0 and +0 tie.  Slot j of a token is its
+ * j-th best expert.  logits: fp32 [M, N]; sel_bias: fp32 [N] or NULL
+ * (sigmoid only); topk_ids: int32 [M, topk]; topk_weights: fp32 [M, topk].
+ * Requires 1 <= topk <= min(N, 32).  NaN logits are outside the contract.
+ */
+int mr_route_topk(const float *logits, int M, int N, int topk, int scoring,
+                  const float *sel_bias, int renormalize, int32_t *topk_ids,
+                  float *topk_weights, void *stream);
+
+/*
+ * Entries the sort writes into sorted_token_ids: the worst case of
+ * sum_e ceil(c_e / block) * block, i.e. M*topk + min(N, M*topk)*(block-1),
+ * rounded up to a multiple of block.  expert_ids holds capacity / block
+ * entries.  Returns -1 for out-of-range arguments.  Pure host function.
+ */
+int64_t mr_sort_capacity(int M, int topk, int N, int block);
+
+/*
+ * a4. Sort of the assignments into padded per-expert blocks [#46691 Summary
+ * and "Changes to existing kernels": aiter's sort; #46652 review diff: the
+ * stable rank of an assignment is the number of earlier (token, slot) pairs
+ * on the same expert].
+ * Layout: assignment f = m*topk + j.  Experts in ascending id; within an
+ * expert, f ascending; each expert's run padded to a multiple of block with
+ * the sentinel M*topk; experts with no assignment take no block.
+ * expert_ids[b] = the expert owning block b.  *num_tokens_post_padded = the
+ * padded total.  Every entry past it, up to capacity (resp. capacity/block),
+ * is written: sentinel M*topk (resp. -1).  Ids outside [0, N) are not placed.
+ * topk_ids: int32 [M, topk]; sorted_token_ids: int32 [capacity];
+ * expert_ids: int32 [capacity / block]; num_tokens_post_padded: int32 [1].
+ * capacity must be >= mr_sort_capacity(M, topk, N, block).  1 <= block <=
+ * 1024.  One launch up to 2048 assignments; two launches above (scratch
+ * used).  Output bits are unique (no freedom in the layout).
+ */
+int mr_moe_sort(const int32_t *topk_ids, int M, int topk, int N, int block,
+                int32_t *sorted_token_ids, int32_t *expert_ids,
+                int32_t *num_tokens_post_padded, int64_t capacity,
+                void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * a5. MXFP8 quantisation of the stage-1 activations [#46691 Summary: sort +
+ * stage-1 activation quant; #46652 Accuracy Tests: MXFP8], per the OCP
+ * Microscaling Formats v1.0 spec: for each row and block of 32 elements
+ * along K, X = floor(log2(amax)) - 8, clamped to [-127, 127] (amax = 0 gives
+ * -127); scale[m, b] = X + 127 (E8M0); q = E4M3(x * 2^-X), round to nearest
+ * even, saturating to +-448, sign kept.  Exact (no fast-math): bf16
+ * subnormals are honoured.  x: bf16 [M, ldx]; q: uint8 [M, K] row-major;
+ * scale: uint8 [M, K/32] row-major.  K % 32 == 0.  Any M >= 1.
+ */
+int mr_mxfp8_quant(const void *x, int64_t ldx, int M, int K, uint8_t *q,
+                   uint8_t *scale, void *stream);
+
+/*
+ * a6. The whole path for 1 <= M <= 16 tokens in ONE launch [#46691 Summary:
+ * a one-launch decode router for 1-16 tokens, bitwise equal to router GEMV,
+ * gate and sort; sort + quant in one launch for decode batches].
+ * Arguments as in the four calls above; every output is bitwise equal to
+ * mr_router_gemv -> mr_route_topk -> mr_moe_sort -> mr_mxfp8_quant on the
+ * same inputs.  q and scale may both be NULL to skip the quantisation.
+ * GEMV CTAs hand over by atomic last-arriver tickets (no spin-waits): the
+ * last CTA of each n-block runs the split-K fixup, the last fixup runs the
+ * gate for all tokens and the sort.
+ */
+int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
+                            int M, int N, int K, int topk, int scoring,
+                            const float *sel_bias, int renormalize, int block,
+                            float *logits, int32_t *topk_ids, float *topk_weights,
+                            int32_t *sorted_token_ids, int32_t *expert_ids,
+                            int32_t *num_tokens_post_padded, int64_t capacity,
+                            uint8_t *q, uint8_t *scale,
+                            void *scratch, size_t scratch_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

@@ -1,0 +1,121 @@
+"""The C ABI library on a machine without a GPU: it builds, loads, exports
+every entry point include/moe_route.h declares, and its host-only functions
+(shape predicate, sizes, validation) behave.  No call here reaches a kernel."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_expert_routing_gb300 as mr
+from decode_expert_routing_gb300 import build as mrbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_route.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mrbuild.build()
+    return mr.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mr_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("mr_router_gemv", "mr_route_topk", "mr_moe_sort", "mr_mxfp8_quant",
+              "mr_moe_route_sort_quant", "mr_router_gemv_supported", "mr_scratch_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(mr.SIGNATURES), "binding signatures out of sync with the header"
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mr_abi_version() == 1
+    for s in range(5):
+        assert lib.mr_status_string(s).startswith(b"MR_")
+    assert lib.mr_status_string(99) == b"unknown mr_status"
+
+
+def test_shape_predicate(lib):
+    ok = mr.router_gemv_supported
+    assert ok(1, 128, 6144) and ok(16, 128, 6144) and ok(64, 128, 6144) and ok(512, 128, 6144)
+    assert ok(8, 896, 3584) and ok(32, 896, 3584)
+    assert not ok(513, 128, 6144)          # M > 512
+    assert not ok(1, 128, 6000)            # K % 512
+    assert not ok(1, 100, 6144)            # N % BLOCK_N
+    assert not ok(1, 2048, 6144)           # N > 1024
+    assert not ok(0, 128, 6144)
+    assert not ok(1, 128, 6144, 6143)      # ldx < K
+    assert not ok(1, 128, 6144, 6148)      # ldx % 8
+    assert ok(1, 128, 6144, 6144 + 64)
+
+
+def test_sort_capacity(lib):
+    assert mr.sort_capacity(1, 8, 128, 16) == 128
+    assert mr.sort_capacity(3, 2, 4, 2) == 10
+    assert mr.sort_capacity(32, 16, 896, 16) == 512 + 512 * 15
+    assert mr.sort_capacity(4096, 8, 128, 64) == 32768 + 128 * 63
+    assert mr.sort_capacity(0, 8, 128, 16) == -1
+
+
+def test_scratch_bytes(lib):
+    b = mr.scratch_bytes(64, 128, 6144, 8)
+    assert b >= 32768 and b % 256 == 0
+    # covers the largest split-K partial plane of any M up to M_max
+    assert mr.scratch_bytes(512, 128, 6144, 8) >= b
+    assert mr.scratch_bytes(4096, 128, 6144, 8) >= 32768 + 4 * 32768
+    assert mr.scratch_bytes(0, 128, 6144, 8) == 0
+
+
+def test_validation_returns_before_any_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: validation fails first
+    # null x
+    assert lib.mr_router_gemv(None, 6144, fake, fake, 1, 128, 6144, fake, 1 << 20, None) == mr.MR_ERR_INVALID_ARG
+    # misaligned x
+    assert lib.mr_router_gemv(P(0x1002), 6144, fake, fake, 1, 128, 6144, fake, 1 << 20, None) == mr.MR_ERR_INVALID_ARG
+    # unsupported K
+    assert lib.mr_router_gemv(fake, 6000, fake, fake, 1, 128, 6000, fake, 1 << 20, None) == mr.MR_ERR_UNSUPPORTED
+    # scratch too small
+    assert lib.mr_router_gemv(fake, 6144, fake, fake, 1, 128, 6144, fake, 100, None) == mr.MR_ERR_SCRATCH_TOO_SMALL
+    # gate: topk > N, bad scoring, N too large
+    assert lib.mr_route_topk(fake, 1, 8, 9, 0, None, 1, fake, fake, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_route_topk(fake, 1, 128, 8, 7, None, 1, fake, fake, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_route_topk(fake, 1, 2048, 8, 0, None, 1, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
+    assert lib.mr_route_topk(fake, 1, 128, 33, 0, None, 1, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
+    # sort: capacity too small
+    assert lib.mr_moe_sort(fake, 1, 8, 128, 16, fake, fake, fake, 64, None, 0, None) == mr.MR_ERR_INVALID_ARG
+    # sort of a large batch without scratch
+    assert lib.mr_moe_sort(fake, 4096, 8, 128, 64, fake, fake, fake, 40832, None, 0, None) == mr.MR_ERR_INVALID_ARG
+    # quant: K % 32
+    assert lib.mr_mxfp8_quant(fake, 48, 1, 40, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
+    # fused: M > 16
+    assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 17, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
+                                       fake, fake, fake, 1 << 20, fake, fake, fake, 1 << 20, None) == mr.MR_ERR_UNSUPPORTED
+    # fused: q without scale
+    assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 1, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
+                                       fake, fake, fake, 128, fake, None, fake, 1 << 20, None) == mr.MR_ERR_INVALID_ARG
+    # reset: buffer below the counter prefix
+    assert lib.mr_scratch_reset(fake, 100, None) == mr.MR_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = mr._lib
+    try:
+        mr._lib = None
+        with pytest.raises(RuntimeError, match="not found"):
+            mr.load_library(str(tmp_path / "nope.so"))
+    finally:
+        mr._lib = saved
