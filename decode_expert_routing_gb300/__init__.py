@@ -18,7 +18,7 @@ import os
 
 __all__ = [
     "MoeRouteError", "MoeRouteUnsupported", "Scratch", "library_path", "load_library",
-    "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
+    "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
     "moe_sort", "mxfp8_quant", "moe_route_sort_quant",
 ]
 
@@ -53,6 +53,8 @@ _P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size
 SIGNATURES = {
     "mr_status_string": (ctypes.c_char_p, [_I]),
     "mr_abi_version": (_I, []),
+    "mr_set_launch_flags": (_I, [_I]),
+    "mr_get_launch_flags": (_I, []),
     "mr_router_gemv_supported": (_I, [_I, _I, _I, _I64]),
     "mr_scratch_bytes": (_SZ, [_I, _I, _I, _I]),
     "mr_scratch_reset": (_I, [_P, _SZ, _P]),
@@ -125,6 +127,18 @@ def _row_major_2d(x, name):
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError(f"{name} must be 2-D with a contiguous last dimension")
     return x.stride(0)
+
+
+LAUNCH_PDL = 1
+
+
+def set_launch_flags(flags: int) -> None:
+    """Process-wide launch options (LAUNCH_PDL: programmatic dependent launch)."""
+    _check(_load().mr_set_launch_flags(int(flags)), "mr_set_launch_flags")
+
+
+def get_launch_flags() -> int:
+    return int(_load().mr_get_launch_flags())
 
 
 def router_gemv_supported(M: int, N: int, K: int, ldx: int | None = None) -> bool:

@@ -2,6 +2,8 @@
 // Nothing here allocates device memory.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe_route.h"
 #include "internal.h"
 
@@ -39,9 +41,34 @@ int check_sort_args(int M, int topk, int N, int block, int64_t capacity) {
     return MR_OK;
 }
 
+std::atomic<int> g_launch_flags{0};
+std::atomic<void*> g_trace{nullptr};
+
 }  // namespace
 
+namespace mr {
+int launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+void* trace_buffer() { return g_trace.load(std::memory_order_relaxed); }
+}  // namespace mr
+
 extern "C" {
+
+int mr_set_launch_flags(int flags) {
+    if (flags & ~MR_LAUNCH_PDL) return MR_ERR_INVALID_ARG;
+    g_launch_flags.store(flags, std::memory_order_relaxed);
+    return MR_OK;
+}
+
+int mr_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
+
+#ifdef MR_TRACE
+// Tracing builds only: device buffer of gridDim * 8 u64 stamps for the next
+// launches (nullptr stops tracing).
+int mr_trace_set_buffer(void* device_buffer) {
+    g_trace.store(device_buffer, std::memory_order_relaxed);
+    return MR_OK;
+}
+#endif
 
 const char* mr_status_string(int status) {
     switch (status) {

@@ -36,12 +36,21 @@ __device__ __forceinline__ void mma_bf16_m16n8k16(float (&c)[4], uint32_t a0, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Programmatic dependent launch.  pdl_wait() blocks until the kernel
+// launched before this one on the stream has completed and its writes are
+// visible (a no-op when the launch did not allow overlap); pdl_trigger()
+// lets the next kernel on the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Last-arriver ticket: returns the counter value before this CTA's increment.
-// Every thread must have written what it publishes before the call; the
-// whole CTA calls it.  acq_rel at gpu scope plus the fences make the other
-// CTAs' published writes visible to the CTA that draws the last ticket.
+// The whole CTA calls it after writing what it publishes.  Each thread's
+// release fence orders its own writes before the barrier; thread 0's
+// acq_rel atomic publishes them at gpu scope and, in the CTA that draws the
+// last ticket, acquires every other CTA's; the barrier passes that on to the
+// CTA's threads, which then read the published data through L2 (ld.cg).
 __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_slot) {
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     __syncthreads();
     if (threadIdx.x == 0) {
         unsigned old;
@@ -49,10 +58,25 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
         *s_slot = old;
     }
     __syncthreads();
-    unsigned t = *s_slot;
-    __threadfence();
-    return t;
+    return *s_slot;
 }
+
+// Optional per-CTA phase stamps (compile with -DMR_TRACE): thread 0 writes
+// %globaltimer (ns) to trace[(blockIdx.y * gridDim.x + blockIdx.x) * 8 + slot].
+#ifdef MR_TRACE
+#define MR_TRACE_STAMP(trace, slot)                                                  \
+    do {                                                                             \
+        if (threadIdx.x == 0 && (trace) != nullptr) {                               \
+            unsigned long long t_;                                                   \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                   \
+            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 8 + (slot)] = t_;        \
+        }                                                                            \
+    } while (0)
+#else
+#define MR_TRACE_STAMP(trace, slot) \
+    do {                            \
+    } while (0)
+#endif
 
 // Orderable image of an fp32 key: larger float -> larger unsigned.  The key
 // is first canonicalised (-0 -> +0) so that the two zeros tie.

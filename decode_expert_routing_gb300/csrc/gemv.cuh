@@ -37,6 +37,7 @@ struct GemvArgs {
     int M, N, K;
     int split_k;           // CTAs along K
     int nblocks;           // N / BLOCK_N
+    unsigned long long* trace;  // phase stamps (tracing builds only), or nullptr
 };
 
 // Where the fused kernel puts MXFP8 codes of the x fragments it loads.
@@ -80,6 +81,9 @@ __device__ __forceinline__ void gemv_tile(const GemvArgs& a, int nblk, int split
     const uint16_t* wrow = a.w + (int64_t)n * a.K + kbeg;
 #pragma unroll
     for (int s = 0; s < C::KS; ++s) wv[s] = ld_stream_v4(wrow + s * 32);
+    // The gate weight is never written by the preceding kernel; everything
+    // else (x, scratch, outputs) is touched only after it has completed.
+    pdl_wait();
 
     uint4 xa[C::MT][C::KS], xb[C::MT][C::KS];
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -192,6 +196,7 @@ __device__ __forceinline__ bool gemv_cta(const GemvArgs& a, int nblk, int split,
                                          float* red, unsigned* s_ticket, const QuantOut* qo) {
     float acc[C::MT][4];
     gemv_tile<C>(a, nblk, split, rt, acc, red, qo);
+    MR_TRACE_STAMP(a.trace, 1);
     if (a.split_k == 1) {
         gemv_store<C>(a, a.logits, nblk, rt, acc);
         return true;
@@ -199,8 +204,10 @@ __device__ __forceinline__ bool gemv_cta(const GemvArgs& a, int nblk, int split,
     gemv_store<C>(a, a.partials + (int64_t)split * a.M * a.N, nblk, rt, acc);
     unsigned* ctr = a.counters + rt * a.nblocks + nblk;
     const unsigned ticket = cta_ticket(ctr, s_ticket);
+    MR_TRACE_STAMP(a.trace, 2);
     if (ticket != (unsigned)(a.split_k - 1)) return false;
-    // fixup: sum the partials of every split in split order
+    // fixup: sum the partials of every split in split order (loads of up to
+    // 8 splits in flight at once, adds in order)
     const int rows = min(C::ROWS, a.M - rt * C::ROWS);
     const int64_t plane = (int64_t)a.M * a.N;
     for (int e = threadIdx.x; e < rows * C::BLOCK_N; e += C::NTHR) {
@@ -208,10 +215,18 @@ __device__ __forceinline__ bool gemv_cta(const GemvArgs& a, int nblk, int split,
         const int col = nblk * C::BLOCK_N + e % C::BLOCK_N;
         const float* p = a.partials + (int64_t)r * a.N + col;
         float s = 0.0f;
-        for (int sp = 0; sp < a.split_k; ++sp) s = __fadd_rn(s, __ldcg(p + sp * plane));
+        for (int sp0 = 0; sp0 < a.split_k; sp0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = (sp0 + i < a.split_k) ? __ldcg(p + (sp0 + i) * plane) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (sp0 + i < a.split_k) s = __fadd_rn(s, v[i]);
+        }
         a.logits[(int64_t)r * a.N + col] = s;
     }
     if (threadIdx.x == 0) *ctr = 0u;
+    MR_TRACE_STAMP(a.trace, 3);
     return true;
 }
 

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace mr {
 
 // Counter slots inside the scratch prefix (MR_SCRATCH_COUNTER_BYTES = 32 KiB).
@@ -53,6 +55,31 @@ cudaError_t launch_fused(const GemvPlan& p, const void* x, int64_t ldx, const vo
                          float* weights, int32_t* sorted, int32_t* expert_ids, int32_t* ntpp,
                          int64_t capacity, uint8_t* q, uint8_t* scale, void* scratch,
                          cudaStream_t st);
+
+// Launch options (MR_LAUNCH_* bits of mr_set_launch_flags).
+int launch_flags();
+// Device buffer for phase stamps of tracing builds (nullptr otherwise).
+void* trace_buffer();
+
+// Launches kernel<<<grid, block, smem, st>>>(args...) through
+// cudaLaunchKernelEx, allowing programmatic dependent launch when the
+// MR_LAUNCH_PDL flag is set; returns the launch status.
+template <class... KArgs, class... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (launch_flags() & 1) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // Opt a kernel into more than 48 KiB of dynamic shared memory, once per
 // device.

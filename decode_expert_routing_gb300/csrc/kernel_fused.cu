@@ -34,6 +34,8 @@ template <class C, int NPL>
 __global__ void __launch_bounds__(C::NTHR) fused_route_kernel(FusedArgs f) {
     extern __shared__ __align__(16) int sm[];
     __shared__ unsigned s_ticket;
+    MR_TRACE_STAMP(f.g.trace, 0);
+    pdl_trigger();
     const int nblk = blockIdx.x % f.g.nblocks, split = blockIdx.x / f.g.nblocks;
     QuantOut qo{f.q, f.scale};
     const bool quant_here = f.q != nullptr && nblk == 0;
@@ -41,6 +43,7 @@ __global__ void __launch_bounds__(C::NTHR) fused_route_kernel(FusedArgs f) {
                      quant_here ? &qo : nullptr))
         return;
     const unsigned t = cta_ticket(f.done_counter, &s_ticket);
+    MR_TRACE_STAMP(f.g.trace, 4);
     if (t != (unsigned)(f.g.nblocks - 1)) return;
 
     // gate of every token, then the sort, in this CTA
@@ -51,8 +54,10 @@ __global__ void __launch_bounds__(C::NTHR) fused_route_kernel(FusedArgs f) {
     int* ids_s = warp_tot + 32;
     cta_topk_rows<NPL>(f.t, 0, f.g.M, ids_s);
     __syncthreads();
+    MR_TRACE_STAMP(f.g.trace, 5);
     cta_sort(f.s, ids_s, rs, start, warp_tot);
     if (threadIdx.x == 0) *f.done_counter = 0u;
+    MR_TRACE_STAMP(f.g.trace, 6);
 }
 
 template <class C>
@@ -62,12 +67,11 @@ static cudaError_t launch_fused_cfg(const FusedArgs& f, int npl, int nthr, cudaS
     const int smem = 4 * (sort_ints > C::RED_FLOATS ? sort_ints : C::RED_FLOATS);
     dim3 grid(f.g.nblocks * f.g.split_k);
     switch (npl) {
-        case 4: fused_route_kernel<C, 4><<<grid, nthr, smem, st>>>(f); break;
-        case 8: fused_route_kernel<C, 8><<<grid, nthr, smem, st>>>(f); break;
-        case 16: fused_route_kernel<C, 16><<<grid, nthr, smem, st>>>(f); break;
-        default: fused_route_kernel<C, 32><<<grid, nthr, smem, st>>>(f); break;
+        case 4: return launch_kernel(fused_route_kernel<C, 4>, grid, dim3(nthr), smem, st, f);
+        case 8: return launch_kernel(fused_route_kernel<C, 8>, grid, dim3(nthr), smem, st, f);
+        case 16: return launch_kernel(fused_route_kernel<C, 16>, grid, dim3(nthr), smem, st, f);
+        default: return launch_kernel(fused_route_kernel<C, 32>, grid, dim3(nthr), smem, st, f);
     }
-    return cudaGetLastError();
 }
 
 // Only the M <= 8 and M <= 16 rows of the tiling table carry a fused kernel.
@@ -97,6 +101,7 @@ cudaError_t launch_fused(const GemvPlan& p, const void* x, int64_t ldx, const vo
     f.g.K = K;
     f.g.split_k = p.split_k;
     f.g.nblocks = p.nblocks;
+    f.g.trace = static_cast<unsigned long long*>(trace_buffer());
     f.t = TopkArgs{logits, bias, ids, weights, M, N, topk, scoring, renormalize};
     f.s = SortArgs{ids, M * topk, N, block, sorted, expert_ids, ntpp, capacity};
     f.q = q;

@@ -11,6 +11,8 @@ constexpr int kTopkWarps = 4;
 
 template <int NPL>
 __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(TopkArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int m = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
     if (m < a.M) warp_topk_row<NPL>(a, m, nullptr);
 }
@@ -22,13 +24,13 @@ cudaError_t launch_topk(const float* logits, int M, int N, int topk, int scoring
                         cudaStream_t st) {
     TopkArgs a{logits, bias, ids, weights, M, N, topk, scoring, renormalize};
     dim3 grid((M + kTopkWarps - 1) / kTopkWarps);
+    const dim3 block(32 * kTopkWarps);
     switch (topk_npl(N)) {
-        case 4: topk_kernel<4><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
-        case 8: topk_kernel<8><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
-        case 16: topk_kernel<16><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
-        default: topk_kernel<32><<<grid, 32 * kTopkWarps, 0, st>>>(a); break;
+        case 4: return launch_kernel(topk_kernel<4>, grid, block, 0, st, a);
+        case 8: return launch_kernel(topk_kernel<8>, grid, block, 0, st, a);
+        case 16: return launch_kernel(topk_kernel<16>, grid, block, 0, st, a);
+        default: return launch_kernel(topk_kernel<32>, grid, block, 0, st, a);
     }
-    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ sort
@@ -48,6 +50,8 @@ cudaError_t ensure_smem(const void* func, int bytes, int* done_per_device) {
 // Whole sort of <= kSortChunk assignments by one CTA.
 __global__ void __launch_bounds__(kSortThreads) sort_cta_kernel(SortArgs a) {
     extern __shared__ __align__(16) int sm[];
+    pdl_trigger();
+    pdl_wait();
     const int nw = blockDim.x >> 5;
     RankSmem rs{sm, sm + nw * a.N, sm + nw * a.N + a.N};
     int* start = rs.lrank + a.n_assign;
@@ -89,6 +93,8 @@ __global__ void __launch_bounds__(kSortThreads) sort_count_kernel(SortArgs a, So
                                                                   unsigned* counter) {
     extern __shared__ __align__(16) int sm[];
     __shared__ unsigned s_ticket;
+    pdl_trigger();
+    pdl_wait();
     const int nw = blockDim.x >> 5, tid = threadIdx.x, nthr = blockDim.x;
     const int C = gridDim.x, c = blockIdx.x, N = a.N;
     const int beg = c * kSortChunk, n = min(kSortChunk, a.n_assign - beg);
@@ -134,6 +140,8 @@ __global__ void __launch_bounds__(kSortThreads) sort_count_kernel(SortArgs a, So
 
 // Pass 2: place every assignment, fill the padding and the tail.
 __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(SortArgs a, SortWork w) {
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x, nthr = blockDim.x, c = blockIdx.x, N = a.N, B = a.block;
     const int beg = c * kSortChunk, n = min(kSortChunk, a.n_assign - beg);
     for (int i = tid; i < n; i += nthr) {
@@ -164,8 +172,7 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
         const int smem = 4 * cta_sort_smem_ints(nw, N, a.n_assign);
         cudaError_t e = ensure_smem((const void*)sort_cta_kernel, smem, g_sort_cta_smem);
         if (e != cudaSuccess) return e;
-        sort_cta_kernel<<<1, kSortThreads, smem, st>>>(a);
-        return cudaGetLastError();
+        return launch_kernel(sort_cta_kernel, dim3(1), dim3(kSortThreads), smem, st, a);
     }
     const int C = (a.n_assign + kSortChunk - 1) / kSortChunk;
     SortWork w = sort_work(scratch, a.n_assign, N);
@@ -173,11 +180,9 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
     cudaError_t e = ensure_smem((const void*)sort_count_kernel, smem, g_sort_count_smem);
     if (e != cudaSuccess) return e;
     unsigned* counter = static_cast<unsigned*>(scratch) + kSortCounterSlot;
-    sort_count_kernel<<<C, kSortThreads, smem, st>>>(a, w, counter);
-    e = cudaGetLastError();
+    e = launch_kernel(sort_count_kernel, dim3(C), dim3(kSortThreads), smem, st, a, w, counter);
     if (e != cudaSuccess) return e;
-    sort_scatter_kernel<<<C, kSortThreads, 0, st>>>(a, w);
-    return cudaGetLastError();
+    return launch_kernel(sort_scatter_kernel, dim3(C), dim3(kSortThreads), 0, st, a, w);
 }
 
 // ------------------------------------------------------------------ quant
@@ -191,6 +196,8 @@ constexpr int kQuantUnroll = 4;
 __global__ void __launch_bounds__(kQuantThreads) mxfp8_quant_kernel(const uint16_t* x, int64_t ldx,
                                                                     int M, int K, uint8_t* q,
                                                                     uint8_t* scale) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t vpr = K / 8;                   // vectors per row
     const int64_t total = (int64_t)M * vpr;
@@ -233,9 +240,8 @@ cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, u
     int64_t ctas = (vectors + per_cta - 1) / per_cta;
     const int64_t cap = (int64_t)sms * 8;  // 8 resident CTAs per SM, grid-stride beyond
     if (ctas > cap) ctas = cap;
-    mxfp8_quant_kernel<<<(unsigned)ctas, kQuantThreads, 0, st>>>(static_cast<const uint16_t*>(x), ldx, M,
-                                                                 K, q, scale);
-    return cudaGetLastError();
+    return launch_kernel(mxfp8_quant_kernel, dim3((unsigned)ctas), dim3(kQuantThreads), 0, st,
+                         static_cast<const uint16_t*>(x), ldx, M, K, q, scale);
 }
 
 }  // namespace mr

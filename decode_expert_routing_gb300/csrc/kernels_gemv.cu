@@ -9,6 +9,8 @@ template <class C>
 __global__ void __launch_bounds__(C::NTHR) router_gemv_kernel(GemvArgs a) {
     __shared__ __align__(16) float red[C::RED_FLOATS > 0 ? C::RED_FLOATS : 4];
     __shared__ unsigned s_ticket;
+    MR_TRACE_STAMP(a.trace, 0);
+    pdl_trigger();
     const int nblk = blockIdx.x % a.nblocks, split = blockIdx.x / a.nblocks;
     gemv_cta<C>(a, nblk, split, blockIdx.y, red, &s_ticket, nullptr);
 }
@@ -59,18 +61,18 @@ cudaError_t launch_router_gemv(const GemvPlan& p, const void* x, int64_t ldx, co
     a.K = K;
     a.split_k = p.split_k;
     a.nblocks = p.nblocks;
+    a.trace = static_cast<unsigned long long*>(trace_buffer());
     dim3 grid(p.nblocks * p.split_k, p.row_tiles);
     switch (p.cfg) {
 #define MR_LAUNCH_ROW(I, MT, HALF, NW, KW, KS)                                              \
     case I:                                                                                 \
-        router_gemv_kernel<GemvCfg<MT, HALF, NW, KW, KS>><<<grid, 32 * (NW) * (KW), 0, st>>>(a); \
-        break;
+        return launch_kernel(router_gemv_kernel<GemvCfg<MT, HALF, NW, KW, KS>>, grid,            \
+                             dim3(32 * (NW) * (KW)), 0, st, a);
         MR_GEMV_CONFIGS(MR_LAUNCH_ROW)
 #undef MR_LAUNCH_ROW
         default:
             return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace mr

@@ -38,15 +38,20 @@ template <int NPL>
 __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids_smem) {
     const int lane = threadIdx.x & 31;
     const float* row = a.logits + (int64_t)m * a.N;
+    float val[NPL];
     unsigned key[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+        const int id = lane + 32 * j;
+        val[j] = id < a.N ? __ldcg(row + id) : 0.0f;
+    }
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
         const int id = lane + 32 * j;
         unsigned kv = 0u;  // below every real key: never selected while real keys remain
         if (id < a.N) {
-            const float l = __ldcg(row + id);
-            float sel = l;
-            if (a.scoring == 1) sel = __fadd_rn(sigmoid_score(l), a.bias ? __ldg(a.bias + id) : 0.0f);
+            float sel = val[j];
+            if (a.scoring == 1) sel = __fadd_rn(sigmoid_score(val[j]), a.bias ? __ldg(a.bias + id) : 0.0f);
             kv = ordered_key(sel);
         }
         key[j] = kv;
@@ -58,38 +63,42 @@ __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids
         if (key[j] > best) { best = key[j]; bestj = j; }
 
     int my_id = 0;
+    float my_val = 0.0f;
     for (int r = 0; r < a.k; ++r) {
         const unsigned kmax = __reduce_max_sync(kFull, best);
         const unsigned cand = (best == kmax) ? (unsigned)(lane + 32 * bestj) : 0xFFFFFFFFu;
         const unsigned win = __reduce_min_sync(kFull, cand);
-        if (lane == r) my_id = (int)win;
-        if (lane == (int)(win & 31u)) {
-            const int wj = (int)(win >> 5);
+        const int owner = (int)(win & 31u), wj = (int)(win >> 5);
+        float wv = 0.0f;
+        if (lane == owner) {
             best = 0u;
             bestj = 0;
 #pragma unroll
             for (int j = 0; j < NPL; ++j) {
-                if (j == wj) key[j] = 0u;
+                if (j == wj) { wv = val[j]; key[j] = 0u; }
                 if (key[j] > best) { best = key[j]; bestj = j; }
             }
         }
+        wv = __shfl_sync(kFull, wv, owner);
+        if (lane == r) { my_id = (int)win; my_val = wv; }
     }
 
     // weights: lane r < k owns slot r
     const bool live = lane < a.k;
-    const float lsel = live ? __ldcg(row + my_id) : 0.0f;
     float num = 0.0f, den;
     if (a.scoring == 1) {
-        num = live ? sigmoid_score(lsel) : 0.0f;
+        num = live ? sigmoid_score(my_val) : 0.0f;
         den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
     } else {
-        const float lmax = __shfl_sync(kFull, lsel, 0);  // slot 0 holds the largest logit
-        num = live ? expf(__fadd_rn(lsel, -lmax)) : 0.0f;
+        const float lmax = __shfl_sync(kFull, my_val, 0);  // slot 0 holds the largest logit
+        num = live ? expf(__fadd_rn(my_val, -lmax)) : 0.0f;
         if (a.renormalize) {
             den = warp_sum_fixed(num);
         } else {
             float part = 0.0f;
-            for (int id = lane; id < a.N; id += 32) part = __fadd_rn(part, expf(__fadd_rn(__ldcg(row + id), -lmax)));
+#pragma unroll
+            for (int j = 0; j < NPL; ++j)
+                if (lane + 32 * j < a.N) part = __fadd_rn(part, expf(__fadd_rn(val[j], -lmax)));
             den = warp_sum_fixed(part);
         }
     }

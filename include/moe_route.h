@@ -77,6 +77,22 @@ typedef enum mr_scoring {
     MR_SCORE_SIGMOID = 1         /* select by sigmoid + bias; weights = sigmoid */
 } mr_scoring;
 
+/* Launch options, process-wide (bits for mr_set_launch_flags). */
+#define MR_LAUNCH_PDL 1  /* programmatic dependent launch, see below */
+
+/*
+ * Sets the launch options of every later call in this process; returns
+ * MR_ERR_INVALID_ARG for unknown bits.  With MR_LAUNCH_PDL each kernel is
+ * launched with programmatic stream serialization: it may start while the
+ * kernel before it on the stream is still running, issues its loads of the
+ * gate weight w at once, and waits for that kernel to complete before it
+ * touches anything else (x, logits, ids, scratch, outputs).  The caller must
+ * then not write w in the kernel launched just before the routing call on
+ * the same stream.  Default: 0 (plain stream order).
+ */
+int mr_set_launch_flags(int flags);
+int mr_get_launch_flags(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mr_status_string(int status);
 
