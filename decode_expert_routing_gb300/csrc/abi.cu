@@ -6,6 +6,7 @@
 
 #include "../../include/moe_route.h"
 #include "internal.h"
+#include "route_plan.h"
 
 namespace {
 
@@ -84,8 +85,12 @@ const char* mr_status_string(int status) {
 int mr_abi_version(void) { return MR_ABI_VERSION; }
 
 int mr_router_gemv_supported(int M, int N, int K, int64_t ldx) {
+    if (ldx < K || ldx % 8 != 0 || K % MR_GEMV_K_MULTIPLE != 0) return 0;
+    if (M <= mr::kRouteMaxM) {
+        mr::RoutePlan rp;
+        return mr::route_plan(M, N, K, 1, 0, 16, &rp) ? 1 : 0;
+    }
     GemvPlan p;
-    if (ldx < K || ldx % 8 != 0) return 0;
     return mr::gemv_plan(M, N, K, &p) ? 1 : 0;
 }
 
@@ -102,7 +107,7 @@ size_t mr_scratch_bytes(int M_max, int N, int K, int topk) {
     if (M_max < 1 || N < 1 || K < 1 || topk < 1) return 0;
     size_t work = 0;
     const int Mg = M_max < MR_MAX_GEMV_ROWS ? M_max : MR_MAX_GEMV_ROWS;
-    for (int M = 1; M <= Mg; ++M) {
+    for (int M = mr::kRouteMaxM + 1; M <= Mg; ++M) {
         GemvPlan p;
         if (mr::gemv_plan(M, N, K, &p)) {
             const size_t b = mr::gemv_work_bytes(p, M, N);
@@ -122,13 +127,51 @@ int mr_scratch_reset(void* scratch, size_t scratch_bytes, void* stream) {
     return cuda_status(cudaMemsetAsync(scratch, 0, scratch_bytes, as_stream(stream)));
 }
 
+// Fills the cluster route arguments shared by the GEMV-only and full modes.
+static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t ldx, const void* w, int M,
+                                int N, int K, int mode) {
+    mr::RouteArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.ldx = ldx;
+    a.w = static_cast<const uint16_t*>(w);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.mode = mode;
+    a.cs = p.cs;
+    a.kc = p.kc;
+    a.spw = p.spw;
+    a.wpt = p.wpt;
+    a.units = p.units;
+    a.tok = p.tok;
+    a.gwarps = p.gwarps;
+    a.xpitch = p.xpitch;
+    a.off_x = p.off_x;
+    a.off_recv = p.off_recv;
+    a.off_row = p.off_row;
+    a.off_cand = p.off_cand;
+    a.off_ids = p.off_ids;
+    a.off_mask = p.off_mask;
+    a.off_start = p.off_start;
+    a.trace = static_cast<unsigned long long*>(mr::trace_buffer());
+    return a;
+}
+
 int mr_router_gemv(const void* x, int64_t ldx, const void* w, float* logits, int M, int N, int K,
                    void* scratch, size_t scratch_bytes, void* stream) {
     int s = check_x(x, ldx, M, K);
     if (s != MR_OK) return s;
-    if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) ||
-        scratch == nullptr || !aligned(scratch, 256) || N < 1)
+    if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) || N < 1)
         return MR_ERR_INVALID_ARG;
+    if (K % MR_GEMV_K_MULTIPLE != 0) return MR_ERR_UNSUPPORTED;
+    if (M <= mr::kRouteMaxM) {
+        mr::RoutePlan rp;
+        if (!mr::route_plan(M, N, K, 1, 0, mr::route_cluster_size(), &rp)) return MR_ERR_UNSUPPORTED;
+        mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 0);
+        a.logits = logits;
+        return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
+    }
+    if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;
     GemvPlan p;
     if (!mr::gemv_plan(M, N, K, &p)) return MR_ERR_UNSUPPORTED;
     if (scratch_bytes < mr::kWorkOffset + mr::gemv_work_bytes(p, M, N)) return MR_ERR_SCRATCH_TOO_SMALL;
@@ -180,28 +223,39 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
                             int32_t* sorted_token_ids, int32_t* expert_ids,
                             int32_t* num_tokens_post_padded, int64_t capacity, uint8_t* q,
                             uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
+    (void)scratch;
+    (void)scratch_bytes;
     int s = check_x(x, ldx, M, K);
     if (s != MR_OK) return s;
     if ((s = check_gate_args(M, N, topk, scoring)) != MR_OK) return s;
     if ((s = check_sort_args(M, topk, N, block, capacity)) != MR_OK) return s;
-    if (M > MR_MAX_FUSED_ROWS) return MR_ERR_UNSUPPORTED;
+    if (M > MR_MAX_FUSED_ROWS || K % MR_GEMV_K_MULTIPLE != 0) return MR_ERR_UNSUPPORTED;
     if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) ||
         topk_ids == nullptr || !aligned(topk_ids, 4) || topk_weights == nullptr ||
         !aligned(topk_weights, 4) || sorted_token_ids == nullptr || !aligned(sorted_token_ids, 4) ||
         expert_ids == nullptr || !aligned(expert_ids, 4) || num_tokens_post_padded == nullptr ||
-        !aligned(num_tokens_post_padded, 4) || scratch == nullptr || !aligned(scratch, 256) ||
-        (sel_bias && !aligned(sel_bias, 4)))
+        !aligned(num_tokens_post_padded, 4) || (sel_bias && !aligned(sel_bias, 4)))
         return MR_ERR_INVALID_ARG;
     if ((q == nullptr) != (scale == nullptr)) return MR_ERR_INVALID_ARG;
     if (q != nullptr && !aligned(q, 8)) return MR_ERR_INVALID_ARG;
-    GemvPlan p;
-    if (!mr::gemv_plan(M, N, K, &p)) return MR_ERR_UNSUPPORTED;
-    if (scratch_bytes < mr::kWorkOffset + mr::gemv_work_bytes(p, M, N)) return MR_ERR_SCRATCH_TOO_SMALL;
-    return cuda_status(mr::launch_fused(p, x, ldx, w, M, N, K, topk, scoring,
-                                        scoring == MR_SCORE_SIGMOID ? sel_bias : nullptr,
-                                        renormalize ? 1 : 0, block, logits, topk_ids, topk_weights,
-                                        sorted_token_ids, expert_ids, num_tokens_post_padded, capacity,
-                                        q, scale, scratch, as_stream(stream)));
+    mr::RoutePlan rp;
+    if (!mr::route_plan(M, N, K, topk, 1, mr::route_cluster_size(), &rp)) return MR_ERR_UNSUPPORTED;
+    mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 1);
+    a.bias = scoring == MR_SCORE_SIGMOID ? sel_bias : nullptr;
+    a.logits = logits;
+    a.ids = topk_ids;
+    a.weights = topk_weights;
+    a.sorted = sorted_token_ids;
+    a.expert_ids = expert_ids;
+    a.ntpp = num_tokens_post_padded;
+    a.capacity = capacity;
+    a.q = q;
+    a.scale = scale;
+    a.topk = topk;
+    a.block = block;
+    a.scoring = scoring;
+    a.renormalize = renormalize ? 1 : 0;
+    return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
 }
 
 }  // extern "C"

@@ -62,14 +62,14 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
 }
 
 // Optional per-CTA phase stamps (compile with -DMR_TRACE): thread 0 writes
-// %globaltimer (ns) to trace[(blockIdx.y * gridDim.x + blockIdx.x) * 8 + slot].
+// %globaltimer (ns) to trace[(blockIdx.y * gridDim.x + blockIdx.x) * 16 + slot].
 #ifdef MR_TRACE
 #define MR_TRACE_STAMP(trace, slot)                                                  \
     do {                                                                             \
         if (threadIdx.x == 0 && (trace) != nullptr) {                               \
             unsigned long long t_;                                                   \
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                   \
-            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 8 + (slot)] = t_;        \
+            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 16 + (slot)] = t_;       \
         }                                                                            \
     } while (0)
 #else

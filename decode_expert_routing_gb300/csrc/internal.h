@@ -49,12 +49,11 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
                         cudaStream_t st);
 cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale,
                          cudaStream_t st);
-cudaError_t launch_fused(const GemvPlan& p, const void* x, int64_t ldx, const void* w, int M,
-                         int N, int K, int topk, int scoring, const float* bias,
-                         int renormalize, int block, float* logits, int32_t* ids,
-                         float* weights, int32_t* sorted, int32_t* expert_ids, int32_t* ntpp,
-                         int64_t capacity, uint8_t* q, uint8_t* scale, void* scratch,
-                         cudaStream_t st);
+struct RoutePlan;
+struct RouteArgs;
+// Cluster route kernel (M <= 64): logits only (mode 0) or the whole route.
+int route_cluster_size();  // 16 when the device runs 16-CTA clusters, else 8
+cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStream_t st);
 
 // Launch options (MR_LAUNCH_* bits of mr_set_launch_flags).
 int launch_flags();

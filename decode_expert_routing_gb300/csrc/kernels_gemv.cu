@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(C::NTHR) router_gemv_kernel(GemvArgs a) {
 
 bool gemv_plan(int M, int N, int K, GemvPlan* p) {
     if (M < 1 || M > 512 || N < 8 || N > 1024 || K < 512 || K % 512 != 0) return false;
-    int cfg = M <= 8 ? MR_GEMV_CFG_M8 : M <= 16 ? MR_GEMV_CFG_M16 : M <= 32 ? MR_GEMV_CFG_M32 : MR_GEMV_CFG_M64;
+    int cfg = MR_GEMV_CFG_ROWS64;
     GemvPlan q{};
     q.cfg = cfg;
     switch (cfg) {

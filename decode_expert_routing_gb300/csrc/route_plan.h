@@ -1,0 +1,103 @@
+// Plan and arguments of the cluster route kernel (kernel_route.cu).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mr {
+
+constexpr int kRouteThreads = 512;        // 16 warps per CTA
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteBatch = 2;            // (tile, k-part) units whose loads a warp keeps in flight
+constexpr int kRouteSpwMax = 8;           // 32-wide k steps per unit, at most
+constexpr int kRouteSmemMax = 200 * 1024; // dynamic shared memory, at most
+constexpr int kRouteMaxM = 64;
+
+struct RouteArgs {
+    const uint16_t* x;
+    int64_t ldx;
+    const uint16_t* w;
+    const float* bias;
+    float* logits;
+    int32_t* ids;
+    float* weights;
+    int32_t* sorted;
+    int32_t* expert_ids;
+    int32_t* ntpp;
+    int64_t capacity;
+    uint8_t* q;
+    uint8_t* scale;
+    int M, N, K, topk, block, scoring, renormalize;
+    int mode;        // 0: logits only, 1: whole route
+    int cs;          // CTAs in the cluster
+    int kc;          // K per CTA
+    int spw;         // 32-wide k steps per unit
+    int wpt;         // k-parts per 8-expert tile
+    int units;       // (tile, part) units per CTA
+    int tok;         // token rows owned per CTA
+    int gwarps;      // gate warps per row (128-expert segments)
+    int xpitch;      // bytes per x row in shared memory
+    int off_x, off_recv, off_row, off_cand, off_ids, off_mask, off_start;
+    unsigned long long* trace;
+};
+
+struct RoutePlan {
+    int cs, kc, spw, wpt, units, tok, gwarps, xpitch, mt;
+    bool half;
+    int smem;
+    int off_x, off_recv, off_row, off_cand, off_ids, off_mask, off_start;
+};
+
+inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Returns false when (M, N, K, topk) is outside what the cluster kernel
+// covers with cluster size cs.
+inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePlan* p) {
+    if (M < 1 || M > kRouteMaxM || N < 8 || N > 1024 || N % 8 != 0) return false;
+    if (K < 32 * cs || K % (32 * cs) != 0) return false;
+    RoutePlan q{};
+    q.cs = cs;
+    q.kc = K / cs;
+    const int S = q.kc / 32, NT = N / 8;
+    int w = 0;
+    for (int d = 1; d <= S; ++d)
+        if (S % d == 0 && S / d <= kRouteSpwMax) {
+            w = d;
+            break;
+        }
+    if (w == 0) return false;
+    // more k-parts while the CTA has fewer units than warps
+    for (int d = w + 1; d <= S && NT * w < kRouteWarps; ++d)
+        if (S % d == 0) w = d;
+    q.wpt = w;
+    q.spw = S / w;
+    q.units = NT * w;
+    q.tok = (M + cs - 1) / cs;
+    q.gwarps = N <= 128 ? 1 : (N + 127) / 128;
+    if (mode == 1 && (topk < 1 || topk > 32 || topk > N || q.gwarps > 8 || q.tok * q.gwarps > kRouteWarps))
+        return false;
+    q.mt = M <= 16 ? 1 : M <= 32 ? 2 : 4;
+    q.half = M <= 8;
+    q.xpitch = q.kc * 2 + (((q.kc * 2) % 128 == 0) ? 64 : 0);
+    int off = 0;
+    q.off_x = off;
+    off = align_up(off + M * q.xpitch, 16);
+    q.off_recv = off;
+    off = align_up(off + cs * w * q.tok * N * 4, 16);
+    q.off_row = off;
+    off = align_up(off + q.tok * N * 4, 16);
+    q.off_cand = off;
+    off = align_up(off + q.tok * q.gwarps * 32 * 12, 16);
+    q.off_ids = off;
+    off = align_up(off + M * (mode == 1 ? topk : 0) * 4, 16);
+    q.off_mask = off;
+    off = align_up(off + (mode == 1 ? N : 0) * 8, 16);
+    q.off_start = off;
+    off = align_up(off + (mode == 1 ? N + 32 : 0) * 4, 16);
+    q.smem = off;
+    if (q.smem > kRouteSmemMax) return false;
+    *p = q;
+    return true;
+}
+
+}  // namespace mr

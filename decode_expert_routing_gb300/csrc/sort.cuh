@@ -118,13 +118,16 @@ struct SortArgs {
 // Whole sort by one CTA (n_assign <= 2048).  ids_src may be shared or global.
 // start needs N + ... ints; warp_tot 32 ints.
 __device__ __forceinline__ void cta_sort(const SortArgs& a, const int* ids_src, const RankSmem& s,
-                                         int* start, int* warp_tot) {
+                                         int* start, int* warp_tot,
+                                         unsigned long long* trace = nullptr) {
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int N = a.N, B = a.block;
     const int seg = cta_rank(ids_src, a.n_assign, N, s);
+    MR_TRACE_STAMP(trace, 7);
     for (int e = tid; e < N; e += nthr) start[e] = (s.cnt[e] + B - 1) / B * B;
     __syncthreads();
     const int total = block_exclusive_scan(start, N, warp_tot);
+    MR_TRACE_STAMP(trace, 8);
     const int sentinel = a.n_assign;
     for (int i = tid; i < a.n_assign; i += nthr) {
         const int e = ids_src[i];
@@ -132,6 +135,7 @@ __device__ __forceinline__ void cta_sort(const SortArgs& a, const int* ids_src, 
         const int w = i / seg;
         a.sorted[start[e] + s.wcnt[w * N + e] + s.lrank[i]] = i;
     }
+    MR_TRACE_STAMP(trace, 9);
     for (int e = tid; e < N; e += nthr) {
         const int st = start[e], c = s.cnt[e], p = (c + B - 1) / B * B;
         for (int i = c; i < p; ++i) a.sorted[st + i] = sentinel;

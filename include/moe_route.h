@@ -61,7 +61,7 @@ extern "C" {
 #define MR_MAX_EXPERTS 1024
 #define MR_MAX_TOPK 32
 #define MR_MAX_GEMV_ROWS 512
-#define MR_MAX_FUSED_ROWS 16
+#define MR_MAX_FUSED_ROWS 64
 #define MR_GEMV_K_MULTIPLE 512
 
 typedef enum mr_status {

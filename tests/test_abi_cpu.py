@@ -54,7 +54,8 @@ def test_shape_predicate(lib):
     assert ok(8, 896, 3584) and ok(32, 896, 3584)
     assert not ok(513, 128, 6144)          # M > 512
     assert not ok(1, 128, 6000)            # K % 512
-    assert not ok(1, 100, 6144)            # N % BLOCK_N
+    assert not ok(1, 100, 6144)            # N % 8
+    assert not ok(100, 100, 6144)          # N % BLOCK_N of the split-K GEMV
     assert not ok(1, 2048, 6144)           # N > 1024
     assert not ok(0, 128, 6144)
     assert not ok(1, 128, 6144, 6143)      # ldx < K
@@ -88,8 +89,9 @@ def test_validation_returns_before_any_launch(lib):
     assert lib.mr_router_gemv(P(0x1002), 6144, fake, fake, 1, 128, 6144, fake, 1 << 20, None) == mr.MR_ERR_INVALID_ARG
     # unsupported K
     assert lib.mr_router_gemv(fake, 6000, fake, fake, 1, 128, 6000, fake, 1 << 20, None) == mr.MR_ERR_UNSUPPORTED
-    # scratch too small
-    assert lib.mr_router_gemv(fake, 6144, fake, fake, 1, 128, 6144, fake, 100, None) == mr.MR_ERR_SCRATCH_TOO_SMALL
+    # scratch too small (the split-K GEMV of more than 64 rows needs scratch)
+    assert lib.mr_router_gemv(fake, 6144, fake, fake, 100, 128, 6144, fake, 100, None) == mr.MR_ERR_SCRATCH_TOO_SMALL
+    assert lib.mr_router_gemv(fake, 6144, fake, fake, 100, 128, 6144, None, 0, None) == mr.MR_ERR_INVALID_ARG
     # gate: topk > N, bad scoring, N too large
     assert lib.mr_route_topk(fake, 1, 8, 9, 0, None, 1, fake, fake, None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_route_topk(fake, 1, 128, 8, 7, None, 1, fake, fake, None) == mr.MR_ERR_INVALID_ARG
@@ -101,8 +103,8 @@ def test_validation_returns_before_any_launch(lib):
     assert lib.mr_moe_sort(fake, 4096, 8, 128, 64, fake, fake, fake, 40832, None, 0, None) == mr.MR_ERR_INVALID_ARG
     # quant: K % 32
     assert lib.mr_mxfp8_quant(fake, 48, 1, 40, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
-    # fused: M > 16
-    assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 17, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
+    # fused: M > 64
+    assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 65, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
                                        fake, fake, fake, 1 << 20, fake, fake, fake, 1 << 20, None) == mr.MR_ERR_UNSUPPORTED
     # fused: q without scale
     assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 1, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,

@@ -36,8 +36,8 @@ def _bits(t):
     return a.view(np.uint32) if a.dtype == np.float32 else a
 
 
-@pytest.mark.parametrize("cid,M", [(1, 1), (2, 2), (2, 4), (2, 8), (2, 16), (3, 1), (3, 8), (3, 16),
-                                   (2, 3), (2, 11)])
+@pytest.mark.parametrize("cid,M", [(1, 1), (2, 2), (2, 4), (2, 8), (2, 16), (2, 32), (2, 64), (3, 1),
+                                   (3, 8), (3, 16), (3, 32), (2, 3), (2, 11), (2, 17), (2, 47), (5, 64)])
 def test_fused_equals_chain_and_oracle(mr, cid, M):
     c = inputs.CONFIGS[cid]
     x, w = inputs.router_inputs(M, c["K"], c["N"], cid)
@@ -66,11 +66,13 @@ def test_fused_without_quant(mr):
     check_gate(host(out["logits"]), host(out["topk_ids"]), host(out["topk_weights"]), 8, "softmax")
 
 
-@pytest.mark.parametrize("M", [2, 4, 8, 16, 32, 64])
-def test_1000_launches_reuse_one_scratch(mr, M):
-    """Config 2: 1000 back-to-back launches on one scratch/counter buffer;
-    every launch's outputs land in a ring and each is checked against the
-    reference outputs of its input variant."""
+@pytest.mark.parametrize("M,chain", [(2, "fused"), (4, "fused"), (8, "fused"), (16, "fused"), (32, "fused"),
+                                     (64, "fused"), (32, "four calls"), (64, "four calls")])
+def test_1000_launches_reuse_one_scratch(mr, M, chain):
+    """Config 2: 1000 back-to-back launches on one scratch/counter buffer
+    (the one-launch route, and the four separate calls); every launch's
+    outputs land in a ring and each is checked against the reference outputs
+    of its input variant."""
     import torch
     c = inputs.CONFIGS[2]
     K, N, k, B = c["K"], c["N"], c["topk"], c["block"]
@@ -94,7 +96,7 @@ def test_1000_launches_reuse_one_scratch(mr, M):
     for i in range(L):
         v = i % nvar
         out = {key: t[i] for key, t in ring.items()}
-        if M <= 16:
+        if chain == "fused":
             mr.moe_route_sort_quant(xds[v], wds[v], k, B, out=out, scratch=scratch)
         else:
             mr.router_gemv(xds[v], wds[v], out=out["logits"], scratch=scratch)

@@ -54,6 +54,16 @@ def test_router_gemv_matches_oracle(mr, cid, M):
     assert int(scratch.counters().abs().sum()) == 0, "split-K counters not re-zeroed"
 
 
+@pytest.mark.parametrize("M", [65, 100, 129])
+def test_router_gemv_split_k_rows_past_64(mr, M):
+    """The split-K GEMV with last-arriver fixup (M > 64): ragged row tiles."""
+    x, w = inputs.router_inputs(M, 6144, 128, 7)
+    scratch = mr.Scratch(M, 128, 6144, 8)
+    g = mr.router_gemv(to_dev_bf16(x), to_dev_bf16(w), scratch=scratch)
+    assert_logits_close(host(g), oracle.router_gemv(x, w))
+    assert int(scratch.counters().abs().sum()) == 0
+
+
 def test_router_gemv_strided_x(mr):
     M, K, N = 5, 6144, 128
     x, w = inputs.router_inputs(M, K, N, 21)
