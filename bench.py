@@ -350,6 +350,7 @@ def run_ours(args):
         return 4
 
     launches_per_step = sum(1 if M <= FUSED_MAX_M else 4 for M in MS)
+    assert launches_per_step == len(MS), "the step is one route launch per M"
 
     # eager warm-up of every slot (first launches, attributes), then capture
     stream = torch.cuda.Stream(device=dev)
@@ -359,22 +360,13 @@ def run_ours(args):
                 call(M, xs[M][s], ws[M][s])
     stream.synchronize()
 
-    fused_ms = [M for M in MS if M <= FUSED_MAX_M]
     rt = CudaRT()
     sp = stream.cuda_stream
-    events = {}
     graphs = []
     for s in range(SLOTS):
         def body(s=s):
             for M in MS:
-                if M in fused_ms:
-                    ev = (rt.event(), rt.event())
-                    rt.record_node(ev[0], sp)
-                    call(M, xs[M][s], ws[M][s])
-                    rt.record_node(ev[1], sp)
-                    events[(s, M)] = ev
-                else:
-                    call(M, xs[M][s], ws[M][s])
+                call(M, xs[M][s], ws[M][s])
         with torch.cuda.stream(stream):
             graphs.append(rt.capture(sp, body))
 
@@ -420,21 +412,19 @@ def run_ours(args):
     total_bytes = STEP_BYTES * args.steps * world
     value = total_bytes / (ms_max * 1e-3) / 1e9
 
-    # dominant kernel: the fused route; durations from the events around its
-    # launches in the last replay of each slot graph (the final timed steps)
+    # dominant kernel: every launch of the step is the one-launch route
+    # kernel, so its average launch duration is the timed region divided by
+    # the launches in it (events on the launching stream, no extra nodes in
+    # the graphs that would serialise the launches)
     peak, peak_kind = load_peaks()
-    durs, nbytes = [], 0
-    for (s, M), (e0, e1) in events.items():
-        if s < min(SLOTS, args.steps):
-            durs.append(rt.elapsed_ms(e0, e1))
-            nbytes += algorithmic_bytes(M)
-    roofline = None
-    if durs:
-        achieved = nbytes / (sum(durs) * 1e-3) / 1e9
-        roofline = {"kernel": "mr::fused_route_kernel", "bound": "hbm", "achieved": round(achieved, 2),
-                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                    "traffic": committed_traffic(), "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
-                    "launches_sampled": len(durs), "avg_launch_us": round(sum(durs) / len(durs) * 1e3, 3)}
+    launches = launches_per_step * args.steps
+    avg_launch_us = ms_max * 1e3 / launches
+    achieved = STEP_BYTES / launches_per_step / (avg_launch_us * 1e-6) / 1e9
+    roofline = {"kernel": "mr::route_cluster_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": committed_traffic(),
+                "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "launches_timed": launches,
+                "avg_launch_us": round(avg_launch_us, 3),
+                "algorithmic_bytes_per_launch": round(STEP_BYTES / launches_per_step)}
 
     # per-M microseconds per call (graph of 64 calls on rotating slots)
     per_m = {}

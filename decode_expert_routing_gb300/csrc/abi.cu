@@ -149,6 +149,7 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.off_x = p.off_x;
     a.off_recv = p.off_recv;
     a.off_row = p.off_row;
+    a.off_key = p.off_key;
     a.off_cand = p.off_cand;
     a.off_ids = p.off_ids;
     a.off_mask = p.off_mask;

@@ -32,7 +32,6 @@
 #include "common.cuh"
 #include "internal.h"
 #include "route_plan.h"
-#include "sort.cuh"
 
 namespace mr {
 
@@ -68,74 +67,30 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
     return *reinterpret_cast<const uint4*>(p);
 }
 
-// Top-k of candidates held NPL per lane (key = order-preserving image, 0 =
-// absent; ids unique).  After the call lane r < k holds the r-th best
-// (id, val, key), ties to the lower id.
-template <int NPL>
-__device__ __forceinline__ void warp_select(unsigned (&key)[NPL], const int (&id)[NPL],
-                                            const float (&val)[NPL], int k, int* out_id,
-                                            float* out_val, unsigned* out_key) {
-    const int lane = threadIdx.x & 31;
-    unsigned best = 0u;
-    int bid = 0x7FFFFFFF;
-    float bval = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NPL; ++j)
-        if (key[j] > best || (key[j] == best && key[j] != 0u && id[j] < bid)) {
-            best = key[j];
-            bid = id[j];
-            bval = val[j];
-        }
-    int my_id = 0;
-    float my_val = 0.0f;
-    unsigned my_key = 0u;
-    for (int r = 0; r < k; ++r) {
-        const unsigned kmax = __reduce_max_sync(kFull, best);
-        const unsigned cand = (best == kmax && best != 0u) ? (unsigned)bid : 0xFFFFFFFFu;
-        const unsigned win = __reduce_min_sync(kFull, cand);
-        const bool mine = cand == win && best != 0u;
-        const int owner = __ffs(__ballot_sync(kFull, mine)) - 1;
-        const float wv = __shfl_sync(kFull, bval, owner < 0 ? 0 : owner);
-        if (lane == r) {
-            my_id = (int)win;
-            my_val = wv;
-            my_key = kmax;
-        }
-        if (mine) {
-            best = 0u;
-            bid = 0x7FFFFFFF;
-#pragma unroll
-            for (int j = 0; j < NPL; ++j) {
-                if ((unsigned)id[j] == win) key[j] = 0u;
-                if (key[j] > best || (key[j] == best && key[j] != 0u && id[j] < bid)) {
-                    best = key[j];
-                    bid = id[j];
-                    bval = val[j];
-                }
-            }
-        }
-    }
-    *out_id = my_id;
-    *out_val = my_val;
-    *out_key = my_key;
-}
-
-// Gate-weight fragments of batch b of this warp's (tile, part) units.
+// Gate-weight fragments of batch b of this warp's units.  A warp keeps one
+// k-part p = warp % wpt for all its units, so the x fragments it loads serve
+// every unit of a batch; unit i of the warp is tile (warp / wpt) + i * (16 / wpt).
 __device__ __forceinline__ void load_w_batch(const RouteArgs& a, int64_t kslice, int warp, int g, int t,
                                              int b, uint4 (&wv)[kRouteBatch][kRouteSpwMax]) {
+    const int p = warp % a.wpt, tiles_per_pass = kRouteWarps / a.wpt;
 #pragma unroll
     for (int uu = 0; uu < kRouteBatch; ++uu) {
-        const int u = warp + kRouteWarps * (b * kRouteBatch + uu);
-        const int j = u / a.wpt, p = u - j * a.wpt;
+        const int j = warp / a.wpt + tiles_per_pass * (b * kRouteBatch + uu);
+        const bool ok = j < a.N / 8;
         const uint16_t* wp = a.w + (int64_t)(j * 8 + g) * a.K + kslice + (int64_t)p * a.spw * 32 + 8 * t;
 #pragma unroll
         for (int s = 0; s < kRouteSpwMax; ++s)
-            wv[uu][s] = (u < a.units && s < a.spw) ? ld_stream_v4(wp + s * 32) : make_uint4(0u, 0u, 0u, 0u);
+            wv[uu][s] = (ok && s < a.spw) ? ld_stream_v4(wp + s * 32) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// Weights of the final selection (lane r < k holds slot r): identical
-// arithmetic to the standalone gate kernel.
+// Selection order as one 64-bit integer: larger key first, then lower id.
+__device__ __forceinline__ unsigned long long composite(unsigned key, int id) {
+    return ((unsigned long long)key << 32) | (unsigned)(0x7FFFFFFF - id);
+}
+
+// Weight of slot r = lane (lane < k holds (val) of slot r): the same
+// arithmetic as the standalone gate kernel.
 __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* row, float my_val) {
     const int lane = threadIdx.x & 31;
     const bool live = lane < a.topk;
@@ -164,17 +119,19 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int g = lane >> 2, t = lane & 3;
     const int c = (int)cluster_rank();
     MR_TRACE_STAMP(a.trace, 0);
-    cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM store
+    cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM access
     pdl_trigger();
 
-    const int N = a.N, M = a.M, spw = a.spw, wpt = a.wpt, U = a.units, tok = a.tok;
-    (void)spw;
+    const int N = a.N, M = a.M, wpt = a.wpt, tok = a.tok, K = a.K;
     const int64_t kslice = (int64_t)c * a.kc;
+    unsigned long long* mask = reinterpret_cast<unsigned long long*>(sm + a.off_mask);
 
     // ---- gate-weight loads of the first batch (the weight is never written
     //      by the preceding kernel, so they may precede the wait)
     uint4 wv[kRouteBatch][kRouteSpwMax];
     load_w_batch(a, kslice, warp, g, t, 0, wv);
+    if (a.mode == 1 && c == 0)
+        for (int e = tid; e < N; e += kRouteThreads) mask[e] = 0ull;  // token bitmasks (2 x 32 bits per expert)
     pdl_wait();
 
     // ---- x slice -> shared memory
@@ -188,55 +145,44 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     __syncthreads();
     MR_TRACE_STAMP(a.trace, 1);
 
-    // ---- MXFP8 of the x slice (one lane quad per 32-block)
-    if (a.q != nullptr) {
-        const int nvec = M * vpr;
-        const int64_t K32 = a.K / 32;
-        for (int base = warp * 32; base < nvec; base += kRouteThreads) {
-            const int v = base + lane;
-            const int r = v / vpr, cv = v - r * vpr;
-            const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
-            unsigned sb;
-            const uint2 q8 = mx_quant_quad(d, &sb);
-            if (v < nvec) {
-                const int64_t k = kslice + cv * 8;
-                *reinterpret_cast<uint2*>(a.q + (int64_t)r * a.K + k) = q8;
-                if ((cv & 3) == 0) a.scale[(int64_t)r * K32 + k / 32] = (uint8_t)sb;
-            }
-        }
-    }
-
-    // ---- MMA units; partial tiles straight to their owners' receive buffers
+    // ---- MMA: batches of units sharing one k-part; partial tiles go
+    //      straight to the receive buffers of the rows' owners
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
     const uint32_t recv_local = smem_u32(sm + a.off_recv);
-    const int nb = (U - warp + kRouteWarps * kRouteBatch - 1) / (kRouteWarps * kRouteBatch);
+    const int p = warp % wpt, tiles_per_pass = kRouteWarps / wpt, NT = N / 8;
+    const int my_tiles = warp / wpt < NT ? (NT - warp / wpt + tiles_per_pass - 1) / tiles_per_pass : 0;
+    const int nb = (my_tiles + kRouteBatch - 1) / kRouteBatch;
+    const int slot = c * wpt + p;
     for (int b = 0; b < nb; ++b) {
         if (b > 0) load_w_batch(a, kslice, warp, g, t, b, wv);
+        float acc[kRouteBatch][MT][4];
 #pragma unroll
-        for (int uu = 0; uu < kRouteBatch; ++uu) {
-            const int u = warp + kRouteWarps * (b * kRouteBatch + uu);
-            if (u >= U) break;
-            const int j = u / wpt, p = u - j * wpt;
-            float acc[MT][4];
+        for (int uu = 0; uu < kRouteBatch; ++uu)
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+            for (int mt = 0; mt < MT; ++mt) acc[uu][mt][0] = acc[uu][mt][1] = acc[uu][mt][2] = acc[uu][mt][3] = 0.0f;
 #pragma unroll
-            for (int s = 0; s < kRouteSpwMax; ++s) {
-                if (s < spw) {
-                    const int kk = (p * spw + s) * 32 + 8 * t;
+        for (int s = 0; s < kRouteSpwMax; ++s) {
+            if (s < a.spw) {
+                const int kk = (p * a.spw + s) * 32 + 8 * t;
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const int r0 = mt * 16 + g, r1 = r0 + 8;
-                        const uint4 xa = r0 < M ? lds128(xs + r0 * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
-                        const uint4 xb = (!HALF && r1 < M) ? lds128(xs + r1 * a.xpitch + kk * 2)
-                                                           : make_uint4(0u, 0u, 0u, 0u);
-                        mma_bf16_m16n8k16(acc[mt], xa.x, xb.x, xa.y, xb.y, wv[uu][s].x, wv[uu][s].y);
-                        mma_bf16_m16n8k16(acc[mt], xa.z, xb.z, xa.w, xb.w, wv[uu][s].z, wv[uu][s].w);
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int r0 = mt * 16 + g, r1 = r0 + 8;
+                    const uint4 xa = r0 < M ? lds128(xs + r0 * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 xb = (!HALF && r1 < M) ? lds128(xs + r1 * a.xpitch + kk * 2)
+                                                       : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int uu = 0; uu < kRouteBatch; ++uu) {
+                        mma_bf16_m16n8k16(acc[uu][mt], xa.x, xb.x, xa.y, xb.y, wv[uu][s].x, wv[uu][s].y);
+                        mma_bf16_m16n8k16(acc[uu][mt], xa.z, xb.z, xa.w, xb.w, wv[uu][s].z, wv[uu][s].w);
                     }
                 }
             }
+        }
+#pragma unroll
+        for (int uu = 0; uu < kRouteBatch; ++uu) {
+            const int j = warp / wpt + tiles_per_pass * (b * kRouteBatch + uu);
+            if (j >= NT) break;
             const int col = j * 8 + 2 * t;
-            const int slot = c * wpt + p;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -245,134 +191,208 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                     if (r < M) {
                         const int own = r / tok, rl = r - own * tok;
                         const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * N + col) * 4);
-                        st_cluster_f2(map_rank(la, (unsigned)own), acc[mt][2 * h], acc[mt][2 * h + 1]);
+                        st_cluster_f2(map_rank(la, (unsigned)own), acc[uu][mt][2 * h], acc[uu][mt][2 * h + 1]);
                     }
                 }
             }
         }
     }
-    cluster_sync_acq_rel();  // barrier 1: every partial has reached its owner
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // barrier 1
+    // ---- MXFP8 of the x slice while the other CTAs finish (one lane quad per 32-block)
+    if (a.q != nullptr) {
+        const int nvec = M * vpr;
+        const int64_t K32 = K / 32;
+        for (int base = warp * 32; base < nvec; base += kRouteThreads) {
+            const int v = base + lane;
+            const int r = v / vpr, cv = v - r * vpr;
+            const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
+            unsigned sb;
+            const uint2 q8 = mx_quant_quad(d, &sb);
+            if (v < nvec) {
+                const int64_t k = kslice + cv * 8;
+                *reinterpret_cast<uint2*>(a.q + (int64_t)r * K + k) = q8;
+                if ((cv & 3) == 0) a.scale[(int64_t)r * K32 + k / 32] = (uint8_t)sb;
+            }
+        }
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     MR_TRACE_STAMP(a.trace, 2);
 
-    // ---- owner: fixed-order split-K sum -> logits
+    // ---- owner: fixed-order split-K sum -> logits (kept in shared memory)
     const float* recv = reinterpret_cast<const float*>(sm + a.off_recv);
     float* rowbuf = reinterpret_cast<float*>(sm + a.off_row);
     const int nslots = a.cs * wpt;
     const int my_rows = max(0, min(tok, M - c * tok));
     for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
-        const int rl = idx / N, n = idx - rl * N;
-        const float* p = recv + (int64_t)rl * N + n;
-        float s = 0.0f;
-        for (int sl = 0; sl < nslots; ++sl) s = __fadd_rn(s, p[(int64_t)sl * tok * N]);
-        rowbuf[idx] = s;
-        a.logits[(int64_t)(c * tok + rl) * N + n] = s;
+        const float* pp = recv + idx;
+        float sum = 0.0f;
+        for (int sl = 0; sl < nslots; ++sl) sum = __fadd_rn(sum, pp[(int64_t)sl * tok * N]);
+        rowbuf[idx] = sum;
     }
-    if (a.mode == 0) return;  // GEMV only: nothing else reads this CTA's memory
+    if (a.mode == 0) {
+        for (int idx = tid; idx < my_rows * N; idx += kRouteThreads)
+            a.logits[(int64_t)c * tok * N + idx] = rowbuf[idx];
+        return;  // nothing else reads this CTA's shared memory
+    }
     __syncthreads();
     MR_TRACE_STAMP(a.trace, 3);
 
-    // ---- gate: warp (row rl, segment sg) selects within experts [128 sg, 128 sg + 128)
-    const int G = a.gwarps;
-    unsigned* ckey = reinterpret_cast<unsigned*>(sm + a.off_cand);
-    int* cid = reinterpret_cast<int*>(ckey + tok * G * 32);
-    float* cval = reinterpret_cast<float*>(cid + tok * G * 32);
-    const uint32_t ids_all_local = smem_u32(sm + a.off_ids);
-    {
-        const int rl = warp / G, sg = warp - rl * G;
-        if (rl < my_rows) {
-            const float* row = rowbuf + rl * N;
-            unsigned key[4];
-            int id[4];
-            float val[4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int e = sg * 128 + lane + 32 * jj;
-                id[jj] = e;
-                val[jj] = e < N ? row[e] : 0.0f;
-                float sel = val[jj];
-                if (a.scoring == 1 && e < N)
-                    sel = __fadd_rn(sigmoid_score(val[jj]), a.bias ? __ldg(a.bias + e) : 0.0f);
-                key[jj] = e < N ? ordered_key(sel) : 0u;
-            }
-            const int seg_len = max(0, min(128, N - sg * 128));
-            const int kk = min(a.topk, seg_len);
-            int my_id;
-            float my_val;
-            unsigned my_key;
-            warp_select<4>(key, id, val, kk, &my_id, &my_val, &my_key);
+    // ---- gate by ranks: a key's rank is the number of keys that beat it.
+    //      Stage 1 ranks inside 128-expert segments; the k best of every
+    //      segment become candidates; stage 2 ranks the candidates.
+    const int k = a.topk, G = a.gwarps, GK = G * k;
+    unsigned long long* ccomp = reinterpret_cast<unsigned long long*>(sm + a.off_cand);
+    float* cval = reinterpret_cast<float*>(ccomp + tok * GK);
+    int* oid = reinterpret_cast<int*>(cval + tok * GK);
+    float* oval = reinterpret_cast<float*>(oid + tok * k);
+    unsigned long long* comp = reinterpret_cast<unsigned long long*>(sm + a.off_key);
+    for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
+        const int n = idx % N;
+        float sel = rowbuf[idx];
+        if (a.scoring == 1) sel = __fadd_rn(sigmoid_score(sel), a.bias ? __ldg(a.bias + n) : 0.0f);
+        comp[idx] = composite(ordered_key(sel), n);
+    }
+    for (int idx = tid; idx < my_rows * GK; idx += kRouteThreads) ccomp[idx] = 0ull;  // segments shorter than k
+    __syncthreads();
+    MR_TRACE_STAMP(a.trace, 6);
+    // TPK adjacent lanes share a key's count; part p reads the 16-byte pairs
+    // p, p + TPK, p + 2 TPK, ... of the segment, so the lanes of one key hit
+    // consecutive banks and lanes of different keys read the same addresses
+    int tpk = 1;
+    while (tpk < 8 && 2 * tpk * my_rows * N <= kRouteThreads) tpk *= 2;
+    for (int base = warp * 32; base < my_rows * N * tpk; base += kRouteThreads) {
+        const int item = base + lane;
+        const bool on = item < my_rows * N * tpk;
+        const int key_idx = item / tpk, part = item - key_idx * tpk;
+        const int rl = key_idx / N, n = key_idx - rl * N, sg = n >> 7;
+        const unsigned long long* cr = comp + rl * N;
+        const unsigned long long cn = on ? cr[n] : ~0ull;
+        const int lo = sg << 7, hi = on ? min(N, lo + 128) : lo;
+        int rank = 0;
+        for (int j = lo + 2 * part; j < hi; j += 2 * tpk) {
+            const ulonglong2 q2 = *reinterpret_cast<const ulonglong2*>(cr + j);  // N % 8 == 0: aligned, in range
+            rank += (int)(q2.x > cn) + (int)(q2.y > cn);
+        }
+        for (int o = 1; o < tpk; o <<= 1) rank += __shfl_xor_sync(kFull, rank, o);
+        if (on && part == 0 && rank < k) {
             if (G == 1) {
-                const float wgt = gate_weight(a, row, my_val);
-                if (lane < a.topk) {
-                    const int m = c * tok + rl;
-                    a.ids[(int64_t)m * a.topk + lane] = my_id;
-                    a.weights[(int64_t)m * a.topk + lane] = wgt;
-                    st_cluster_s32(map_rank(ids_all_local + (uint32_t)((m * a.topk + lane) * 4), 0u), my_id);
-                }
+                oid[rl * k + rank] = n;
+                oval[rl * k + rank] = rowbuf[key_idx];
             } else {
-                const int o = (rl * G + sg) * 32 + lane;
-                ckey[o] = lane < kk ? my_key : 0u;
-                cid[o] = lane < kk ? my_id : 0x7FFFFFFF - lane;
-                cval[o] = my_val;
+                const int o = rl * GK + sg * k + rank;
+                ccomp[o] = cn;
+                cval[o] = rowbuf[key_idx];
             }
         }
     }
+    __syncthreads();
+    MR_TRACE_STAMP(a.trace, 7);
     if (G > 1) {
-        __syncthreads();
-        const int rl = warp;  // one merging warp per row
-        if (rl < my_rows) {
-            unsigned key[8];
-            int id[8];
-            float val[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const int sg = jj, o = (rl * G + sg) * 32 + lane;
-                const bool ok = sg < G;
-                key[jj] = ok ? ckey[o] : 0u;
-                id[jj] = ok ? cid[o] : 0x7FFFFFFF - 32 * jj - lane;
-                val[jj] = ok ? cval[o] : 0.0f;
-            }
-            int my_id;
-            float my_val;
-            unsigned my_key;
-            warp_select<8>(key, id, val, a.topk, &my_id, &my_val, &my_key);
-            const float wgt = gate_weight(a, rowbuf + rl * N, my_val);
-            if (lane < a.topk) {
-                const int m = c * tok + rl;
-                a.ids[(int64_t)m * a.topk + lane] = my_id;
-                a.weights[(int64_t)m * a.topk + lane] = wgt;
-                st_cluster_s32(map_rank(ids_all_local + (uint32_t)((m * a.topk + lane) * 4), 0u), my_id);
+        for (int idx = tid; idx < my_rows * GK; idx += kRouteThreads) {
+            const int rl = idx / GK;
+            const unsigned long long cn = ccomp[idx];
+            if (cn == 0ull) continue;
+            const unsigned long long* cr = ccomp + rl * GK;
+            int rank = 0;
+            for (int j = 0; j < GK; ++j) rank += (int)(cr[j] > cn);
+            if (rank < k) {
+                oid[rl * k + rank] = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
+                oval[rl * k + rank] = cval[idx];
             }
         }
+        __syncthreads();
     }
-    cluster_sync_acq_rel();  // barrier 2: CTA 0 holds every token's ids
+    MR_TRACE_STAMP(a.trace, 8);
+    // ---- weights; ids to CTA 0
+    const uint32_t ids_all_local = smem_u32(sm + a.off_ids);
+    int out_id = 0;
+    float out_w = 0.0f;
+    if (warp < my_rows) {
+        const int rl = warp, m = c * tok + rl;
+        const bool live = lane < k;
+        const int id = live ? oid[rl * k + lane] : 0;
+        const float val = live ? oval[rl * k + lane] : 0.0f;
+        out_w = gate_weight(a, rowbuf + rl * N, val);
+        out_id = id;
+        if (live) st_cluster_s32(map_rank(ids_all_local + (uint32_t)((m * k + lane) * 4), 0u), id);
+    }
+    MR_TRACE_STAMP(a.trace, 9);
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // barrier 2
+    MR_TRACE_STAMP(a.trace, 10);
+    // global outputs of this CTA's rows while CTA 0 waits for the others
+    for (int idx = tid; idx < my_rows * N; idx += kRouteThreads)
+        a.logits[(int64_t)c * tok * N + idx] = rowbuf[idx];
+    if (warp < my_rows && lane < k) {
+        const int m = c * tok + warp;
+        a.ids[(int64_t)m * k + lane] = out_id;
+        a.weights[(int64_t)m * k + lane] = out_w;
+    }
+    MR_TRACE_STAMP(a.trace, 11);
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     MR_TRACE_STAMP(a.trace, 4);
     if (c != 0) return;
 
-    // ---- sort (CTA 0): token bitmask per expert
+    // ---- sort (CTA 0): rank of (m, j) inside expert e = number of set bits
+    //      below m in the token mask of e (two 32-bit words: tokens 0-31, 32-63)
     const int* ids_all = reinterpret_cast<const int*>(sm + a.off_ids);
-    unsigned long long* mask = reinterpret_cast<unsigned long long*>(sm + a.off_mask);
     int* start = reinterpret_cast<int*>(sm + a.off_start);
     int* warp_tot = start + N;
-    const int MK = M * a.topk, B = a.block;
-    for (int e = tid; e < N; e += kRouteThreads) mask[e] = 0ull;
-    __syncthreads();
-    for (int f = tid; f < MK; f += kRouteThreads) atomicOr(&mask[ids_all[f]], 1ull << (f / a.topk));
-    __syncthreads();
-    for (int e = tid; e < N; e += kRouteThreads) start[e] = (__popcll(mask[e]) + B - 1) / B * B;
-    __syncthreads();
-    const int total = block_exclusive_scan(start, N, warp_tot);
+    const int MK = M * k, B = a.block;
+    unsigned* mlo = reinterpret_cast<unsigned*>(mask);
+    unsigned* mhi = mlo + N;
     for (int f = tid; f < MK; f += kRouteThreads) {
-        const int e = ids_all[f], m = f / a.topk;
-        const int rank = __popcll(mask[e] & ((1ull << m) - 1ull));
-        a.sorted[start[e] + rank] = f;
+        const int m = f / k;
+        atomicOr(m < 32 ? &mlo[ids_all[f]] : &mhi[ids_all[f]], 1u << (m & 31));
     }
-    for (int e = tid; e < N; e += kRouteThreads) {
-        const int st = start[e], cnt = __popcll(mask[e]), pad = (cnt + B - 1) / B * B;
-        for (int i = cnt; i < pad; ++i) a.sorted[st + i] = MK;
-        for (int b = st / B; b < (st + pad) / B; ++b) a.expert_ids[b] = e;
+    __syncthreads();
+    MR_TRACE_STAMP(a.trace, 12);
+    // exclusive scan of the padded counts, two experts per thread, one barrier
+    const int e0 = 2 * tid, e1 = e0 + 1;
+    const int c0 = e0 < N ? __popc(mlo[e0]) + __popc(mhi[e0]) : 0;
+    const int c1 = e1 < N ? __popc(mlo[e1]) + __popc(mhi[e1]) : 0;
+    const int v0 = (c0 + B - 1) / B * B, v1 = (c1 + B - 1) / B * B;
+    const int local = v0 + v1;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += u;
     }
-    for (int64_t i = total + tid; i < a.capacity; i += kRouteThreads) a.sorted[i] = MK;
-    for (int64_t b = total / B + tid; b < a.capacity / B; b += kRouteThreads) a.expert_ids[b] = -1;
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kRouteWarps; ++w2) {
+        const int wt = warp_tot[w2];
+        before += w2 < warp ? wt : 0;
+        total += wt;
+    }
+    const int s0 = before + incl - local;
+    if (e0 < N) start[e0] = s0;
+    if (e1 < N) start[e1] = s0 + v0;
+    // sentinels everywhere (coalesced 16-byte stores), expert ids of every block
+    if ((reinterpret_cast<uintptr_t>(a.sorted) & 15u) == 0) {
+        int4* st4 = reinterpret_cast<int4*>(a.sorted);
+        const int64_t n4 = a.capacity / 4;
+        for (int64_t i = tid; i < n4; i += kRouteThreads) st4[i] = make_int4(MK, MK, MK, MK);
+        for (int64_t i = n4 * 4 + tid; i < a.capacity; i += kRouteThreads) a.sorted[i] = MK;
+    } else {
+        for (int64_t i = tid; i < a.capacity; i += kRouteThreads) a.sorted[i] = MK;
+    }
+    if (e0 < N)
+        for (int bb = s0 / B; bb < (s0 + v0) / B; ++bb) a.expert_ids[bb] = e0;
+    if (e1 < N)
+        for (int bb = (s0 + v0) / B; bb < (s0 + v0 + v1) / B; ++bb) a.expert_ids[bb] = e1;
+    for (int64_t bb = total / B + tid; bb < a.capacity / B; bb += kRouteThreads) a.expert_ids[bb] = -1;
+    __syncthreads();  // orders the sentinel stores before the real entries below
+    MR_TRACE_STAMP(a.trace, 13);
+    for (int f = tid; f < MK; f += kRouteThreads) {
+        const int e = ids_all[f], m = f / k;
+        const unsigned below = m < 32 ? __popc(mlo[e] & ((1u << m) - 1u))
+                                      : __popc(mlo[e]) + __popc(mhi[e] & ((1u << (m - 32)) - 1u));
+        a.sorted[start[e] + (int)below] = f;
+    }
+    MR_TRACE_STAMP(a.trace, 14);
     if (tid == 0) *a.ntpp = total;
     MR_TRACE_STAMP(a.trace, 5);
 }

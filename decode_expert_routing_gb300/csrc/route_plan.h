@@ -37,7 +37,7 @@ struct RouteArgs {
     int tok;         // token rows owned per CTA
     int gwarps;      // gate warps per row (128-expert segments)
     int xpitch;      // bytes per x row in shared memory
-    int off_x, off_recv, off_row, off_cand, off_ids, off_mask, off_start;
+    int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
     unsigned long long* trace;
 };
 
@@ -45,7 +45,7 @@ struct RoutePlan {
     int cs, kc, spw, wpt, units, tok, gwarps, xpitch, mt;
     bool half;
     int smem;
-    int off_x, off_recv, off_row, off_cand, off_ids, off_mask, off_start;
+    int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
 };
 
 inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -59,23 +59,23 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.cs = cs;
     q.kc = K / cs;
     const int S = q.kc / 32, NT = N / 8;
+    // k-parts per tile: a power of two (a warp keeps one part for all its
+    // tiles) dividing S with at most kRouteSpwMax steps per part; more parts
+    // while the CTA has fewer tiles than warps
     int w = 0;
-    for (int d = 1; d <= S; ++d)
+    for (int d = 1; d <= kRouteWarps && d <= S; d *= 2)
         if (S % d == 0 && S / d <= kRouteSpwMax) {
             w = d;
             break;
         }
     if (w == 0) return false;
-    // more k-parts while the CTA has fewer units than warps
-    for (int d = w + 1; d <= S && NT * w < kRouteWarps; ++d)
-        if (S % d == 0) w = d;
+    while (NT * w < kRouteWarps && 2 * w <= kRouteWarps && S % (2 * w) == 0) w *= 2;
     q.wpt = w;
     q.spw = S / w;
     q.units = NT * w;
     q.tok = (M + cs - 1) / cs;
-    q.gwarps = N <= 128 ? 1 : (N + 127) / 128;
-    if (mode == 1 && (topk < 1 || topk > 32 || topk > N || q.gwarps > 8 || q.tok * q.gwarps > kRouteWarps))
-        return false;
+    q.gwarps = (N + 127) / 128;  // 128-expert segments of the gate
+    if (mode == 1 && (topk < 1 || topk > 32 || topk > N || q.tok > kRouteWarps)) return false;
     q.mt = M <= 16 ? 1 : M <= 32 ? 2 : 4;
     q.half = M <= 8;
     q.xpitch = q.kc * 2 + (((q.kc * 2) % 128 == 0) ? 64 : 0);
@@ -86,8 +86,10 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     off = align_up(off + cs * w * q.tok * N * 4, 16);
     q.off_row = off;
     off = align_up(off + q.tok * N * 4, 16);
-    q.off_cand = off;
-    off = align_up(off + q.tok * q.gwarps * 32 * 12, 16);
+    q.off_key = off;  // 64-bit selection composites
+    off = align_up(off + (mode == 1 ? q.tok * N : 0) * 8, 16);
+    q.off_cand = off;  // per row: G*k composites, G*k values, k ids, k values
+    off = align_up(off + (mode == 1 ? q.tok * (q.gwarps * topk * 12 + topk * 8) : 0), 16);
     q.off_ids = off;
     off = align_up(off + M * (mode == 1 ? topk : 0) * 4, 16);
     q.off_mask = off;
