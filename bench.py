@@ -77,7 +77,7 @@ def committed_traffic():
     """dram bytes per launch of the fused kernel from the committed ncu
     summary, if it was taken on the current kernel sources (else None)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "fused_route_decode.md")
+    path = os.path.join(ROOT, "profiles", "route_cluster_kernel_decode_buckets.md")
     if not os.path.exists(path):
         return None
     h = hashlib.sha256()
