@@ -19,7 +19,7 @@ import os
 __all__ = [
     "MoeRouteError", "MoeRouteUnsupported", "Scratch", "library_path", "load_library",
     "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
-    "moe_sort", "mxfp8_quant", "moe_route_sort_quant",
+    "moe_sort", "mxfp8_quant", "moe_route_sort_quant", "router_gemv_noalloc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -65,6 +65,7 @@ SIGNATURES = {
     "mr_mxfp8_quant": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
     "mr_moe_route_sort_quant": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P,
                                      _P, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
+    "mr_router_gemv_noalloc": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P]),
 }
 
 
@@ -196,6 +197,26 @@ def router_gemv(x, w, out=None, scratch: Scratch | None = None, stream=None):
     _check(_load().mr_router_gemv(_dev_ptr(x, "x", torch.bfloat16), ldx, _dev_ptr(w, "w", torch.bfloat16),
                                   _dev_ptr(out, "out", torch.float32), M, N, K, scratch.ptr,
                                   scratch.nbytes, _stream_ptr(stream)), "mr_router_gemv")
+    return out
+
+
+def router_gemv_noalloc(x, w, out=None, stream=None):
+    """Router GEMV using the library's own fixed-size device scratch (no
+    scratch argument, nothing allocated by the library).  For callers that
+    cannot allocate; calls on one device share that scratch, so overlapping
+    calls race.  The first call per device does a one-time set-up."""
+    torch = _torch()
+    ldx = _row_major_2d(x, "x")
+    M, K = x.shape
+    N = w.shape[0]
+    if not w.is_contiguous() or w.shape[1] != K:
+        raise ValueError("w must be contiguous [N, K]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(_load().mr_router_gemv_noalloc(_dev_ptr(x, "x", torch.bfloat16), ldx,
+                                          _dev_ptr(w, "w", torch.bfloat16),
+                                          _dev_ptr(out, "out", torch.float32), M, N, K,
+                                          _stream_ptr(stream)), "mr_router_gemv_noalloc")
     return out
 
 

@@ -216,6 +216,37 @@ int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
                             uint8_t *q, uint8_t *scale,
                             void *scratch, size_t scratch_bytes, void *stream);
 
+/* Bytes of the library-owned scratch of mr_router_gemv_noalloc (8 MiB). */
+#define MR_NOALLOC_SCRATCH_BYTES 8388608
+
+/*
+ * Router GEMV that allocates nothing and takes no scratch argument.  The
+ * pages have no counterpart: this entry point exists for callers that cannot
+ * call cudaMalloc or cannot hand this library a scratch buffer -- plugins
+ * whose host framework owns all device memory and exposes no allocator to
+ * them, or code paths that must not enter the driver's allocator (it can
+ * synchronise the device and can fail once memory is fragmented).
+ * Same arithmetic as mr_router_gemv's split-K kernel with the last-arriver
+ * fixup (for every M here, including M <= 64, where mr_router_gemv runs its
+ * cluster kernel instead, so the two agree within fp32 rounding, not bit
+ * for bit).  The scratch is MR_NOALLOC_SCRATCH_BYTES of device memory that
+ * this library declares at file scope; every GPU that loads the library
+ * holds it until the process exits.
+ *  - The FIRST call on each device does the set-up (looks up the array's
+ *    device address and zeroes its counters, synchronously on that device);
+ *    make that first call before any stream capture.
+ *  - Every call on a device shares the one array, and the array keeps the
+ *    last call's contents: calls that can overlap on the GPU (different
+ *    streams, concurrent threads) race and corrupt each other's results.
+ *    Issue them on one stream, or serialise them.
+ *  - Problems whose split-K partials do not fit (32 KiB counters plus
+ *    SPLIT_K*M*N*4 bytes; e.g. M = 512, N = 128, K = 6144 fits) return
+ *    MR_ERR_UNSUPPORTED without launching; so do shapes outside
+ *    mr_router_gemv's cover.  Arguments as mr_router_gemv.
+ */
+int mr_router_gemv_noalloc(const void *x, int64_t ldx, const void *w, float *logits,
+                           int M, int N, int K, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
