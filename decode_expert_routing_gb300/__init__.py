@@ -301,7 +301,7 @@ def alloc_route_outputs(M: int, N: int, K: int, topk: int, block: int, device, q
 def moe_route_sort_quant(x, w, topk: int, block: int, scoring: str = "softmax", bias=None,
                          renormalize: bool = True, quant: bool = True, out=None,
                          scratch: Scratch | None = None, stream=None):
-    """The whole path for M <= 16 tokens in one launch; returns a dict of outputs."""
+    """The whole path for M <= 64 tokens in one launch; returns a dict of outputs."""
     torch = _torch()
     ldx = _row_major_2d(x, "x")
     M, K = x.shape

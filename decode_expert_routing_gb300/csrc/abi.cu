@@ -63,7 +63,7 @@ int mr_set_launch_flags(int flags) {
 int mr_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
 
 #ifdef MR_TRACE
-// Tracing builds only: device buffer of gridDim * 8 u64 stamps for the next
+// Tracing builds only: device buffer of gridDim * 32 u64 stamps for the next
 // launches (nullptr stops tracing).
 int mr_trace_set_buffer(void* device_buffer) {
     g_trace.store(device_buffer, std::memory_order_relaxed);
@@ -114,6 +114,11 @@ size_t mr_scratch_bytes(int M_max, int N, int K, int topk) {
             if (b > work) work = b;
         }
     }
+    if (M_max > mr::kRouteRowsPerCluster) {  // fused route over several clusters: every token's ids
+        const int Mf = M_max < mr::kRouteMaxM ? M_max : mr::kRouteMaxM;
+        const size_t b = (size_t)Mf * topk * 4;
+        if (b > work) work = b;
+    }
     const int64_t n_assign = (int64_t)M_max * topk;
     if (n_assign > mr::kSortChunk && n_assign < ((int64_t)1 << 30)) {
         const size_t b = mr::sort_work_bytes((int)n_assign, N);
@@ -139,6 +144,8 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.K = K;
     a.mode = mode;
     a.cs = p.cs;
+    a.cs_shift = mr::ilog2_exact(p.cs);
+    a.clusters = p.clusters;
     a.kc = p.kc;
     a.spw = p.spw;
     a.wpt = p.wpt;
@@ -154,6 +161,10 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.off_ids = p.off_ids;
     a.off_mask = p.off_mask;
     a.off_start = p.off_start;
+    a.tok_shift = mr::ilog2_exact(p.tok);
+    a.wpt_shift = mr::ilog2_exact(p.wpt);
+    a.mag_n = mr::div_magic(N);
+    a.mag_vpr = mr::div_magic(p.kc / 8);
     a.trace = static_cast<unsigned long long*>(mr::trace_buffer());
     return a;
 }
@@ -224,8 +235,6 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
                             int32_t* sorted_token_ids, int32_t* expert_ids,
                             int32_t* num_tokens_post_padded, int64_t capacity, uint8_t* q,
                             uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
-    (void)scratch;
-    (void)scratch_bytes;
     int s = check_x(x, ldx, M, K);
     if (s != MR_OK) return s;
     if ((s = check_gate_args(M, N, topk, scoring)) != MR_OK) return s;
@@ -242,6 +251,12 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
     mr::RoutePlan rp;
     if (!mr::route_plan(M, N, K, topk, 1, mr::route_cluster_size(), &rp)) return MR_ERR_UNSUPPORTED;
     mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 1);
+    if (rp.clusters > 1) {  // the clusters meet in scratch: a ticket and every token's ids
+        if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;
+        if (scratch_bytes < mr::kWorkOffset + (size_t)M * topk * 4) return MR_ERR_SCRATCH_TOO_SMALL;
+        a.counter = static_cast<unsigned*>(scratch) + mr::kFusedCounterSlot;
+        a.ids_scratch = reinterpret_cast<int32_t*>(static_cast<char*>(scratch) + mr::kWorkOffset);
+    }
     a.bias = scoring == MR_SCORE_SIGMOID ? sel_bias : nullptr;
     a.logits = logits;
     a.ids = topk_ids;
@@ -254,6 +269,9 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
     a.scale = scale;
     a.topk = topk;
     a.block = block;
+    a.mag_k = mr::div_magic(topk);
+    a.mag_block = mr::div_magic(block);
+    a.mag_gk = mr::div_magic(rp.gwarps * topk);
     a.scoring = scoring;
     a.renormalize = renormalize ? 1 : 0;
     return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));

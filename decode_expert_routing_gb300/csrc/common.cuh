@@ -25,11 +25,12 @@ __device__ __forceinline__ uint4 ld_ro_v4(const void* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.
+// D += A * B for one m16n8k16 bf16 tile with fp32 accumulation (no side
+// effects beyond its outputs, so the compiler may interleave independent ones).
 __device__ __forceinline__ void mma_bf16_m16n8k16(float (&c)[4], uint32_t a0, uint32_t a1,
                                                   uint32_t a2, uint32_t a3, uint32_t b0,
                                                   uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -62,14 +63,14 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
 }
 
 // Optional per-CTA phase stamps (compile with -DMR_TRACE): thread 0 writes
-// %globaltimer (ns) to trace[(blockIdx.y * gridDim.x + blockIdx.x) * 16 + slot].
+// %globaltimer (ns) to trace[(blockIdx.y * gridDim.x + blockIdx.x) * 32 + slot].
 #ifdef MR_TRACE
 #define MR_TRACE_STAMP(trace, slot)                                                  \
     do {                                                                             \
         if (threadIdx.x == 0 && (trace) != nullptr) {                               \
             unsigned long long t_;                                                   \
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                   \
-            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 16 + (slot)] = t_;       \
+            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 32 + (slot)] = t_;       \
         }                                                                            \
     } while (0)
 #else

@@ -12,7 +12,7 @@ namespace mr {
 // Counter slots inside the scratch prefix (MR_SCRATCH_COUNTER_BYTES = 32 KiB).
 constexpr int kCounterSlots = 8192;
 constexpr int kGemvCounterSlots = 4096;   // [row_tile * nblocks + nblk]
-constexpr int kFusedCounterSlot = 4096;   // fused route: completed n-blocks
+constexpr int kFusedCounterSlot = 4096;   // fused route, several clusters: clusters done
 constexpr int kSortCounterSlot = 4097;    // multi-CTA sort: completed chunks
 constexpr size_t kWorkOffset = 32768;     // work area (partials or sort tables)
 

@@ -1,5 +1,5 @@
-// The decode route as one thread-block cluster: router GEMV, split-K
-// reduction, top-k gate, sort and MXFP8 quant in ONE launch for M <= 64.
+// The decode route in ONE launch for M <= 64: router GEMV, split-K
+// reduction, top-k gate, sort and MXFP8 quant.
 //
 // The pages' one-launch decode router (sglang #46691 Summary: a router for
 // 1-16 tokens bitwise equal to router GEMV, gate and sort; sort + stage-1
@@ -24,6 +24,9 @@
 //      k ids of a token are distinct, the stable rank of (m, j) inside expert
 //      e is popc(mask_e & ((1 << m) - 1)) where mask_e is the bitmask of the
 //      tokens that chose e.
+//   More than 16 tokens: one cluster per 16 tokens, each running steps 1-3 on
+//   its rows; the CTA 0s publish their ids and take a last-arriver ticket
+//   (the pages' hand-off), and the last one sorts every assignment.
 //
 // No spin-waits: all waits are hardware cluster/CTA barriers.  Nothing is
 // left in scratch, so no counter needs re-zeroing.  The GEMV alone (mode 0)
@@ -66,17 +69,21 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
 __device__ __forceinline__ uint4 lds128(const void* p) {
     return *reinterpret_cast<const uint4*>(p);
 }
+// x / d for 0 <= x < 2^21 with mag = ceil(2^32 / d) (host-computed)
+__device__ __forceinline__ int fdiv(int x, unsigned long long mag) {
+    return (int)(((unsigned long long)(unsigned)x * mag) >> 32);
+}
 
 // Gate-weight fragments of batch b of this warp's units.  A warp keeps one
 // k-part p = warp % wpt for all its units, so the x fragments it loads serve
 // every unit of a batch; unit i of the warp is tile (warp / wpt) + i * (16 / wpt).
 __device__ __forceinline__ void load_w_batch(const RouteArgs& a, int64_t kslice, int warp, int g, int t,
                                              int b, uint4 (&wv)[kRouteBatch][kRouteSpwMax]) {
-    const int p = warp % a.wpt, tiles_per_pass = kRouteWarps / a.wpt;
+    const int p = warp & (a.wpt - 1), tiles_per_pass = kRouteWarps >> a.wpt_shift;
 #pragma unroll
     for (int uu = 0; uu < kRouteBatch; ++uu) {
-        const int j = warp / a.wpt + tiles_per_pass * (b * kRouteBatch + uu);
-        const bool ok = j < a.N / 8;
+        const int j = (warp >> a.wpt_shift) + tiles_per_pass * (b * kRouteBatch + uu);
+        const bool ok = j < (a.N >> 3);
         const uint16_t* wp = a.w + (int64_t)(j * 8 + g) * a.K + kslice + (int64_t)p * a.spw * 32 + 8 * t;
 #pragma unroll
         for (int s = 0; s < kRouteSpwMax; ++s)
@@ -112,9 +119,10 @@ __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* ro
     return __fdiv_rn(num, den);
 }
 
-template <int MT, bool HALF>
+template <bool HALF>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
+    __shared__ unsigned s_ticket;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int c = (int)cluster_rank();
@@ -122,8 +130,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM access
     pdl_trigger();
 
-    const int N = a.N, M = a.M, wpt = a.wpt, tok = a.tok, K = a.K;
+    // this cluster's token rows: [row0, row0 + Mq)
+    const int row0 = (int)(blockIdx.x >> a.cs_shift) * kRouteRowsPerCluster;
+    const int Mq = min(kRouteRowsPerCluster, a.M - row0);
+    const int N = a.N, wpt = a.wpt, tok = a.tok, K = a.K;
     const int64_t kslice = (int64_t)c * a.kc;
+    const uint16_t* xq = a.x + (int64_t)row0 * a.ldx;
     unsigned long long* mask = reinterpret_cast<unsigned long long*>(sm + a.off_mask);
 
     // ---- gate-weight loads of the first batch (the weight is never written
@@ -134,12 +146,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         for (int e = tid; e < N; e += kRouteThreads) mask[e] = 0ull;  // token bitmasks (2 x 32 bits per expert)
     pdl_wait();
 
-    // ---- x slice -> shared memory
+    // ---- this CTA's x slice -> shared memory
     unsigned char* xs = sm + a.off_x;
     const int vpr = a.kc / 8;
-    for (int v = tid; v < M * vpr; v += kRouteThreads) {
-        const int r = v / vpr, cv = v - r * vpr;
-        const uint4 d = ld_ro_v4(a.x + (int64_t)r * a.ldx + kslice + cv * 8);
+    for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
+        const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
+        const uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
         *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
     }
     __syncthreads();
@@ -149,50 +161,45 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      straight to the receive buffers of the rows' owners
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
     const uint32_t recv_local = smem_u32(sm + a.off_recv);
-    const int p = warp % wpt, tiles_per_pass = kRouteWarps / wpt, NT = N / 8;
-    const int my_tiles = warp / wpt < NT ? (NT - warp / wpt + tiles_per_pass - 1) / tiles_per_pass : 0;
+    const int p = warp & (wpt - 1), tiles_per_pass = kRouteWarps >> a.wpt_shift, NT = N >> 3;
+    const int j0 = warp >> a.wpt_shift;
+    const int my_tiles = j0 < NT ? (NT - j0 + tiles_per_pass - 1) >> (4 - a.wpt_shift) : 0;
     const int nb = (my_tiles + kRouteBatch - 1) / kRouteBatch;
     const int slot = c * wpt + p;
+    const int r0 = g, r1 = g + 8;
     for (int b = 0; b < nb; ++b) {
         if (b > 0) load_w_batch(a, kslice, warp, g, t, b, wv);
-        float acc[kRouteBatch][MT][4];
+        float acc[kRouteBatch][4];
 #pragma unroll
-        for (int uu = 0; uu < kRouteBatch; ++uu)
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) acc[uu][mt][0] = acc[uu][mt][1] = acc[uu][mt][2] = acc[uu][mt][3] = 0.0f;
+        for (int uu = 0; uu < kRouteBatch; ++uu) acc[uu][0] = acc[uu][1] = acc[uu][2] = acc[uu][3] = 0.0f;
 #pragma unroll
         for (int s = 0; s < kRouteSpwMax; ++s) {
             if (s < a.spw) {
                 const int kk = (p * a.spw + s) * 32 + 8 * t;
+                const uint4 xa = r0 < Mq ? lds128(xs + r0 * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 xb = (!HALF && r1 < Mq) ? lds128(xs + r1 * a.xpitch + kk * 2)
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+                // consecutive MMAs go to different accumulators
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int r0 = mt * 16 + g, r1 = r0 + 8;
-                    const uint4 xa = r0 < M ? lds128(xs + r0 * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 xb = (!HALF && r1 < M) ? lds128(xs + r1 * a.xpitch + kk * 2)
-                                                       : make_uint4(0u, 0u, 0u, 0u);
+                for (int uu = 0; uu < kRouteBatch; ++uu)
+                    mma_bf16_m16n8k16(acc[uu], xa.x, xb.x, xa.y, xb.y, wv[uu][s].x, wv[uu][s].y);
 #pragma unroll
-                    for (int uu = 0; uu < kRouteBatch; ++uu) {
-                        mma_bf16_m16n8k16(acc[uu][mt], xa.x, xb.x, xa.y, xb.y, wv[uu][s].x, wv[uu][s].y);
-                        mma_bf16_m16n8k16(acc[uu][mt], xa.z, xb.z, xa.w, xb.w, wv[uu][s].z, wv[uu][s].w);
-                    }
-                }
+                for (int uu = 0; uu < kRouteBatch; ++uu)
+                    mma_bf16_m16n8k16(acc[uu], xa.z, xb.z, xa.w, xb.w, wv[uu][s].z, wv[uu][s].w);
             }
         }
 #pragma unroll
         for (int uu = 0; uu < kRouteBatch; ++uu) {
-            const int j = warp / wpt + tiles_per_pass * (b * kRouteBatch + uu);
+            const int j = j0 + tiles_per_pass * (b * kRouteBatch + uu);
             if (j >= NT) break;
             const int col = j * 8 + 2 * t;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-                for (int h = 0; h < (HALF ? 1 : 2); ++h) {
-                    const int r = mt * 16 + g + 8 * h;
-                    if (r < M) {
-                        const int own = r / tok, rl = r - own * tok;
-                        const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * N + col) * 4);
-                        st_cluster_f2(map_rank(la, (unsigned)own), acc[uu][mt][2 * h], acc[uu][mt][2 * h + 1]);
-                    }
+            for (int h = 0; h < (HALF ? 1 : 2); ++h) {
+                const int r = g + 8 * h;
+                if (r < Mq) {
+                    const int own = r >> a.tok_shift, rl = r & (tok - 1);
+                    const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * N + col) * 4);
+                    st_cluster_f2(map_rank(la, (unsigned)own), acc[uu][2 * h], acc[uu][2 * h + 1]);
                 }
             }
         }
@@ -200,18 +207,18 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // barrier 1
     // ---- MXFP8 of the x slice while the other CTAs finish (one lane quad per 32-block)
     if (a.q != nullptr) {
-        const int nvec = M * vpr;
+        const int nvec = Mq * vpr;
         const int64_t K32 = K / 32;
         for (int base = warp * 32; base < nvec; base += kRouteThreads) {
             const int v = base + lane;
-            const int r = v / vpr, cv = v - r * vpr;
+            const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
             const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
             unsigned sb;
             const uint2 q8 = mx_quant_quad(d, &sb);
             if (v < nvec) {
                 const int64_t k = kslice + cv * 8;
-                *reinterpret_cast<uint2*>(a.q + (int64_t)r * K + k) = q8;
-                if ((cv & 3) == 0) a.scale[(int64_t)r * K32 + k / 32] = (uint8_t)sb;
+                *reinterpret_cast<uint2*>(a.q + (int64_t)(row0 + r) * K + k) = q8;
+                if ((cv & 3) == 0) a.scale[(int64_t)(row0 + r) * K32 + k / 32] = (uint8_t)sb;
             }
         }
     }
@@ -222,7 +229,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const float* recv = reinterpret_cast<const float*>(sm + a.off_recv);
     float* rowbuf = reinterpret_cast<float*>(sm + a.off_row);
     const int nslots = a.cs * wpt;
-    const int my_rows = max(0, min(tok, M - c * tok));
+    const int my_rows = max(0, min(tok, Mq - c * tok));
+    const int grow = row0 + c * tok;  // global index of this CTA's first row
     for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
         const float* pp = recv + idx;
         float sum = 0.0f;
@@ -230,8 +238,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         rowbuf[idx] = sum;
     }
     if (a.mode == 0) {
-        for (int idx = tid; idx < my_rows * N; idx += kRouteThreads)
-            a.logits[(int64_t)c * tok * N + idx] = rowbuf[idx];
+        for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) a.logits[(int64_t)grow * N + idx] = rowbuf[idx];
         return;  // nothing else reads this CTA's shared memory
     }
     __syncthreads();
@@ -247,24 +254,24 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     float* oval = reinterpret_cast<float*>(oid + tok * k);
     unsigned long long* comp = reinterpret_cast<unsigned long long*>(sm + a.off_key);
     for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
-        const int n = idx % N;
+        const int n = idx - fdiv(idx, a.mag_n) * N;
         float sel = rowbuf[idx];
         if (a.scoring == 1) sel = __fadd_rn(sigmoid_score(sel), a.bias ? __ldg(a.bias + n) : 0.0f);
         comp[idx] = composite(ordered_key(sel), n);
     }
     for (int idx = tid; idx < my_rows * GK; idx += kRouteThreads) ccomp[idx] = 0ull;  // segments shorter than k
     __syncthreads();
-    MR_TRACE_STAMP(a.trace, 6);
     // TPK adjacent lanes share a key's count; part p reads the 16-byte pairs
     // p, p + TPK, p + 2 TPK, ... of the segment, so the lanes of one key hit
     // consecutive banks and lanes of different keys read the same addresses
-    int tpk = 1;
-    while (tpk < 8 && 2 * tpk * my_rows * N <= kRouteThreads) tpk *= 2;
+    int tpk_shift = 0;
+    while (tpk_shift < 3 && (2 << tpk_shift) * my_rows * N <= kRouteThreads) ++tpk_shift;
+    const int tpk = 1 << tpk_shift;
     for (int base = warp * 32; base < my_rows * N * tpk; base += kRouteThreads) {
         const int item = base + lane;
         const bool on = item < my_rows * N * tpk;
-        const int key_idx = item / tpk, part = item - key_idx * tpk;
-        const int rl = key_idx / N, n = key_idx - rl * N, sg = n >> 7;
+        const int key_idx = item >> tpk_shift, part = item & (tpk - 1);
+        const int rl = fdiv(key_idx, a.mag_n), n = key_idx - rl * N, sg = n >> 7;
         const unsigned long long* cr = comp + rl * N;
         const unsigned long long cn = on ? cr[n] : ~0ull;
         const int lo = sg << 7, hi = on ? min(N, lo + 128) : lo;
@@ -286,10 +293,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         }
     }
     __syncthreads();
-    MR_TRACE_STAMP(a.trace, 7);
     if (G > 1) {
         for (int idx = tid; idx < my_rows * GK; idx += kRouteThreads) {
-            const int rl = idx / GK;
+            const int rl = fdiv(idx, a.mag_gk);
             const unsigned long long cn = ccomp[idx];
             if (cn == 0ull) continue;
             const unsigned long long* cr = ccomp + rl * GK;
@@ -302,55 +308,62 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         }
         __syncthreads();
     }
-    MR_TRACE_STAMP(a.trace, 8);
-    // ---- weights; ids to CTA 0
+    MR_TRACE_STAMP(a.trace, 4);
+    // ---- weights; ids to CTA 0 of the cluster (its local rows)
     const uint32_t ids_all_local = smem_u32(sm + a.off_ids);
     int out_id = 0;
     float out_w = 0.0f;
     if (warp < my_rows) {
-        const int rl = warp, m = c * tok + rl;
+        const int rl = warp, ml = c * tok + rl;  // row inside the cluster
         const bool live = lane < k;
         const int id = live ? oid[rl * k + lane] : 0;
         const float val = live ? oval[rl * k + lane] : 0.0f;
         out_w = gate_weight(a, rowbuf + rl * N, val);
         out_id = id;
-        if (live) st_cluster_s32(map_rank(ids_all_local + (uint32_t)((m * k + lane) * 4), 0u), id);
+        if (live) st_cluster_s32(map_rank(ids_all_local + (uint32_t)((ml * k + lane) * 4), 0u), id);
     }
-    MR_TRACE_STAMP(a.trace, 9);
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // barrier 2
-    MR_TRACE_STAMP(a.trace, 10);
     // global outputs of this CTA's rows while CTA 0 waits for the others
-    for (int idx = tid; idx < my_rows * N; idx += kRouteThreads)
-        a.logits[(int64_t)c * tok * N + idx] = rowbuf[idx];
+    for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) a.logits[(int64_t)grow * N + idx] = rowbuf[idx];
     if (warp < my_rows && lane < k) {
-        const int m = c * tok + warp;
+        const int m = grow + warp;
         a.ids[(int64_t)m * k + lane] = out_id;
         a.weights[(int64_t)m * k + lane] = out_w;
     }
-    MR_TRACE_STAMP(a.trace, 11);
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    MR_TRACE_STAMP(a.trace, 4);
+    MR_TRACE_STAMP(a.trace, 5);
     if (c != 0) return;
 
-    // ---- sort (CTA 0): rank of (m, j) inside expert e = number of set bits
-    //      below m in the token mask of e (two 32-bit words: tokens 0-31, 32-63)
-    const int* ids_all = reinterpret_cast<const int*>(sm + a.off_ids);
+    // ---- sort.  One cluster: CTA 0 holds every id.  Several clusters: each
+    //      CTA 0 publishes its rows' ids and takes a ticket; the last one
+    //      gathers all ids and sorts.
+    int* ids_all = reinterpret_cast<int*>(sm + a.off_ids);
+    const int M = a.M, MK = M * k, B = a.block;
+    if (a.clusters > 1) {
+        for (int f = tid; f < Mq * k; f += kRouteThreads) a.ids_scratch[row0 * k + f] = ids_all[f];
+        const unsigned ticket = cta_ticket(a.counter, &s_ticket);
+        if (ticket != (unsigned)(a.clusters - 1)) return;
+        for (int f = tid; f < MK; f += kRouteThreads) ids_all[f] = __ldcg(a.ids_scratch + f);
+        if (tid == 0) *a.counter = 0u;
+        __syncthreads();
+    }
+    MR_TRACE_STAMP(a.trace, 6);
+    // rank of (m, j) inside expert e = number of set bits below m in the token
+    // mask of e (two 32-bit words: tokens 0-31, 32-63)
     int* start = reinterpret_cast<int*>(sm + a.off_start);
     int* warp_tot = start + N;
-    const int MK = M * k, B = a.block;
     unsigned* mlo = reinterpret_cast<unsigned*>(mask);
     unsigned* mhi = mlo + N;
     for (int f = tid; f < MK; f += kRouteThreads) {
-        const int m = f / k;
+        const int m = fdiv(f, a.mag_k);
         atomicOr(m < 32 ? &mlo[ids_all[f]] : &mhi[ids_all[f]], 1u << (m & 31));
     }
     __syncthreads();
-    MR_TRACE_STAMP(a.trace, 12);
     // exclusive scan of the padded counts, two experts per thread, one barrier
     const int e0 = 2 * tid, e1 = e0 + 1;
     const int c0 = e0 < N ? __popc(mlo[e0]) + __popc(mhi[e0]) : 0;
     const int c1 = e1 < N ? __popc(mlo[e1]) + __popc(mhi[e1]) : 0;
-    const int v0 = (c0 + B - 1) / B * B, v1 = (c1 + B - 1) / B * B;
+    const int v0 = fdiv(c0 + B - 1, a.mag_block) * B, v1 = fdiv(c1 + B - 1, a.mag_block) * B;
     const int local = v0 + v1;
     int incl = local;
 #pragma unroll
@@ -371,45 +384,45 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     if (e0 < N) start[e0] = s0;
     if (e1 < N) start[e1] = s0 + v0;
     // sentinels everywhere (coalesced 16-byte stores), expert ids of every block
+    const int cap = (int)a.capacity;  // < 2^31, checked on the host
     if ((reinterpret_cast<uintptr_t>(a.sorted) & 15u) == 0) {
         int4* st4 = reinterpret_cast<int4*>(a.sorted);
-        const int64_t n4 = a.capacity / 4;
-        for (int64_t i = tid; i < n4; i += kRouteThreads) st4[i] = make_int4(MK, MK, MK, MK);
-        for (int64_t i = n4 * 4 + tid; i < a.capacity; i += kRouteThreads) a.sorted[i] = MK;
+        const int n4 = cap >> 2;
+        for (int i = tid; i < n4; i += kRouteThreads) st4[i] = make_int4(MK, MK, MK, MK);
+        for (int i = (n4 << 2) + tid; i < cap; i += kRouteThreads) a.sorted[i] = MK;
     } else {
-        for (int64_t i = tid; i < a.capacity; i += kRouteThreads) a.sorted[i] = MK;
+        for (int i = tid; i < cap; i += kRouteThreads) a.sorted[i] = MK;
     }
     if (e0 < N)
-        for (int bb = s0 / B; bb < (s0 + v0) / B; ++bb) a.expert_ids[bb] = e0;
+        for (int bb = fdiv(s0, a.mag_block), be = fdiv(s0 + v0, a.mag_block); bb < be; ++bb) a.expert_ids[bb] = e0;
     if (e1 < N)
-        for (int bb = (s0 + v0) / B; bb < (s0 + v0 + v1) / B; ++bb) a.expert_ids[bb] = e1;
-    for (int64_t bb = total / B + tid; bb < a.capacity / B; bb += kRouteThreads) a.expert_ids[bb] = -1;
+        for (int bb = fdiv(s0 + v0, a.mag_block), be = fdiv(s0 + v0 + v1, a.mag_block); bb < be; ++bb)
+            a.expert_ids[bb] = e1;
+    for (int bb = fdiv(total, a.mag_block) + tid, be = fdiv(cap, a.mag_block); bb < be; bb += kRouteThreads)
+        a.expert_ids[bb] = -1;
     __syncthreads();  // orders the sentinel stores before the real entries below
-    MR_TRACE_STAMP(a.trace, 13);
     for (int f = tid; f < MK; f += kRouteThreads) {
-        const int e = ids_all[f], m = f / k;
+        const int e = ids_all[f], m = fdiv(f, a.mag_k);
         const unsigned below = m < 32 ? __popc(mlo[e] & ((1u << m) - 1u))
                                       : __popc(mlo[e]) + __popc(mhi[e] & ((1u << (m - 32)) - 1u));
         a.sorted[start[e] + (int)below] = f;
     }
-    MR_TRACE_STAMP(a.trace, 14);
     if (tid == 0) *a.ntpp = total;
-    MR_TRACE_STAMP(a.trace, 5);
+    MR_TRACE_STAMP(a.trace, 7);
 }
 
 // ------------------------------------------------------------------ host
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
-static int g_attr_done[64][4];  // per device and instantiation
+static int g_attr_done[64][2];  // per device and instantiation
 
-template <int MT, bool HALF>
-static cudaError_t prepare(int dev, int idx, int cs) {
-    if (g_attr_done[dev][idx]) return cudaSuccess;
-    auto k = route_cluster_kernel<MT, HALF>;
+template <bool HALF>
+static cudaError_t prepare(int dev) {
+    if (g_attr_done[dev][HALF ? 1 : 0]) return cudaSuccess;
+    auto k = route_cluster_kernel<HALF>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess) g_attr_done[dev][idx] = 1;
-    (void)cs;
+    if (e == cudaSuccess) g_attr_done[dev][HALF ? 1 : 0] = 1;
     return e;
 }
 
@@ -417,7 +430,7 @@ int route_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (g_cluster16[dev] == 0) {
-        cudaError_t e = prepare<1, false>(dev, 1, 16);
+        cudaError_t e = prepare<false>(dev);
         int n = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -431,7 +444,7 @@ int route_cluster_size() {
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<1, false>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false>, &cfg);
         }
         g_cluster16[dev] = (e == cudaSuccess && n >= 1) ? 1 : -1;
         cudaGetLastError();  // a refused query leaves no sticky error
@@ -444,17 +457,17 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int idx = p.half ? 0 : (p.mt == 1 ? 1 : p.mt == 2 ? 2 : 3);
     void (*kernel)(RouteArgs) = nullptr;
-    switch (idx) {
-        case 0: e = prepare<1, true>(dev, 0, p.cs); kernel = route_cluster_kernel<1, true>; break;
-        case 1: e = prepare<1, false>(dev, 1, p.cs); kernel = route_cluster_kernel<1, false>; break;
-        case 2: e = prepare<2, false>(dev, 2, p.cs); kernel = route_cluster_kernel<2, false>; break;
-        default: e = prepare<4, false>(dev, 3, p.cs); kernel = route_cluster_kernel<4, false>; break;
+    if (p.half) {
+        e = prepare<true>(dev);
+        kernel = route_cluster_kernel<true>;
+    } else {
+        e = prepare<false>(dev);
+        kernel = route_cluster_kernel<false>;
     }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.cs);
+    cfg.gridDim = dim3(p.cs * p.clusters);
     cfg.blockDim = dim3(kRouteThreads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = st;

@@ -12,6 +12,7 @@ constexpr int kRouteBatch = 2;            // (tile, k-part) units whose loads a 
 constexpr int kRouteSpwMax = 8;           // 32-wide k steps per unit, at most
 constexpr int kRouteSmemMax = 200 * 1024; // dynamic shared memory, at most
 constexpr int kRouteMaxM = 64;
+constexpr int kRouteRowsPerCluster = 16;  // token rows per cluster (one m16 MMA tile)
 
 struct RouteArgs {
     const uint16_t* x;
@@ -30,6 +31,8 @@ struct RouteArgs {
     int M, N, K, topk, block, scoring, renormalize;
     int mode;        // 0: logits only, 1: whole route
     int cs;          // CTAs in the cluster
+    int cs_shift;    // log2(cs)
+    int clusters;    // clusters in the grid: one per 16 token rows
     int kc;          // K per CTA
     int spw;         // 32-wide k steps per unit
     int wpt;         // k-parts per 8-expert tile
@@ -38,11 +41,27 @@ struct RouteArgs {
     int gwarps;      // gate warps per row (128-expert segments)
     int xpitch;      // bytes per x row in shared memory
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
+    int tok_shift, wpt_shift;  // log2 of tok and wpt (both powers of two)
+    // q = (x * magic) >> 32 equals x / d for 0 <= x < 2^21, d <= 1024
+    unsigned long long mag_n, mag_k, mag_block, mag_vpr, mag_gk;
     unsigned long long* trace;
+    int32_t* ids_scratch;   // clusters > 1: every token's ids, gathered for the sort
+    unsigned* counter;      // clusters > 1: last-arriver ticket, zero between launches
 };
 
+// Multiplier for division by d (1 <= d <= 2^11) of dividends below 2^21:
+// floor(x * ceil(2^32 / d) / 2^32) == floor(x / d).
+inline unsigned long long div_magic(int d) {
+    return (((unsigned long long)1 << 32) + (unsigned long long)d - 1) / (unsigned long long)d;
+}
+inline int ilog2_exact(int v) {
+    int s = 0;
+    while ((1 << s) < v) ++s;
+    return (1 << s) == v ? s : -1;
+}
+
 struct RoutePlan {
-    int cs, kc, spw, wpt, units, tok, gwarps, xpitch, mt;
+    int cs, kc, spw, wpt, units, tok, gwarps, xpitch, clusters;
     bool half;
     int smem;
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
@@ -73,15 +92,20 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.wpt = w;
     q.spw = S / w;
     q.units = NT * w;
-    q.tok = (M + cs - 1) / cs;
+    // one cluster per 16 token rows; rows owned per CTA: a power of two
+    // covering ceil(rows of a cluster / cs)
+    q.clusters = (M + kRouteRowsPerCluster - 1) / kRouteRowsPerCluster;
+    const int Mc = M < kRouteRowsPerCluster ? M : kRouteRowsPerCluster;
+    q.tok = 1;
+    while (q.tok * cs < Mc) q.tok *= 2;
     q.gwarps = (N + 127) / 128;  // 128-expert segments of the gate
     if (mode == 1 && (topk < 1 || topk > 32 || topk > N || q.tok > kRouteWarps)) return false;
-    q.mt = M <= 16 ? 1 : M <= 32 ? 2 : 4;
+    if (ilog2_exact(q.tok) < 0 || ilog2_exact(w) < 0 || ilog2_exact(cs) < 0) return false;
     q.half = M <= 8;
     q.xpitch = q.kc * 2 + (((q.kc * 2) % 128 == 0) ? 64 : 0);
     int off = 0;
     q.off_x = off;
-    off = align_up(off + M * q.xpitch, 16);
+    off = align_up(off + Mc * q.xpitch, 16);
     q.off_recv = off;
     off = align_up(off + cs * w * q.tok * N * 4, 16);
     q.off_row = off;
@@ -90,7 +114,7 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     off = align_up(off + (mode == 1 ? q.tok * N : 0) * 8, 16);
     q.off_cand = off;  // per row: G*k composites, G*k values, k ids, k values
     off = align_up(off + (mode == 1 ? q.tok * (q.gwarps * topk * 12 + topk * 8) : 0), 16);
-    q.off_ids = off;
+    q.off_ids = off;  // every token's ids in the CTA that sorts
     off = align_up(off + M * (mode == 1 ? topk : 0) * 4, 16);
     q.off_mask = off;
     off = align_up(off + (mode == 1 ? N : 0) * 8, 16);

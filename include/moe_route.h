@@ -197,15 +197,18 @@ int mr_mxfp8_quant(const void *x, int64_t ldx, int M, int K, uint8_t *q,
                    uint8_t *scale, void *stream);
 
 /*
- * a6. The whole path for 1 <= M <= 16 tokens in ONE launch [#46691 Summary:
+ * a6. The whole path for 1 <= M <= 64 tokens in ONE launch [#46691 Summary:
  * a one-launch decode router for 1-16 tokens, bitwise equal to router GEMV,
  * gate and sort; sort + quant in one launch for decode batches].
  * Arguments as in the four calls above; every output is bitwise equal to
  * mr_router_gemv -> mr_route_topk -> mr_moe_sort -> mr_mxfp8_quant on the
  * same inputs.  q and scale may both be NULL to skip the quantisation.
- * GEMV CTAs hand over by atomic last-arriver tickets (no spin-waits): the
- * last CTA of each n-block runs the split-K fixup, the last fixup runs the
- * gate for all tokens and the sort.
+ * K % 512 == 0, N % 8 == 0, N <= 1024, topk <= 32.
+ * One thread-block cluster per 16 tokens.  M <= 16 uses no scratch (scratch
+ * may be NULL).  M > 16: the clusters hand over through scratch by an atomic
+ * last-arriver ticket (no spin-waits) and the last cluster sorts; scratch
+ * must hold mr_scratch_bytes(M, N, K, topk) bytes (MR_ERR_INVALID_ARG if
+ * NULL, MR_ERR_SCRATCH_TOO_SMALL if short).
  */
 int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
                             int M, int N, int K, int topk, int scoring,

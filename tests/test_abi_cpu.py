@@ -78,6 +78,8 @@ def test_scratch_bytes(lib):
     assert mr.scratch_bytes(512, 128, 6144, 8) >= b
     assert mr.scratch_bytes(4096, 128, 6144, 8) >= 32768 + 4 * 32768
     assert mr.scratch_bytes(0, 128, 6144, 8) == 0
+    # the fused route over several clusters gathers every token's ids
+    assert mr.scratch_bytes(64, 1024, 512, 32) >= 32768 + 64 * 32 * 4
 
 
 def test_validation_returns_before_any_launch(lib):
@@ -109,6 +111,12 @@ def test_validation_returns_before_any_launch(lib):
     # fused: q without scale
     assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 1, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
                                        fake, fake, fake, 128, fake, None, fake, 1 << 20, None) == mr.MR_ERR_INVALID_ARG
+    # fused over several clusters (M > 16): the ticket and the ids live in scratch
+    assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 17, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
+                                       fake, fake, fake, 1 << 20, fake, fake, None, 0, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 17, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
+                                       fake, fake, fake, 1 << 20, fake, fake, fake, 32768 + 17 * 8 * 4 - 4,
+                                       None) == mr.MR_ERR_SCRATCH_TOO_SMALL
     # reset: buffer below the counter prefix
     assert lib.mr_scratch_reset(fake, 100, None) == mr.MR_ERR_INVALID_ARG
 

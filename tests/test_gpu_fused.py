@@ -1,4 +1,4 @@
-"""The one-launch route (M <= 16): bitwise equal to the four-call chain, and
+"""The one-launch route (M <= 64): bitwise equal to the four-call chain, and
 to the oracle where the oracle is exact; 1000 back-to-back launches on one
 scratch buffer, every launch checked."""
 
