@@ -18,7 +18,8 @@ import os
 
 __all__ = [
     "MoeRouteError", "MoeRouteUnsupported", "Scratch", "library_path", "load_library",
-    "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
+    "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "LAUNCH_TEST_STALL", "set_wait_limit_ns",
+    "device_error", "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
     "moe_sort", "mxfp8_quant", "moe_route_sort_quant", "router_gemv_noalloc",
 ]
 
@@ -26,7 +27,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libmoe_route.so")
 _lib = None
 
-MR_OK, MR_ERR_UNSUPPORTED, MR_ERR_INVALID_ARG, MR_ERR_SCRATCH_TOO_SMALL, MR_ERR_CUDA = range(5)
+MR_OK, MR_ERR_UNSUPPORTED, MR_ERR_INVALID_ARG, MR_ERR_SCRATCH_TOO_SMALL, MR_ERR_CUDA, MR_ERR_TIMEOUT = range(6)
 SCORING = {"softmax": 0, "sigmoid": 1}
 SCRATCH_COUNTER_BYTES = 32768
 
@@ -66,6 +67,8 @@ SIGNATURES = {
     "mr_moe_route_sort_quant": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P,
                                      _P, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
     "mr_router_gemv_noalloc": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P]),
+    "mr_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+    "mr_device_error": (_I, [_I]),
 }
 
 
@@ -131,6 +134,7 @@ def _row_major_2d(x, name):
 
 
 LAUNCH_PDL = 1
+LAUNCH_TEST_STALL = 2  # test hook: the cluster kernels' bounded waits run out
 
 
 def set_launch_flags(flags: int) -> None:
@@ -140,6 +144,20 @@ def set_launch_flags(flags: int) -> None:
 
 def get_launch_flags() -> int:
     return int(_load().mr_get_launch_flags())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of every bounded wait inside the cluster kernels (default 1 s)."""
+    _check(_load().mr_set_wait_limit_ns(int(ns)), "mr_set_wait_limit_ns")
+
+
+def device_error(clear: bool = False) -> int:
+    """MR_OK, or MR_ERR_TIMEOUT once a bounded wait ran out on the current
+    device (synchronous; call after the streams have finished)."""
+    st = int(_load().mr_device_error(int(clear)))
+    if st not in (MR_OK, MR_ERR_TIMEOUT):
+        _check(st, "mr_device_error")
+    return st
 
 
 def router_gemv_supported(M: int, N: int, K: int, ldx: int | None = None) -> bool:

@@ -43,27 +43,40 @@ int check_sort_args(int M, int topk, int N, int block, int64_t capacity) {
 }
 
 std::atomic<int> g_launch_flags{0};
+std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 std::atomic<void*> g_trace{nullptr};
 
 }  // namespace
 
 namespace mr {
 int launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 void* trace_buffer() { return g_trace.load(std::memory_order_relaxed); }
 }  // namespace mr
 
 extern "C" {
 
 int mr_set_launch_flags(int flags) {
-    if (flags & ~MR_LAUNCH_PDL) return MR_ERR_INVALID_ARG;
+    if (flags & ~(MR_LAUNCH_PDL | MR_LAUNCH_TEST_STALL)) return MR_ERR_INVALID_ARG;
     g_launch_flags.store(flags, std::memory_order_relaxed);
     return MR_OK;
 }
 
 int mr_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
 
+int mr_set_wait_limit_ns(uint64_t ns) {
+    if (ns < 1000ull || ns > 60000000000ull) return MR_ERR_INVALID_ARG;
+    g_wait_ns.store(ns, std::memory_order_relaxed);
+    return MR_OK;
+}
+
+int mr_device_error(int clear) {
+    const int v = mr::route_device_error(clear);
+    return v < 0 ? MR_ERR_CUDA : v ? MR_ERR_TIMEOUT : MR_OK;
+}
+
 #ifdef MR_TRACE
-// Tracing builds only: device buffer of gridDim * 32 u64 stamps for the next
+// Tracing builds only: device buffer of gridDim * 256 u64 stamps for the next
 // launches (nullptr stops tracing).
 int mr_trace_set_buffer(void* device_buffer) {
     g_trace.store(device_buffer, std::memory_order_relaxed);
@@ -78,6 +91,7 @@ const char* mr_status_string(int status) {
         case MR_ERR_INVALID_ARG: return "MR_ERR_INVALID_ARG: null or misaligned pointer, or bad size";
         case MR_ERR_SCRATCH_TOO_SMALL: return "MR_ERR_SCRATCH_TOO_SMALL: scratch_bytes below what the call needs";
         case MR_ERR_CUDA: return "MR_ERR_CUDA: the CUDA runtime reported an error";
+        case MR_ERR_TIMEOUT: return "MR_ERR_TIMEOUT: a kernel's bounded wait for data from other CTAs ran out";
         default: return "unknown mr_status";
     }
 }
@@ -151,7 +165,6 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.wpt = p.wpt;
     a.units = p.units;
     a.tok = p.tok;
-    a.gwarps = p.gwarps;
     a.xpitch = p.xpitch;
     a.off_x = p.off_x;
     a.off_recv = p.off_recv;
@@ -166,6 +179,8 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.mag_n = mr::div_magic(N);
     a.mag_vpr = mr::div_magic(p.kc / 8);
     a.trace = static_cast<unsigned long long*>(mr::trace_buffer());
+    a.flags = mr::launch_flags();
+    a.wait_ns = mr::wait_limit_ns();
     return a;
 }
 
@@ -271,7 +286,6 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
     a.block = block;
     a.mag_k = mr::div_magic(topk);
     a.mag_block = mr::div_magic(block);
-    a.mag_gk = mr::div_magic(rp.gwarps * topk);
     a.scoring = scoring;
     a.renormalize = renormalize ? 1 : 0;
     return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));

@@ -62,19 +62,31 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
     return *s_slot;
 }
 
-// Optional per-CTA phase stamps (compile with -DMR_TRACE): thread 0 writes
-// %globaltimer (ns) to trace[(blockIdx.y * gridDim.x + blockIdx.x) * 32 + slot].
+// Optional phase stamps (compile with -DMR_TRACE), %globaltimer in ns, 256
+// u64 per CTA at trace + (blockIdx.y * gridDim.x + blockIdx.x) * 256:
+// MR_TRACE_STAMP: thread 0 writes slot (< 32); MR_TRACE_WARP: lane 0 of every
+// warp writes slot 32 + 16 * phase + warp (phase < 14, 16 warps at most).
 #ifdef MR_TRACE
+#define MR_TRACE_AT(trace, slot)                                                     \
+    do {                                                                             \
+        unsigned long long t_;                                                       \
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                       \
+        (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 256 + (slot)] = t_;          \
+    } while (0)
 #define MR_TRACE_STAMP(trace, slot)                                                  \
     do {                                                                             \
-        if (threadIdx.x == 0 && (trace) != nullptr) {                               \
-            unsigned long long t_;                                                   \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                   \
-            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 32 + (slot)] = t_;       \
-        }                                                                            \
+        if (threadIdx.x == 0 && (trace) != nullptr) MR_TRACE_AT(trace, slot);        \
+    } while (0)
+#define MR_TRACE_WARP(trace, phase)                                                  \
+    do {                                                                             \
+        if ((threadIdx.x & 31) == 0 && (trace) != nullptr)                           \
+            MR_TRACE_AT(trace, 32 + 16 * (phase) + (threadIdx.x >> 5));              \
     } while (0)
 #else
 #define MR_TRACE_STAMP(trace, slot) \
+    do {                            \
+    } while (0)
+#define MR_TRACE_WARP(trace, phase) \
     do {                            \
     } while (0)
 #endif

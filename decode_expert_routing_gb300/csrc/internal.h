@@ -53,6 +53,10 @@ struct RoutePlan;
 struct RouteArgs;
 // Cluster route kernel (M <= 64): logits only (mode 0) or the whole route.
 int route_cluster_size();  // 16 when the device runs 16-CTA clusters, else 8
+// 1 if a bounded wait of the route kernel ran out on the current device, 0
+// if not, -1 on a CUDA error; clear resets the flag.  Synchronous.
+int route_device_error(int clear);
+unsigned long long wait_limit_ns();
 cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStream_t st);
 
 // Launch options (MR_LAUNCH_* bits of mr_set_launch_flags).

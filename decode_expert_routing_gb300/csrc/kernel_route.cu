@@ -28,8 +28,10 @@
 //   its rows; the CTA 0s publish their ids and take a last-arriver ticket
 //   (the pages' hand-off), and the last one sorts every assignment.
 //
-// No spin-waits: all waits are hardware cluster/CTA barriers.  Nothing is
-// left in scratch, so no counter needs re-zeroing.  The GEMV alone (mode 0)
+// Hand-offs inside a cluster are st.async stores counted on an mbarrier of
+// the receiving CTA (no release fences); each wait for them is bounded in
+// time and sets a device flag when it runs out.  One cluster leaves nothing
+// in scratch; several clusters leave their ticket counter at zero again.  The GEMV alone (mode 0)
 // is what the standalone router GEMV runs for M <= 64, so the logits of the
 // two are bitwise equal.
 #include "common.cuh"
@@ -46,9 +48,6 @@ __device__ __forceinline__ unsigned cluster_rank() {
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_sync_acq_rel() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
@@ -60,11 +59,62 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t local, unsigned rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
-    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+
+// Hand-offs between the CTAs of a cluster: the sender writes with st.async,
+// which also counts the bytes on an mbarrier in the receiving CTA; the
+// receiver has announced the bytes it expects, so the barrier's phase 0
+// completes when the last byte has landed.  No release fence on either side.
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait0(uint32_t bar) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void st_async_f2(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "f"(a), "f"(b), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_s32(uint32_t addr, int v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.s32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+                 "r"(bar)
+                 : "memory");
+}
+
+// Set when a bounded wait of the route kernel ran out (read by the host).
+__device__ int g_route_timeout;
+
+// Thread 0 waits for phase 0 of the local mbarrier, at most limit_ns; the
+// whole CTA learns the outcome (the barrier orders the data for every thread).
+__device__ __forceinline__ bool cta_wait_bytes(uint32_t bar, unsigned long long limit_ns, int* s_ok) {
+    if (threadIdx.x == 0) {
+        bool ok = mbar_try_wait0(bar);
+        if (!ok) {
+            const unsigned long long t0 = global_ns();
+            while (!(ok = mbar_try_wait0(bar)) && global_ns() - t0 < limit_ns) {
+            }
+            if (!ok) atomicExch(&g_route_timeout, 1);
+        }
+        *s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return *s_ok != 0;
 }
 __device__ __forceinline__ uint4 lds128(const void* p) {
     return *reinterpret_cast<const uint4*>(p);
@@ -122,26 +172,49 @@ __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* ro
 template <bool HALF>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
+    __shared__ __align__(8) unsigned long long s_bar[2];  // [0] partial logits in, [1] ids in (CTA 0)
+    __shared__ int s_ok[2];
     __shared__ unsigned s_ticket;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int c = (int)cluster_rank();
     MR_TRACE_STAMP(a.trace, 0);
-    cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM access
-    pdl_trigger();
-
-    // this cluster's token rows: [row0, row0 + Mq)
+#ifdef MR_TRACE
+    if (tid == 0 && a.trace) a.trace[blockIdx.x * 256 + 24] = clock64();
+#endif
+    // this cluster's token rows: [row0, row0 + Mq); this CTA owns rows
+    // [c * tok, c * tok + my_rows) of them
     const int row0 = (int)(blockIdx.x >> a.cs_shift) * kRouteRowsPerCluster;
     const int Mq = min(kRouteRowsPerCluster, a.M - row0);
-    const int N = a.N, wpt = a.wpt, tok = a.tok, K = a.K;
+    const int N = a.N, wpt = a.wpt, tok = a.tok, K = a.K, k = a.topk;
+    const int nslots = a.cs * wpt;
+    const int my_rows = max(0, min(tok, Mq - c * tok));
+    const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]);
+    if (tid == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar1, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const unsigned stall = (a.flags & 2) ? 16u : 0u;  // test hook: bytes that never come
+        if (my_rows > 0) mbar_expect_tx(bar0, (unsigned)(my_rows * nslots * N * 4) + stall);
+        if (a.mode == 1 && c == 0) mbar_expect_tx(bar1, (unsigned)(Mq * k * 4));
+    }
+    cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM access
+    pdl_trigger();
     const int64_t kslice = (int64_t)c * a.kc;
     const uint16_t* xq = a.x + (int64_t)row0 * a.ldx;
     unsigned long long* mask = reinterpret_cast<unsigned long long*>(sm + a.off_mask);
 
-    // ---- gate-weight loads of the first batch (the weight is never written
-    //      by the preceding kernel, so they may precede the wait)
+    // ---- loads of the gate weight (first batch) and of the selection bias:
+    //      parameters, never written by the preceding kernel, so they may
+    //      precede the wait
     uint4 wv[kRouteBatch][kRouteSpwMax];
     load_w_batch(a, kslice, warp, g, t, 0, wv);
+    float bpre0 = 0.0f, bpre1 = 0.0f;  // bias of the first two owner-sum items of this thread
+    if (a.bias != nullptr) {
+        const int i0 = tid, i1 = tid + kRouteThreads;
+        if (i0 < my_rows * N) bpre0 = __ldg(a.bias + (i0 - fdiv(i0, a.mag_n) * N));
+        if (i1 < my_rows * N) bpre1 = __ldg(a.bias + (i1 - fdiv(i1, a.mag_n) * N));
+    }
     if (a.mode == 1 && c == 0)
         for (int e = tid; e < N; e += kRouteThreads) mask[e] = 0ull;  // token bitmasks (2 x 32 bits per expert)
     pdl_wait();
@@ -154,6 +227,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         const uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
         *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
     }
+    MR_TRACE_WARP(a.trace, 0);
     __syncthreads();
     MR_TRACE_STAMP(a.trace, 1);
 
@@ -161,6 +235,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      straight to the receive buffers of the rows' owners
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
     const uint32_t recv_local = smem_u32(sm + a.off_recv);
+    uint32_t owner_bar[2] = {0u, 0u};  // mbarrier of the owner of rows g and g + 8
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        if (g + 8 * h < Mq) owner_bar[h] = map_rank(bar0, (unsigned)((g + 8 * h) >> a.tok_shift));
     const int p = warp & (wpt - 1), tiles_per_pass = kRouteWarps >> a.wpt_shift, NT = N >> 3;
     const int j0 = warp >> a.wpt_shift;
     const int my_tiles = j0 < NT ? (NT - j0 + tiles_per_pass - 1) >> (4 - a.wpt_shift) : 0;
@@ -199,13 +277,13 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                 if (r < Mq) {
                     const int own = r >> a.tok_shift, rl = r & (tok - 1);
                     const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * N + col) * 4);
-                    st_cluster_f2(map_rank(la, (unsigned)own), acc[uu][2 * h], acc[uu][2 * h + 1]);
+                    st_async_f2(map_rank(la, (unsigned)own), acc[uu][2 * h], acc[uu][2 * h + 1], owner_bar[h]);
                 }
             }
         }
     }
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // barrier 1
-    // ---- MXFP8 of the x slice while the other CTAs finish (one lane quad per 32-block)
+    MR_TRACE_WARP(a.trace, 1);
+    // ---- MXFP8 of the x slice while the partials travel (one lane quad per 32-block)
     if (a.q != nullptr) {
         const int nvec = Mq * vpr;
         const int64_t K32 = K / 32;
@@ -222,21 +300,34 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
         }
     }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    MR_TRACE_WARP(a.trace, 2);
+    // a CTA that owns no rows is done: nothing is ever sent to it
+    if (my_rows == 0) return;
+    if (!cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
     MR_TRACE_STAMP(a.trace, 2);
 
     // ---- owner: fixed-order split-K sum -> logits (kept in shared memory)
+    //      and, for the gate, the selection composites
     const float* recv = reinterpret_cast<const float*>(sm + a.off_recv);
     float* rowbuf = reinterpret_cast<float*>(sm + a.off_row);
-    const int nslots = a.cs * wpt;
-    const int my_rows = max(0, min(tok, Mq - c * tok));
+    unsigned long long* comp = reinterpret_cast<unsigned long long*>(sm + a.off_key);
     const int grow = row0 + c * tok;  // global index of this CTA's first row
-    for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
+    for (int idx = tid, it = 0; idx < my_rows * N; idx += kRouteThreads, ++it) {
         const float* pp = recv + idx;
         float sum = 0.0f;
         for (int sl = 0; sl < nslots; ++sl) sum = __fadd_rn(sum, pp[(int64_t)sl * tok * N]);
         rowbuf[idx] = sum;
+        if (a.mode == 1) {
+            const int n = idx - fdiv(idx, a.mag_n) * N;
+            float sel = sum;
+            if (a.scoring == 1) {
+                const float b = a.bias == nullptr ? 0.0f : it == 0 ? bpre0 : it == 1 ? bpre1 : __ldg(a.bias + n);
+                sel = __fadd_rn(sigmoid_score(sum), b);
+            }
+            comp[idx] = composite(ordered_key(sel), n);
+        }
     }
+    MR_TRACE_WARP(a.trace, 3);
     if (a.mode == 0) {
         for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) a.logits[(int64_t)grow * N + idx] = rowbuf[idx];
         return;  // nothing else reads this CTA's shared memory
@@ -244,85 +335,78 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     __syncthreads();
     MR_TRACE_STAMP(a.trace, 3);
 
-    // ---- gate by ranks: a key's rank is the number of keys that beat it.
-    //      Stage 1 ranks inside 128-expert segments; the k best of every
-    //      segment become candidates; stage 2 ranks the candidates.
-    const int k = a.topk, G = a.gwarps, GK = G * k;
-    unsigned long long* ccomp = reinterpret_cast<unsigned long long*>(sm + a.off_cand);
-    float* cval = reinterpret_cast<float*>(ccomp + tok * GK);
-    int* oid = reinterpret_cast<int*>(cval + tok * GK);
+    // ---- gate: one warp per owned row, no CTA barrier.  Selection order is
+    //      the 64-bit composite (key, ~id): unique, larger first.  Lane l
+    //      owns experts l, l + 32, ...; the lane maxima come from disjoint
+    //      sets, so the k-th largest of them, thr, is at most the k-th largest
+    //      key: every top-k key is >= thr.  The keys >= thr (candidates) are
+    //      ranked among themselves; a candidate's rank is the number of
+    //      candidates that beat it.
+    unsigned long long* ccand = reinterpret_cast<unsigned long long*>(sm + a.off_cand);
+    int* oid = reinterpret_cast<int*>(ccand + tok * N);
     float* oval = reinterpret_cast<float*>(oid + tok * k);
-    unsigned long long* comp = reinterpret_cast<unsigned long long*>(sm + a.off_key);
-    for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
-        const int n = idx - fdiv(idx, a.mag_n) * N;
-        float sel = rowbuf[idx];
-        if (a.scoring == 1) sel = __fadd_rn(sigmoid_score(sel), a.bias ? __ldg(a.bias + n) : 0.0f);
-        comp[idx] = composite(ordered_key(sel), n);
-    }
-    for (int idx = tid; idx < my_rows * GK; idx += kRouteThreads) ccomp[idx] = 0ull;  // segments shorter than k
-    __syncthreads();
-    // TPK adjacent lanes share a key's count; part p reads the 16-byte pairs
-    // p, p + TPK, p + 2 TPK, ... of the segment, so the lanes of one key hit
-    // consecutive banks and lanes of different keys read the same addresses
-    int tpk_shift = 0;
-    while (tpk_shift < 3 && (2 << tpk_shift) * my_rows * N <= kRouteThreads) ++tpk_shift;
-    const int tpk = 1 << tpk_shift;
-    for (int base = warp * 32; base < my_rows * N * tpk; base += kRouteThreads) {
-        const int item = base + lane;
-        const bool on = item < my_rows * N * tpk;
-        const int key_idx = item >> tpk_shift, part = item & (tpk - 1);
-        const int rl = fdiv(key_idx, a.mag_n), n = key_idx - rl * N, sg = n >> 7;
-        const unsigned long long* cr = comp + rl * N;
-        const unsigned long long cn = on ? cr[n] : ~0ull;
-        const int lo = sg << 7, hi = on ? min(N, lo + 128) : lo;
-        int rank = 0;
-        for (int j = lo + 2 * part; j < hi; j += 2 * tpk) {
-            const ulonglong2 q2 = *reinterpret_cast<const ulonglong2*>(cr + j);  // N % 8 == 0: aligned, in range
-            rank += (int)(q2.x > cn) + (int)(q2.y > cn);
-        }
-        for (int o = 1; o < tpk; o <<= 1) rank += __shfl_xor_sync(kFull, rank, o);
-        if (on && part == 0 && rank < k) {
-            if (G == 1) {
-                oid[rl * k + rank] = n;
-                oval[rl * k + rank] = rowbuf[key_idx];
-            } else {
-                const int o = rl * GK + sg * k + rank;
-                ccomp[o] = cn;
-                cval[o] = rowbuf[key_idx];
-            }
-        }
-    }
-    __syncthreads();
-    if (G > 1) {
-        for (int idx = tid; idx < my_rows * GK; idx += kRouteThreads) {
-            const int rl = fdiv(idx, a.mag_gk);
-            const unsigned long long cn = ccomp[idx];
-            if (cn == 0ull) continue;
-            const unsigned long long* cr = ccomp + rl * GK;
-            int rank = 0;
-            for (int j = 0; j < GK; ++j) rank += (int)(cr[j] > cn);
-            if (rank < k) {
-                oid[rl * k + rank] = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
-                oval[rl * k + rank] = cval[idx];
-            }
-        }
-        __syncthreads();
-    }
-    MR_TRACE_STAMP(a.trace, 4);
-    // ---- weights; ids to CTA 0 of the cluster (its local rows)
     const uint32_t ids_all_local = smem_u32(sm + a.off_ids);
     int out_id = 0;
     float out_w = 0.0f;
     if (warp < my_rows) {
         const int rl = warp, ml = c * tok + rl;  // row inside the cluster
+        const float* row = rowbuf + rl * N;
+        const unsigned long long* cr = comp + rl * N;
+        unsigned long long* cc = ccand + rl * N;  // 16-byte aligned (N % 8 == 0)
+        unsigned long long lmax = 0ull;           // 0: no key (every composite is > 0)
+        for (int n = lane; n < N; n += 32) {
+            const unsigned long long cn = cr[n];
+            lmax = cn > lmax ? cn : lmax;
+        }
+        int lrank = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) lrank += (int)(__shfl_sync(kFull, lmax, j) > lmax);
+        // at least k lanes hold keys (k <= N, k <= 32): exactly one lane has rank k - 1
+        const int tl = __ffs(__ballot_sync(kFull, lrank == k - 1 && lmax != 0ull)) - 1;
+        const unsigned long long thr = __shfl_sync(kFull, lmax, tl);
+        int cnt = 0;
+        for (int n = lane; n < N; n += 32) cnt += (int)(cr[n] >= thr);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += u;
+        }
+        const int C = __shfl_sync(kFull, incl, 31);
+        int pos = incl - cnt;
+        for (int n = lane; n < N; n += 32) {
+            const unsigned long long cn = cr[n];
+            if (cn >= thr) cc[pos++] = cn;
+        }
+        if (C & 1) cc[C] = 0ull;  // pad to a 16-byte pair (C < N when odd: N is even)
+        __syncwarp();
+        for (int i = lane; i < C; i += 32) {
+            const unsigned long long cn = cc[i];
+            int r0 = 0, r1 = 0;
+            for (int j = 0; j < C; j += 2) {
+                const ulonglong2 q2 = *reinterpret_cast<const ulonglong2*>(cc + j);
+                r0 += (int)(q2.x > cn);
+                r1 += (int)(q2.y > cn);
+            }
+            const int r = r0 + r1;
+            if (r < k) {
+                const int id = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
+                oid[rl * k + r] = id;
+                oval[rl * k + r] = row[id];
+            }
+        }
+        __syncwarp();
+        MR_TRACE_STAMP(a.trace, 4);
+        // ---- weights; ids to CTA 0 of the cluster (its local rows)
         const bool live = lane < k;
         const int id = live ? oid[rl * k + lane] : 0;
         const float val = live ? oval[rl * k + lane] : 0.0f;
-        out_w = gate_weight(a, rowbuf + rl * N, val);
+        out_w = gate_weight(a, row, val);
         out_id = id;
-        if (live) st_cluster_s32(map_rank(ids_all_local + (uint32_t)((ml * k + lane) * 4), 0u), id);
+        if (live)
+            st_async_s32(map_rank(ids_all_local + (uint32_t)((ml * k + lane) * 4), 0u), id, map_rank(bar1, 0u));
     }
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // barrier 2
+    MR_TRACE_WARP(a.trace, 7);
     // global outputs of this CTA's rows while CTA 0 waits for the others
     for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) a.logits[(int64_t)grow * N + idx] = rowbuf[idx];
     if (warp < my_rows && lane < k) {
@@ -330,9 +414,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         a.ids[(int64_t)m * k + lane] = out_id;
         a.weights[(int64_t)m * k + lane] = out_w;
     }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    MR_TRACE_STAMP(a.trace, 5);
+    MR_TRACE_WARP(a.trace, 8);
     if (c != 0) return;
+    if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
+    MR_TRACE_STAMP(a.trace, 5);
+    MR_TRACE_WARP(a.trace, 9);
 
     // ---- sort.  One cluster: CTA 0 holds every id.  Several clusters: each
     //      CTA 0 publishes its rows' ids and takes a ticket; the last one
@@ -359,6 +445,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         atomicOr(m < 32 ? &mlo[ids_all[f]] : &mhi[ids_all[f]], 1u << (m & 31));
     }
     __syncthreads();
+    MR_TRACE_WARP(a.trace, 10);
     // exclusive scan of the padded counts, two experts per thread, one barrier
     const int e0 = 2 * tid, e1 = e0 + 1;
     const int c0 = e0 < N ? __popc(mlo[e0]) + __popc(mhi[e0]) : 0;
@@ -380,6 +467,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         before += w2 < warp ? wt : 0;
         total += wt;
     }
+    MR_TRACE_WARP(a.trace, 11);
     const int s0 = before + incl - local;
     if (e0 < N) start[e0] = s0;
     if (e1 < N) start[e1] = s0 + v0;
@@ -400,6 +488,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             a.expert_ids[bb] = e1;
     for (int bb = fdiv(total, a.mag_block) + tid, be = fdiv(cap, a.mag_block); bb < be; bb += kRouteThreads)
         a.expert_ids[bb] = -1;
+    MR_TRACE_WARP(a.trace, 12);
     __syncthreads();  // orders the sentinel stores before the real entries below
     for (int f = tid; f < MK; f += kRouteThreads) {
         const int e = ids_all[f], m = fdiv(f, a.mag_k);
@@ -407,11 +496,25 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                                       : __popc(mlo[e]) + __popc(mhi[e] & ((1u << (m - 32)) - 1u));
         a.sorted[start[e] + (int)below] = f;
     }
+    MR_TRACE_WARP(a.trace, 13);
+#ifdef MR_TRACE
+    if (tid == 0 && a.trace) a.trace[blockIdx.x * 256 + 25] = clock64();
+#endif
     if (tid == 0) *a.ntpp = total;
     MR_TRACE_STAMP(a.trace, 7);
 }
 
 // ------------------------------------------------------------------ host
+
+int route_device_error(int clear) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_route_timeout, sizeof(int)) != cudaSuccess) return -1;
+    if (clear && v != 0) {
+        const int z = 0;
+        if (cudaMemcpyToSymbol(g_route_timeout, &z, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
 static int g_attr_done[64][2];  // per device and instantiation

@@ -38,13 +38,14 @@ struct RouteArgs {
     int wpt;         // k-parts per 8-expert tile
     int units;       // (tile, part) units per CTA
     int tok;         // token rows owned per CTA
-    int gwarps;      // gate warps per row (128-expert segments)
     int xpitch;      // bytes per x row in shared memory
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
     int tok_shift, wpt_shift;  // log2 of tok and wpt (both powers of two)
     // q = (x * magic) >> 32 equals x / d for 0 <= x < 2^21, d <= 1024
-    unsigned long long mag_n, mag_k, mag_block, mag_vpr, mag_gk;
+    unsigned long long mag_n, mag_k, mag_block, mag_vpr;
     unsigned long long* trace;
+    int flags;                   // launch flags (bit 1: test stall, see moe_route.h)
+    unsigned long long wait_ns;  // limit of every wait for bytes from other CTAs
     int32_t* ids_scratch;   // clusters > 1: every token's ids, gathered for the sort
     unsigned* counter;      // clusters > 1: last-arriver ticket, zero between launches
 };
@@ -61,7 +62,7 @@ inline int ilog2_exact(int v) {
 }
 
 struct RoutePlan {
-    int cs, kc, spw, wpt, units, tok, gwarps, xpitch, clusters;
+    int cs, kc, spw, wpt, units, tok, xpitch, clusters;
     bool half;
     int smem;
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
@@ -98,7 +99,6 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     const int Mc = M < kRouteRowsPerCluster ? M : kRouteRowsPerCluster;
     q.tok = 1;
     while (q.tok * cs < Mc) q.tok *= 2;
-    q.gwarps = (N + 127) / 128;  // 128-expert segments of the gate
     if (mode == 1 && (topk < 1 || topk > 32 || topk > N || q.tok > kRouteWarps)) return false;
     if (ilog2_exact(q.tok) < 0 || ilog2_exact(w) < 0 || ilog2_exact(cs) < 0) return false;
     q.half = M <= 8;
@@ -112,8 +112,8 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     off = align_up(off + q.tok * N * 4, 16);
     q.off_key = off;  // 64-bit selection composites
     off = align_up(off + (mode == 1 ? q.tok * N : 0) * 8, 16);
-    q.off_cand = off;  // per row: G*k composites, G*k values, k ids, k values
-    off = align_up(off + (mode == 1 ? q.tok * (q.gwarps * topk * 12 + topk * 8) : 0), 16);
+    q.off_cand = off;  // per row: N candidate composites, k ids, k values
+    off = align_up(off + (mode == 1 ? q.tok * (N * 8 + topk * 8) : 0), 16);
     q.off_ids = off;  // every token's ids in the CTA that sorts
     off = align_up(off + M * (mode == 1 ? topk : 0) * 4, 16);
     q.off_mask = off;

@@ -69,7 +69,8 @@ typedef enum mr_status {
     MR_ERR_UNSUPPORTED = 1,      /* shape / layout outside the kernels' cover  */
     MR_ERR_INVALID_ARG = 2,      /* null or misaligned pointer, bad size       */
     MR_ERR_SCRATCH_TOO_SMALL = 3,/* scratch_bytes below what the call needs    */
-    MR_ERR_CUDA = 4              /* the CUDA runtime reported an error         */
+    MR_ERR_CUDA = 4,             /* the CUDA runtime reported an error         */
+    MR_ERR_TIMEOUT = 5           /* mr_device_error: a bounded wait ran out    */
 } mr_status;
 
 typedef enum mr_scoring {
@@ -78,7 +79,8 @@ typedef enum mr_scoring {
 } mr_scoring;
 
 /* Launch options, process-wide (bits for mr_set_launch_flags). */
-#define MR_LAUNCH_PDL 1  /* programmatic dependent launch, see below */
+#define MR_LAUNCH_PDL 1         /* programmatic dependent launch, see below */
+#define MR_LAUNCH_TEST_STALL 2  /* test hook for the timeout path, see below */
 
 /*
  * Sets the launch options of every later call in this process; returns
@@ -92,6 +94,26 @@ typedef enum mr_scoring {
  */
 int mr_set_launch_flags(int flags);
 int mr_get_launch_flags(void);
+
+/*
+ * Bounded waits.  The router GEMV for M <= 64 and the one-launch route hand
+ * data between the CTAs of a thread-block cluster (split-K partials to the
+ * CTA that owns a token, chosen ids to the CTA that sorts).  Each receiving
+ * CTA waits for the bytes it expects at most the wait limit (default 1 s).
+ * When a wait runs out the kernel sets a device-side flag and returns early;
+ * the outputs of that call are undefined, and after a call with M > 16 the
+ * scratch counters must be zeroed again (mr_scratch_reset).
+ * mr_set_wait_limit_ns: 1e3 <= ns <= 6e10, else MR_ERR_INVALID_ARG;
+ * process-wide, for later calls.
+ * mr_device_error: MR_ERR_TIMEOUT if a wait ran out on the current device
+ * since the flag was last cleared, else MR_OK (MR_ERR_CUDA if the flag could
+ * not be read); clear != 0 also clears it.  Synchronous: call it after the
+ * routing calls' streams have finished.
+ * MR_LAUNCH_TEST_STALL (a test of this path, never for production): every
+ * receiving CTA expects 16 bytes more than are sent, so its wait runs out.
+ */
+int mr_set_wait_limit_ns(uint64_t ns);
+int mr_device_error(int clear);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mr_status_string(int status);

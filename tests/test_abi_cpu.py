@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.mr_abi_version() == 1
-    for s in range(5):
+    for s in range(6):
         assert lib.mr_status_string(s).startswith(b"MR_")
     assert lib.mr_status_string(99) == b"unknown mr_status"
 
@@ -117,6 +117,11 @@ def test_validation_returns_before_any_launch(lib):
     assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 17, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
                                        fake, fake, fake, 1 << 20, fake, fake, fake, 32768 + 17 * 8 * 4 - 4,
                                        None) == mr.MR_ERR_SCRATCH_TOO_SMALL
+    # launch options and the wait limit (host-only settings)
+    assert lib.mr_set_launch_flags(4) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_set_wait_limit_ns(999) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_set_wait_limit_ns(60_000_000_001) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_set_wait_limit_ns(1_000_000_000) == mr.MR_OK
     # reset: buffer below the counter prefix
     assert lib.mr_scratch_reset(fake, 100, None) == mr.MR_ERR_INVALID_ARG
 

@@ -71,13 +71,27 @@ def test_fused_without_quant(mr):
     check_gate(host(out["logits"]), host(out["topk_ids"]), host(out["topk_weights"]), 8, "softmax")
 
 
-@pytest.mark.parametrize("M,chain", [(2, "fused"), (4, "fused"), (8, "fused"), (16, "fused"), (32, "fused"),
-                                     (64, "fused"), (32, "four calls"), (64, "four calls")])
-def test_1000_launches_reuse_one_scratch(mr, M, chain):
+@pytest.mark.parametrize("M,chain,pdl", [(2, "fused", 0), (4, "fused", 0), (8, "fused", 0), (16, "fused", 0),
+                                         (32, "fused", 0), (64, "fused", 0), (32, "four calls", 0),
+                                         (64, "four calls", 0), (4, "fused", 1), (17, "fused", 1),
+                                         (64, "fused", 1), (64, "four calls", 1)])
+def test_1000_launches_reuse_one_scratch(mr, M, chain, pdl):
     """Config 2: 1000 back-to-back launches on one scratch/counter buffer
-    (the one-launch route, and the four separate calls); every launch's
-    outputs land in a ring and each is checked against the reference outputs
-    of its input variant."""
+    (the one-launch route, and the four separate calls), in plain stream
+    order and with programmatic dependent launch (each kernel starting while
+    the previous one runs); every launch's outputs land in a ring and each is
+    checked against the reference outputs of its input variant."""
+    import torch
+    flags = mr.get_launch_flags()
+    mr.set_launch_flags(mr.LAUNCH_PDL if pdl else 0)
+    try:
+        _run_1000(mr, M, chain)
+    finally:
+        mr.set_launch_flags(flags)
+    assert mr.device_error() == mr.MR_OK
+
+
+def _run_1000(mr, M, chain):
     import torch
     c = inputs.CONFIGS[2]
     K, N, k, B = c["K"], c["N"], c["topk"], c["block"]
@@ -123,3 +137,36 @@ def test_1000_launches_reuse_one_scratch(mr, M, chain):
         check_sort(host(first["topk_ids"]), N, B, host(first["sorted_token_ids"]),
                    host(first["expert_ids"]), host(first["num_tokens_post_padded"]))
         check_quant(xs[v], host(first["q"]), host(first["scale"]))
+
+
+def test_bounded_wait_runs_out_and_reports(mr):
+    """The cluster kernels' waits for bytes from other CTAs are bounded: with
+    the test hook every receiving CTA expects 16 bytes that never come, so
+    each wait ends at the limit, the device flag is set, and the context
+    stays usable (a normal call afterwards is exact)."""
+    import torch
+    c = inputs.CONFIGS[2]
+    x, w = inputs.router_inputs(4, c["K"], c["N"], 2)
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    torch.cuda.synchronize()
+    assert mr.device_error() == mr.MR_OK  # no earlier call ran out
+    flags = mr.get_launch_flags()
+    mr.set_wait_limit_ns(20_000_000)
+    mr.set_launch_flags(flags | mr.LAUNCH_TEST_STALL)
+    try:
+        mr.moe_route_sort_quant(xd, wd, c["topk"], c["block"])
+        mr.router_gemv(xd, wd)
+        torch.cuda.synchronize()
+    finally:
+        mr.set_launch_flags(flags)
+        mr.set_wait_limit_ns(1_000_000_000)
+    assert mr.device_error(clear=True) == mr.MR_ERR_TIMEOUT
+    assert mr.device_error() == mr.MR_OK
+    out = mr.moe_route_sort_quant(xd, wd, c["topk"], c["block"])
+    lh = host(out["logits"])
+    assert_logits_close(lh, oracle.router_gemv(x, w))
+    check_gate(lh, host(out["topk_ids"]), host(out["topk_weights"]), c["topk"], c["scoring"], None)
+    check_sort(host(out["topk_ids"]), c["N"], c["block"], host(out["sorted_token_ids"]),
+               host(out["expert_ids"]), host(out["num_tokens_post_padded"]))
+    torch.cuda.synchronize()
+    assert mr.device_error() == mr.MR_OK
