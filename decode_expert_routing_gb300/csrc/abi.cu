@@ -283,6 +283,14 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
     a.q = q;
     a.scale = scale;
     a.topk = topk;
+    {  // gate threshold lane groups: the largest power of two <= 32 threads
+       // leaving at least topk groups that hold experts (thread t: experts t
+       // and t + 512)
+        const int lanes = N < 512 ? N : 512;
+        int gsh = 5;
+        while (gsh > 0 && (lanes + (1 << gsh) - 1) >> gsh < topk) --gsh;
+        a.gs_shift = gsh;
+    }
     a.block = block;
     a.mag_k = mr::div_magic(topk);
     a.mag_block = mr::div_magic(block);

@@ -62,16 +62,17 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
     return *s_slot;
 }
 
-// Optional phase stamps (compile with -DMR_TRACE), %globaltimer in ns, 256
-// u64 per CTA at trace + (blockIdx.y * gridDim.x + blockIdx.x) * 256:
+// Optional phase stamps (compile with -DMR_TRACE), 512 u64 per CTA at
+// trace + (blockIdx.y * gridDim.x + blockIdx.x) * 512.  %globaltimer (ns):
 // MR_TRACE_STAMP: thread 0 writes slot (< 32); MR_TRACE_WARP: lane 0 of every
 // warp writes slot 32 + 16 * phase + warp (phase < 14, 16 warps at most).
+// %clock64 (SM cycles): MR_TRACE_CLK: thread 0 writes slot 256 + slot.
 #ifdef MR_TRACE
 #define MR_TRACE_AT(trace, slot)                                                     \
     do {                                                                             \
         unsigned long long t_;                                                       \
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                       \
-        (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 256 + (slot)] = t_;          \
+        (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 512 + (slot)] = t_;          \
     } while (0)
 #define MR_TRACE_STAMP(trace, slot)                                                  \
     do {                                                                             \
@@ -82,7 +83,15 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
         if ((threadIdx.x & 31) == 0 && (trace) != nullptr)                           \
             MR_TRACE_AT(trace, 32 + 16 * (phase) + (threadIdx.x >> 5));              \
     } while (0)
+#define MR_TRACE_CLK(trace, slot)                                                    \
+    do {                                                                             \
+        if (threadIdx.x == 0 && (trace) != nullptr)                                  \
+            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 512 + 256 + (slot)] = clock64(); \
+    } while (0)
 #else
+#define MR_TRACE_CLK(trace, slot) \
+    do {                          \
+    } while (0)
 #define MR_TRACE_STAMP(trace, slot) \
     do {                            \
     } while (0)

@@ -175,12 +175,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     __shared__ __align__(8) unsigned long long s_bar[2];  // [0] partial logits in, [1] ids in (CTA 0)
     __shared__ int s_ok[2];
     __shared__ unsigned s_ticket;
+    __shared__ __align__(16) unsigned s_wmin[kRouteWarps];  // gate: per warp, smallest group maximum
+    __shared__ int s_ccount;                                  // gate: candidates so far
+    __shared__ __align__(16) int s_wtot[2 * kRouteWarps];     // sort: blocks per warp (experts t, t + 512)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int c = (int)cluster_rank();
     MR_TRACE_STAMP(a.trace, 0);
 #ifdef MR_TRACE
-    if (tid == 0 && a.trace) a.trace[blockIdx.x * 256 + 24] = clock64();
+    if (tid == 0 && a.trace) a.trace[blockIdx.x * 512 + 24] = clock64();
 #endif
     // this cluster's token rows: [row0, row0 + Mq); this CTA owns rows
     // [c * tok, c * tok + my_rows) of them
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int my_rows = max(0, min(tok, Mq - c * tok));
     const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]);
     if (tid == 0) {
+        s_ccount = 0;
         mbar_init(bar0, 1);
         mbar_init(bar1, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -200,6 +204,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     }
     cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM access
     pdl_trigger();
+    {   // Every launch gets a fresh copy of its parameters in constant memory:
+        // touch each 32-byte line of it now, so that no later phase stalls on
+        // a first-use miss.
+        const unsigned long long acc =
+            (unsigned long long)a.x ^ (unsigned long long)a.logits ^ (unsigned long long)a.expert_ids ^
+            (unsigned long long)a.scale ^ (unsigned long long)a.renormalize ^ (unsigned long long)a.units ^
+            (unsigned long long)a.off_ids ^ a.mag_n ^ (unsigned long long)a.trace ^ (unsigned long long)a.counter;
+        asm volatile("" ::"l"(acc));
+    }
     const int64_t kslice = (int64_t)c * a.kc;
     const uint16_t* xq = a.x + (int64_t)row0 * a.ldx;
     unsigned long long* mask = reinterpret_cast<unsigned long long*>(sm + a.off_mask);
@@ -209,15 +222,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      precede the wait
     uint4 wv[kRouteBatch][kRouteSpwMax];
     load_w_batch(a, kslice, warp, g, t, 0, wv);
-    float bpre0 = 0.0f, bpre1 = 0.0f;  // bias of the first two owner-sum items of this thread
+    float bpre0 = 0.0f, bpre1 = 0.0f;  // selection bias of this thread's experts t and t + 512
     if (a.bias != nullptr) {
-        const int i0 = tid, i1 = tid + kRouteThreads;
-        if (i0 < my_rows * N) bpre0 = __ldg(a.bias + (i0 - fdiv(i0, a.mag_n) * N));
-        if (i1 < my_rows * N) bpre1 = __ldg(a.bias + (i1 - fdiv(i1, a.mag_n) * N));
+        if (tid < N) bpre0 = __ldg(a.bias + tid);
+        if (tid + kRouteThreads < N) bpre1 = __ldg(a.bias + tid + kRouteThreads);
     }
     if (a.mode == 1 && c == 0)
         for (int e = tid; e < N; e += kRouteThreads) mask[e] = 0ull;  // token bitmasks (2 x 32 bits per expert)
     pdl_wait();
+    MR_TRACE_STAMP(a.trace, 8);
 
     // ---- this CTA's x slice -> shared memory
     unsigned char* xs = sm + a.off_x;
@@ -300,120 +313,154 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
         }
     }
+    // sentinels in every slot of sorted_token_ids and -1 in every block of
+    // expert_ids, early: the sort later overwrites the real entries.  The
+    // CTA that sorts is ordered after these stores (same CTA, or through the
+    // clusters' ticket).
+    if (a.mode == 1 && blockIdx.x == 0) {
+        const int MKall = a.M * k, cap = (int)a.capacity;  // < 2^31, checked on the host
+        if ((reinterpret_cast<uintptr_t>(a.sorted) & 15u) == 0) {
+            int4* st4 = reinterpret_cast<int4*>(a.sorted);
+            const int n4 = cap >> 2;
+            for (int i = tid; i < n4; i += kRouteThreads) st4[i] = make_int4(MKall, MKall, MKall, MKall);
+            for (int i = (n4 << 2) + tid; i < cap; i += kRouteThreads) a.sorted[i] = MKall;
+        } else {
+            for (int i = tid; i < cap; i += kRouteThreads) a.sorted[i] = MKall;
+        }
+        for (int bb = tid, be = cap / a.block; bb < be; bb += kRouteThreads) a.expert_ids[bb] = -1;
+    }
     MR_TRACE_WARP(a.trace, 2);
     // a CTA that owns no rows is done: nothing is ever sent to it
     if (my_rows == 0) return;
     if (!cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
+    MR_TRACE_CLK(a.trace, 0);
     MR_TRACE_STAMP(a.trace, 2);
 
-    // ---- owner: fixed-order split-K sum -> logits (kept in shared memory)
-    //      and, for the gate, the selection composites
+    // ---- per owned row: split-K sum, logits, gate.
+    //      Owner sum: thread t sums expert t (and t + 512) over the split-K
+    //      slots in a fixed order (the GEMV-only mode runs the same code).
+    //      Gate: selection order is the 64-bit composite (key, ~id): unique,
+    //      larger first.  Lane groups of GL = 2^gs_shift <= 32 threads hold
+    //      disjoint expert sets, G >= k of them hold experts; T, the smallest
+    //      group maximum key, has at least G >= k keys at or above it, so
+    //      every top-k expert has key >= T.  The experts with key >= T
+    //      (candidates) are ranked among themselves: a candidate's rank is
+    //      the number of candidates that beat it.  The winners' ids go out at
+    //      once (to CTA 0 for the sort, and to HBM).
     const float* recv = reinterpret_cast<const float*>(sm + a.off_recv);
     float* rowbuf = reinterpret_cast<float*>(sm + a.off_row);
-    unsigned long long* comp = reinterpret_cast<unsigned long long*>(sm + a.off_key);
+    unsigned long long* ccand = reinterpret_cast<unsigned long long*>(sm + a.off_cand);
+    float* oval = reinterpret_cast<float*>(ccand + N);
     const int grow = row0 + c * tok;  // global index of this CTA's first row
-    for (int idx = tid, it = 0; idx < my_rows * N; idx += kRouteThreads, ++it) {
-        const float* pp = recv + idx;
-        float sum = 0.0f;
-        for (int sl = 0; sl < nslots; ++sl) sum = __fadd_rn(sum, pp[(int64_t)sl * tok * N]);
-        rowbuf[idx] = sum;
-        if (a.mode == 1) {
-            const int n = idx - fdiv(idx, a.mag_n) * N;
-            float sel = sum;
-            if (a.scoring == 1) {
-                const float b = a.bias == nullptr ? 0.0f : it == 0 ? bpre0 : it == 1 ? bpre1 : __ldg(a.bias + n);
-                sel = __fadd_rn(sigmoid_score(sum), b);
+    const int plane = tok * N;        // floats between two slots of the receive buffer
+    const int n0 = tid, n1 = tid + kRouteThreads;
+    const bool h0 = n0 < N, h1 = n1 < N;
+    const int gl = 1 << a.gs_shift;
+    const unsigned gmask = gl == 32 ? kFull : ((1u << gl) - 1u) << (lane & ~(gl - 1));
+    const bool group_has = (tid & ~(gl - 1)) < N;  // the lane group's first expert exists
+    for (int rl = 0; rl < my_rows; ++rl) {
+        float sum0 = 0.0f, sum1 = 0.0f;
+        if (h0) {
+            const float* pp = recv + rl * N + n0;
+            for (int sl = 0; sl < nslots; sl += 8) {  // nslots % 8 == 0; loads first, then the adds in order
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = pp[(sl + u) * plane];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) sum0 = __fadd_rn(sum0, v[u]);
             }
-            comp[idx] = composite(ordered_key(sel), n);
         }
+        if (h1) {
+            const float* pp = recv + rl * N + n1;
+            for (int sl = 0; sl < nslots; sl += 8) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = pp[(sl + u) * plane];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) sum1 = __fadd_rn(sum1, v[u]);
+            }
+        }
+        const int64_t lrow = (int64_t)(grow + rl) * N;
+        if (h0) {
+            rowbuf[rl * N + n0] = sum0;
+            a.logits[lrow + n0] = sum0;
+        }
+        if (h1) {
+            rowbuf[rl * N + n1] = sum1;
+            a.logits[lrow + n1] = sum1;
+        }
+        if (a.mode == 0) continue;
+        float sel0 = sum0, sel1 = sum1;
+        if (a.scoring == 1) {
+            sel0 = __fadd_rn(sigmoid_score(sum0), bpre0);
+            sel1 = __fadd_rn(sigmoid_score(sum1), bpre1);
+        }
+        const unsigned long long c0 = h0 ? composite(ordered_key(sel0), n0) : 0ull;
+        const unsigned long long c1 = h1 ? composite(ordered_key(sel1), n1) : 0ull;
+        const unsigned k0 = (unsigned)(c0 >> 32), k1 = (unsigned)(c1 >> 32);
+        // the warp's smallest maximum over its groups that hold experts
+        const unsigned gmax = __reduce_max_sync(gmask, max(k0, k1));
+        const unsigned wx = __reduce_min_sync(kFull, group_has ? gmax : 0xFFFFFFFFu);
+        if (lane == 0) s_wmin[warp] = wx;
+        MR_TRACE_CLK(a.trace, 1);
+        __syncthreads();  // s_wmin; rowbuf of this row
+        MR_TRACE_CLK(a.trace, 3);
+        const unsigned T = __reduce_min_sync(kFull, lane < kRouteWarps ? s_wmin[lane] : 0xFFFFFFFFu);
+        MR_TRACE_CLK(a.trace, 4);
+        const bool p0 = h0 && k0 >= T, p1 = h1 && k1 >= T;
+        const unsigned b0 = __ballot_sync(kFull, p0), b1 = __ballot_sync(kFull, p1);
+        const int wc = __popc(b0) + __popc(b1);
+        int base = 0;
+        if (lane == 0 && wc != 0) base = atomicAdd(&s_ccount, wc);
+        base = __shfl_sync(kFull, base, 0);
+        const unsigned lt = (1u << lane) - 1u;
+        if (p0) ccand[base + __popc(b0 & lt)] = c0;
+        if (p1) ccand[base + __popc(b0) + __popc(b1 & lt)] = c1;
+        __syncthreads();
+        MR_TRACE_CLK(a.trace, 5);
+        // PR adjacent lanes per candidate, each counting the beaters among
+        // candidates part, part + PR, ...; a segmented reduction adds them
+        const int C = s_ccount;
+        int prs = 5;
+        while (prs > 0 && (C << prs) > kRouteThreads) --prs;
+        const int PR = 1 << prs;
+        const unsigned pmask = PR == 32 ? kFull : ((1u << PR) - 1u) << (lane & ~(PR - 1));
+        const int ml = c * tok + rl, m = grow + rl;
+        for (int base2 = warp * 32; base2 < (C << prs); base2 += kRouteThreads) {
+            const int item = base2 + lane, ci = item >> prs, part = item & (PR - 1);
+            if (ci < C) {  // whole segments of PR lanes
+                const unsigned long long cn = ccand[ci];
+                int r = 0;
+                for (int j = part; j < C; j += PR) r += (int)(ccand[j] > cn);
+                r = (int)__reduce_add_sync(pmask, (unsigned)r);
+                if (part == 0 && r < k) {
+                    const int id = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
+                    st_async_s32(map_rank(smem_u32(sm + a.off_ids) + (uint32_t)((ml * k + r) * 4), 0u), id,
+                                 map_rank(bar1, 0u));
+                    a.ids[(int64_t)m * k + r] = id;
+                    oval[rl * k + r] = rowbuf[rl * N + id];
+                }
+            }
+        }
+        __syncthreads();  // oval complete; every thread has read s_ccount
+        if (tid == 0) s_ccount = 0;  // before the next row's second barrier
     }
     MR_TRACE_WARP(a.trace, 3);
-    if (a.mode == 0) {
-        for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) a.logits[(int64_t)grow * N + idx] = rowbuf[idx];
-        return;  // nothing else reads this CTA's shared memory
-    }
-    __syncthreads();
-    MR_TRACE_STAMP(a.trace, 3);
-
-    // ---- gate: one warp per owned row, no CTA barrier.  Selection order is
-    //      the 64-bit composite (key, ~id): unique, larger first.  Lane l
-    //      owns experts l, l + 32, ...; the lane maxima come from disjoint
-    //      sets, so the k-th largest of them, thr, is at most the k-th largest
-    //      key: every top-k key is >= thr.  The keys >= thr (candidates) are
-    //      ranked among themselves; a candidate's rank is the number of
-    //      candidates that beat it.
-    unsigned long long* ccand = reinterpret_cast<unsigned long long*>(sm + a.off_cand);
-    int* oid = reinterpret_cast<int*>(ccand + tok * N);
-    float* oval = reinterpret_cast<float*>(oid + tok * k);
-    const uint32_t ids_all_local = smem_u32(sm + a.off_ids);
-    int out_id = 0;
-    float out_w = 0.0f;
-    if (warp < my_rows) {
-        const int rl = warp, ml = c * tok + rl;  // row inside the cluster
-        const float* row = rowbuf + rl * N;
-        const unsigned long long* cr = comp + rl * N;
-        unsigned long long* cc = ccand + rl * N;  // 16-byte aligned (N % 8 == 0)
-        unsigned long long lmax = 0ull;           // 0: no key (every composite is > 0)
-        for (int n = lane; n < N; n += 32) {
-            const unsigned long long cn = cr[n];
-            lmax = cn > lmax ? cn : lmax;
-        }
-        int lrank = 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) lrank += (int)(__shfl_sync(kFull, lmax, j) > lmax);
-        // at least k lanes hold keys (k <= N, k <= 32): exactly one lane has rank k - 1
-        const int tl = __ffs(__ballot_sync(kFull, lrank == k - 1 && lmax != 0ull)) - 1;
-        const unsigned long long thr = __shfl_sync(kFull, lmax, tl);
-        int cnt = 0;
-        for (int n = lane; n < N; n += 32) cnt += (int)(cr[n] >= thr);
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += u;
-        }
-        const int C = __shfl_sync(kFull, incl, 31);
-        int pos = incl - cnt;
-        for (int n = lane; n < N; n += 32) {
-            const unsigned long long cn = cr[n];
-            if (cn >= thr) cc[pos++] = cn;
-        }
-        if (C & 1) cc[C] = 0ull;  // pad to a 16-byte pair (C < N when odd: N is even)
-        __syncwarp();
-        for (int i = lane; i < C; i += 32) {
-            const unsigned long long cn = cc[i];
-            int r0 = 0, r1 = 0;
-            for (int j = 0; j < C; j += 2) {
-                const ulonglong2 q2 = *reinterpret_cast<const ulonglong2*>(cc + j);
-                r0 += (int)(q2.x > cn);
-                r1 += (int)(q2.y > cn);
-            }
-            const int r = r0 + r1;
-            if (r < k) {
-                const int id = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
-                oid[rl * k + r] = id;
-                oval[rl * k + r] = row[id];
-            }
-        }
-        __syncwarp();
-        MR_TRACE_STAMP(a.trace, 4);
-        // ---- weights; ids to CTA 0 of the cluster (its local rows)
+    if (a.mode == 0) return;  // nothing else reads this CTA's shared memory
+    MR_TRACE_STAMP(a.trace, 4);
+    MR_TRACE_CLK(a.trace, 9);
+    // ---- weights, off the path of the ids: the last warps (warp 15: row 0)
+    if (warp >= kRouteWarps - my_rows) {
+        const int rl = kRouteWarps - 1 - warp, m = grow + rl;
         const bool live = lane < k;
-        const int id = live ? oid[rl * k + lane] : 0;
         const float val = live ? oval[rl * k + lane] : 0.0f;
-        out_w = gate_weight(a, row, val);
-        out_id = id;
-        if (live)
-            st_async_s32(map_rank(ids_all_local + (uint32_t)((ml * k + lane) * 4), 0u), id, map_rank(bar1, 0u));
+        const float wgt = gate_weight(a, rowbuf + rl * N, val);
+        MR_TRACE_CLK(a.trace, 10);
+        if (live) a.weights[(int64_t)m * k + lane] = wgt;
     }
+    MR_TRACE_CLK(a.trace, 11);
     MR_TRACE_WARP(a.trace, 7);
-    // global outputs of this CTA's rows while CTA 0 waits for the others
-    for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) a.logits[(int64_t)grow * N + idx] = rowbuf[idx];
-    if (warp < my_rows && lane < k) {
-        const int m = grow + warp;
-        a.ids[(int64_t)m * k + lane] = out_id;
-        a.weights[(int64_t)m * k + lane] = out_w;
-    }
+    MR_TRACE_CLK(a.trace, 12);
     MR_TRACE_WARP(a.trace, 8);
     if (c != 0) return;
     if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
@@ -422,22 +469,24 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
 
     // ---- sort.  One cluster: CTA 0 holds every id.  Several clusters: each
     //      CTA 0 publishes its rows' ids and takes a ticket; the last one
-    //      gathers all ids and sorts.
+    //      gathers all ids and sorts.  The sentinels and the -1 block ids are
+    //      already in place (first CTA of the grid, right after the quant).
     int* ids_all = reinterpret_cast<int*>(sm + a.off_ids);
     const int M = a.M, MK = M * k, B = a.block;
     if (a.clusters > 1) {
         for (int f = tid; f < Mq * k; f += kRouteThreads) a.ids_scratch[row0 * k + f] = ids_all[f];
         const unsigned ticket = cta_ticket(a.counter, &s_ticket);
         if (ticket != (unsigned)(a.clusters - 1)) return;
+        // every row from scratch (this cluster's own ids sit at local offsets)
         for (int f = tid; f < MK; f += kRouteThreads) ids_all[f] = __ldcg(a.ids_scratch + f);
         if (tid == 0) *a.counter = 0u;
         __syncthreads();
     }
     MR_TRACE_STAMP(a.trace, 6);
+    MR_TRACE_CLK(a.trace, 13);
     // rank of (m, j) inside expert e = number of set bits below m in the token
     // mask of e (two 32-bit words: tokens 0-31, 32-63)
     int* start = reinterpret_cast<int*>(sm + a.off_start);
-    int* warp_tot = start + N;
     unsigned* mlo = reinterpret_cast<unsigned*>(mask);
     unsigned* mhi = mlo + N;
     for (int f = tid; f < MK; f += kRouteThreads) {
@@ -445,62 +494,70 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         atomicOr(m < 32 ? &mlo[ids_all[f]] : &mhi[ids_all[f]], 1u << (m & 31));
     }
     __syncthreads();
+    MR_TRACE_CLK(a.trace, 14);
     MR_TRACE_WARP(a.trace, 10);
-    // exclusive scan of the padded counts, two experts per thread, one barrier
-    const int e0 = 2 * tid, e1 = e0 + 1;
-    const int c0 = e0 < N ? __popc(mlo[e0]) + __popc(mhi[e0]) : 0;
-    const int c1 = e1 < N ? __popc(mlo[e1]) + __popc(mhi[e1]) : 0;
-    const int v0 = fdiv(c0 + B - 1, a.mag_block) * B, v1 = fdiv(c1 + B - 1, a.mag_block) * B;
-    const int local = v0 + v1;
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += u;
+    MR_TRACE_CLK(a.trace, 15);
+    // blocks per expert nb = ceil(count / B); thread t: experts t and t + 512.
+    // Exclusive scan over the experts: inside a warp from the ballots of the
+    // bits of nb (nb <= ceil(M / B) < 2^nbits), across warps from the warp
+    // totals; then the block starts and the expert id of every real block
+    // (padding blocks already hold -1).
+    const int e0 = tid, e1 = tid + kRouteThreads;
+    const int nb0 = e0 < N ? fdiv(__popc(mlo[e0]) + __popc(mhi[e0]) + B - 1, a.mag_block) : 0;
+    const int nb1 = e1 < N ? fdiv(__popc(mlo[e1]) + __popc(mhi[e1]) + B - 1, a.mag_block) : 0;
+    const int nbits = 32 - __clz(fdiv(M + B - 1, a.mag_block));
+    const unsigned lt = (1u << lane) - 1u;
+    int pre0 = 0, pre1 = 0, wt0 = 0, wt1 = 0;
+    for (int bit = 0; bit < nbits; ++bit) {
+        const unsigned q0 = __ballot_sync(kFull, (nb0 >> bit) & 1), q1 = __ballot_sync(kFull, (nb1 >> bit) & 1);
+        pre0 += __popc(q0 & lt) << bit;
+        pre1 += __popc(q1 & lt) << bit;
+        wt0 += __popc(q0) << bit;
+        wt1 += __popc(q1) << bit;
     }
-    if (lane == 31) warp_tot[warp] = incl;
+    if (lane == 0) {
+        s_wtot[warp] = wt0;
+        s_wtot[kRouteWarps + warp] = wt1;
+    }
+    MR_TRACE_CLK(a.trace, 16);
     __syncthreads();
-    int before = 0, total = 0;
+    int before0 = 0, tot0 = 0, before1 = 0, tot1 = 0;
 #pragma unroll
-    for (int w2 = 0; w2 < kRouteWarps; ++w2) {
-        const int wt = warp_tot[w2];
-        before += w2 < warp ? wt : 0;
-        total += wt;
+    for (int q = 0; q < kRouteWarps / 4; ++q) {
+        const int4 u = reinterpret_cast<const int4*>(s_wtot)[q];
+        const int4 v = reinterpret_cast<const int4*>(s_wtot + kRouteWarps)[q];
+        const int w0 = 4 * q;
+        before0 += (w0 < warp ? u.x : 0) + (w0 + 1 < warp ? u.y : 0) + (w0 + 2 < warp ? u.z : 0) + (w0 + 3 < warp ? u.w : 0);
+        before1 += (w0 < warp ? v.x : 0) + (w0 + 1 < warp ? v.y : 0) + (w0 + 2 < warp ? v.z : 0) + (w0 + 3 < warp ? v.w : 0);
+        tot0 += (u.x + u.y) + (u.z + u.w);
+        tot1 += (v.x + v.y) + (v.z + v.w);
     }
-    MR_TRACE_WARP(a.trace, 11);
-    const int s0 = before + incl - local;
-    if (e0 < N) start[e0] = s0;
-    if (e1 < N) start[e1] = s0 + v0;
-    // sentinels everywhere (coalesced 16-byte stores), expert ids of every block
-    const int cap = (int)a.capacity;  // < 2^31, checked on the host
-    if ((reinterpret_cast<uintptr_t>(a.sorted) & 15u) == 0) {
-        int4* st4 = reinterpret_cast<int4*>(a.sorted);
-        const int n4 = cap >> 2;
-        for (int i = tid; i < n4; i += kRouteThreads) st4[i] = make_int4(MK, MK, MK, MK);
-        for (int i = (n4 << 2) + tid; i < cap; i += kRouteThreads) a.sorted[i] = MK;
-    } else {
-        for (int i = tid; i < cap; i += kRouteThreads) a.sorted[i] = MK;
+    MR_TRACE_CLK(a.trace, 17);
+    const int sb0 = before0 + pre0, sb1 = tot0 + before1 + pre1;  // first block of e0 / e1
+    if (e0 < N) {
+        start[e0] = sb0 * B;
+        for (int i = 0; i < nb0; ++i) a.expert_ids[sb0 + i] = e0;
     }
-    if (e0 < N)
-        for (int bb = fdiv(s0, a.mag_block), be = fdiv(s0 + v0, a.mag_block); bb < be; ++bb) a.expert_ids[bb] = e0;
-    if (e1 < N)
-        for (int bb = fdiv(s0 + v0, a.mag_block), be = fdiv(s0 + v0 + v1, a.mag_block); bb < be; ++bb)
-            a.expert_ids[bb] = e1;
-    for (int bb = fdiv(total, a.mag_block) + tid, be = fdiv(cap, a.mag_block); bb < be; bb += kRouteThreads)
-        a.expert_ids[bb] = -1;
+    if (e1 < N) {
+        start[e1] = sb1 * B;
+        for (int i = 0; i < nb1; ++i) a.expert_ids[sb1 + i] = e1;
+    }
+    if (tid == 0) *a.ntpp = (tot0 + tot1) * B;
+    MR_TRACE_CLK(a.trace, 19);
     MR_TRACE_WARP(a.trace, 12);
-    __syncthreads();  // orders the sentinel stores before the real entries below
+    __syncthreads();  // start[] complete
+    MR_TRACE_CLK(a.trace, 22);
     for (int f = tid; f < MK; f += kRouteThreads) {
         const int e = ids_all[f], m = fdiv(f, a.mag_k);
         const unsigned below = m < 32 ? __popc(mlo[e] & ((1u << m) - 1u))
                                       : __popc(mlo[e]) + __popc(mhi[e] & ((1u << (m - 32)) - 1u));
         a.sorted[start[e] + (int)below] = f;
     }
+    MR_TRACE_CLK(a.trace, 23);
     MR_TRACE_WARP(a.trace, 13);
 #ifdef MR_TRACE
-    if (tid == 0 && a.trace) a.trace[blockIdx.x * 256 + 25] = clock64();
+    if (tid == 0 && a.trace) a.trace[blockIdx.x * 512 + 25] = clock64();
 #endif
-    if (tid == 0) *a.ntpp = total;
     MR_TRACE_STAMP(a.trace, 7);
 }
 

@@ -41,6 +41,7 @@ struct RouteArgs {
     int xpitch;      // bytes per x row in shared memory
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
     int tok_shift, wpt_shift;  // log2 of tok and wpt (both powers of two)
+    int gs_shift;    // gate threshold: log2 of the lane-group size (<= 32 threads)
     // q = (x * magic) >> 32 equals x / d for 0 <= x < 2^21, d <= 1024
     unsigned long long mag_n, mag_k, mag_block, mag_vpr;
     unsigned long long* trace;
@@ -90,6 +91,7 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
         }
     if (w == 0) return false;
     while (NT * w < kRouteWarps && 2 * w <= kRouteWarps && S % (2 * w) == 0) w *= 2;
+    if ((cs * w) % 8 != 0) return false;  // the owner sums split-K slots in groups of 8
     q.wpt = w;
     q.spw = S / w;
     q.units = NT * w;
@@ -103,6 +105,7 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     if (ilog2_exact(q.tok) < 0 || ilog2_exact(w) < 0 || ilog2_exact(cs) < 0) return false;
     q.half = M <= 8;
     q.xpitch = q.kc * 2 + (((q.kc * 2) % 128 == 0) ? 64 : 0);
+
     int off = 0;
     q.off_x = off;
     off = align_up(off + Mc * q.xpitch, 16);
@@ -110,10 +113,9 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     off = align_up(off + cs * w * q.tok * N * 4, 16);
     q.off_row = off;
     off = align_up(off + q.tok * N * 4, 16);
-    q.off_key = off;  // 64-bit selection composites
-    off = align_up(off + (mode == 1 ? q.tok * N : 0) * 8, 16);
-    q.off_cand = off;  // per row: N candidate composites, k ids, k values
-    off = align_up(off + (mode == 1 ? q.tok * (N * 8 + topk * 8) : 0), 16);
+    q.off_key = off;  // (unused: the selection keys stay in registers)
+    q.off_cand = off;  // N candidate composites (one row at a time); per row k values
+    off = align_up(off + (mode == 1 ? N * 8 + q.tok * topk * 8 : 0), 16);
     q.off_ids = off;  // every token's ids in the CTA that sorts
     off = align_up(off + M * (mode == 1 ? topk : 0) * 4, 16);
     q.off_mask = off;
