@@ -169,6 +169,56 @@ __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* ro
     return __fdiv_rn(num, den);
 }
 
+// MXFP8 of this CTA's x slice (rows row0 .. row0 + Mq, columns kslice ..
+// kslice + kc), one lane quad per 32-element block; every thread of the CTA
+// takes part.
+__device__ __forceinline__ void quant_slice(const RouteArgs& a, const unsigned char* xs, int Mq, int row0,
+                                            int64_t kslice) {
+    if (a.q == nullptr) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int vpr = a.kc / 8, nvec = Mq * vpr;
+    const int64_t K = a.K, K32 = K / 32;
+    for (int base = warp * 32; base < nvec; base += kRouteThreads) {
+        const int v = base + lane;
+        const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
+        const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
+        unsigned sb;
+        const uint2 q8 = mx_quant_quad(d, &sb);
+        if (v < nvec) {
+            const int64_t kk = kslice + cv * 8;
+            *reinterpret_cast<uint2*>(a.q + (int64_t)(row0 + r) * K + kk) = q8;
+            if ((cv & 3) == 0) a.scale[(int64_t)(row0 + r) * K32 + kk / 32] = (uint8_t)sb;
+        }
+    }
+}
+
+// Sentinel MK in every slot of sorted_token_ids and -1 in every block of
+// expert_ids (the sort then writes the real entries); all threads take part.
+__device__ __forceinline__ void fill_sort_padding(const RouteArgs& a, int MK) {
+    const int tid = threadIdx.x, cap = (int)a.capacity;  // < 2^31, checked on the host
+    if ((reinterpret_cast<uintptr_t>(a.sorted) & 15u) == 0) {
+        int4* st4 = reinterpret_cast<int4*>(a.sorted);
+        const int n4 = cap >> 2;
+        for (int i = tid; i < n4; i += kRouteThreads) st4[i] = make_int4(MK, MK, MK, MK);
+        for (int i = (n4 << 2) + tid; i < cap; i += kRouteThreads) a.sorted[i] = MK;
+    } else {
+        for (int i = tid; i < cap; i += kRouteThreads) a.sorted[i] = MK;
+    }
+    for (int bb = tid, be = cap / a.block; bb < be; bb += kRouteThreads) a.expert_ids[bb] = -1;
+}
+
+// Gate weights of the CTA's owned rows: warp 15 - rl handles row rl.
+__device__ __forceinline__ void row_weights(const RouteArgs& a, const float* rowbuf, const float* oval, int my_rows,
+                                            int grow) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, k = a.topk;
+    if (warp >= kRouteWarps - my_rows) {
+        const int rl = kRouteWarps - 1 - warp;
+        const bool live = lane < k;
+        const float wgt = gate_weight(a, rowbuf + rl * a.N, live ? oval[rl * k + lane] : 0.0f);
+        if (live) a.weights[(int64_t)(grow + rl) * k + lane] = wgt;
+    }
+}
+
 template <bool HALF>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
@@ -192,6 +242,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int N = a.N, wpt = a.wpt, tok = a.tok, K = a.K, k = a.topk;
     const int nslots = a.cs * wpt;
     const int my_rows = max(0, min(tok, Mq - c * tok));
+    // the CTA that sorts the cluster's assignments: one that owns no row when
+    // there is one (it is idle while the others run the gate), else CTA 0
+    const int sorter = Mq <= (a.cs - 1) * tok ? a.cs - 1 : 0;
+    const bool sorts = a.mode == 1 && c == sorter;
     const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]);
     if (tid == 0) {
         s_ccount = 0;
@@ -200,7 +254,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         const unsigned stall = (a.flags & 2) ? 16u : 0u;  // test hook: bytes that never come
         if (my_rows > 0) mbar_expect_tx(bar0, (unsigned)(my_rows * nslots * N * 4) + stall);
-        if (a.mode == 1 && c == 0) mbar_expect_tx(bar1, (unsigned)(Mq * k * 4));
+        if (sorts) mbar_expect_tx(bar1, (unsigned)(Mq * k * 4));
     }
     cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM access
     pdl_trigger();
@@ -227,7 +281,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         if (tid < N) bpre0 = __ldg(a.bias + tid);
         if (tid + kRouteThreads < N) bpre1 = __ldg(a.bias + tid + kRouteThreads);
     }
-    if (a.mode == 1 && c == 0)
+    if (sorts)
         for (int e = tid; e < N; e += kRouteThreads) mask[e] = 0ull;  // token bitmasks (2 x 32 bits per expert)
     pdl_wait();
     MR_TRACE_STAMP(a.trace, 8);
@@ -296,43 +350,20 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         }
     }
     MR_TRACE_WARP(a.trace, 1);
-    // ---- MXFP8 of the x slice while the partials travel (one lane quad per 32-block)
-    if (a.q != nullptr) {
-        const int nvec = Mq * vpr;
-        const int64_t K32 = K / 32;
-        for (int base = warp * 32; base < nvec; base += kRouteThreads) {
-            const int v = base + lane;
-            const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
-            const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
-            unsigned sb;
-            const uint2 q8 = mx_quant_quad(d, &sb);
-            if (v < nvec) {
-                const int64_t k = kslice + cv * 8;
-                *reinterpret_cast<uint2*>(a.q + (int64_t)(row0 + r) * K + k) = q8;
-                if ((cv & 3) == 0) a.scale[(int64_t)(row0 + r) * K32 + k / 32] = (uint8_t)sb;
-            }
-        }
-    }
-    // sentinels in every slot of sorted_token_ids and -1 in every block of
-    // expert_ids, early: the sort later overwrites the real entries.  The
-    // CTA that sorts is ordered after these stores (same CTA, or through the
-    // clusters' ticket).
-    if (a.mode == 1 && blockIdx.x == 0) {
-        const int MKall = a.M * k, cap = (int)a.capacity;  // < 2^31, checked on the host
-        if ((reinterpret_cast<uintptr_t>(a.sorted) & 15u) == 0) {
-            int4* st4 = reinterpret_cast<int4*>(a.sorted);
-            const int n4 = cap >> 2;
-            for (int i = tid; i < n4; i += kRouteThreads) st4[i] = make_int4(MKall, MKall, MKall, MKall);
-            for (int i = (n4 << 2) + tid; i < cap; i += kRouteThreads) a.sorted[i] = MKall;
-        } else {
-            for (int i = tid; i < cap; i += kRouteThreads) a.sorted[i] = MKall;
-        }
-        for (int bb = tid, be = cap / a.block; bb < be; bb += kRouteThreads) a.expert_ids[bb] = -1;
-    }
     MR_TRACE_WARP(a.trace, 2);
-    // a CTA that owns no rows is done: nothing is ever sent to it
-    if (my_rows == 0) return;
-    if (!cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
+    // The sorter quantises its slice now (and, with one cluster, fills the
+    // sentinels and the -1 block ids; the real entries overwrite them after
+    // barriers of this CTA).  A CTA that owns no rows and does not sort is
+    // done once its slice is quantised: nothing is ever sent to it.  Owners
+    // quantise later, off the path of the gate.
+    if (sorts) {
+        quant_slice(a, xs, Mq, row0, kslice);
+        if (a.clusters == 1) fill_sort_padding(a, a.M * k);
+    } else if (my_rows == 0) {
+        quant_slice(a, xs, Mq, row0, kslice);
+        return;
+    }
+    if (my_rows > 0 && !cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
     MR_TRACE_CLK(a.trace, 0);
     MR_TRACE_STAMP(a.trace, 2);
 
@@ -435,8 +466,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                 r = (int)__reduce_add_sync(pmask, (unsigned)r);
                 if (part == 0 && r < k) {
                     const int id = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
-                    st_async_s32(map_rank(smem_u32(sm + a.off_ids) + (uint32_t)((ml * k + r) * 4), 0u), id,
-                                 map_rank(bar1, 0u));
+                    st_async_s32(map_rank(smem_u32(sm + a.off_ids) + (uint32_t)((ml * k + r) * 4), (unsigned)sorter),
+                                 id, map_rank(bar1, (unsigned)sorter));
                     a.ids[(int64_t)m * k + r] = id;
                     oval[rl * k + r] = rowbuf[rl * N + id];
                 }
@@ -449,28 +480,22 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     if (a.mode == 0) return;  // nothing else reads this CTA's shared memory
     MR_TRACE_STAMP(a.trace, 4);
     MR_TRACE_CLK(a.trace, 9);
-    // ---- weights, off the path of the ids: the last warps (warp 15: row 0)
-    if (warp >= kRouteWarps - my_rows) {
-        const int rl = kRouteWarps - 1 - warp, m = grow + rl;
-        const bool live = lane < k;
-        const float val = live ? oval[rl * k + lane] : 0.0f;
-        const float wgt = gate_weight(a, rowbuf + rl * N, val);
-        MR_TRACE_CLK(a.trace, 10);
-        if (live) a.weights[(int64_t)m * k + lane] = wgt;
-    }
     MR_TRACE_CLK(a.trace, 11);
     MR_TRACE_WARP(a.trace, 7);
-    MR_TRACE_CLK(a.trace, 12);
-    MR_TRACE_WARP(a.trace, 8);
-    if (c != 0) return;
+    if (!sorts) {  // the weights and the quantisation finish this CTA
+        row_weights(a, rowbuf, oval, my_rows, grow);
+        quant_slice(a, xs, Mq, row0, kslice);
+        return;
+    }
+    row_weights(a, rowbuf, oval, my_rows, grow);
     if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
     MR_TRACE_STAMP(a.trace, 5);
     MR_TRACE_WARP(a.trace, 9);
 
     // ---- sort.  One cluster: CTA 0 holds every id.  Several clusters: each
     //      CTA 0 publishes its rows' ids and takes a ticket; the last one
-    //      gathers all ids and sorts.  The sentinels and the -1 block ids are
-    //      already in place (first CTA of the grid, right after the quant).
+    //      gathers all ids and sorts (with several clusters its first phase
+    //      also fills the sentinels and the -1 block ids).
     int* ids_all = reinterpret_cast<int*>(sm + a.off_ids);
     const int M = a.M, MK = M * k, B = a.block;
     if (a.clusters > 1) {
@@ -493,6 +518,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         const int m = fdiv(f, a.mag_k);
         atomicOr(m < 32 ? &mlo[ids_all[f]] : &mhi[ids_all[f]], 1u << (m & 31));
     }
+    if (a.clusters > 1) fill_sort_padding(a, MK);
     __syncthreads();
     MR_TRACE_CLK(a.trace, 14);
     MR_TRACE_WARP(a.trace, 10);
