@@ -4,34 +4,34 @@
 // The pages' one-launch decode router (sglang #46691 Summary: a router for
 // 1-16 tokens bitwise equal to router GEMV, gate and sort; sort + stage-1
 // quant in one launch) chains its stages through global memory.  On GB300 a
-// global last-arriver ticket costs ~0.7 us and a cluster barrier ~0.2 us, so
-// this kernel keeps every hand-off inside one cluster of CS CTAs (16 when the
-// device allows it, else 8) and distributed shared memory:
+// global last-arriver ticket costs ~0.7 us and a DSMEM message ~0.2 us, so
+// this kernel keeps the hand-offs of up to 16 tokens inside one cluster of CS
+// CTAs (16 when the device allows it, else 8):
 //
 //   1. CTA c owns the K slice [c*K/CS, (c+1)*K/CS) for ALL experts.  Warps
 //      take (8-expert tile, k-part) units and run m16n8k16 bf16 MMAs with
 //      fp32 accumulation; gate-weight fragments come straight from global
 //      memory with 16-byte loads issued before the kernel waits on its
 //      predecessor (programmatic dependent launch), x fragments from the
-//      CTA's x slice in shared memory.  The CTA quantises its x slice (MXFP8).
-//   2. Split-K reduction: every unit's partial tile goes, as 8-byte DSMEM
-//      stores, to the CTA that owns the tile's token rows (token m belongs to
-//      CTA m / TOK).  After one cluster barrier the owner sums the CS*WPT
-//      partials of each logit in a fixed order and writes the logits.
-//   3. Gate: the owner runs the top-k of its rows, one warp per 128-expert
-//      segment, segments merged by one warp; the chosen ids also go to CTA 0.
-//   4. After a second cluster barrier CTA 0 sorts the assignments: since the
-//      k ids of a token are distinct, the stable rank of (m, j) inside expert
-//      e is popc(mask_e & ((1 << m) - 1)) where mask_e is the bitmask of the
-//      tokens that chose e.
+//      CTA's x slice in shared memory.
+//   2. Split-K reduction: every unit's partial tile goes by st.async to the
+//      CTA that owns the tile's token rows (token m belongs to CTA m / TOK),
+//      counted on that CTA's mbarrier; the owner waits for the bytes it
+//      expects and sums the CS*WPT partials of each logit in a fixed order.
+//   3. Gate, the owner's whole CTA per row: a threshold below the k-th
+//      largest key from group maxima, then a parallel ranking of the few
+//      candidates; the chosen ids go at once to the sorting CTA (st.async).
+//   4. The sorting CTA (one that owns no row when there is one, else CTA 0)
+//      sorts the assignments: since the k ids of a token are distinct, the
+//      stable rank of (m, j) inside expert e is popc(mask_e & ((1 << m) - 1))
+//      where mask_e is the bitmask of the tokens that chose e.
 //   More than 16 tokens: one cluster per 16 tokens, each running steps 1-3 on
-//   its rows; the CTA 0s publish their ids and take a last-arriver ticket
-//   (the pages' hand-off), and the last one sorts every assignment.
+//   its rows; the sorting CTAs publish their ids and take a last-arriver
+//   ticket (the pages' hand-off), and the last one sorts every assignment.
 //
-// Hand-offs inside a cluster are st.async stores counted on an mbarrier of
-// the receiving CTA (no release fences); each wait for them is bounded in
-// time and sets a device flag when it runs out.  One cluster leaves nothing
-// in scratch; several clusters leave their ticket counter at zero again.  The GEMV alone (mode 0)
+// Every wait for bytes from other CTAs is bounded in time and sets a device
+// flag when it runs out.  One cluster leaves nothing in scratch; several
+// clusters leave their ticket counter at zero again.  The GEMV alone (mode 0)
 // is what the standalone router GEMV runs for M <= 64, so the logits of the
 // two are bitwise equal.
 #include "common.cuh"
