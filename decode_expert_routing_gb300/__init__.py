@@ -18,7 +18,7 @@ import os
 
 __all__ = [
     "MoeRouteError", "MoeRouteUnsupported", "Scratch", "library_path", "load_library",
-    "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "LAUNCH_TEST_STALL", "set_wait_limit_ns",
+    "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "LAUNCH_TEST_STALL", "LAUNCH_LEGACY_MMA", "set_wait_limit_ns",
     "device_error", "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
     "moe_sort", "mxfp8_quant", "moe_route_sort_quant", "router_gemv_noalloc",
 ]
@@ -135,6 +135,7 @@ def _row_major_2d(x, name):
 
 LAUNCH_PDL = 1
 LAUNCH_TEST_STALL = 2  # test hook: the cluster kernels' bounded waits run out
+LAUNCH_LEGACY_MMA = 4  # router GEMV of more than 64 rows: split-K mma.sync kernel instead of tcgen05
 
 
 def set_launch_flags(flags: int) -> None:

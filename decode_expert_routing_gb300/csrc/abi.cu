@@ -50,6 +50,11 @@ std::atomic<void*> g_trace{nullptr};
 
 namespace mr {
 int launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+}  // namespace mr
+namespace {
+bool allow_tc() { return (mr::launch_flags() & MR_LAUNCH_LEGACY_MMA) == 0; }
+}  // namespace
+namespace mr {
 unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 void* trace_buffer() { return g_trace.load(std::memory_order_relaxed); }
 }  // namespace mr
@@ -57,7 +62,7 @@ void* trace_buffer() { return g_trace.load(std::memory_order_relaxed); }
 extern "C" {
 
 int mr_set_launch_flags(int flags) {
-    if (flags & ~(MR_LAUNCH_PDL | MR_LAUNCH_TEST_STALL)) return MR_ERR_INVALID_ARG;
+    if (flags & ~(MR_LAUNCH_PDL | MR_LAUNCH_TEST_STALL | MR_LAUNCH_LEGACY_MMA)) return MR_ERR_INVALID_ARG;
     g_launch_flags.store(flags, std::memory_order_relaxed);
     return MR_OK;
 }
@@ -100,10 +105,9 @@ int mr_abi_version(void) { return MR_ABI_VERSION; }
 
 int mr_router_gemv_supported(int M, int N, int K, int64_t ldx) {
     if (ldx < K || ldx % 8 != 0 || K % MR_GEMV_K_MULTIPLE != 0) return 0;
-    if (M <= mr::kRouteMaxM) {
-        mr::RoutePlan rp;
-        return mr::route_plan(M, N, K, 1, 0, 16, &rp) ? 1 : 0;
-    }
+    mr::RoutePlan rp;
+    if (mr::route_plan(M, N, K, 1, 0, 16, &rp)) return 1;
+    if (M <= mr::kRouteMaxM) return 0;
     GemvPlan p;
     return mr::gemv_plan(M, N, K, &p) ? 1 : 0;
 }
@@ -159,6 +163,7 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.mode = mode;
     a.cs = p.cs;
     a.cs_shift = mr::ilog2_exact(p.cs);
+    a.rpc = p.rpc;
     a.clusters = p.clusters;
     a.kc = p.kc;
     a.spw = p.spw;
@@ -178,6 +183,14 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.wpt_shift = mr::ilog2_exact(p.wpt);
     a.mag_n = mr::div_magic(N);
     a.mag_vpr = mr::div_magic(p.kc / 8);
+    a.mag_n4 = mr::div_magic(N / 4 > 0 ? N / 4 : 1);
+    a.tc = p.tc;
+    a.nmma = p.nmma;
+    a.tmem_cols = p.tmem_cols;
+    a.nslots = p.nslots;
+    a.off_a = p.off_a;
+    a.off_b = p.off_b;
+    a.off_dst = p.off_dst;
     a.trace = static_cast<unsigned long long*>(mr::trace_buffer());
     a.flags = mr::launch_flags();
     a.wait_ns = mr::wait_limit_ns();
@@ -191,12 +204,15 @@ int mr_router_gemv(const void* x, int64_t ldx, const void* w, float* logits, int
     if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) || N < 1)
         return MR_ERR_INVALID_ARG;
     if (K % MR_GEMV_K_MULTIPLE != 0) return MR_ERR_UNSUPPORTED;
-    if (M <= mr::kRouteMaxM) {
+    {   // the cluster kernel (no scratch) whenever its plan fits; above 64 rows
+        // the split-K GEMV with last-arriver fixup takes the rest
         mr::RoutePlan rp;
-        if (!mr::route_plan(M, N, K, 1, 0, mr::route_cluster_size(), &rp)) return MR_ERR_UNSUPPORTED;
-        mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 0);
-        a.logits = logits;
-        return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
+        if (mr::route_plan(M, N, K, 1, 0, mr::route_cluster_size(), &rp, allow_tc())) {
+            mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 0);
+            a.logits = logits;
+            return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
+        }
+        if (M <= mr::kRouteMaxM) return MR_ERR_UNSUPPORTED;
     }
     if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;
     GemvPlan p;
@@ -264,7 +280,7 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
     if ((q == nullptr) != (scale == nullptr)) return MR_ERR_INVALID_ARG;
     if (q != nullptr && !aligned(q, 8)) return MR_ERR_INVALID_ARG;
     mr::RoutePlan rp;
-    if (!mr::route_plan(M, N, K, topk, 1, mr::route_cluster_size(), &rp)) return MR_ERR_UNSUPPORTED;
+    if (!mr::route_plan(M, N, K, topk, 1, mr::route_cluster_size(), &rp, allow_tc())) return MR_ERR_UNSUPPORTED;
     mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 1);
     if (rp.clusters > 1) {  // the clusters meet in scratch: a ticket and every token's ids
         if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;

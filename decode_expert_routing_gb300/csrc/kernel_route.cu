@@ -97,6 +97,36 @@ __device__ __forceinline__ void st_async_s32(uint32_t addr, int v, uint32_t bar)
                  : "memory");
 }
 
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// ---- tcgen05 (5th-generation tensor core, accumulator in tensor memory)
+// Shared-memory matrix descriptor of a K-major tile without swizzle: start
+// address, leading (k) and stride (8-row group) byte offsets, each >> 4, and
+// the fixed descriptor version bit.
+__device__ __forceinline__ unsigned long long tc_desc(uint32_t addr) {
+    return (unsigned long long)((addr >> 4) & 0x3FFFu) | ((unsigned long long)(kTcLbo >> 4) << 16) |
+           ((unsigned long long)(kTcSbo >> 4) << 32) | (1ull << 46);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 and M >> 4.
+__device__ __forceinline__ uint32_t tc_idesc(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// Byte offset of 16-byte chunk cc (k elements 8 cc .. 8 cc + 7) of row r in a
+// K-major tile whose 16-wide k-steps lie `step` bytes apart.
+__device__ __forceinline__ uint32_t tc_off(int r, int cc, int step) {
+    return (uint32_t)((cc >> 1) * step + (r >> 3) * kTcSbo + (cc & 1) * kTcLbo + (r & 7) * 16);
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
 // Set when a bounded wait of the route kernel ran out (read by the host).
 __device__ int g_route_timeout;
 
@@ -219,11 +249,14 @@ __device__ __forceinline__ void row_weights(const RouteArgs& a, const float* row
     }
 }
 
-template <bool HALF>
+// HALF: at most 8 token rows (half of the m16 tile live).  TC: the router
+// GEMV on tcgen05 (GEMV alone, 64-row clusters) instead of mma.sync.
+template <bool HALF, bool TC>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
-    __shared__ __align__(8) unsigned long long s_bar[2];  // [0] partial logits in, [1] ids in (CTA 0)
-    __shared__ int s_ok[2];
+    __shared__ __align__(8) unsigned long long s_bar[3];  // [0] partial logits in, [1] ids in, [2] MMAs done
+    __shared__ int s_ok[3];
+    __shared__ uint32_t s_tmem;  // tcgen05: base address of the accumulator
     __shared__ unsigned s_ticket;
     __shared__ __align__(16) unsigned s_wmin[kRouteWarps];  // gate: per warp, smallest group maximum
     __shared__ int s_ccount;                                  // gate: candidates so far
@@ -237,20 +270,21 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
 #endif
     // this cluster's token rows: [row0, row0 + Mq); this CTA owns rows
     // [c * tok, c * tok + my_rows) of them
-    const int row0 = (int)(blockIdx.x >> a.cs_shift) * kRouteRowsPerCluster;
-    const int Mq = min(kRouteRowsPerCluster, a.M - row0);
+    const int row0 = (int)(blockIdx.x >> a.cs_shift) * a.rpc;
+    const int Mq = min(a.rpc, a.M - row0);
     const int N = a.N, wpt = a.wpt, tok = a.tok, K = a.K, k = a.topk;
-    const int nslots = a.cs * wpt;
+    const int nslots = a.nslots;
     const int my_rows = max(0, min(tok, Mq - c * tok));
     // the CTA that sorts the cluster's assignments: one that owns no row when
     // there is one (it is idle while the others run the gate), else CTA 0
     const int sorter = Mq <= (a.cs - 1) * tok ? a.cs - 1 : 0;
     const bool sorts = a.mode == 1 && c == sorter;
-    const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]);
+    const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]), bar2 = smem_u32(&s_bar[2]);
     if (tid == 0) {
         s_ccount = 0;
         mbar_init(bar0, 1);
         mbar_init(bar1, 1);
+        mbar_init(bar2, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         const unsigned stall = (a.flags & 2) ? 16u : 0u;  // test hook: bytes that never come
         if (my_rows > 0) mbar_expect_tx(bar0, (unsigned)(my_rows * nslots * N * 4) + stall);
@@ -275,7 +309,23 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      parameters, never written by the preceding kernel, so they may
     //      precede the wait
     uint4 wv[kRouteBatch][kRouteSpwMax];
-    load_w_batch(a, kslice, warp, g, t, 0, wv);
+    const int vpr = a.kc / 8;  // 16-byte chunks per row of the CTA's K slice
+    if constexpr (TC) {
+        if (warp == 0) {  // accumulator columns in tensor memory (one CTA per SM: never contended)
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                         "r"(a.tmem_cols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+        const uint32_t at = smem_u32(sm + a.off_a);
+        for (int i = tid; i < N * vpr; i += kRouteThreads) {
+            const int e = fdiv(i, a.mag_vpr), cc = i - e * vpr;
+            cp_async16(at + tc_off(e, cc, kTcAStep), a.w + (int64_t)e * K + kslice + cc * 8);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    } else {
+        load_w_batch(a, kslice, warp, g, t, 0, wv);
+    }
     float bpre0 = 0.0f, bpre1 = 0.0f;  // selection bias of this thread's experts t and t + 512
     if (a.bias != nullptr) {
         if (tid < N) bpre0 = __ldg(a.bias + tid);
@@ -288,20 +338,86 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
 
     // ---- this CTA's x slice -> shared memory
     unsigned char* xs = sm + a.off_x;
-    const int vpr = a.kc / 8;
+    const bool keep_xs = !(TC && a.mode == 0);  // row-major copy for mma.sync / the quantiser
     for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
         const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
         const uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
-        *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
+        if (keep_xs) *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
+        if constexpr (TC) *reinterpret_cast<uint4*>(sm + a.off_b + tc_off(r, cv, a.nmma * 32)) = d;
     }
     MR_TRACE_WARP(a.trace, 0);
+    if constexpr (TC) {  // the weight tile has landed; both tiles are visible to the tensor core
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+    }
     __syncthreads();
+    if constexpr (TC) tc_fence_after();
     MR_TRACE_STAMP(a.trace, 1);
 
     // ---- MMA: batches of units sharing one k-part; partial tiles go
     //      straight to the receive buffers of the rows' owners
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
     const uint32_t recv_local = smem_u32(sm + a.off_recv);
+    if constexpr (TC) {
+        // one thread issues the K slice's MMAs: D[128 experts x NMMA tokens]
+        // += W tile [128 x 16] . x tile [NMMA x 16]^T per 16-wide k-step
+        const uint32_t tmem = s_tmem;
+        if (tid == 0) {
+            const unsigned long long ad0 = tc_desc(smem_u32(sm + a.off_a)), bd0 = tc_desc(smem_u32(sm + a.off_b));
+            const uint32_t idesc = tc_idesc(128, a.nmma);
+            const int nq = a.kc / 16;
+            const unsigned long long bstep = (unsigned long long)((a.nmma * 32) >> 4);
+            for (int q = 0; q < nq; ++q) {
+                const unsigned long long ad = ad0 + (unsigned long long)q * (kTcAStep >> 4), bd = bd0 + (unsigned long long)q * bstep;
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+                    "l"(ad), "l"(bd), "r"(idesc), "r"((uint32_t)(q > 0))
+                    : "memory");
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar2)
+                         : "memory");
+        }
+        quant_slice(a, xs, Mq, row0, kslice);  // while the tensor core works
+        const bool ok = cta_wait_bytes(bar2, a.wait_ns, &s_ok[2]);
+        tc_fence_after();
+        if (ok && warp < 4) {  // warp w reads accumulator lanes (experts) 32 w .. 32 w + 31
+            float* dst = reinterpret_cast<float*>(sm + a.off_dst);  // [token][expert]
+            const int e = warp * 32 + lane;
+            for (int cb = 0; cb < a.nmma / 16; ++cb) {
+                uint32_t v[16];
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                    : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 16)));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (e < N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (cb * 16 + j < Mq) dst[(cb * 16 + j) * N + e] = __uint_as_float(v[j]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+        }
+        if (!ok) return;
+        // 16-byte messages: row r's N partial logits to the row's owner
+        const float* dsrc = reinterpret_cast<const float*>(sm + a.off_dst);
+        const int n4 = N >> 2;
+        for (int item = tid; item < Mq * n4; item += kRouteThreads) {
+            const int r = fdiv(item, a.mag_n4), c4 = item - r * n4;
+            const int own = r >> a.tok_shift, rl = r & (tok - 1);
+            const uint32_t la = recv_local + (uint32_t)(((c * tok + rl) * N + 4 * c4) * 4);
+            st_async_f4(map_rank(la, (unsigned)own), *reinterpret_cast<const float4*>(dsrc + r * N + 4 * c4),
+                        map_rank(bar0, (unsigned)own));
+        }
+    } else {
     uint32_t owner_bar[2] = {0u, 0u};  // mbarrier of the owner of rows g and g + 8
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -311,7 +427,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int my_tiles = j0 < NT ? (NT - j0 + tiles_per_pass - 1) >> (4 - a.wpt_shift) : 0;
     const int nb = (my_tiles + kRouteBatch - 1) / kRouteBatch;
     const int slot = c * wpt + p;
-    const int r0 = g, r1 = g + 8;
+    const int r0 = g, r1 = g + 8;  // one m16 tile: at most 16 token rows per cluster here
     for (int b = 0; b < nb; ++b) {
         if (b > 0) load_w_batch(a, kslice, warp, g, t, b, wv);
         float acc[kRouteBatch][4];
@@ -333,6 +449,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                     mma_bf16_m16n8k16(acc[uu], xa.z, xb.z, xa.w, xb.w, wv[uu][s].z, wv[uu][s].w);
             }
         }
+        MR_TRACE_WARP(a.trace, 4);
 #pragma unroll
         for (int uu = 0; uu < kRouteBatch; ++uu) {
             const int j = j0 + tiles_per_pass * (b * kRouteBatch + uu);
@@ -349,6 +466,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
         }
     }
+    }  // mma.sync path
     MR_TRACE_WARP(a.trace, 1);
     MR_TRACE_WARP(a.trace, 2);
     // The sorter quantises its slice now (and, with one cluster, fills the
@@ -356,11 +474,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // barriers of this CTA).  A CTA that owns no rows and does not sort is
     // done once its slice is quantised: nothing is ever sent to it.  Owners
     // quantise later, off the path of the gate.
+    // (On the tensor-core path every CTA has quantised during its MMAs.)
     if (sorts) {
-        quant_slice(a, xs, Mq, row0, kslice);
+        if (!TC) quant_slice(a, xs, Mq, row0, kslice);
         if (a.clusters == 1) fill_sort_padding(a, a.M * k);
     } else if (my_rows == 0) {
-        quant_slice(a, xs, Mq, row0, kslice);
+        if (!TC) quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
     if (my_rows > 0 && !cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
@@ -484,7 +603,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     MR_TRACE_WARP(a.trace, 7);
     if (!sorts) {  // the weights and the quantisation finish this CTA
         row_weights(a, rowbuf, oval, my_rows, grow);
-        quant_slice(a, xs, Mq, row0, kslice);
+        if (!TC) quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
     row_weights(a, rowbuf, oval, my_rows, grow);
@@ -600,15 +719,17 @@ int route_device_error(int clear) {
 }
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
-static int g_attr_done[64][2];  // per device and instantiation
+static int g_attr_done[64][4];  // per device and instantiation
 
-template <bool HALF>
+template <bool HALF, bool TC>
 static cudaError_t prepare(int dev) {
-    if (g_attr_done[dev][HALF ? 1 : 0]) return cudaSuccess;
-    auto k = route_cluster_kernel<HALF>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteSmemMax);
+    const int slot = (HALF ? 1 : 0) + (TC ? 2 : 0);
+    if (g_attr_done[dev][slot]) return cudaSuccess;
+    auto k = route_cluster_kernel<HALF, TC>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TC ? kRouteSmemMaxTc : kRouteSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess) g_attr_done[dev][HALF ? 1 : 0] = 1;
+    if (e == cudaSuccess) g_attr_done[dev][slot] = 1;
     return e;
 }
 
@@ -616,7 +737,7 @@ int route_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (g_cluster16[dev] == 0) {
-        cudaError_t e = prepare<false>(dev);
+        cudaError_t e = prepare<false, false>(dev);
         int n = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -630,7 +751,7 @@ int route_cluster_size() {
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false>, &cfg);
         }
         g_cluster16[dev] = (e == cudaSuccess && n >= 1) ? 1 : -1;
         cudaGetLastError();  // a refused query leaves no sticky error
@@ -644,12 +765,15 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     void (*kernel)(RouteArgs) = nullptr;
-    if (p.half) {
-        e = prepare<true>(dev);
-        kernel = route_cluster_kernel<true>;
+    if (p.tc) {
+        e = prepare<false, true>(dev);
+        kernel = route_cluster_kernel<false, true>;
+    } else if (p.half) {
+        e = prepare<true, false>(dev);
+        kernel = route_cluster_kernel<true, false>;
     } else {
-        e = prepare<false>(dev);
-        kernel = route_cluster_kernel<false>;
+        e = prepare<false, false>(dev);
+        kernel = route_cluster_kernel<false, false>;
     }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -10,9 +10,12 @@ constexpr int kRouteThreads = 512;        // 16 warps per CTA
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteBatch = 2;            // (tile, k-part) units whose loads a warp keeps in flight
 constexpr int kRouteSpwMax = 8;           // 32-wide k steps per unit, at most
-constexpr int kRouteSmemMax = 200 * 1024; // dynamic shared memory, at most
+constexpr int kRouteSmemMax = 200 * 1024;    // dynamic shared memory, at most (mma.sync kernels)
+constexpr int kRouteSmemMaxTc = 220 * 1024;  // the tcgen05 kernel (weight and x tiles)
 constexpr int kRouteMaxM = 64;
-constexpr int kRouteRowsPerCluster = 16;  // token rows per cluster (one m16 MMA tile)
+constexpr int kRouteRowsPerCluster = 16;  // token rows per cluster of the whole route (one m16 MMA tile)
+constexpr int kRouteGemvRowsPerCluster = 64;  // GEMV-only launches of more than 64 rows (four m16 tiles)
+constexpr int kRouteGemvMaxM = 512;
 
 struct RouteArgs {
     const uint16_t* x;
@@ -32,6 +35,7 @@ struct RouteArgs {
     int mode;        // 0: logits only, 1: whole route
     int cs;          // CTAs in the cluster
     int cs_shift;    // log2(cs)
+    int rpc;         // token rows per cluster
     int clusters;    // clusters in the grid: one per 16 token rows
     int kc;          // K per CTA
     int spw;         // 32-wide k steps per unit
@@ -42,8 +46,13 @@ struct RouteArgs {
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
     int tok_shift, wpt_shift;  // log2 of tok and wpt (both powers of two)
     int gs_shift;    // gate threshold: log2 of the lane-group size (<= 32 threads)
+    int tc;          // 1: the GEMV runs on tcgen05 (TMEM accumulator), 0: on mma.sync
+    int nmma;        // tcgen05: token columns of the MMA (16..64, multiple of 16)
+    int tmem_cols;   // tcgen05: TMEM columns allocated (power of two >= 32)
+    int nslots;      // split-K partials per logit at the owner
+    int off_a, off_b, off_dst;  // tcgen05: weight tile, x tile, transposed accumulator
     // q = (x * magic) >> 32 equals x / d for 0 <= x < 2^21, d <= 1024
-    unsigned long long mag_n, mag_k, mag_block, mag_vpr;
+    unsigned long long mag_n, mag_k, mag_block, mag_vpr, mag_n4;
     unsigned long long* trace;
     int flags;                   // launch flags (bit 1: test stall, see moe_route.h)
     unsigned long long wait_ns;  // limit of every wait for bytes from other CTAs
@@ -63,7 +72,8 @@ inline int ilog2_exact(int v) {
 }
 
 struct RoutePlan {
-    int cs, kc, spw, wpt, units, tok, xpitch, clusters;
+    int cs, kc, spw, wpt, units, tok, xpitch, clusters, rpc;
+    int tc, nmma, tmem_cols, nslots, off_a, off_b, off_dst;
     bool half;
     int smem;
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
@@ -73,8 +83,14 @@ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Returns false when (M, N, K, topk) is outside what the cluster kernel
 // covers with cluster size cs.
-inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePlan* p) {
-    if (M < 1 || M > kRouteMaxM || N < 8 || N > 1024 || N % 8 != 0) return false;
+// tcgen05 operand tiles (K-major, no swizzle): core matrices of 8 rows x 16 B;
+// inside one 16-wide k-step, core matrix (row group rg, k half kh) sits at
+// rg * kTcSbo + kh * kTcLbo.  The weight tile always spans 128 rows (the MMA's M).
+constexpr int kTcLbo = 128, kTcSbo = 256;
+constexpr int kTcAStep = 128 * 16 * 2;  // bytes of the weight tile per 16-wide k-step
+
+inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePlan* p, bool allow_tc = true) {
+    if (M < 1 || M > (mode == 1 ? kRouteMaxM : kRouteGemvMaxM) || N < 8 || N > 1024 || N % 8 != 0) return false;
     if (K < 32 * cs || K % (32 * cs) != 0) return false;
     RoutePlan q{};
     q.cs = cs;
@@ -95,22 +111,36 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.wpt = w;
     q.spw = S / w;
     q.units = NT * w;
-    // one cluster per 16 token rows; rows owned per CTA: a power of two
-    // covering ceil(rows of a cluster / cs)
-    q.clusters = (M + kRouteRowsPerCluster - 1) / kRouteRowsPerCluster;
-    const int Mc = M < kRouteRowsPerCluster ? M : kRouteRowsPerCluster;
+    // one cluster per 16 token rows (GEMV alone above 64 rows: per 64 rows);
+    // rows owned per CTA: a power of two covering ceil(rows of a cluster / cs)
+    // (64-row clusters only on tcgen05: without it more than 64 rows take the
+    // split-K GEMV with last-arriver fixup)
+    const bool big = mode == 0 && M > kRouteMaxM;
+    if (big && !(allow_tc && N <= 128 && q.kc % 16 == 0)) return false;
+    q.rpc = big ? kRouteGemvRowsPerCluster : kRouteRowsPerCluster;
+    q.clusters = (M + q.rpc - 1) / q.rpc;
+    const int Mc = M < q.rpc ? M : q.rpc;
     q.tok = 1;
     while (q.tok * cs < Mc) q.tok *= 2;
     if (mode == 1 && (topk < 1 || topk > 32 || topk > N || q.tok > kRouteWarps)) return false;
     if (ilog2_exact(q.tok) < 0 || ilog2_exact(w) < 0 || ilog2_exact(cs) < 0) return false;
     q.half = M <= 8;
     q.xpitch = q.kc * 2 + (((q.kc * 2) % 128 == 0) ? 64 : 0);
+    // tcgen05 for the GEMV alone above 64 rows (64 token columns per MMA) when
+    // the CTA's weight slice fits one 128-row tile.  At 16 rows its chain of
+    // K/16 dependent MMAs issued by one thread plus the accumulator read-back
+    // is slower than 16 warps of mma.sync (measured), so the decode route
+    // keeps mma.sync.
+    q.tc = big ? 1 : 0;
+    q.nmma = (Mc + 15) / 16 * 16;
+    q.tmem_cols = q.nmma <= 32 ? 32 : 64;
+    q.nslots = q.tc ? cs : cs * w;
 
     int off = 0;
-    q.off_x = off;
-    off = align_up(off + Mc * q.xpitch, 16);
+    q.off_x = off;  // row-major x slice (MMA operand of mma.sync; quantiser input)
+    off = align_up(off + ((q.tc && mode == 0) ? 0 : Mc * q.xpitch), 16);
     q.off_recv = off;
-    off = align_up(off + cs * w * q.tok * N * 4, 16);
+    off = align_up(off + q.nslots * q.tok * N * 4, 16);
     q.off_row = off;
     off = align_up(off + q.tok * N * 4, 16);
     q.off_key = off;  // (unused: the selection keys stay in registers)
@@ -122,8 +152,22 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     off = align_up(off + (mode == 1 ? N : 0) * 8, 16);
     q.off_start = off;
     off = align_up(off + (mode == 1 ? N + 32 : 0) * 4, 16);
+    if (q.tc) {
+        off = align_up(off, 128);
+        q.off_a = off;  // weight tile, then (after the MMAs) the transposed accumulator
+        const int a_bytes = (q.kc / 16) * kTcAStep, d_bytes = q.nmma * N * 4;
+        off = align_up(off + a_bytes, 128);
+        q.off_b = off;
+        off = align_up(off + (q.kc / 16) * q.nmma * 32, 128);
+        if (d_bytes <= a_bytes) {
+            q.off_dst = q.off_a;
+        } else {
+            q.off_dst = off;
+            off = align_up(off + d_bytes, 16);
+        }
+    }
     q.smem = off;
-    if (q.smem > kRouteSmemMax) return false;
+    if (q.smem > (q.tc ? kRouteSmemMaxTc : kRouteSmemMax)) return false;
     *p = q;
     return true;
 }

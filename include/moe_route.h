@@ -81,6 +81,7 @@ typedef enum mr_scoring {
 /* Launch options, process-wide (bits for mr_set_launch_flags). */
 #define MR_LAUNCH_PDL 1         /* programmatic dependent launch, see below */
 #define MR_LAUNCH_TEST_STALL 2  /* test hook for the timeout path, see below */
+#define MR_LAUNCH_LEGACY_MMA 4  /* router GEMV on mma.sync instead of tcgen05 */
 
 /*
  * Sets the launch options of every later call in this process; returns
@@ -90,7 +91,12 @@ typedef enum mr_scoring {
  * gate weight w at once, and waits for that kernel to complete before it
  * touches anything else (x, logits, ids, scratch, outputs).  The caller must
  * then not write w in the kernel launched just before the routing call on
- * the same stream.  Default: 0 (plain stream order).
+ * the same stream.  With MR_LAUNCH_LEGACY_MMA the router GEMV of more than
+ * 64 rows runs as the split-K GEMV with last-arriver fixup on warp-level
+ * mma.sync instead of the tcgen05 cluster kernel (the two sum the split-K
+ * partials in different orders, so their logits agree within fp32 rounding,
+ * not bit for bit); up to 64 rows it always runs on mma.sync.
+ * Default: 0 (plain stream order, tcgen05 where the weight tile fits).
  */
 int mr_set_launch_flags(int flags);
 int mr_get_launch_flags(void);

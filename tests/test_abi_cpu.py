@@ -91,9 +91,10 @@ def test_validation_returns_before_any_launch(lib):
     assert lib.mr_router_gemv(P(0x1002), 6144, fake, fake, 1, 128, 6144, fake, 1 << 20, None) == mr.MR_ERR_INVALID_ARG
     # unsupported K
     assert lib.mr_router_gemv(fake, 6000, fake, fake, 1, 128, 6000, fake, 1 << 20, None) == mr.MR_ERR_UNSUPPORTED
-    # scratch too small (the split-K GEMV of more than 64 rows needs scratch)
-    assert lib.mr_router_gemv(fake, 6144, fake, fake, 100, 128, 6144, fake, 100, None) == mr.MR_ERR_SCRATCH_TOO_SMALL
-    assert lib.mr_router_gemv(fake, 6144, fake, fake, 100, 128, 6144, None, 0, None) == mr.MR_ERR_INVALID_ARG
+    # scratch too small (above 64 rows, a shape the cluster kernel does not
+    # hold in shared memory goes to the split-K GEMV, which needs scratch)
+    assert lib.mr_router_gemv(fake, 6144, fake, fake, 100, 1024, 6144, fake, 100, None) == mr.MR_ERR_SCRATCH_TOO_SMALL
+    assert lib.mr_router_gemv(fake, 6144, fake, fake, 100, 1024, 6144, None, 0, None) == mr.MR_ERR_INVALID_ARG
     # gate: topk > N, bad scoring, N too large
     assert lib.mr_route_topk(fake, 1, 8, 9, 0, None, 1, fake, fake, None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_route_topk(fake, 1, 128, 8, 7, None, 1, fake, fake, None) == mr.MR_ERR_INVALID_ARG
@@ -118,7 +119,10 @@ def test_validation_returns_before_any_launch(lib):
                                        fake, fake, fake, 1 << 20, fake, fake, fake, 32768 + 17 * 8 * 4 - 4,
                                        None) == mr.MR_ERR_SCRATCH_TOO_SMALL
     # launch options and the wait limit (host-only settings)
-    assert lib.mr_set_launch_flags(4) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_set_launch_flags(8) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_set_launch_flags(mr.LAUNCH_LEGACY_MMA) == mr.MR_OK
+    assert lib.mr_get_launch_flags() == mr.LAUNCH_LEGACY_MMA
+    assert lib.mr_set_launch_flags(0) == mr.MR_OK
     assert lib.mr_set_wait_limit_ns(999) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_set_wait_limit_ns(60_000_000_001) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_set_wait_limit_ns(1_000_000_000) == mr.MR_OK

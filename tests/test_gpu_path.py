@@ -54,11 +54,30 @@ def test_router_gemv_matches_oracle(mr, cid, M):
     assert int(scratch.counters().abs().sum()) == 0, "split-K counters not re-zeroed"
 
 
-@pytest.mark.parametrize("M", [65, 100, 129])
-def test_router_gemv_split_k_rows_past_64(mr, M):
-    """The split-K GEMV with last-arriver fixup (M > 64): ragged row tiles."""
+@pytest.mark.parametrize("M,legacy", [(65, 0), (100, 0), (129, 0), (200, 0), (512, 0), (100, 1), (512, 1)])
+def test_router_gemv_rows_past_64(mr, M, legacy):
+    """More than 64 rows: cluster split-K over 64-row clusters on tcgen05
+    (ragged last cluster), or with the legacy launch option the split-K
+    mma.sync GEMV with last-arriver fixup."""
     x, w = inputs.router_inputs(M, 6144, 128, 7)
     scratch = mr.Scratch(M, 128, 6144, 8)
+    flags = mr.get_launch_flags()
+    if legacy:
+        mr.set_launch_flags(flags | mr.LAUNCH_LEGACY_MMA)
+    try:
+        g = mr.router_gemv(to_dev_bf16(x), to_dev_bf16(w), scratch=scratch)
+    finally:
+        mr.set_launch_flags(flags)
+    assert_logits_close(host(g), oracle.router_gemv(x, w))
+    assert int(scratch.counters().abs().sum()) == 0
+
+
+@pytest.mark.parametrize("M", [100, 300])
+def test_router_gemv_split_k_ticket_path(mr, M):
+    """Shapes the cluster kernel cannot hold in shared memory (N = 1024)
+    take the split-K GEMV with last-arriver fixup; its counters re-zero."""
+    x, w = inputs.router_inputs(M, 6144, 1024, 7)
+    scratch = mr.Scratch(M, 1024, 6144, 8)
     g = mr.router_gemv(to_dev_bf16(x), to_dev_bf16(w), scratch=scratch)
     assert_logits_close(host(g), oracle.router_gemv(x, w))
     assert int(scratch.counters().abs().sum()) == 0
