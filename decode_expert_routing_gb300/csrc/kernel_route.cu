@@ -381,17 +381,20 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         }
         quant_slice(a, xs, Mq, row0, kslice);  // while the tensor core works
         const bool ok = cta_wait_bytes(bar2, a.wait_ns, &s_ok[2]);
+        MR_TRACE_STAMP(a.trace, 9);
         tc_fence_after();
-        if (ok && warp < 4) {  // warp w reads accumulator lanes (experts) 32 w .. 32 w + 31
+        // warp w reads accumulator lanes (experts) 32 (w % 4) .. + 31, column
+        // blocks w / 4, w / 4 + 4, ... (a warp may touch only its lane quarter)
+        if (ok) {
             float* dst = reinterpret_cast<float*>(sm + a.off_dst);  // [token][expert]
-            const int e = warp * 32 + lane;
-            for (int cb = 0; cb < a.nmma / 16; ++cb) {
+            const int q4 = warp & 3, e = q4 * 32 + lane;
+            for (int cb = warp >> 2; cb < a.nmma / 16; cb += kRouteWarps / 4) {
                 uint32_t v[16];
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
                       "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-                    : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cb * 16)));
+                    : "r"(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(cb * 16)));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 if (e < N) {
 #pragma unroll
@@ -407,6 +410,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
         }
         if (!ok) return;
+        MR_TRACE_STAMP(a.trace, 10);
         // 16-byte messages: row r's N partial logits to the row's owner
         const float* dsrc = reinterpret_cast<const float*>(sm + a.off_dst);
         const int n4 = N >> 2;
@@ -508,6 +512,22 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int gl = 1 << a.gs_shift;
     const unsigned gmask = gl == 32 ? kFull : ((1u << gl) - 1u) << (lane & ~(gl - 1));
     const bool group_has = (tid & ~(gl - 1)) < N;  // the lane group's first expert exists
+    if (a.mode == 0) {  // GEMV alone: every (owned row, expert) in parallel
+        for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
+            const int rl = fdiv(idx, a.mag_n), n = idx - rl * N;
+            const float* pp = recv + rl * N + n;
+            float sum = 0.0f;
+            for (int sl = 0; sl < nslots; sl += 8) {  // the same order as below
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = pp[(sl + u) * plane];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) sum = __fadd_rn(sum, v[u]);
+            }
+            a.logits[(int64_t)(grow + rl) * N + n] = sum;
+        }
+        return;  // nothing else reads this CTA's shared memory
+    }
     for (int rl = 0; rl < my_rows; ++rl) {
         float sum0 = 0.0f, sum1 = 0.0f;
         if (h0) {
