@@ -543,6 +543,30 @@ def run_ours(args):
     return 0
 
 
+def run_gemv_rows(ms):
+    """Three router_gemv calls at each M (K = 6144, N = 128, the prefill x):
+    a short program for a profiler to capture the GEMV kernels."""
+    import torch
+    from decode_expert_routing_gb300 import build as mrbuild
+    mrbuild.build()
+    import decode_expert_routing_gb300 as mr
+    from decode_expert_routing_gb300 import inputs
+    mr.load_library()
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    wd = dev_bf16(inputs.router_inputs(2, K_HID, N_EXP, 2)[1])
+    for M in ms:
+        xd = dev_bf16(inputs.prefill_x(M, K_HID))
+        out = torch.empty((M, N_EXP), dtype=torch.float32, device="cuda")
+        scratch = mr.Scratch(M, N_EXP, K_HID, TOPK)
+        for _ in range(3):
+            mr.router_gemv(xd, wd, out=out, scratch=scratch)
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -550,7 +574,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--gemv-rows", default="",
+                    help="profiling aid: only run router_gemv three times at each of these M "
+                         "(comma-separated) and exit, printing no JSON line")
     args = ap.parse_args()
+    if args.gemv_rows:
+        return run_gemv_rows([int(v) for v in args.gemv_rows.split(",")])
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
