@@ -89,6 +89,7 @@ def bf16_bits_to_f32(b) -> np.ndarray:
 
 # Tensor tags inside one workload's key space.
 TAG_X, TAG_W, TAG_BIAS, TAG_ROWS, TAG_EDGE, TAG_VARIANT = 1, 2, 3, 4, 5, 6
+TAG_RMS, TAG_NORMW = 7, 8
 
 
 def normal_bf16(shape, std: float, config_id: int, tag: int, seed: int = 0) -> np.ndarray:
@@ -144,6 +145,26 @@ def prefill_x(M: int, K: int, config_id: int = 4, seed: int = 0, variant: int = 
     z = normal(stream_key(config_id, TAG_X | (variant << 8), seed), M * K).reshape(M, K)
     z[scaled_rows(M, config_id, seed)] *= 50.0
     return f64_to_bf16_bits(z)
+
+
+def norm_inputs(M: int, K: int, config_id: int = 6, seed: int = 0, variant: int = 0):
+    """Un-normalised residual rows, their rstd and a Gemma-style norm weight.
+
+    Row m has its own magnitude a_m ~ U(0.5, 8): sres[m] = bf16(a_m * z),
+    z ~ N(0, 1); rstd[m] = float32(1 / a_m) stands for what the norm in
+    front of the router publishes (the router only multiplies by it, so any
+    positive value of that size exercises the same arithmetic); the norm
+    weight g ~ N(0, 0.1) in bf16 (offsets around 0, applied as 1 + g by a
+    Gemma RMSNorm).  Returns (sres bf16 bits [M, K], rstd float32 [M],
+    g bf16 bits [K]).
+    """
+    vtag = variant << 8
+    amp = 0.5 + 7.5 * uniform01(stream_key(config_id, TAG_RMS | vtag, seed), M)
+    z = normal(stream_key(config_id, TAG_X | vtag, seed), M * K).reshape(M, K)
+    sres = f64_to_bf16_bits(z * amp[:, None])
+    rstd = (1.0 / amp).astype(np.float32)
+    g = normal_bf16((K,), 0.1, config_id, TAG_NORMW | vtag, seed)
+    return sres, rstd, g
 
 
 def tied_gate(w: np.ndarray, pairs=((10, 11), (50, 51))) -> np.ndarray:
@@ -228,4 +249,7 @@ CONFIGS = {
             N=128, topk=8, block=64, scoring="softmax", Ms=(128, 256, 512), prefill_M=4096),
     5: dict(name="adversarial M=64, K=6144, N=128, top-8: skew, ties, quant edges", K=6144,
             N=128, topk=8, block=16, scoring="softmax", Ms=(64,)),
+    6: dict(name="route on the norm's scale: residual rows + rstd + Gemma norm weight, M=1..64, "
+                 "K=6144, N=128, softmax top-8, block 16", K=6144, N=128, topk=8, block=16,
+            scoring="softmax", Ms=(1, 2, 4, 8, 16, 32, 64)),
 }

@@ -50,6 +50,9 @@ def _load():
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_encode_array.argtypes = [P, i64, P]
         lib.oracle_mxfp8_quant.argtypes = [P, i64, i32, i32, P, P]
+        lib.oracle_bf16_round.argtypes = [ctypes.c_float]
+        lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_norm_apply.argtypes = [P, i64, P, P, i32, i32, i32, P]
         _lib = lib
     return _lib
 
@@ -147,3 +150,32 @@ def route_sort_quant(x_bf16, w_bf16, topk, block, scoring="softmax", bias=None,
     q, s = mxfp8_quant(x_bf16)
     return dict(logits=logits, topk_ids=ids, topk_weights=wts, sorted_token_ids=st,
                 expert_ids=ex, num_tokens_post_padded=nt, q=q, scale=s)
+
+
+NORM_KINDS = {"rms": 0, "gemma": 1}
+
+
+def bf16_round(f: float) -> int:
+    """bf16 bits of the nearest bf16 to the float32 value f (ties to even)."""
+    return int(_load().oracle_bf16_round(float(np.float32(f))))
+
+
+def norm_apply(x_bf16: np.ndarray, rstd: np.ndarray, g_bf16: np.ndarray, kind: str = "gemma") -> np.ndarray:
+    """xn = bf16((x * rstd[m]) * s[k]) in fp32 steps, s = g or 1 + g (bf16 bits [M, K])."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    r = _c(rstd, np.float32).ravel()
+    g = _c(g_bf16, np.uint16).ravel()
+    assert r.shape[0] == M and g.shape[0] == K
+    out = np.empty((M, K), dtype=np.uint16)
+    _load().oracle_norm_apply(_ptr(x), K, _ptr(r), _ptr(g), NORM_KINDS[kind], M, K, _ptr(out))
+    return out
+
+
+def route_sort_quant_norm(sres_bf16, rstd, g_bf16, kind, w_bf16, topk, block, scoring="softmax",
+                          bias=None, renormalize=True):
+    """The route of norm_apply's output (dict of outputs plus "xn")."""
+    xn = norm_apply(sres_bf16, rstd, g_bf16, kind)
+    out = route_sort_quant(xn, w_bf16, topk, block, scoring, bias, renormalize)
+    out["xn"] = xn
+    return out

@@ -320,3 +320,55 @@ void oracle_mxfp8_quant(const uint16_t *x, int64_t ldx, int M, int K,
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Next row: the router on the norm's scale.                           */
+/* sgl-amd-mono #56 page, entry #59 "[Perf] minimax_m31: Run o_proj in */
+/* the launch, route on the norm's scale, read B operands from LDS",   */
+/* Modifications, "Route on the norm's scale": the RMSNorm in front of */
+/* the router hands over each token's rstd, and the router forms the   */
+/* normalised activations of its own columns from the un-normalised    */
+/* residual sum, so that it sees the norm's output bit for bit.        */
+/* READING (the pages print no formula): the norm's output is          */
+/*   xn[m, k] = bf16( (x[m, k] * rstd[m]) * s[k] )                     */
+/* with both products in fp32, each rounded to nearest even, and       */
+/* s[k] = g[k] (plain RMSNorm) or s[k] = 1 + g[k] in fp32 (Gemma       */
+/* RMSNorm, the norm the MiniMax-M3 producers of sglang #46691 use,    */
+/* "Changes to existing kernels").  bf16 rounding: nearest, ties to    */
+/* the even code, as every bf16 store on the pages.                    */
+/* ------------------------------------------------------------------ */
+
+/* Nearest bf16 to the finite float f, ties to the even code (the       */
+/* definition: compare the distances to the two neighbours exactly).    */
+static uint16_t bf16_nearest_even(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t lo = u & 0xFFFF0000u;             /* toward zero, same sign */
+    uint32_t hi = lo + 0x10000u;               /* away from zero */
+    float flo, fhi;
+    memcpy(&flo, &lo, sizeof flo);
+    memcpy(&fhi, &hi, sizeof fhi);
+    double v = fabs((double)f), a = fabs((double)flo);
+    double b = ((hi & 0x7F800000u) == 0x7F800000u) ? 0x1p128 : fabs((double)fhi);
+    if (v - a < b - v) return (uint16_t)(lo >> 16);
+    if (v - a > b - v) return (uint16_t)(hi >> 16);
+    return (uint16_t)((((lo >> 16) & 1u) == 0u) ? (lo >> 16) : (hi >> 16));
+}
+
+uint16_t oracle_bf16_round(float f) { return bf16_nearest_even(f); }
+
+void oracle_norm_apply(const uint16_t *x, int64_t ldx, const float *rstd,
+                       const uint16_t *g, int gemma, int M, int K, uint16_t *xn)
+{
+    for (int m = 0; m < M; ++m) {
+        for (int k = 0; k < K; ++k) {
+            float xv = (float)bf16_value(x[(int64_t)m * ldx + k]);
+            float gv = (float)bf16_value(g[k]);
+            float s = gemma ? 1.0f + gv : gv;
+            float t = xv * rstd[m];
+            float p = t * s;
+            xn[(int64_t)m * K + k] = bf16_nearest_even(p);
+        }
+    }
+}
