@@ -4,8 +4,8 @@ sort -> MXFP8 quant) on GB300.  Prints ONE JSON line on rank 0.
 
 Workload (decode batch buckets): K = 6144, N = 128 experts, softmax top-8,
 sort block 16, MXFP8 quant of x, swept over M in {2, 4, 8, 16, 32, 64}.  One
-step = the whole path once for every M: the one-launch route for M <= 16,
-the four-call chain for M = 32 and 64.  Every call reads its own copy of x
+step = the whole path once for every M, one launch of the route kernel per
+M.  Every call reads its own copy of x
 and W from a ring of 32 slots (~350 MB, > 2x the 129 MB L2), so the gate
 weight streams from HBM as it does in a real decode step; each step replays
 one CUDA graph per slot.
@@ -478,6 +478,117 @@ def run_ours(args):
         rt.destroy(g)
         del xb, lg, sk
 
+    def graph_us(body, calls, reps=10):
+        """Microseconds per call of body (calls launches) captured as one graph."""
+        with torch.cuda.stream(stream):
+            g = rt.capture(sp, body)
+        for _ in range(3):
+            rt.launch(g, sp)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(reps):
+                rt.launch(g, sp)
+            e1.record()
+        torch.cuda.synchronize()
+        rt.destroy(g)
+        return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+    # 896 experts, hidden 3584, sigmoid score + selection bias, top-16
+    # (one launch per call; 32 rotating copies of the 6.4 MB gate weight)
+    k3 = {}
+    K3K, K3N, K3TOP = 3584, 896, 16
+    k3w_base = [dev_bf16(inputs.router_inputs(1, K3K, K3N, 3, variant=v)[1]) for v in range(DISTINCT)]
+    k3w = [k3w_base[s % DISTINCT].clone() for s in range(SLOTS)]
+    del k3w_base
+    k3bias = torch.from_numpy(inputs.selection_bias(K3N)).to(dev)
+    k3scratch = mr.Scratch(32, K3N, K3K, K3TOP, device=dev)
+    for M in (1, 8, 16, 32):
+        k3x = [dev_bf16(inputs.router_inputs(M, K3K, K3N, 3, variant=v)[0]) for v in range(DISTINCT)]
+        k3o = mr.alloc_route_outputs(M, K3N, K3K, K3TOP, BLOCK, dev)
+
+        def body(M=M, k3x=k3x, k3o=k3o):
+            for r in range(64):
+                mr.moe_route_sort_quant(k3x[r % DISTINCT], k3w[r % SLOTS], K3TOP, BLOCK, scoring="sigmoid",
+                                        bias=k3bias, out=k3o, scratch=k3scratch)
+        with torch.cuda.stream(stream):
+            body()
+        us = graph_us(body, 64)
+        k3[str(M)] = {"us_per_call": round(us, 3),
+                      "GBs": round(algorithmic_bytes(M, K3K, K3N, K3TOP, BLOCK) / (us * 1e-6) / 1e9, 1)}
+        del k3x, k3o
+    del k3w, k3scratch
+
+    # the route on the norm's scale (residual rows, per-token rstd, Gemma
+    # norm weight normalised inside the route kernel) against the norm's
+    # output written out by its own launch and routed after it
+    normed = {}
+    ngd = dev_bf16(inputs.norm_inputs(1, K_HID)[2])
+    for M in MS:
+        nin = [inputs.norm_inputs(M, K_HID, variant=v) for v in range(DISTINCT)]
+        nsd = [dev_bf16(t[0]) for t in nin]
+        nrd = [torch.from_numpy(t[1]).to(dev) for t in nin]
+        xn_buf = torch.empty((M, K_HID), dtype=torch.bfloat16, device=dev)
+        o = outs[M]
+
+        def body_f(M=M, nsd=nsd, nrd=nrd, o=o):
+            for r in range(64):
+                mr.moe_route_sort_quant_norm(nsd[r % DISTINCT], nrd[r % DISTINCT], ngd, ws[M][r % SLOTS], TOPK,
+                                             BLOCK, "gemma", out=o, scratch=scratch)
+
+        def body_c(M=M, nsd=nsd, nrd=nrd, o=o, xn_buf=xn_buf):
+            for r in range(64):
+                mr.norm_apply(nsd[r % DISTINCT], nrd[r % DISTINCT], ngd, "gemma", out=xn_buf)
+                mr.moe_route_sort_quant(xn_buf, ws[M][r % SLOTS], TOPK, BLOCK, out=o, scratch=scratch)
+        with torch.cuda.stream(stream):
+            body_f()
+            body_c()
+        uf, uc = graph_us(body_f, 64), graph_us(body_c, 64)
+        nb = algorithmic_bytes(M) + 4 * M + 2 * K_HID   # + rstd and the norm weight
+        normed[str(M)] = {"us_per_call": round(uf, 3), "GBs": round(nb / (uf * 1e-6) / 1e9, 1),
+                          "written_out_chain_us": round(uc, 3)}
+        del nin, nsd, nrd, xn_buf
+    del ngd
+
+    # prefill: MXFP8 quant of x [4096, 6144] (four copies, 200 MB) and the
+    # sort of its top-8 ids into blocks of 64 (ids from the GEMV + gate on
+    # the same x, 512 rows per GEMV call)
+    PM, PB = 4096, 64
+    px = [dev_bf16(inputs.prefill_x(PM, K_HID, variant=v)) for v in range(2)]
+    px += [t.clone() for t in px]
+    pq = torch.empty((PM, K_HID), dtype=torch.uint8, device=dev)
+    ps = torch.empty((PM, K_HID // 32), dtype=torch.uint8, device=dev)
+    plog = torch.empty((PM, N_EXP), dtype=torch.float32, device=dev)
+    psk = mr.Scratch(512, N_EXP, K_HID, TOPK, device=dev)
+    with torch.cuda.stream(stream):
+        for r0 in range(0, PM, 512):
+            mr.router_gemv(px[0][r0:r0 + 512], ws[MS[0]][0], out=plog[r0:r0 + 512], scratch=psk)
+        pids, _ = mr.route_topk(plog, TOPK)
+    torch.cuda.synchronize()
+    pcap = mr.sort_capacity(PM, TOPK, N_EXP, PB)
+    psort = (torch.empty(pcap, dtype=torch.int32, device=dev), torch.empty(pcap // PB, dtype=torch.int32, device=dev),
+             torch.empty(1, dtype=torch.int32, device=dev))
+    pssk = mr.Scratch(PM, N_EXP, 512, TOPK, device=dev)
+
+    def body_q():
+        for r in range(8):
+            mr.mxfp8_quant(px[r % 4], out=(pq, ps))
+
+    def body_s():
+        for r in range(8):
+            mr.moe_sort(pids, N_EXP, PB, out=psort, scratch=pssk)
+    with torch.cuda.stream(stream):
+        body_q()
+        body_s()
+    q_us, s_us = graph_us(body_q, 8), graph_us(body_s, 8)
+    q_bytes = 2 * PM * K_HID + PM * K_HID + PM * K_HID // 32
+    s_bytes = 4 * PM * TOPK + 4 * pcap + 4 * (pcap // PB) + 4
+    prefill = {"mxfp8_quant": {"us_per_call": round(q_us, 3), "GBs": round(q_bytes / (q_us * 1e-6) / 1e9, 1),
+                               "frac_of_peak": round(q_bytes / (q_us * 1e-6) / 1e9 / peak, 4)},
+               "moe_sort_block64": {"us_per_call": round(s_us, 3),
+                                    "GBs": round(s_bytes / (s_us * 1e-6) / 1e9, 1)}}
+    del px, pq, ps, plog, psk, pids, psort, pssk
+
     # end to end through the public API: pinned host x in, outputs back out
     e2e_steps = min(args.steps, 2000)
     hx = {M: torch.from_numpy(np.ascontiguousarray(host[M][0][0]).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -528,6 +639,9 @@ def run_ours(args):
             "us_per_call": round(ms_max * 1e3 / args.steps / len(MS), 3),
             "per_m": per_m,
             "split_k_gemv_rows_128_512": split_k,
+            "route_896_experts_sigmoid_top16": k3,
+            "route_on_norm_scale_gemma": normed,
+            "prefill_4096_rows": prefill,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,

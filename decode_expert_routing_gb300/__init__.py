@@ -29,6 +29,7 @@ _lib = None
 
 MR_OK, MR_ERR_UNSUPPORTED, MR_ERR_INVALID_ARG, MR_ERR_SCRATCH_TOO_SMALL, MR_ERR_CUDA, MR_ERR_TIMEOUT = range(6)
 SCORING = {"softmax": 0, "sigmoid": 1}
+NORM_KIND = {"rms": 0, "gemma": 1}
 SCRATCH_COUNTER_BYTES = 32768
 
 
@@ -67,6 +68,9 @@ SIGNATURES = {
     "mr_moe_route_sort_quant": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P,
                                      _P, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
     "mr_router_gemv_noalloc": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P]),
+    "mr_moe_route_sort_quant_norm": (_I, [_P, _I64, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P,
+                                          _P, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
+    "mr_norm_apply": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "mr_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "mr_device_error": (_I, [_I]),
 }
@@ -344,4 +348,62 @@ def moe_route_sort_quant(x, w, topk: int, block: int, scoring: str = "softmax", 
         out["sorted_token_ids"].numel(), _dev_ptr(q, "q", torch.uint8, allow_none=True),
         _dev_ptr(s, "scale", torch.uint8, allow_none=True), scratch.ptr, scratch.nbytes,
         _stream_ptr(stream)), "mr_moe_route_sort_quant")
+    return out
+
+
+def norm_apply(sres, rstd, norm_weight, norm: str = "gemma", out=None, stream=None):
+    """The router input on the norm's scale, written out: bf16 [M, K] with
+    xn[m, k] = bf16((sres[m, k] * rstd[m]) * s[k]), s = g or 1 + g."""
+    torch = _torch()
+    ldx = _row_major_2d(sres, "sres")
+    M, K = sres.shape
+    _check_norm_args(rstd, norm_weight, M, K)
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=sres.device)
+    if not out.is_contiguous() or tuple(out.shape) != (M, K):
+        raise ValueError("out must be contiguous [M, K]")
+    _check(_load().mr_norm_apply(_dev_ptr(sres, "sres", torch.bfloat16), ldx, _dev_ptr(rstd, "rstd", torch.float32),
+                                 _dev_ptr(norm_weight, "norm_weight", torch.bfloat16), NORM_KIND[norm], M, K,
+                                 _dev_ptr(out, "out", torch.bfloat16), _stream_ptr(stream)), "mr_norm_apply")
+    return out
+
+
+def _check_norm_args(rstd, norm_weight, M, K):
+    if rstd.dim() != 1 or rstd.shape[0] != M or not rstd.is_contiguous():
+        raise ValueError("rstd must be contiguous [M]")
+    if norm_weight.dim() != 1 or norm_weight.shape[0] != K or not norm_weight.is_contiguous():
+        raise ValueError("norm_weight must be contiguous [K]")
+
+
+def moe_route_sort_quant_norm(sres, rstd, norm_weight, w, topk: int, block: int, norm: str = "gemma",
+                              scoring: str = "softmax", bias=None, renormalize: bool = True, quant: bool = True,
+                              out=None, scratch: Scratch | None = None, stream=None):
+    """The one-launch route with its input on the norm's scale (residual rows,
+    per-token rstd, norm weight); returns a dict of outputs."""
+    torch = _torch()
+    ldx = _row_major_2d(sres, "sres")
+    M, K = sres.shape
+    N = w.shape[0]
+    if not w.is_contiguous() or w.shape[1] != K:
+        raise ValueError("w must be contiguous [N, K]")
+    _check_norm_args(rstd, norm_weight, M, K)
+    if out is None:
+        out = alloc_route_outputs(M, N, K, topk, block, sres.device, quant)
+    if scratch is None:
+        scratch = Scratch(M, N, K, topk, device=sres.device)
+    q = out.get("q") if quant else None
+    s = out.get("scale") if quant else None
+    _check(_load().mr_moe_route_sort_quant_norm(
+        _dev_ptr(sres, "sres", torch.bfloat16), ldx, _dev_ptr(rstd, "rstd", torch.float32),
+        _dev_ptr(norm_weight, "norm_weight", torch.bfloat16), NORM_KIND[norm],
+        _dev_ptr(w, "w", torch.bfloat16), M, N, K, topk,
+        SCORING[scoring], _dev_ptr(bias, "bias", torch.float32, allow_none=True), int(renormalize), block,
+        _dev_ptr(out["logits"], "logits", torch.float32), _dev_ptr(out["topk_ids"], "topk_ids", torch.int32),
+        _dev_ptr(out["topk_weights"], "topk_weights", torch.float32),
+        _dev_ptr(out["sorted_token_ids"], "sorted_token_ids", torch.int32),
+        _dev_ptr(out["expert_ids"], "expert_ids", torch.int32),
+        _dev_ptr(out["num_tokens_post_padded"], "num_tokens_post_padded", torch.int32),
+        out["sorted_token_ids"].numel(), _dev_ptr(q, "q", torch.uint8, allow_none=True),
+        _dev_ptr(s, "scale", torch.uint8, allow_none=True), scratch.ptr, scratch.nbytes,
+        _stream_ptr(stream)), "mr_moe_route_sort_quant_norm")
     return out

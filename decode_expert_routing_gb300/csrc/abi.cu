@@ -260,12 +260,16 @@ int mr_mxfp8_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t
     return cuda_status(mr::launch_quant(x, ldx, M, K, q, scale, as_stream(stream)));
 }
 
-int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, int N, int K, int topk,
-                            int scoring, const float* sel_bias, int renormalize, int block,
-                            float* logits, int32_t* topk_ids, float* topk_weights,
-                            int32_t* sorted_token_ids, int32_t* expert_ids,
-                            int32_t* num_tokens_post_padded, int64_t capacity, uint8_t* q,
-                            uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
+}  // extern "C"
+
+// The one-launch route; rstd != nullptr puts the router input on the norm's
+// scale (residual rows x rstd x norm weight, rounded to bf16 in the kernel).
+static int route_sort_quant(const void* x, int64_t ldx, const float* rstd, const void* norm_w, int norm_kind,
+                            const void* w, int M, int N, int K, int topk, int scoring, const float* sel_bias,
+                            int renormalize, int block, float* logits, int32_t* topk_ids, float* topk_weights,
+                            int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* num_tokens_post_padded,
+                            int64_t capacity, uint8_t* q, uint8_t* scale, void* scratch, size_t scratch_bytes,
+                            void* stream) {
     int s = check_x(x, ldx, M, K);
     if (s != MR_OK) return s;
     if ((s = check_gate_args(M, N, topk, scoring)) != MR_OK) return s;
@@ -312,7 +316,53 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
     a.mag_block = mr::div_magic(block);
     a.scoring = scoring;
     a.renormalize = renormalize ? 1 : 0;
+    a.rstd = rstd;
+    a.norm_w = static_cast<const uint16_t*>(norm_w);
+    a.norm_gemma = norm_kind == MR_NORM_GEMMA ? 1 : 0;
     return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
+}
+
+static int check_norm(const float* rstd, const void* norm_w, int norm_kind) {
+    if (rstd == nullptr || !aligned(rstd, 4) || norm_w == nullptr || !aligned(norm_w, 16)) return MR_ERR_INVALID_ARG;
+    if (norm_kind != MR_NORM_RMS && norm_kind != MR_NORM_GEMMA) return MR_ERR_INVALID_ARG;
+    return MR_OK;
+}
+
+extern "C" {
+
+int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, int N, int K, int topk,
+                            int scoring, const float* sel_bias, int renormalize, int block,
+                            float* logits, int32_t* topk_ids, float* topk_weights,
+                            int32_t* sorted_token_ids, int32_t* expert_ids,
+                            int32_t* num_tokens_post_padded, int64_t capacity, uint8_t* q,
+                            uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
+    return route_sort_quant(x, ldx, nullptr, nullptr, 0, w, M, N, K, topk, scoring, sel_bias, renormalize, block,
+                            logits, topk_ids, topk_weights, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                            capacity, q, scale, scratch, scratch_bytes, stream);
+}
+
+int mr_moe_route_sort_quant_norm(const void* sres, int64_t ldx, const float* rstd, const void* norm_weight,
+                                 int norm_kind, const void* w, int M, int N, int K, int topk, int scoring,
+                                 const float* sel_bias, int renormalize, int block, float* logits,
+                                 int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
+                                 int32_t* expert_ids, int32_t* num_tokens_post_padded, int64_t capacity,
+                                 uint8_t* q, uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
+    const int s = check_norm(rstd, norm_weight, norm_kind);
+    if (s != MR_OK) return s;
+    return route_sort_quant(sres, ldx, rstd, norm_weight, norm_kind, w, M, N, K, topk, scoring, sel_bias,
+                            renormalize, block, logits, topk_ids, topk_weights, sorted_token_ids, expert_ids,
+                            num_tokens_post_padded, capacity, q, scale, scratch, scratch_bytes, stream);
+}
+
+int mr_norm_apply(const void* sres, int64_t ldx, const float* rstd, const void* norm_weight, int norm_kind, int M,
+                  int K, void* xn, void* stream) {
+    int s = check_x(sres, ldx, M, K);
+    if (s != MR_OK) return s;
+    if ((s = check_norm(rstd, norm_weight, norm_kind)) != MR_OK) return s;
+    if (K % 8 != 0) return MR_ERR_UNSUPPORTED;
+    if (xn == nullptr || !aligned(xn, 16)) return MR_ERR_INVALID_ARG;
+    return cuda_status(mr::launch_norm_apply(sres, ldx, rstd, norm_weight, norm_kind == MR_NORM_GEMMA ? 1 : 0, M,
+                                             K, xn, as_stream(stream)));
 }
 
 }  // extern "C"

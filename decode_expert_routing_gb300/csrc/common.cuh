@@ -37,6 +37,30 @@ __device__ __forceinline__ void mma_bf16_m16n8k16(float (&c)[4], uint32_t a0, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Router input on the norm's scale: two bf16 residual values (one 32-bit
+// pair) -> bf16((x * rstd) * s) with s = g or, for a Gemma RMSNorm, 1 + g;
+// each fp32 step rounds to nearest even (no contraction), and the bf16
+// store rounds to nearest even.  Subnormals are kept (no -ftz).
+__device__ __forceinline__ uint32_t norm_pair(uint32_t xp, uint32_t gp, float rstd, bool gemma) {
+    const float x0 = __uint_as_float(xp << 16), x1 = __uint_as_float(xp & 0xffff0000u);
+    float s0 = __uint_as_float(gp << 16), s1 = __uint_as_float(gp & 0xffff0000u);
+    if (gemma) {
+        s0 = __fadd_rn(1.0f, s0);
+        s1 = __fadd_rn(1.0f, s1);
+    }
+    const float p0 = __fmul_rn(__fmul_rn(x0, rstd), s0);
+    const float p1 = __fmul_rn(__fmul_rn(x1, rstd), s1);
+    uint32_t d;  // upper half from the first source operand
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(p1), "f"(p0));
+    return d;
+}
+
+// Eight consecutive elements of a row (one 16-byte chunk) through norm_pair.
+__device__ __forceinline__ uint4 norm_chunk(uint4 x, uint4 g, float rstd, bool gemma) {
+    return make_uint4(norm_pair(x.x, g.x, rstd, gemma), norm_pair(x.y, g.y, rstd, gemma),
+                      norm_pair(x.z, g.z, rstd, gemma), norm_pair(x.w, g.w, rstd, gemma));
+}
+
 // Programmatic dependent launch.  pdl_wait() blocks until the kernel
 // launched before this one on the stream has completed and its writes are
 // visible (a no-op when the launch did not allow overlap); pdl_trigger()

@@ -49,6 +49,8 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
                         cudaStream_t st);
 cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale,
                          cudaStream_t st);
+cudaError_t launch_norm_apply(const void* x, int64_t ldx, const float* rstd, const void* g, int gemma, int M,
+                              int K, void* xn, cudaStream_t st);
 struct RoutePlan;
 struct RouteArgs;
 // Cluster route kernel (M <= 64): logits only (mode 0) or the whole route.

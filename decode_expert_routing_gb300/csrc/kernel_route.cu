@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         const unsigned long long acc =
             (unsigned long long)a.x ^ (unsigned long long)a.logits ^ (unsigned long long)a.expert_ids ^
             (unsigned long long)a.scale ^ (unsigned long long)a.renormalize ^ (unsigned long long)a.units ^
-            (unsigned long long)a.off_ids ^ a.mag_n ^ (unsigned long long)a.trace ^ (unsigned long long)a.counter;
+            (unsigned long long)a.off_ids ^ a.mag_n ^ (unsigned long long)a.trace ^ (unsigned long long)a.counter ^
+            (unsigned long long)a.norm_gemma;
         asm volatile("" ::"l"(acc));
     }
     const int64_t kslice = (int64_t)c * a.kc;
@@ -336,12 +337,17 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     pdl_wait();
     MR_TRACE_STAMP(a.trace, 8);
 
-    // ---- this CTA's x slice -> shared memory
+    // ---- this CTA's x slice -> shared memory (on the norm's scale: the
+    //      residual rows times rstd and the norm weight, rounded to bf16 as
+    //      the norm would store them)
     unsigned char* xs = sm + a.off_x;
     const bool keep_xs = !(TC && a.mode == 0);  // row-major copy for mma.sync / the quantiser
+    const bool norm = a.rstd != nullptr;
     for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
         const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
-        const uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
+        uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
+        if (norm)
+            d = norm_chunk(d, ld_ro_v4(a.norm_w + kslice + cv * 8), __ldg(a.rstd + row0 + r), a.norm_gemma != 0);
         if (keep_xs) *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
         if constexpr (TC) *reinterpret_cast<uint4*>(sm + a.off_b + tc_off(r, cv, a.nmma * 32)) = d;
     }

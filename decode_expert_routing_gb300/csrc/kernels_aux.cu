@@ -244,4 +244,37 @@ cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, u
                          static_cast<const uint16_t*>(x), ldx, M, K, q, scale);
 }
 
+// Router input on the norm's scale, written out: xn[m, k] = bf16((x[m, k] *
+// rstd[m]) * s[k]) for the unfused chain (one thread per 16-byte chunk,
+// grid-stride).  xn is row-major [M, K].
+__global__ void __launch_bounds__(256) norm_apply_kernel(const uint16_t* x, int64_t ldx, const float* rstd,
+                                                         const uint16_t* g, int gemma, int M, int K,
+                                                         uint16_t* xn) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t vpr = K / 8;
+    const int64_t total = (int64_t)M * vpr;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / vpr, c = i - r * vpr;
+        const uint4 d = norm_chunk(ld_stream_v4(x + r * ldx + c * 8), ld_ro_v4(g + c * 8), __ldg(rstd + r),
+                                   gemma != 0);
+        *reinterpret_cast<uint4*>(xn + r * K + c * 8) = d;
+    }
+}
+
+cudaError_t launch_norm_apply(const void* x, int64_t ldx, const float* rstd, const void* g, int gemma, int M,
+                              int K, void* xn, cudaStream_t st) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t vectors = (int64_t)M * (K / 8);
+    int64_t ctas = (vectors + 255) / 256;
+    const int64_t cap = (int64_t)sms * 8;
+    if (ctas > cap) ctas = cap;
+    return launch_kernel(norm_apply_kernel, dim3((unsigned)ctas), dim3(256), 0, st, static_cast<const uint16_t*>(x),
+                         ldx, rstd, static_cast<const uint16_t*>(g), gemma, M, K, static_cast<uint16_t*>(xn));
+}
+
 }  // namespace mr

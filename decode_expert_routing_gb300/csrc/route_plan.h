@@ -58,6 +58,11 @@ struct RouteArgs {
     unsigned long long wait_ns;  // limit of every wait for bytes from other CTAs
     int32_t* ids_scratch;   // clusters > 1: every token's ids, gathered for the sort
     unsigned* counter;      // clusters > 1: last-arriver ticket, zero between launches
+    // router input on the norm's scale (rstd == nullptr: x is the router input
+    // as given): x[m, k] -> bf16((x * rstd[m]) * s[k]), s = g or 1 + g
+    const float* rstd;
+    const uint16_t* norm_w;
+    int norm_gemma;
 };
 
 // Multiplier for division by d (1 <= d <= 2^11) of dividends below 2^21:

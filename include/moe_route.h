@@ -78,6 +78,11 @@ typedef enum mr_scoring {
     MR_SCORE_SIGMOID = 1         /* select by sigmoid + bias; weights = sigmoid */
 } mr_scoring;
 
+typedef enum mr_norm_kind {
+    MR_NORM_RMS = 0,             /* RMSNorm: scale = g                         */
+    MR_NORM_GEMMA = 1            /* Gemma RMSNorm: scale = 1 + g (fp32)        */
+} mr_norm_kind;
+
 /* Launch options, process-wide (bits for mr_set_launch_flags). */
 #define MR_LAUNCH_PDL 1         /* programmatic dependent launch, see below */
 #define MR_LAUNCH_TEST_STALL 2  /* test hook for the timeout path, see below */
@@ -246,6 +251,45 @@ int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
                             int32_t *num_tokens_post_padded, int64_t capacity,
                             uint8_t *q, uint8_t *scale,
                             void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * a6 on the norm's scale [sgl-amd-mono #56 page, entry #59 "[Perf]
+ * minimax_m31: Run o_proj in the launch, route on the norm's scale, read B
+ * operands from LDS", Modifications, "Route on the norm's scale": the
+ * RMSNorm in front of the router publishes each token's rstd, and the router
+ * normalises its own columns of the residual sum instead of waiting for the
+ * norm's output].  The router input is
+ *     xn[m, k] = bf16( (sres[m, k] * rstd[m]) * s[k] ),
+ * both products fp32 with round-to-nearest-even, the bf16 store rounding to
+ * nearest even; s = norm_weight[k] (MR_NORM_RMS) or 1 + norm_weight[k] in
+ * fp32 (MR_NORM_GEMMA, the Gemma RMSNorm of the MiniMax-M3 producers in
+ * sglang #46691, "Changes to existing kernels").  Every output (logits, ids,
+ * weights, sort, and q / scale, the MXFP8 of xn) is bitwise equal to
+ * mr_norm_apply -> mr_moe_route_sort_quant on the same inputs.
+ * sres: bf16 [M, ldx] (the un-normalised residual rows, 16-byte aligned);
+ * rstd: fp32 [M] (4-byte aligned), read after the previous kernel on the
+ * stream has finished; norm_weight: bf16 [K] (16-byte aligned).  The rest as
+ * mr_moe_route_sort_quant, with its limits.  A NULL rstd or norm_weight, or
+ * an unknown norm_kind, returns MR_ERR_INVALID_ARG.
+ */
+int mr_moe_route_sort_quant_norm(const void *sres, int64_t ldx, const float *rstd,
+                                 const void *norm_weight, int norm_kind, const void *w,
+                                 int M, int N, int K, int topk, int scoring,
+                                 const float *sel_bias, int renormalize, int block,
+                                 float *logits, int32_t *topk_ids, float *topk_weights,
+                                 int32_t *sorted_token_ids, int32_t *expert_ids,
+                                 int32_t *num_tokens_post_padded, int64_t capacity,
+                                 uint8_t *q, uint8_t *scale,
+                                 void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * The router input on the norm's scale, written out (the norm's XN; the
+ * unfused half of mr_moe_route_sort_quant_norm): xn[m, k] as defined there,
+ * row-major [M, K], 16-byte aligned.  Any M >= 1; K % 8 == 0 (else
+ * MR_ERR_UNSUPPORTED).  One launch.
+ */
+int mr_norm_apply(const void *sres, int64_t ldx, const float *rstd, const void *norm_weight,
+                  int norm_kind, int M, int K, void *xn, void *stream);
 
 /* Bytes of the library-owned scratch of mr_router_gemv_noalloc (8 MiB). */
 #define MR_NOALLOC_SCRATCH_BYTES 8388608

@@ -118,6 +118,19 @@ def test_validation_returns_before_any_launch(lib):
     assert lib.mr_moe_route_sort_quant(fake, 6144, fake, 17, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake,
                                        fake, fake, fake, 1 << 20, fake, fake, fake, 32768 + 17 * 8 * 4 - 4,
                                        None) == mr.MR_ERR_SCRATCH_TOO_SMALL
+    # route on the norm's scale: null rstd, misaligned norm weight, unknown
+    # norm kind; then the fused route's own checks (M > 64)
+    args = (fake, 128, 6144, 8, 0, None, 1, 16, fake, fake, fake, fake, fake, fake, 1 << 20, fake, fake, fake,
+            1 << 20, None)
+    assert lib.mr_moe_route_sort_quant_norm(fake, 6144, None, fake, 1, fake, 1, *args[1:]) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_moe_route_sort_quant_norm(fake, 6144, fake, P(0x1008), 1, fake, 1,
+                                            *args[1:]) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_moe_route_sort_quant_norm(fake, 6144, fake, fake, 2, fake, 1, *args[1:]) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_moe_route_sort_quant_norm(fake, 6144, fake, fake, 1, fake, 65, *args[1:]) == mr.MR_ERR_UNSUPPORTED
+    # written-out norm: K % 8, null output, bad kind
+    assert lib.mr_norm_apply(fake, 48, fake, fake, 0, 2, 44, fake, None) == mr.MR_ERR_UNSUPPORTED
+    assert lib.mr_norm_apply(fake, 48, fake, fake, 0, 2, 48, None, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_norm_apply(fake, 48, fake, fake, 5, 2, 48, fake, None) == mr.MR_ERR_INVALID_ARG
     # launch options and the wait limit (host-only settings)
     assert lib.mr_set_launch_flags(8) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_set_launch_flags(mr.LAUNCH_LEGACY_MMA) == mr.MR_OK
