@@ -53,6 +53,10 @@ def _load():
         lib.oracle_bf16_round.argtypes = [ctypes.c_float]
         lib.oracle_bf16_round.restype = ctypes.c_uint16
         lib.oracle_norm_apply.argtypes = [P, i64, P, P, i32, i32, i32, P]
+        lib.oracle_e2m1_encode.argtypes = [ctypes.c_double]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+        lib.oracle_e2m1_encode_array.argtypes = [P, i64, P]
+        lib.oracle_mxfp4_quant.argtypes = [P, i64, i32, i32, P, P]
         _lib = lib
     return _lib
 
@@ -179,3 +183,25 @@ def route_sort_quant_norm(sres_bf16, rstd, g_bf16, kind, w_bf16, topk, block, sc
     out = route_sort_quant(xn, w_bf16, topk, block, scoring, bias, renormalize)
     out["xn"] = xn
     return out
+
+
+def e2m1_encode(v: float) -> int:
+    return int(_load().oracle_e2m1_encode(float(v)))
+
+
+def e2m1_encode_array(values) -> np.ndarray:
+    v = _c(values, np.float64).ravel()
+    out = np.empty(v.shape[0], dtype=np.uint8)
+    _load().oracle_e2m1_encode_array(_ptr(v), v.shape[0], _ptr(out))
+    return out.reshape(np.shape(values))
+
+
+def mxfp4_quant(x_bf16: np.ndarray):
+    """(q uint8 [M, K/2] packed e2m1 codes, scale uint8 [M, K/32] e8m0 bytes)."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert K % 32 == 0
+    q = np.empty((M, K // 2), dtype=np.uint8)
+    s = np.empty((M, K // 32), dtype=np.uint8)
+    _load().oracle_mxfp4_quant(_ptr(x), K, M, K, _ptr(q), _ptr(s))
+    return q, s

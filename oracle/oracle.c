@@ -372,3 +372,75 @@ void oracle_norm_apply(const uint16_t *x, int64_t ldx, const float *rstd,
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Next row: MXFP4 stage-1 activations.                                */
+/* sglang #46691, Summary ("MoE sorting + quant"): the MiniMax-M3.1    */
+/* sort kernels quantise the stage-1 activations to MXFP4.  The pages  */
+/* give no formula; READING: the OCP Microscaling Formats v1.0 MXFP4   */
+/* element and scale rules, laid out like the MXFP8 output.            */
+/* ------------------------------------------------------------------ */
+
+/*
+ * E2M1 (OCP FP4: 1 sign, 2 exponent bits with bias 1, 1 mantissa bit; no
+ * infinities or NaN) of an exact value v: the nearest of the magnitudes
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7), ties to the even code;
+ * magnitudes above 6 saturate to 6 (READING, as for E4M3).  Sign bit 3 is
+ * kept, so values that round to zero from below give 0x8.
+ */
+uint8_t oracle_e2m1_encode(double v)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs(v);
+    if (a >= 6.0) return sign | 0x7;
+    int best = 0;
+    for (int i = 1; i < 8; ++i) {
+        double d = fabs(a - mag[i]), db = fabs(a - mag[best]);
+        if (d < db || (d == db && (i & 1) == 0)) best = i;
+    }
+    return sign | (uint8_t)best;
+}
+
+void oracle_e2m1_encode_array(const double *v, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_encode(v[i]);
+}
+
+/*
+ * Shared scale of one block of 32: X = floor(log2(amax)) - 2 (2 = emax of
+ * E2M1), clamped to [-127, 127]; an all-zero block takes X = -127 (byte 0).
+ * Elements: e2m1(x * 2^-X).  Output: q [M, K/2] row-major, two elements a
+ * byte, element 2j in the low nibble and 2j + 1 in the high nibble (READING:
+ * the usual fp4x2 packing); scale [M, K/32] row-major E8M0 bytes X + 127.
+ */
+void oracle_mxfp4_quant(const uint16_t *x, int64_t ldx, int M, int K,
+                        uint8_t *q, uint8_t *scale)
+{
+    for (int m = 0; m < M; ++m) {
+        for (int b = 0; b < K / 32; ++b) {
+            const uint16_t *blk = x + (int64_t)m * ldx + (int64_t)b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs(bf16_value(blk[i]));
+                if (a > amax) amax = a;
+            }
+            int X;
+            if (amax == 0.0) {
+                X = -127;
+            } else {
+                int e2;
+                frexp(amax, &e2);
+                X = (e2 - 1) - 2;
+                if (X < -127) X = -127;
+                if (X > 127) X = 127;
+            }
+            scale[(int64_t)m * (K / 32) + b] = (uint8_t)(X + 127);
+            for (int i = 0; i < 32; i += 2) {
+                uint8_t lo = oracle_e2m1_encode(ldexp(bf16_value(blk[i]), -X));
+                uint8_t hi = oracle_e2m1_encode(ldexp(bf16_value(blk[i + 1]), -X));
+                q[(int64_t)m * (K / 2) + (int64_t)b * 16 + i / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+}
