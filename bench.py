@@ -494,6 +494,24 @@ def run_ours(args):
         rt.destroy(g)
         return e0.elapsed_time(e1) * 1e3 / (reps * calls)
 
+    # A/B of the split-K hand-off: the one launch (partials summed in a fixed
+    # order by the row's owner, then the gate) against the four-call chain
+    # (GEMV with its own in-kernel reduction, gate, sort, quant launches)
+    for M in MS:
+        o = outs[M]
+
+        def body_chain(M=M, o=o):
+            for r in range(64):
+                x, w = xs[M][r % SLOTS], ws[M][r % SLOTS]
+                mr.router_gemv(x, w, out=o["logits"], scratch=scratch)
+                mr.route_topk(o["logits"], TOPK, ids=o["topk_ids"], weights=o["topk_weights"])
+                mr.moe_sort(o["topk_ids"], N_EXP, BLOCK, scratch=scratch,
+                            out=(o["sorted_token_ids"], o["expert_ids"], o["num_tokens_post_padded"]))
+                mr.mxfp8_quant(x, out=(o["q"], o["scale"]))
+        with torch.cuda.stream(stream):
+            body_chain()
+        per_m[str(M)]["four_call_chain_us"] = round(graph_us(body_chain, 64), 3)
+
     # 896 experts, hidden 3584, sigmoid score + selection bias, top-16
     # (one launch per call; 32 rotating copies of the 6.4 MB gate weight)
     k3 = {}
@@ -574,20 +592,30 @@ def run_ours(args):
         for r in range(8):
             mr.mxfp8_quant(px[r % 4], out=(pq, ps))
 
+    pq4 = torch.empty((PM, K_HID // 2), dtype=torch.uint8, device=dev)
+
+    def body_q4():
+        for r in range(8):
+            mr.mxfp4_quant(px[r % 4], out=(pq4, ps))
+
     def body_s():
         for r in range(8):
             mr.moe_sort(pids, N_EXP, PB, out=psort, scratch=pssk)
     with torch.cuda.stream(stream):
         body_q()
+        body_q4()
         body_s()
-    q_us, s_us = graph_us(body_q, 8), graph_us(body_s, 8)
+    q_us, q4_us, s_us = graph_us(body_q, 8), graph_us(body_q4, 8), graph_us(body_s, 8)
+    q4_bytes = 2 * PM * K_HID + PM * K_HID // 2 + PM * K_HID // 32
     q_bytes = 2 * PM * K_HID + PM * K_HID + PM * K_HID // 32
     s_bytes = 4 * PM * TOPK + 4 * pcap + 4 * (pcap // PB) + 4
     prefill = {"mxfp8_quant": {"us_per_call": round(q_us, 3), "GBs": round(q_bytes / (q_us * 1e-6) / 1e9, 1),
                                "frac_of_peak": round(q_bytes / (q_us * 1e-6) / 1e9 / peak, 4)},
+               "mxfp4_quant": {"us_per_call": round(q4_us, 3), "GBs": round(q4_bytes / (q4_us * 1e-6) / 1e9, 1),
+                               "frac_of_peak": round(q4_bytes / (q4_us * 1e-6) / 1e9 / peak, 4)},
                "moe_sort_block64": {"us_per_call": round(s_us, 3),
                                     "GBs": round(s_bytes / (s_us * 1e-6) / 1e9, 1)}}
-    del px, pq, ps, plog, psk, pids, psort, pssk
+    del px, pq, pq4, ps, plog, psk, pids, psort, pssk
 
     # end to end through the public API: pinned host x in, outputs back out
     e2e_steps = min(args.steps, 2000)

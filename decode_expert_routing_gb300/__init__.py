@@ -30,6 +30,7 @@ _lib = None
 MR_OK, MR_ERR_UNSUPPORTED, MR_ERR_INVALID_ARG, MR_ERR_SCRATCH_TOO_SMALL, MR_ERR_CUDA, MR_ERR_TIMEOUT = range(6)
 SCORING = {"softmax": 0, "sigmoid": 1}
 NORM_KIND = {"rms": 0, "gemma": 1}
+QUANT_FORMAT = {None: 0, "mxfp8": 1, "mxfp4": 2}
 SCRATCH_COUNTER_BYTES = 32768
 
 
@@ -71,6 +72,8 @@ SIGNATURES = {
     "mr_moe_route_sort_quant_norm": (_I, [_P, _I64, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P,
                                           _P, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
     "mr_norm_apply": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
+    "mr_mxfp4_quant": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
+    "mr_moe_route": (_I, [_P, _P]),
     "mr_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "mr_device_error": (_I, [_I]),
 }
@@ -303,8 +306,24 @@ def mxfp8_quant(x, out=None, stream=None):
     return q, s
 
 
-def alloc_route_outputs(M: int, N: int, K: int, topk: int, block: int, device, quant: bool = True):
-    """Output tensors of moe_route_sort_quant (a dict)."""
+def mxfp4_quant(x, out=None, stream=None):
+    """(q uint8 [M, K/2] packed e2m1 codes, element 2j in the low nibble;
+    scale uint8 [M, K/32] e8m0)."""
+    torch = _torch()
+    ldx = _row_major_2d(x, "x")
+    M, K = x.shape
+    if out is None:
+        out = (torch.empty((M, K // 2), dtype=torch.uint8, device=x.device),
+               torch.empty((M, K // 32), dtype=torch.uint8, device=x.device))
+    q, s = out
+    _check(_load().mr_mxfp4_quant(_dev_ptr(x, "x", torch.bfloat16), ldx, M, K, _dev_ptr(q, "q", torch.uint8),
+                                  _dev_ptr(s, "scale", torch.uint8), _stream_ptr(stream)), "mr_mxfp4_quant")
+    return q, s
+
+
+def alloc_route_outputs(M: int, N: int, K: int, topk: int, block: int, device, quant=True):
+    """Output tensors of the one-launch route (a dict).  quant: True or
+    "mxfp8" (q [M, K]), "mxfp4" (q [M, K/2]), False or None (no q / scale)."""
     torch = _torch()
     cap = sort_capacity(M, topk, N, block)
     out = dict(
@@ -316,7 +335,7 @@ def alloc_route_outputs(M: int, N: int, K: int, topk: int, block: int, device, q
         num_tokens_post_padded=torch.empty(1, dtype=torch.int32, device=device),
     )
     if quant:
-        out["q"] = torch.empty((M, K), dtype=torch.uint8, device=device)
+        out["q"] = torch.empty((M, K // 2 if quant == "mxfp4" else K), dtype=torch.uint8, device=device)
         out["scale"] = torch.empty((M, K // 32), dtype=torch.uint8, device=device)
     return out
 
@@ -406,4 +425,74 @@ def moe_route_sort_quant_norm(sres, rstd, norm_weight, w, topk: int, block: int,
         out["sorted_token_ids"].numel(), _dev_ptr(q, "q", torch.uint8, allow_none=True),
         _dev_ptr(s, "scale", torch.uint8, allow_none=True), scratch.ptr, scratch.nbytes,
         _stream_ptr(stream)), "mr_moe_route_sort_quant_norm")
+    return out
+
+
+class RouteParams(ctypes.Structure):
+    """mr_route_params of moe_route.h, field for field."""
+    _fields_ = [
+        ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("rstd", ctypes.c_void_p),
+        ("norm_weight", ctypes.c_void_p), ("norm_kind", ctypes.c_int), ("w", ctypes.c_void_p),
+        ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int), ("topk", ctypes.c_int),
+        ("scoring", ctypes.c_int), ("sel_bias", ctypes.c_void_p), ("renormalize", ctypes.c_int),
+        ("block", ctypes.c_int), ("quant_format", ctypes.c_int), ("logits", ctypes.c_void_p),
+        ("topk_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p), ("sorted_token_ids", ctypes.c_void_p),
+        ("expert_ids", ctypes.c_void_p), ("num_tokens_post_padded", ctypes.c_void_p), ("capacity", ctypes.c_int64),
+        ("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("scratch", ctypes.c_void_p),
+        ("scratch_bytes", ctypes.c_size_t),
+    ]
+
+
+def moe_route(x, w, topk: int, block: int, scoring: str = "softmax", bias=None, renormalize: bool = True,
+              quant="mxfp8", rstd=None, norm_weight=None, norm: str = "gemma", out=None,
+              scratch: Scratch | None = None, stream=None):
+    """The one-launch route with every option (mr_moe_route): quant "mxfp8",
+    "mxfp4" or None; with rstd (and norm_weight) x holds the residual rows
+    and the route runs on the norm's scale.  Returns a dict of outputs."""
+    torch = _torch()
+    ldx = _row_major_2d(x, "x")
+    M, K = x.shape
+    N = w.shape[0]
+    if not w.is_contiguous() or w.shape[1] != K:
+        raise ValueError("w must be contiguous [N, K]")
+    if quant not in QUANT_FORMAT:
+        raise ValueError(f"quant must be one of {list(QUANT_FORMAT)}")
+    if rstd is not None:
+        if norm_weight is None:
+            raise ValueError("rstd needs norm_weight")
+        _check_norm_args(rstd, norm_weight, M, K)
+    if out is None:
+        out = alloc_route_outputs(M, N, K, topk, block, x.device, quant)
+    if scratch is None:
+        scratch = Scratch(M, N, K, topk, device=x.device)
+    p = RouteParams()
+    p.x = _dev_ptr(x, "x", torch.bfloat16)
+    p.ldx = ldx
+    p.rstd = _dev_ptr(rstd, "rstd", torch.float32, allow_none=True)
+    p.norm_weight = _dev_ptr(norm_weight, "norm_weight", torch.bfloat16, allow_none=True)
+    p.norm_kind = NORM_KIND[norm]
+    p.w = _dev_ptr(w, "w", torch.bfloat16)
+    p.M, p.N, p.K, p.topk = M, N, K, topk
+    p.scoring = SCORING[scoring]
+    p.sel_bias = _dev_ptr(bias, "bias", torch.float32, allow_none=True)
+    p.renormalize = int(renormalize)
+    p.block = block
+    p.quant_format = QUANT_FORMAT[quant]
+    p.logits = _dev_ptr(out["logits"], "logits", torch.float32)
+    p.topk_ids = _dev_ptr(out["topk_ids"], "topk_ids", torch.int32)
+    p.topk_weights = _dev_ptr(out["topk_weights"], "topk_weights", torch.float32)
+    p.sorted_token_ids = _dev_ptr(out["sorted_token_ids"], "sorted_token_ids", torch.int32)
+    p.expert_ids = _dev_ptr(out["expert_ids"], "expert_ids", torch.int32)
+    p.num_tokens_post_padded = _dev_ptr(out["num_tokens_post_padded"], "num_tokens_post_padded", torch.int32)
+    p.capacity = out["sorted_token_ids"].numel()
+    if quant is not None:
+        qt, st = out["q"], out["scale"]
+        want = K // 2 if quant == "mxfp4" else K
+        if tuple(qt.shape) != (M, want) or tuple(st.shape) != (M, K // 32):
+            raise ValueError(f"q must be [M, {want}] and scale [M, K/32] for {quant}")
+        p.q = _dev_ptr(qt, "q", torch.uint8)
+        p.scale = _dev_ptr(st, "scale", torch.uint8)
+    p.scratch = scratch.ptr
+    p.scratch_bytes = scratch.nbytes
+    _check(_load().mr_moe_route(ctypes.byref(p), _stream_ptr(stream)), "mr_moe_route")
     return out

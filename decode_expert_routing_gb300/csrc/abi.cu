@@ -257,51 +257,63 @@ int mr_mxfp8_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t
     if (s != MR_OK) return s;
     if (K % 32 != 0) return MR_ERR_UNSUPPORTED;
     if (q == nullptr || !aligned(q, 8) || scale == nullptr) return MR_ERR_INVALID_ARG;
-    return cuda_status(mr::launch_quant(x, ldx, M, K, q, scale, as_stream(stream)));
+    return cuda_status(mr::launch_quant(x, ldx, M, K, q, scale, false, as_stream(stream)));
+}
+
+int mr_mxfp4_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, void* stream) {
+    int s = check_x(x, ldx, M, K);
+    if (s != MR_OK) return s;
+    if (K % 32 != 0) return MR_ERR_UNSUPPORTED;
+    if (q == nullptr || !aligned(q, 4) || scale == nullptr) return MR_ERR_INVALID_ARG;
+    return cuda_status(mr::launch_quant(x, ldx, M, K, q, scale, true, as_stream(stream)));
 }
 
 }  // extern "C"
 
-// The one-launch route; rstd != nullptr puts the router input on the norm's
-// scale (residual rows x rstd x norm weight, rounded to bf16 in the kernel).
-static int route_sort_quant(const void* x, int64_t ldx, const float* rstd, const void* norm_w, int norm_kind,
-                            const void* w, int M, int N, int K, int topk, int scoring, const float* sel_bias,
-                            int renormalize, int block, float* logits, int32_t* topk_ids, float* topk_weights,
-                            int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* num_tokens_post_padded,
-                            int64_t capacity, uint8_t* q, uint8_t* scale, void* scratch, size_t scratch_bytes,
-                            void* stream) {
-    int s = check_x(x, ldx, M, K);
+static int check_norm(const float* rstd, const void* norm_w, int norm_kind);
+
+// The one-launch route.  p->rstd != nullptr puts the router input on the
+// norm's scale (residual rows x rstd x norm weight, rounded to bf16 in the
+// kernel); p->quant_format picks the stage-1 activation format.
+static int route_impl(const mr_route_params* p, void* stream) {
+    if (p == nullptr) return MR_ERR_INVALID_ARG;
+    const int M = p->M, N = p->N, K = p->K, topk = p->topk, scoring = p->scoring, block = p->block;
+    int s = check_x(p->x, p->ldx, M, K);
     if (s != MR_OK) return s;
     if ((s = check_gate_args(M, N, topk, scoring)) != MR_OK) return s;
-    if ((s = check_sort_args(M, topk, N, block, capacity)) != MR_OK) return s;
+    if ((s = check_sort_args(M, topk, N, block, p->capacity)) != MR_OK) return s;
+    if (p->rstd != nullptr && (s = check_norm(p->rstd, p->norm_weight, p->norm_kind)) != MR_OK) return s;
     if (M > MR_MAX_FUSED_ROWS || K % MR_GEMV_K_MULTIPLE != 0) return MR_ERR_UNSUPPORTED;
-    if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) ||
-        topk_ids == nullptr || !aligned(topk_ids, 4) || topk_weights == nullptr ||
-        !aligned(topk_weights, 4) || sorted_token_ids == nullptr || !aligned(sorted_token_ids, 4) ||
-        expert_ids == nullptr || !aligned(expert_ids, 4) || num_tokens_post_padded == nullptr ||
-        !aligned(num_tokens_post_padded, 4) || (sel_bias && !aligned(sel_bias, 4)))
+    if (p->w == nullptr || !aligned(p->w, 16) || p->logits == nullptr || !aligned(p->logits, 8) ||
+        p->topk_ids == nullptr || !aligned(p->topk_ids, 4) || p->topk_weights == nullptr ||
+        !aligned(p->topk_weights, 4) || p->sorted_token_ids == nullptr || !aligned(p->sorted_token_ids, 4) ||
+        p->expert_ids == nullptr || !aligned(p->expert_ids, 4) || p->num_tokens_post_padded == nullptr ||
+        !aligned(p->num_tokens_post_padded, 4) || (p->sel_bias && !aligned(p->sel_bias, 4)))
         return MR_ERR_INVALID_ARG;
-    if ((q == nullptr) != (scale == nullptr)) return MR_ERR_INVALID_ARG;
-    if (q != nullptr && !aligned(q, 8)) return MR_ERR_INVALID_ARG;
+    const int qf = p->quant_format;
+    if (qf != MR_QUANT_NONE && qf != MR_QUANT_MXFP8 && qf != MR_QUANT_MXFP4) return MR_ERR_INVALID_ARG;
+    if (qf != MR_QUANT_NONE && (p->q == nullptr || !aligned(p->q, 8) || p->scale == nullptr))
+        return MR_ERR_INVALID_ARG;
     mr::RoutePlan rp;
     if (!mr::route_plan(M, N, K, topk, 1, mr::route_cluster_size(), &rp, allow_tc())) return MR_ERR_UNSUPPORTED;
-    mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 1);
+    mr::RouteArgs a = route_args(rp, p->x, p->ldx, p->w, M, N, K, 1);
     if (rp.clusters > 1) {  // the clusters meet in scratch: a ticket and every token's ids
-        if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;
-        if (scratch_bytes < mr::kWorkOffset + (size_t)M * topk * 4) return MR_ERR_SCRATCH_TOO_SMALL;
-        a.counter = static_cast<unsigned*>(scratch) + mr::kFusedCounterSlot;
-        a.ids_scratch = reinterpret_cast<int32_t*>(static_cast<char*>(scratch) + mr::kWorkOffset);
+        if (p->scratch == nullptr || !aligned(p->scratch, 256)) return MR_ERR_INVALID_ARG;
+        if (p->scratch_bytes < mr::kWorkOffset + (size_t)M * topk * 4) return MR_ERR_SCRATCH_TOO_SMALL;
+        a.counter = static_cast<unsigned*>(p->scratch) + mr::kFusedCounterSlot;
+        a.ids_scratch = reinterpret_cast<int32_t*>(static_cast<char*>(p->scratch) + mr::kWorkOffset);
     }
-    a.bias = scoring == MR_SCORE_SIGMOID ? sel_bias : nullptr;
-    a.logits = logits;
-    a.ids = topk_ids;
-    a.weights = topk_weights;
-    a.sorted = sorted_token_ids;
-    a.expert_ids = expert_ids;
-    a.ntpp = num_tokens_post_padded;
-    a.capacity = capacity;
-    a.q = q;
-    a.scale = scale;
+    a.bias = scoring == MR_SCORE_SIGMOID ? p->sel_bias : nullptr;
+    a.logits = p->logits;
+    a.ids = p->topk_ids;
+    a.weights = p->topk_weights;
+    a.sorted = p->sorted_token_ids;
+    a.expert_ids = p->expert_ids;
+    a.ntpp = p->num_tokens_post_padded;
+    a.capacity = p->capacity;
+    a.q = qf == MR_QUANT_NONE ? nullptr : p->q;
+    a.scale = qf == MR_QUANT_NONE ? nullptr : p->scale;
+    a.quant_fp4 = qf == MR_QUANT_MXFP4 ? 1 : 0;
     a.topk = topk;
     {  // gate threshold lane groups: the largest power of two <= 32 threads
        // leaving at least topk groups that hold experts (thread t: experts t
@@ -315,10 +327,10 @@ static int route_sort_quant(const void* x, int64_t ldx, const float* rstd, const
     a.mag_k = mr::div_magic(topk);
     a.mag_block = mr::div_magic(block);
     a.scoring = scoring;
-    a.renormalize = renormalize ? 1 : 0;
-    a.rstd = rstd;
-    a.norm_w = static_cast<const uint16_t*>(norm_w);
-    a.norm_gemma = norm_kind == MR_NORM_GEMMA ? 1 : 0;
+    a.renormalize = p->renormalize ? 1 : 0;
+    a.rstd = p->rstd;
+    a.norm_w = static_cast<const uint16_t*>(p->norm_weight);
+    a.norm_gemma = p->norm_kind == MR_NORM_GEMMA ? 1 : 0;
     return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
 }
 
@@ -328,7 +340,41 @@ static int check_norm(const float* rstd, const void* norm_w, int norm_kind) {
     return MR_OK;
 }
 
+static mr_route_params fill_params(const void* x, int64_t ldx, const void* w, int M, int N, int K, int topk,
+                                   int scoring, const float* sel_bias, int renormalize, int block, float* logits,
+                                   int32_t* topk_ids, float* topk_weights, int32_t* sorted_token_ids,
+                                   int32_t* expert_ids, int32_t* num_tokens_post_padded, int64_t capacity,
+                                   uint8_t* q, uint8_t* scale, void* scratch, size_t scratch_bytes) {
+    mr_route_params p{};
+    p.x = x;
+    p.ldx = ldx;
+    p.w = w;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.topk = topk;
+    p.scoring = scoring;
+    p.sel_bias = sel_bias;
+    p.renormalize = renormalize;
+    p.block = block;
+    p.logits = logits;
+    p.topk_ids = topk_ids;
+    p.topk_weights = topk_weights;
+    p.sorted_token_ids = sorted_token_ids;
+    p.expert_ids = expert_ids;
+    p.num_tokens_post_padded = num_tokens_post_padded;
+    p.capacity = capacity;
+    p.q = q;
+    p.scale = scale;
+    p.quant_format = (q == nullptr && scale == nullptr) ? MR_QUANT_NONE : MR_QUANT_MXFP8;
+    p.scratch = scratch;
+    p.scratch_bytes = scratch_bytes;
+    return p;
+}
+
 extern "C" {
+
+int mr_moe_route(const mr_route_params* p, void* stream) { return route_impl(p, stream); }
 
 int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, int N, int K, int topk,
                             int scoring, const float* sel_bias, int renormalize, int block,
@@ -336,9 +382,11 @@ int mr_moe_route_sort_quant(const void* x, int64_t ldx, const void* w, int M, in
                             int32_t* sorted_token_ids, int32_t* expert_ids,
                             int32_t* num_tokens_post_padded, int64_t capacity, uint8_t* q,
                             uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
-    return route_sort_quant(x, ldx, nullptr, nullptr, 0, w, M, N, K, topk, scoring, sel_bias, renormalize, block,
-                            logits, topk_ids, topk_weights, sorted_token_ids, expert_ids, num_tokens_post_padded,
-                            capacity, q, scale, scratch, scratch_bytes, stream);
+    if ((q == nullptr) != (scale == nullptr)) return MR_ERR_INVALID_ARG;
+    const mr_route_params p = fill_params(x, ldx, w, M, N, K, topk, scoring, sel_bias, renormalize, block, logits,
+                                          topk_ids, topk_weights, sorted_token_ids, expert_ids,
+                                          num_tokens_post_padded, capacity, q, scale, scratch, scratch_bytes);
+    return route_impl(&p, stream);
 }
 
 int mr_moe_route_sort_quant_norm(const void* sres, int64_t ldx, const float* rstd, const void* norm_weight,
@@ -349,9 +397,14 @@ int mr_moe_route_sort_quant_norm(const void* sres, int64_t ldx, const float* rst
                                  uint8_t* q, uint8_t* scale, void* scratch, size_t scratch_bytes, void* stream) {
     const int s = check_norm(rstd, norm_weight, norm_kind);
     if (s != MR_OK) return s;
-    return route_sort_quant(sres, ldx, rstd, norm_weight, norm_kind, w, M, N, K, topk, scoring, sel_bias,
-                            renormalize, block, logits, topk_ids, topk_weights, sorted_token_ids, expert_ids,
-                            num_tokens_post_padded, capacity, q, scale, scratch, scratch_bytes, stream);
+    if ((q == nullptr) != (scale == nullptr)) return MR_ERR_INVALID_ARG;
+    mr_route_params p = fill_params(sres, ldx, w, M, N, K, topk, scoring, sel_bias, renormalize, block, logits,
+                                    topk_ids, topk_weights, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                                    capacity, q, scale, scratch, scratch_bytes);
+    p.rstd = rstd;
+    p.norm_weight = norm_weight;
+    p.norm_kind = norm_kind;
+    return route_impl(&p, stream);
 }
 
 int mr_norm_apply(const void* sres, int64_t ldx, const float* rstd, const void* norm_weight, int norm_kind, int M,

@@ -144,14 +144,15 @@ __device__ __forceinline__ float warp_sum_fixed(float v) {
 // ---------------------------------------------------------------- MXFP8
 
 // E8M0 exponent X of a 32-block from the largest |x| as a bf16 magnitude
-// pattern (sign cleared): X = floor(log2(amax)) - 8, clamped to [-127, 127];
-// amax == 0 gives -127.  Integer-exact: normal bf16 -> exponent field - 127,
-// subnormal bf16 (value = mant * 2^-133) -> msb(mant) - 133.
-__device__ __forceinline__ int mx_scale_exponent(unsigned amax16) {
+// pattern (sign cleared): X = floor(log2(amax)) - emax (8 for E4M3, 2 for
+// E2M1), clamped to [-127, 127]; amax == 0 gives -127.  Integer-exact:
+// normal bf16 -> exponent field - 127, subnormal bf16 (value = mant * 2^-133)
+// -> msb(mant) - 133.
+__device__ __forceinline__ int mx_scale_exponent(unsigned amax16, int emax) {
     if (amax16 == 0u) return -127;
     unsigned e = amax16 >> 7;
     int fl = (e != 0u) ? (int)e - 127 : (31 - __clz((int)(amax16 & 0x7Fu))) - 133;
-    int X = fl - 8;
+    int X = fl - emax;
     return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 
@@ -171,7 +172,7 @@ __device__ __forceinline__ uint2 mx_quant_quad(uint4 v, unsigned* scale_byte) {
     m = max(m, max_mag16(v.w));
     m = max(m, __shfl_xor_sync(kFull, m, 1));
     m = max(m, __shfl_xor_sync(kFull, m, 2));
-    int X = mx_scale_exponent(m);
+    int X = mx_scale_exponent(m, 8);
     *scale_byte = (unsigned)(X + 127);
     // 2^-X is a normal fp32 for every X reachable from bf16 input (X <= 119).
     float inv = __uint_as_float((unsigned)(127 - X) << 23);
@@ -188,6 +189,50 @@ __device__ __forceinline__ uint2 mx_quant_quad(uint4 v, unsigned* scale_byte) {
             out[i >> 1] = (uint32_t)p;
     }
     return make_uint2(out[0], out[1]);
+}
+
+// ---------------------------------------------------------------- MXFP4
+
+// Eight fp32 values -> eight E2M1 codes (round to nearest even, saturating
+// to +-6, sign kept), element i in bits 4i .. 4i + 3.  The conversion puts
+// its first source operand in the high nibble of each byte.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+    uint32_t d;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(d)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return d;
+}
+
+// MXFP4 of the 8 consecutive bf16 values of v (one lane of the lane quad
+// that holds a 32-block, as mx_quant_quad).  Returns the 8 packed E2M1 codes
+// (element i in nibble i: 4 bytes of the [M, K/2] output) and writes the
+// block's E8M0 byte X + 127, X = floor(log2(amax)) - 2.
+__device__ __forceinline__ uint32_t mx4_quant_quad(uint4 v, unsigned* scale_byte) {
+    unsigned m = max_mag16(v.x);
+    m = max(m, max_mag16(v.y));
+    m = max(m, max_mag16(v.z));
+    m = max(m, max_mag16(v.w));
+    m = max(m, __shfl_xor_sync(kFull, m, 1));
+    m = max(m, __shfl_xor_sync(kFull, m, 2));
+    int X = mx_scale_exponent(m, 2);
+    *scale_byte = (unsigned)(X + 127);
+    // X in [-127, 125] for bf16 input: 2^-X is a normal fp32, and x * 2^-X
+    // is exact wherever it can round to a nonzero code
+    float inv = __uint_as_float((unsigned)(127 - X) << 23);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __fmul_rn(__uint_as_float(w[i] << 16), inv);
+        f[2 * i + 1] = __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv);
+    }
+    return e2m1x8(f);
 }
 
 // ---------------------------------------------------------------- sigmoid

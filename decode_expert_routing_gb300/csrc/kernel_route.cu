@@ -199,9 +199,9 @@ __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* ro
     return __fdiv_rn(num, den);
 }
 
-// MXFP8 of this CTA's x slice (rows row0 .. row0 + Mq, columns kslice ..
-// kslice + kc), one lane quad per 32-element block; every thread of the CTA
-// takes part.
+// MXFP8 (or MXFP4) of this CTA's x slice (rows row0 .. row0 + Mq, columns
+// kslice .. kslice + kc), one lane quad per 32-element block; every thread of
+// the CTA takes part.
 __device__ __forceinline__ void quant_slice(const RouteArgs& a, const unsigned char* xs, int Mq, int row0,
                                             int64_t kslice) {
     if (a.q == nullptr) return;
@@ -213,12 +213,15 @@ __device__ __forceinline__ void quant_slice(const RouteArgs& a, const unsigned c
         const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
         const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
         unsigned sb;
-        const uint2 q8 = mx_quant_quad(d, &sb);
-        if (v < nvec) {
-            const int64_t kk = kslice + cv * 8;
-            *reinterpret_cast<uint2*>(a.q + (int64_t)(row0 + r) * K + kk) = q8;
-            if ((cv & 3) == 0) a.scale[(int64_t)(row0 + r) * K32 + kk / 32] = (uint8_t)sb;
+        const int64_t kk = kslice + cv * 8;
+        if (a.quant_fp4) {  // MXFP4: q [M, K/2], two E2M1 codes a byte
+            const uint32_t q4 = mx4_quant_quad(d, &sb);
+            if (v < nvec) *reinterpret_cast<uint32_t*>(a.q + (int64_t)(row0 + r) * (K / 2) + kk / 2) = q4;
+        } else {
+            const uint2 q8 = mx_quant_quad(d, &sb);
+            if (v < nvec) *reinterpret_cast<uint2*>(a.q + (int64_t)(row0 + r) * K + kk) = q8;
         }
+        if (v < nvec && (cv & 3) == 0) a.scale[(int64_t)(row0 + r) * K32 + kk / 32] = (uint8_t)sb;
     }
 }
 

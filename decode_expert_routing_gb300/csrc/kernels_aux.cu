@@ -188,60 +188,65 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
 // ------------------------------------------------------------------ quant
 
 // One lane quantises 8 consecutive elements; a lane quad is one 32-block.
-// Each warp takes 32 consecutive 16-byte vectors per step (4 rows' worth of
-// blocks never straddle: K % 32 == 0), UNROLL steps in flight.
+// Work is cut into tiles of one row x 32 * kQuantUnroll 16-byte vectors (a
+// warp per tile, kQuantUnroll loads in flight per lane): one 32-bit division
+// per tile locates it, so the per-element cost stays the quantiser's own.
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;
+constexpr int kQuantTileVec = 32 * kQuantUnroll;
 
-__global__ void __launch_bounds__(kQuantThreads) mxfp8_quant_kernel(const uint16_t* x, int64_t ldx,
-                                                                    int M, int K, uint8_t* q,
-                                                                    uint8_t* scale) {
+// FP4: MXFP4 (E2M1 codes, two a byte, q [M, K/2]); else MXFP8 (E4M3, q [M, K]).
+template <bool FP4>
+__global__ void __launch_bounds__(kQuantThreads) mx_quant_kernel(const uint16_t* x, int64_t ldx, int M, int K,
+                                                                 uint8_t* q, uint8_t* scale) {
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
-    const int64_t vpr = K / 8;                   // vectors per row
-    const int64_t total = (int64_t)M * vpr;
-    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t K32 = K / 32;
-    for (int64_t base = warp_id * 32 * kQuantUnroll; base < total; base += nwarps * 32 * kQuantUnroll) {
+    const int vpr = K / 8;                                   // vectors per row
+    const int tpr = (vpr + kQuantTileVec - 1) / kQuantTileVec;  // tiles per row
+    const int tiles = M * tpr;                               // < 2^31: checked on the host
+    const int warp_id = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int K32 = K / 32;
+    for (int tile = warp_id; tile < tiles; tile += nwarps) {
+        const int r = tile / tpr, c0 = (tile - r * tpr) * kQuantTileVec + lane;
+        const uint16_t* xr = x + (int64_t)r * ldx;
         uint4 v[kQuantUnroll];
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < total) {
-                const int64_t r = i / vpr, c = i - r * vpr;
-                v[u] = ld_stream_v4(x + r * ldx + c * 8);
-            }
+            const int c = c0 + u * 32;
+            v[u] = c < vpr ? ld_stream_v4(xr + c * 8) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
+            const int c = c0 + u * 32;
             unsigned sb;
-            const uint2 q8 = mx_quant_quad(v[u], &sb);
-            if (i < total) {
-                const int64_t r = i / vpr, c = i - r * vpr;
-                *reinterpret_cast<uint2*>(q + r * K + c * 8) = q8;
-                if ((lane & 3) == 0) scale[r * K32 + c / 4] = (uint8_t)sb;
+            if constexpr (FP4) {
+                const uint32_t q4 = mx4_quant_quad(v[u], &sb);
+                if (c < vpr) *reinterpret_cast<uint32_t*>(q + (int64_t)r * (K / 2) + c * 4) = q4;
+            } else {
+                const uint2 q8 = mx_quant_quad(v[u], &sb);
+                if (c < vpr) *reinterpret_cast<uint2*>(q + (int64_t)r * K + c * 8) = q8;
             }
+            if (c < vpr && (lane & 3) == 0) scale[(int64_t)r * K32 + c / 4] = (uint8_t)sb;
         }
     }
 }
 
-cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale,
+cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, bool fp4,
                          cudaStream_t st) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int64_t vectors = (int64_t)M * (K / 8);
-    const int64_t per_cta = (int64_t)kQuantThreads * kQuantUnroll;
-    int64_t ctas = (vectors + per_cta - 1) / per_cta;
+    const int64_t tiles = (int64_t)M * ((K / 8 + kQuantTileVec - 1) / kQuantTileVec);
+    if (tiles >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+    const int64_t warps_per_cta = kQuantThreads / 32;
+    int64_t ctas = (tiles + warps_per_cta - 1) / warps_per_cta;
     const int64_t cap = (int64_t)sms * 8;  // 8 resident CTAs per SM, grid-stride beyond
     if (ctas > cap) ctas = cap;
-    return launch_kernel(mxfp8_quant_kernel, dim3((unsigned)ctas), dim3(kQuantThreads), 0, st,
-                         static_cast<const uint16_t*>(x), ldx, M, K, q, scale);
+    return launch_kernel(fp4 ? mx_quant_kernel<true> : mx_quant_kernel<false>, dim3((unsigned)ctas),
+                         dim3(kQuantThreads), 0, st, static_cast<const uint16_t*>(x), ldx, M, K, q, scale);
 }
 
 // Router input on the norm's scale, written out: xn[m, k] = bf16((x[m, k] *
@@ -252,14 +257,27 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const uint16_t* x, int6
                                                          uint16_t* xn) {
     pdl_trigger();
     pdl_wait();
-    const int64_t vpr = K / 8;
-    const int64_t total = (int64_t)M * vpr;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / vpr, c = i - r * vpr;
-        const uint4 d = norm_chunk(ld_stream_v4(x + r * ldx + c * 8), ld_ro_v4(g + c * 8), __ldg(rstd + r),
-                                   gemma != 0);
-        *reinterpret_cast<uint4*>(xn + r * K + c * 8) = d;
+    const int lane = threadIdx.x & 31;
+    const int vpr = K / 8;
+    const int tpr = (vpr + kQuantTileVec - 1) / kQuantTileVec;
+    const int tiles = M * tpr;
+    const int warp_id = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    for (int tile = warp_id; tile < tiles; tile += nwarps) {
+        const int r = tile / tpr, c0 = (tile - r * tpr) * kQuantTileVec + lane;
+        const float rs = __ldg(rstd + r);
+        uint4 v[kQuantUnroll], gv[kQuantUnroll];
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int c = c0 + u * 32;
+            v[u] = c < vpr ? ld_stream_v4(x + (int64_t)r * ldx + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+            gv[u] = c < vpr ? ld_ro_v4(g + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int c = c0 + u * 32;
+            if (c < vpr) *reinterpret_cast<uint4*>(xn + (int64_t)r * K + c * 8) = norm_chunk(v[u], gv[u], rs, gemma != 0);
+        }
     }
 }
 
@@ -269,8 +287,9 @@ cudaError_t launch_norm_apply(const void* x, int64_t ldx, const float* rstd, con
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int64_t vectors = (int64_t)M * (K / 8);
-    int64_t ctas = (vectors + 255) / 256;
+    const int64_t tiles = (int64_t)M * ((K / 8 + kQuantTileVec - 1) / kQuantTileVec);
+    if (tiles >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+    int64_t ctas = (tiles + 7) / 8;  // 8 warps per CTA, a tile each
     const int64_t cap = (int64_t)sms * 8;
     if (ctas > cap) ctas = cap;
     return launch_kernel(norm_apply_kernel, dim3((unsigned)ctas), dim3(256), 0, st, static_cast<const uint16_t*>(x),

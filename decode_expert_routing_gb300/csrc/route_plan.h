@@ -63,6 +63,7 @@ struct RouteArgs {
     const float* rstd;
     const uint16_t* norm_w;
     int norm_gemma;
+    int quant_fp4;  // q holds MXFP4 ([M, K/2]) instead of MXFP8 ([M, K])
 };
 
 // Multiplier for division by d (1 <= d <= 2^11) of dividends below 2^21:

@@ -83,6 +83,12 @@ typedef enum mr_norm_kind {
     MR_NORM_GEMMA = 1            /* Gemma RMSNorm: scale = 1 + g (fp32)        */
 } mr_norm_kind;
 
+typedef enum mr_quant_format {
+    MR_QUANT_NONE = 0,           /* no stage-1 activation quant               */
+    MR_QUANT_MXFP8 = 1,          /* E4M3 codes q [M, K], E8M0 scales [M, K/32] */
+    MR_QUANT_MXFP4 = 2           /* E2M1 codes q [M, K/2], E8M0 scales [M, K/32] */
+} mr_quant_format;
+
 /* Launch options, process-wide (bits for mr_set_launch_flags). */
 #define MR_LAUNCH_PDL 1         /* programmatic dependent launch, see below */
 #define MR_LAUNCH_TEST_STALL 2  /* test hook for the timeout path, see below */
@@ -251,6 +257,62 @@ int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
                             int32_t *num_tokens_post_padded, int64_t capacity,
                             uint8_t *q, uint8_t *scale,
                             void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * a5, MXFP4 variant [sglang #46691 Summary: the MiniMax-M3.1 sort kernels
+ * MXFP4-quantise the stage-1 activations], per the OCP Microscaling Formats
+ * v1.0 spec: for each row and block of 32 elements along K,
+ * X = floor(log2(amax)) - 2 (2 = emax of E2M1), clamped to [-127, 127]
+ * (amax = 0 gives -127); scale[m, b] = X + 127 (E8M0); elements
+ * E2M1(x * 2^-X) (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), round to nearest
+ * even, saturating to +-6, sign kept.  q: uint8 [M, K/2] row-major, two
+ * codes a byte, element 2j in the low nibble (4-byte aligned); scale: uint8
+ * [M, K/32] row-major.  x: bf16 [M, ldx].  K % 32 == 0.  Any M >= 1.
+ */
+int mr_mxfp4_quant(const void *x, int64_t ldx, int M, int K, uint8_t *q,
+                   uint8_t *scale, void *stream);
+
+/*
+ * Every option of the one-launch route (a6) in one call.  Fields as the
+ * arguments of mr_moe_route_sort_quant and mr_moe_route_sort_quant_norm;
+ * in addition:
+ *  - rstd == NULL: x is the router input as given; else x holds the
+ *    un-normalised residual rows and the route runs on the norm's scale
+ *    (rstd, norm_weight, norm_kind as in mr_moe_route_sort_quant_norm);
+ *  - quant_format: MR_QUANT_NONE (q and scale ignored), MR_QUANT_MXFP8
+ *    (q [M, K]) or MR_QUANT_MXFP4 (q [M, K/2], as mr_mxfp4_quant); q must be
+ *    8-byte aligned.  An unknown format returns MR_ERR_INVALID_ARG.
+ * Every output is bitwise equal to the unfused calls on the same input
+ * (mr_norm_apply first when rstd != NULL; mr_mxfp8_quant or mr_mxfp4_quant
+ * for the quant).  The caller owns the struct; it is read during the call
+ * only.
+ */
+typedef struct mr_route_params {
+    const void *x;               /* bf16 [M, ldx] */
+    int64_t ldx;
+    const float *rstd;           /* NULL, or fp32 [M] */
+    const void *norm_weight;     /* bf16 [K] (with rstd) */
+    int norm_kind;               /* MR_NORM_* (with rstd) */
+    const void *w;               /* bf16 [N, K] gate weight */
+    int M, N, K, topk, scoring;
+    const float *sel_bias;       /* fp32 [N] or NULL (sigmoid scoring) */
+    int renormalize;
+    int block;
+    int quant_format;            /* MR_QUANT_* */
+    float *logits;               /* fp32 [M, N] */
+    int32_t *topk_ids;           /* [M, topk] */
+    float *topk_weights;         /* [M, topk] */
+    int32_t *sorted_token_ids;   /* [capacity] */
+    int32_t *expert_ids;         /* [capacity / block] */
+    int32_t *num_tokens_post_padded;  /* [1] */
+    int64_t capacity;
+    uint8_t *q;
+    uint8_t *scale;              /* uint8 [M, K/32] */
+    void *scratch;
+    size_t scratch_bytes;
+} mr_route_params;
+
+int mr_moe_route(const mr_route_params *params, void *stream);
 
 /*
  * a6 on the norm's scale [sgl-amd-mono #56 page, entry #59 "[Perf]

@@ -5,6 +5,7 @@ every entry point include/moe_route.h declares, and its host-only functions
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -151,3 +152,43 @@ def test_missing_library_fails_loudly(tmp_path):
             mr.load_library(str(tmp_path / "nope.so"))
     finally:
         mr._lib = saved
+
+
+def test_route_params_layout_matches_header(tmp_path):
+    # compile a probe against the header with the host C compiler and compare
+    # every field offset and the size with the binding's ctypes structure
+    fields = [f for f, _ in mr.RouteParams._fields_]
+    src = tmp_path / "probe.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "moe_route.h"\nint main(void) {\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(mr_route_params, {f}));\n' for f in fields)
+                   + '  printf("%zu\\n", sizeof(mr_route_params));\n  return 0;\n}\n')
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    want = [getattr(mr.RouteParams, f).offset for f in fields] + [ctypes.sizeof(mr.RouteParams)]
+    assert out == want
+
+
+def test_general_route_and_mxfp4_validation(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert lib.mr_moe_route(None, None) == mr.MR_ERR_INVALID_ARG
+    p = mr.RouteParams()
+    p.x, p.ldx, p.w = 0x1000, 6144, 0x1000
+    p.M, p.N, p.K, p.topk, p.scoring, p.renormalize, p.block = 4, 128, 6144, 8, 0, 1, 16
+    for f in ("logits", "topk_ids", "topk_weights", "sorted_token_ids", "expert_ids", "num_tokens_post_padded",
+              "q", "scale"):
+        setattr(p, f, 0x1000)
+    p.capacity = 1 << 20
+    p.quant_format = 7                       # unknown format
+    assert lib.mr_moe_route(ctypes.byref(p), None) == mr.MR_ERR_INVALID_ARG
+    p.quant_format = 2
+    p.q = 0x1004                             # MXFP4 output must be 8-byte aligned here
+    assert lib.mr_moe_route(ctypes.byref(p), None) == mr.MR_ERR_INVALID_ARG
+    p.q = 0x1000
+    p.M = 65                                 # the one launch covers M <= 64
+    assert lib.mr_moe_route(ctypes.byref(p), None) == mr.MR_ERR_UNSUPPORTED
+    p.M, p.rstd, p.norm_weight, p.norm_kind = 4, 0x1000, 0x1000, 3   # unknown norm kind
+    assert lib.mr_moe_route(ctypes.byref(p), None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_mxfp4_quant(fake, 48, 1, 40, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
+    assert lib.mr_mxfp4_quant(fake, 64, 1, 64, P(0x1002), fake, None) == mr.MR_ERR_INVALID_ARG
