@@ -137,6 +137,11 @@ size_t mr_scratch_bytes(int M_max, int N, int K, int topk) {
         const size_t b = (size_t)Mf * topk * 4;
         if (b > work) work = b;
     }
+    if (N >= mr::kRouteSplitMinN) {  // fused route over expert groups (one token group): their candidates
+        const int Mf = M_max < mr::kRouteRowsPerCluster ? M_max : mr::kRouteRowsPerCluster;
+        const size_t b = (size_t)Mf * mr::kRouteMaxGroups * topk * 12;
+        if (b > work) work = b;
+    }
     const int64_t n_assign = (int64_t)M_max * topk;
     if (n_assign > mr::kSortChunk && n_assign < ((int64_t)1 << 30)) {
         const size_t b = mr::sort_work_bytes((int)n_assign, N);
@@ -158,7 +163,10 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.ldx = ldx;
     a.w = static_cast<const uint16_t*>(w);
     a.M = M;
-    a.N = N;
+    a.N = p.nl;   // experts of one cluster (all of them unless split into groups)
+    a.ldn = N;
+    a.ng = p.ng;
+    a.off_merge = p.off_merge;
     a.K = K;
     a.mode = mode;
     a.cs = p.cs;
@@ -181,7 +189,7 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.off_start = p.off_start;
     a.tok_shift = mr::ilog2_exact(p.tok);
     a.wpt_shift = mr::ilog2_exact(p.wpt);
-    a.mag_n = mr::div_magic(N);
+    a.mag_n = mr::div_magic(p.nl);
     a.mag_vpr = mr::div_magic(p.kc / 8);
     a.mag_n4 = mr::div_magic(N / 4 > 0 ? N / 4 : 1);
     a.tc = p.tc;
@@ -207,7 +215,7 @@ int mr_router_gemv(const void* x, int64_t ldx, const void* w, float* logits, int
     {   // the cluster kernel (no scratch) whenever its plan fits; above 64 rows
         // the split-K GEMV with last-arriver fixup takes the rest
         mr::RoutePlan rp;
-        if (mr::route_plan(M, N, K, 1, 0, mr::route_cluster_size(), &rp, allow_tc())) {
+        if (mr::route_plan(M, N, K, 1, 0, mr::route_cluster_size(), &rp, allow_tc(), mr::route_max_clusters())) {
             mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 0);
             a.logits = logits;
             return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
@@ -295,13 +303,26 @@ static int route_impl(const mr_route_params* p, void* stream) {
     if (qf != MR_QUANT_NONE && (p->q == nullptr || !aligned(p->q, 8) || p->scale == nullptr))
         return MR_ERR_INVALID_ARG;
     mr::RoutePlan rp;
-    if (!mr::route_plan(M, N, K, topk, 1, mr::route_cluster_size(), &rp, allow_tc())) return MR_ERR_UNSUPPORTED;
+    const int cs = mr::route_cluster_size();
+    // expert groups need scratch for their candidates: without it (or with
+    // too little) the route runs its experts in one cluster per 16 tokens
+    const bool have_scratch = p->scratch != nullptr && aligned(p->scratch, 256);
+    if (!mr::route_plan(M, N, K, topk, 1, cs, &rp, allow_tc(), have_scratch ? mr::route_max_clusters() : 1))
+        return MR_ERR_UNSUPPORTED;
+    if (rp.ng > 1 && p->scratch_bytes < mr::kWorkOffset + (size_t)M * rp.ng * topk * 12 &&
+        !mr::route_plan(M, N, K, topk, 1, cs, &rp, allow_tc(), 1))
+        return MR_ERR_UNSUPPORTED;
     mr::RouteArgs a = route_args(rp, p->x, p->ldx, p->w, M, N, K, 1);
     if (rp.clusters > 1) {  // the clusters meet in scratch: a ticket and every token's ids
-        if (p->scratch == nullptr || !aligned(p->scratch, 256)) return MR_ERR_INVALID_ARG;
+        if (!have_scratch) return MR_ERR_INVALID_ARG;
         if (p->scratch_bytes < mr::kWorkOffset + (size_t)M * topk * 4) return MR_ERR_SCRATCH_TOO_SMALL;
         a.counter = static_cast<unsigned*>(p->scratch) + mr::kFusedCounterSlot;
         a.ids_scratch = reinterpret_cast<int32_t*>(static_cast<char*>(p->scratch) + mr::kWorkOffset);
+    }
+    if (rp.ng > 1) {  // each cluster's collector publishes its group candidates and takes a ticket
+        char* work = static_cast<char*>(p->scratch) + mr::kWorkOffset;
+        a.cand_key = reinterpret_cast<unsigned long long*>(work);
+        a.cand_val = reinterpret_cast<float*>(work + (size_t)M * rp.ng * topk * 8);
     }
     a.bias = scoring == MR_SCORE_SIGMOID ? p->sel_bias : nullptr;
     a.logits = p->logits;
@@ -318,7 +339,7 @@ static int route_impl(const mr_route_params* p, void* stream) {
     {  // gate threshold lane groups: the largest power of two <= 32 threads
        // leaving at least topk groups that hold experts (thread t: experts t
        // and t + 512)
-        const int lanes = N < 512 ? N : 512;
+        const int lanes = rp.nl < 512 ? rp.nl : 512;
         int gsh = 5;
         while (gsh > 0 && (lanes + (1 << gsh) - 1) >> gsh < topk) --gsh;
         a.gs_shift = gsh;

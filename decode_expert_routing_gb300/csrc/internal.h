@@ -55,6 +55,7 @@ struct RoutePlan;
 struct RouteArgs;
 // Cluster route kernel (M <= 64): logits only (mode 0) or the whole route.
 int route_cluster_size();  // 16 when the device runs 16-CTA clusters, else 8
+int route_max_clusters();  // clusters of route_cluster_size() CTAs that fit on the device at once
 // 1 if a bounded wait of the route kernel ran out on the current device, 0
 // if not, -1 on a CUDA error; clear resets the flag.  Synchronous.
 int route_device_error(int clear);

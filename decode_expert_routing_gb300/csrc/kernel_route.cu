@@ -157,14 +157,14 @@ __device__ __forceinline__ int fdiv(int x, unsigned long long mag) {
 // Gate-weight fragments of batch b of this warp's units.  A warp keeps one
 // k-part p = warp % wpt for all its units, so the x fragments it loads serve
 // every unit of a batch; unit i of the warp is tile (warp / wpt) + i * (16 / wpt).
-__device__ __forceinline__ void load_w_batch(const RouteArgs& a, int64_t kslice, int warp, int g, int t,
-                                             int b, uint4 (&wv)[kRouteBatch][kRouteSpwMax]) {
+__device__ __forceinline__ void load_w_batch(const RouteArgs& a, const uint16_t* wg, int64_t kslice, int warp,
+                                             int g, int t, int b, uint4 (&wv)[kRouteBatch][kRouteSpwMax]) {
     const int p = warp & (a.wpt - 1), tiles_per_pass = kRouteWarps >> a.wpt_shift;
 #pragma unroll
     for (int uu = 0; uu < kRouteBatch; ++uu) {
         const int j = (warp >> a.wpt_shift) + tiles_per_pass * (b * kRouteBatch + uu);
         const bool ok = j < (a.N >> 3);
-        const uint16_t* wp = a.w + (int64_t)(j * 8 + g) * a.K + kslice + (int64_t)p * a.spw * 32 + 8 * t;
+        const uint16_t* wp = wg + (int64_t)(j * 8 + g) * a.K + kslice + (int64_t)p * a.spw * 32 + 8 * t;
 #pragma unroll
         for (int s = 0; s < kRouteSpwMax; ++s)
             wv[uu][s] = (ok && s < a.spw) ? ld_stream_v4(wp + s * 32) : make_uint4(0u, 0u, 0u, 0u);
@@ -177,8 +177,11 @@ __device__ __forceinline__ unsigned long long composite(unsigned key, int id) {
 }
 
 // Weight of slot r = lane (lane < k holds (val) of slot r): the same
-// arithmetic as the standalone gate kernel.
-__device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* row, float my_val) {
+// arithmetic as the standalone gate kernel.  row: the token's n_row logits
+// (only the full-softmax denominator reads it), in shared memory, or in
+// global memory written by other CTAs (read through L2).
+__device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* row, int n_row, bool global_row,
+                                             float my_val) {
     const int lane = threadIdx.x & 31;
     const bool live = lane < a.topk;
     float num, den;
@@ -193,7 +196,8 @@ __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* ro
         den = warp_sum_fixed(num);
     } else {
         float part = 0.0f;
-        for (int id = lane; id < a.N; id += 32) part = __fadd_rn(part, expf(__fadd_rn(row[id], -lmax)));
+        for (int id = lane; id < n_row; id += 32)
+            part = __fadd_rn(part, expf(__fadd_rn(global_row ? __ldcg(row + id) : row[id], -lmax)));
         den = warp_sum_fixed(part);
     }
     return __fdiv_rn(num, den);
@@ -201,10 +205,11 @@ __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* ro
 
 // MXFP8 (or MXFP4) of this CTA's x slice (rows row0 .. row0 + Mq, columns
 // kslice .. kslice + kc), one lane quad per 32-element block; every thread of
-// the CTA takes part.
-__device__ __forceinline__ void quant_slice(const RouteArgs& a, const unsigned char* xs, int Mq, int row0,
-                                            int64_t kslice) {
-    if (a.q == nullptr) return;
+// the CTA takes part.  The MXFP4 loop is one out-of-line copy: inlined at
+// every call site beside the MXFP8 loop it made the kernel's code larger,
+// and launches with a cold instruction cache measured 0.4-0.9 us slower.
+__device__ __noinline__ void quant_slice_fp4(const RouteArgs& a, const unsigned char* xs, int Mq, int row0,
+                                             int64_t kslice) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int vpr = a.kc / 8, nvec = Mq * vpr;
     const int64_t K = a.K, K32 = K / 32;
@@ -214,13 +219,30 @@ __device__ __forceinline__ void quant_slice(const RouteArgs& a, const unsigned c
         const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
         unsigned sb;
         const int64_t kk = kslice + cv * 8;
-        if (a.quant_fp4) {  // MXFP4: q [M, K/2], two E2M1 codes a byte
-            const uint32_t q4 = mx4_quant_quad(d, &sb);
-            if (v < nvec) *reinterpret_cast<uint32_t*>(a.q + (int64_t)(row0 + r) * (K / 2) + kk / 2) = q4;
-        } else {
-            const uint2 q8 = mx_quant_quad(d, &sb);
-            if (v < nvec) *reinterpret_cast<uint2*>(a.q + (int64_t)(row0 + r) * K + kk) = q8;
-        }
+        const uint32_t q4 = mx4_quant_quad(d, &sb);
+        if (v < nvec) *reinterpret_cast<uint32_t*>(a.q + (int64_t)(row0 + r) * (K / 2) + kk / 2) = q4;
+        if (v < nvec && (cv & 3) == 0) a.scale[(int64_t)(row0 + r) * K32 + kk / 32] = (uint8_t)sb;
+    }
+}
+
+__device__ __forceinline__ void quant_slice(const RouteArgs& a, const unsigned char* xs, int Mq, int row0,
+                                            int64_t kslice) {
+    if (a.q == nullptr) return;
+    if (a.quant_fp4) {
+        quant_slice_fp4(a, xs, Mq, row0, kslice);
+        return;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int vpr = a.kc / 8, nvec = Mq * vpr;
+    const int64_t K = a.K, K32 = K / 32;
+    for (int base = warp * 32; base < nvec; base += kRouteThreads) {
+        const int v = base + lane;
+        const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
+        const uint4 d = v < nvec ? lds128(xs + r * a.xpitch + cv * 16) : make_uint4(0u, 0u, 0u, 0u);
+        unsigned sb;
+        const int64_t kk = kslice + cv * 8;
+        const uint2 q8 = mx_quant_quad(d, &sb);
+        if (v < nvec) *reinterpret_cast<uint2*>(a.q + (int64_t)(row0 + r) * K + kk) = q8;
         if (v < nvec && (cv & 3) == 0) a.scale[(int64_t)(row0 + r) * K32 + kk / 32] = (uint8_t)sb;
     }
 }
@@ -247,14 +269,15 @@ __device__ __forceinline__ void row_weights(const RouteArgs& a, const float* row
     if (warp >= kRouteWarps - my_rows) {
         const int rl = kRouteWarps - 1 - warp;
         const bool live = lane < k;
-        const float wgt = gate_weight(a, rowbuf + rl * a.N, live ? oval[rl * k + lane] : 0.0f);
+        const float wgt = gate_weight(a, rowbuf + rl * a.N, a.N, false, live ? oval[rl * k + lane] : 0.0f);
         if (live) a.weights[(int64_t)(grow + rl) * k + lane] = wgt;
     }
 }
 
 // HALF: at most 8 token rows (half of the m16 tile live).  TC: the router
 // GEMV on tcgen05 (GEMV alone, 64-row clusters) instead of mma.sync.
-template <bool HALF, bool TC>
+// GROUPS: the experts are split into a.ng groups, one cluster per group.
+template <bool HALF, bool TC, bool GROUPS>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) unsigned long long s_bar[3];  // [0] partial logits in, [1] ids in, [2] MMAs done
@@ -273,7 +296,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
 #endif
     // this cluster's token rows: [row0, row0 + Mq); this CTA owns rows
     // [c * tok, c * tok + my_rows) of them
-    const int row0 = (int)(blockIdx.x >> a.cs_shift) * a.rpc;
+    // expert groups: cluster cl takes token group cl / ng and experts
+    // [e_off, e_off + N) of ldn (its group, nc = cl % ng)
+    const int cl = (int)(blockIdx.x >> a.cs_shift);
+    const int mc = GROUPS ? cl / a.ng : cl, nc = GROUPS ? cl - mc * a.ng : 0;
+    const int row0 = mc * a.rpc;
     const int Mq = min(a.rpc, a.M - row0);
     const int N = a.N, wpt = a.wpt, tok = a.tok, K = a.K, k = a.topk;
     const int nslots = a.nslots;
@@ -281,7 +308,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // the CTA that sorts the cluster's assignments: one that owns no row when
     // there is one (it is idle while the others run the gate), else CTA 0
     const int sorter = Mq <= (a.cs - 1) * tok ? a.cs - 1 : 0;
+    // (with expert groups it collects the cluster's group candidates, and
+    // the last cluster's collector merges and sorts)
     const bool sorts = a.mode == 1 && c == sorter;
+    const bool quants = nc == 0;  // one expert group per token group quantises x
+    const int e_off = GROUPS ? nc * N : 0;
     const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]), bar2 = smem_u32(&s_bar[2]);
     if (tid == 0) {
         s_ccount = 0;
@@ -291,7 +322,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         const unsigned stall = (a.flags & 2) ? 16u : 0u;  // test hook: bytes that never come
         if (my_rows > 0) mbar_expect_tx(bar0, (unsigned)(my_rows * nslots * N * 4) + stall);
-        if (sorts) mbar_expect_tx(bar1, (unsigned)(Mq * k * 4));
+        if (sorts) mbar_expect_tx(bar1, (unsigned)(Mq * k * (GROUPS ? 12 : 4)));
     }
     cluster_arrive_relaxed();  // completed by cluster_wait() before the first DSMEM access
     pdl_trigger();
@@ -307,6 +338,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     }
     const int64_t kslice = (int64_t)c * a.kc;
     const uint16_t* xq = a.x + (int64_t)row0 * a.ldx;
+    const uint16_t* wg = a.w + (int64_t)e_off * K;  // this cluster's expert rows
     unsigned long long* mask = reinterpret_cast<unsigned long long*>(sm + a.off_mask);
 
     // ---- loads of the gate weight (first batch) and of the selection bias:
@@ -328,12 +360,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     } else {
-        load_w_batch(a, kslice, warp, g, t, 0, wv);
+        load_w_batch(a, wg, kslice, warp, g, t, 0, wv);
     }
     float bpre0 = 0.0f, bpre1 = 0.0f;  // selection bias of this thread's experts t and t + 512
     if (a.bias != nullptr) {
-        if (tid < N) bpre0 = __ldg(a.bias + tid);
-        if (tid + kRouteThreads < N) bpre1 = __ldg(a.bias + tid + kRouteThreads);
+        if (tid < N) bpre0 = __ldg(a.bias + e_off + tid);
+        if (tid + kRouteThreads < N) bpre1 = __ldg(a.bias + e_off + tid + kRouteThreads);
     }
     if (sorts)
         for (int e = tid; e < N; e += kRouteThreads) mask[e] = 0ull;  // token bitmasks (2 x 32 bits per expert)
@@ -388,7 +420,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar2)
                          : "memory");
         }
-        quant_slice(a, xs, Mq, row0, kslice);  // while the tensor core works
+        if (quants) quant_slice(a, xs, Mq, row0, kslice);  // while the tensor core works
         const bool ok = cta_wait_bytes(bar2, a.wait_ns, &s_ok[2]);
         MR_TRACE_STAMP(a.trace, 9);
         tc_fence_after();
@@ -442,7 +474,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int slot = c * wpt + p;
     const int r0 = g, r1 = g + 8;  // one m16 tile: at most 16 token rows per cluster here
     for (int b = 0; b < nb; ++b) {
-        if (b > 0) load_w_batch(a, kslice, warp, g, t, b, wv);
+        if (b > 0) load_w_batch(a, wg, kslice, warp, g, t, b, wv);
         float acc[kRouteBatch][4];
 #pragma unroll
         for (int uu = 0; uu < kRouteBatch; ++uu) acc[uu][0] = acc[uu][1] = acc[uu][2] = acc[uu][3] = 0.0f;
@@ -489,10 +521,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // quantise later, off the path of the gate.
     // (On the tensor-core path every CTA has quantised during its MMAs.)
     if (sorts) {
-        if (!TC) quant_slice(a, xs, Mq, row0, kslice);
+        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
         if (a.clusters == 1) fill_sort_padding(a, a.M * k);
     } else if (my_rows == 0) {
-        if (!TC) quant_slice(a, xs, Mq, row0, kslice);
+        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
     if (my_rows > 0 && !cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
@@ -533,7 +565,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
 #pragma unroll
                 for (int u = 0; u < 8; ++u) sum = __fadd_rn(sum, v[u]);
             }
-            a.logits[(int64_t)(grow + rl) * N + n] = sum;
+            a.logits[(int64_t)(grow + rl) * a.ldn + e_off + n] = sum;
         }
         return;  // nothing else reads this CTA's shared memory
     }
@@ -559,7 +591,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                 for (int u = 0; u < 8; ++u) sum1 = __fadd_rn(sum1, v[u]);
             }
         }
-        const int64_t lrow = (int64_t)(grow + rl) * N;
+        const int64_t lrow = (int64_t)(grow + rl) * a.ldn + e_off;
         if (h0) {
             rowbuf[rl * N + n0] = sum0;
             a.logits[lrow + n0] = sum0;
@@ -574,8 +606,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             sel0 = __fadd_rn(sigmoid_score(sum0), bpre0);
             sel1 = __fadd_rn(sigmoid_score(sum1), bpre1);
         }
-        const unsigned long long c0 = h0 ? composite(ordered_key(sel0), n0) : 0ull;
-        const unsigned long long c1 = h1 ? composite(ordered_key(sel1), n1) : 0ull;
+        const unsigned long long c0 = h0 ? composite(ordered_key(sel0), e_off + n0) : 0ull;
+        const unsigned long long c1 = h1 ? composite(ordered_key(sel1), e_off + n1) : 0ull;
         const unsigned k0 = (unsigned)(c0 >> 32), k1 = (unsigned)(c1 >> 32);
         // the warp's smallest maximum over its groups that hold experts
         const unsigned gmax = __reduce_max_sync(gmask, max(k0, k1));
@@ -612,7 +644,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                 int r = 0;
                 for (int j = part; j < C; j += PR) r += (int)(ccand[j] > cn);
                 r = (int)__reduce_add_sync(pmask, (unsigned)r);
-                if (part == 0 && r < k) {
+                if (GROUPS && part == 0 && r < k) {  // the group's r-th candidate -> the collector
+                    const int id = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
+                    const uint32_t cb = smem_u32(sm + a.off_merge), sbar = map_rank(bar1, (unsigned)sorter);
+                    st_async_f2(map_rank(cb + (uint32_t)((ml * k + r) * 8), (unsigned)sorter),
+                                __uint_as_float((unsigned)cn), __uint_as_float((unsigned)(cn >> 32)), sbar);
+                    st_async_s32(map_rank(cb + (uint32_t)(Mq * k * 8 + (ml * k + r) * 4), (unsigned)sorter),
+                                 __float_as_int(rowbuf[rl * N + id - e_off]), sbar);
+                } else if (part == 0 && r < k) {
                     const int id = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
                     st_async_s32(map_rank(smem_u32(sm + a.off_ids) + (uint32_t)((ml * k + r) * 4), (unsigned)sorter),
                                  id, map_rank(bar1, (unsigned)sorter));
@@ -630,6 +669,101 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     MR_TRACE_CLK(a.trace, 9);
     MR_TRACE_CLK(a.trace, 11);
     MR_TRACE_WARP(a.trace, 7);
+    int* ids_all = reinterpret_cast<int*>(sm + a.off_ids);
+    const int M = a.M, MK = M * k, B = a.block, NS = a.ldn;
+    if constexpr (GROUPS) {
+        // ---- expert groups: the owners have sent their rows' group
+        //      candidates (k per row, in rank order) to the cluster's
+        //      collector, which publishes them and takes a ticket; the last
+        //      collector merges them into each token's top-k, writes the ids
+        //      and weights, and sorts.  The merge ranks candidate (g, r) of
+        //      token m by r plus, for every other group, the count of its
+        //      candidates that beat it (a binary search: each list is
+        //      descending; the composites are unique).
+        if (!sorts) {
+            if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
+            return;
+        }
+        if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
+        MR_TRACE_STAMP(a.trace, 5);
+        {
+            const unsigned long long* ckey = reinterpret_cast<const unsigned long long*>(sm + a.off_merge);
+            const float* cval = reinterpret_cast<const float*>(sm + a.off_merge + Mq * k * 8);
+            for (int f = tid; f < Mq * k; f += kRouteThreads) {
+                const int rr = fdiv(f, a.mag_k), j = f - rr * k;
+                const int64_t slot = ((int64_t)(row0 + rr) * a.ng + nc) * k + j;
+                a.cand_key[slot] = ckey[f];
+                a.cand_val[slot] = cval[f];
+            }
+        }
+        const unsigned ticket = cta_ticket(a.counter, &s_ticket);
+        if (ticket != (unsigned)(a.clusters - 1)) return;
+        // one warp per token: its ng lists of k candidates (each descending)
+        // go to shared memory; lane g < ng holds the head of list g, and k
+        // rounds each take the largest head (two redux.sync maximums: the
+        // high words, then the low words among the lanes that tie on them;
+        // the composites are unique, so one lane wins) and advance that list
+        const int ngk = a.ng * k;
+        unsigned long long* mkey = reinterpret_cast<unsigned long long*>(sm + a.off_merge);
+        float* mval = reinterpret_cast<float*>(mkey + M * ngk);
+        for (int e = tid; e < NS; e += kRouteThreads) mask[e] = 0ull;
+        if (tid == 0) *a.counter = 0u;
+        MR_TRACE_CLK(a.trace, 6);
+        for (int m = warp; m < M; m += kRouteWarps) {
+            unsigned long long* ck = mkey + m * ngk;
+            float* cv = mval + m * ngk;
+            {   // all loads in flight before the stores (ngk <= 8 * 32)
+                unsigned long long kr[kRouteMaxGroups];
+                float vr[kRouteMaxGroups];
+#pragma unroll
+                for (int q = 0; q < kRouteMaxGroups; ++q) {
+                    const int i = lane + 32 * q;
+                    if (i < ngk) {
+                        kr[q] = __ldcg(a.cand_key + (int64_t)m * ngk + i);
+                        vr[q] = __ldcg(a.cand_val + (int64_t)m * ngk + i);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < kRouteMaxGroups; ++q) {
+                    const int i = lane + 32 * q;
+                    if (i < ngk) {
+                        ck[i] = kr[q];
+                        cv[i] = vr[q];
+                    }
+                }
+            }
+            __syncwarp();
+            const bool owns = lane < a.ng;
+            const unsigned long long* L = ck + lane * k;
+            int ptr = 0;
+            unsigned long long head = owns ? L[0] : 0ull;
+            unsigned long long nxt = (owns && k > 1) ? L[1] : 0ull;
+            float myval = 0.0f;  // lane r < k: the logit of slot r
+            for (int r = 0; r < k; ++r) {
+                const unsigned hi = (unsigned)(head >> 32);
+                const unsigned mhi = __reduce_max_sync(kFull, hi);
+                const unsigned mlo = __reduce_max_sync(kFull, hi == mhi ? (unsigned)head : 0u);
+                const bool win = owns && hi == mhi && (unsigned)head == mlo;
+                const unsigned wl = __ballot_sync(kFull, win);
+                const float v = __shfl_sync(kFull, (owns && ptr < k) ? cv[lane * k + ptr] : 0.0f, __ffs(wl) - 1);
+                if (lane == r) myval = v;
+                if (win) {
+                    const int id = 0x7FFFFFFF - (int)mlo;
+                    ids_all[m * k + r] = id;
+                    a.ids[(int64_t)m * k + r] = id;
+                    ++ptr;
+                    head = nxt;
+                    nxt = ptr + 1 < k ? L[ptr + 1] : 0ull;
+                }
+            }
+            MR_TRACE_CLK(a.trace, 7);
+            const bool live = lane < k;
+            const float wgt = gate_weight(a, a.logits + (int64_t)m * NS, NS, true, live ? myval : 0.0f);
+            if (live) a.weights[(int64_t)m * k + lane] = wgt;
+        }
+        __syncthreads();  // every token's ids; the masks zeroed
+        MR_TRACE_CLK(a.trace, 8);
+    } else {
     if (!sorts) {  // the weights and the quantisation finish this CTA
         row_weights(a, rowbuf, oval, my_rows, grow);
         if (!TC) quant_slice(a, xs, Mq, row0, kslice);
@@ -644,8 +778,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      CTA 0 publishes its rows' ids and takes a ticket; the last one
     //      gathers all ids and sorts (with several clusters its first phase
     //      also fills the sentinels and the -1 block ids).
-    int* ids_all = reinterpret_cast<int*>(sm + a.off_ids);
-    const int M = a.M, MK = M * k, B = a.block;
     if (a.clusters > 1) {
         for (int f = tid; f < Mq * k; f += kRouteThreads) a.ids_scratch[row0 * k + f] = ids_all[f];
         const unsigned ticket = cta_ticket(a.counter, &s_ticket);
@@ -655,13 +787,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         if (tid == 0) *a.counter = 0u;
         __syncthreads();
     }
+    }  // one expert group
     MR_TRACE_STAMP(a.trace, 6);
     MR_TRACE_CLK(a.trace, 13);
     // rank of (m, j) inside expert e = number of set bits below m in the token
     // mask of e (two 32-bit words: tokens 0-31, 32-63)
     int* start = reinterpret_cast<int*>(sm + a.off_start);
     unsigned* mlo = reinterpret_cast<unsigned*>(mask);
-    unsigned* mhi = mlo + N;
+    unsigned* mhi = mlo + NS;
     for (int f = tid; f < MK; f += kRouteThreads) {
         const int m = fdiv(f, a.mag_k);
         atomicOr(m < 32 ? &mlo[ids_all[f]] : &mhi[ids_all[f]], 1u << (m & 31));
@@ -677,8 +810,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // totals; then the block starts and the expert id of every real block
     // (padding blocks already hold -1).
     const int e0 = tid, e1 = tid + kRouteThreads;
-    const int nb0 = e0 < N ? fdiv(__popc(mlo[e0]) + __popc(mhi[e0]) + B - 1, a.mag_block) : 0;
-    const int nb1 = e1 < N ? fdiv(__popc(mlo[e1]) + __popc(mhi[e1]) + B - 1, a.mag_block) : 0;
+    const int nb0 = e0 < NS ? fdiv(__popc(mlo[e0]) + __popc(mhi[e0]) + B - 1, a.mag_block) : 0;
+    const int nb1 = e1 < NS ? fdiv(__popc(mlo[e1]) + __popc(mhi[e1]) + B - 1, a.mag_block) : 0;
     const int nbits = 32 - __clz(fdiv(M + B - 1, a.mag_block));
     const unsigned lt = (1u << lane) - 1u;
     int pre0 = 0, pre1 = 0, wt0 = 0, wt1 = 0;
@@ -708,11 +841,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     }
     MR_TRACE_CLK(a.trace, 17);
     const int sb0 = before0 + pre0, sb1 = tot0 + before1 + pre1;  // first block of e0 / e1
-    if (e0 < N) {
+    if (e0 < NS) {
         start[e0] = sb0 * B;
         for (int i = 0; i < nb0; ++i) a.expert_ids[sb0 + i] = e0;
     }
-    if (e1 < N) {
+    if (e1 < NS) {
         start[e1] = sb1 * B;
         for (int i = 0; i < nb1; ++i) a.expert_ids[sb1 + i] = e1;
     }
@@ -748,13 +881,13 @@ int route_device_error(int clear) {
 }
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
-static int g_attr_done[64][4];  // per device and instantiation
+static int g_attr_done[64][8];  // per device and instantiation
 
-template <bool HALF, bool TC>
+template <bool HALF, bool TC, bool GROUPS>
 static cudaError_t prepare(int dev) {
-    const int slot = (HALF ? 1 : 0) + (TC ? 2 : 0);
+    const int slot = (HALF ? 1 : 0) + (TC ? 2 : 0) + (GROUPS ? 4 : 0);
     if (g_attr_done[dev][slot]) return cudaSuccess;
-    auto k = route_cluster_kernel<HALF, TC>;
+    auto k = route_cluster_kernel<HALF, TC, GROUPS>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TC ? kRouteSmemMaxTc : kRouteSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -766,7 +899,7 @@ int route_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (g_cluster16[dev] == 0) {
-        cudaError_t e = prepare<false, false>(dev);
+        cudaError_t e = prepare<false, false, false>(dev);
         int n = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -780,12 +913,38 @@ int route_cluster_size() {
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
         }
         g_cluster16[dev] = (e == cudaSuccess && n >= 1) ? 1 : -1;
         cudaGetLastError();  // a refused query leaves no sticky error
     }
     return g_cluster16[dev] > 0 ? 16 : 8;
+}
+
+static int g_max_clusters[64];  // per device: co-resident clusters of the mma.sync kernel (0: unknown)
+
+int route_max_clusters() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (g_max_clusters[dev] == 0) {
+        const int cs = route_cluster_size();
+        int n = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs);
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = kRouteSmemMax;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = cs;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
+        g_max_clusters[dev] = (e == cudaSuccess && n >= 1) ? n : 1;
+        cudaGetLastError();
+    }
+    return g_max_clusters[dev];
 }
 
 cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStream_t st) {
@@ -795,14 +954,20 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     void (*kernel)(RouteArgs) = nullptr;
     if (p.tc) {
-        e = prepare<false, true>(dev);
-        kernel = route_cluster_kernel<false, true>;
+        e = prepare<false, true, false>(dev);
+        kernel = route_cluster_kernel<false, true, false>;
+    } else if (p.ng > 1 && p.half) {
+        e = prepare<true, false, true>(dev);
+        kernel = route_cluster_kernel<true, false, true>;
+    } else if (p.ng > 1) {
+        e = prepare<false, false, true>(dev);
+        kernel = route_cluster_kernel<false, false, true>;
     } else if (p.half) {
-        e = prepare<true, false>(dev);
-        kernel = route_cluster_kernel<true, false>;
+        e = prepare<true, false, false>(dev);
+        kernel = route_cluster_kernel<true, false, false>;
     } else {
-        e = prepare<false, false>(dev);
-        kernel = route_cluster_kernel<false, false>;
+        e = prepare<false, false, false>(dev);
+        kernel = route_cluster_kernel<false, false, false>;
     }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -16,6 +16,12 @@ constexpr int kRouteMaxM = 64;
 constexpr int kRouteRowsPerCluster = 16;  // token rows per cluster of the whole route (one m16 MMA tile)
 constexpr int kRouteGemvRowsPerCluster = 64;  // GEMV-only launches of more than 64 rows (four m16 tiles)
 constexpr int kRouteGemvMaxM = 512;
+// Expert groups: routes over many experts split them across clusters (each
+// cluster a group of >= kRouteGroupMinN experts) so that more SMs share the
+// gate weight; the groups' top-k candidates meet in scratch.
+constexpr int kRouteSplitMinN = 512;
+constexpr int kRouteGroupMinN = 128;
+constexpr int kRouteMaxGroups = 8;
 
 struct RouteArgs {
     const uint16_t* x;
@@ -58,6 +64,12 @@ struct RouteArgs {
     unsigned long long wait_ns;  // limit of every wait for bytes from other CTAs
     int32_t* ids_scratch;   // clusters > 1: every token's ids, gathered for the sort
     unsigned* counter;      // clusters > 1: last-arriver ticket, zero between launches
+    // expert groups (ng > 1): cluster cl takes token rows (cl / ng) * rpc ..
+    // and experts (cl % ng) * N .. + N of ldn; N above is the group's width
+    int ng, ldn;
+    unsigned long long* cand_key;      // [M][ng][topk] selection composites, per group in rank order
+    float* cand_val;                   // [M][ng][topk] their logits
+    int off_merge;                     // shared memory of the merge (the CTA that arrives last)
     // router input on the norm's scale (rstd == nullptr: x is the router input
     // as given): x[m, k] -> bf16((x * rstd[m]) * s[k]), s = g or 1 + g
     const float* rstd;
@@ -79,6 +91,7 @@ inline int ilog2_exact(int v) {
 
 struct RoutePlan {
     int cs, kc, spw, wpt, units, tok, xpitch, clusters, rpc;
+    int ng, nl, off_merge;  // expert groups, experts per group, merge buffers
     int tc, nmma, tmem_cols, nslots, off_a, off_b, off_dst;
     bool half;
     int smem;
@@ -95,12 +108,28 @@ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 constexpr int kTcLbo = 128, kTcSbo = 256;
 constexpr int kTcAStep = 128 * 16 * 2;  // bytes of the weight tile per 16-wide k-step
 
-inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePlan* p, bool allow_tc = true) {
+// max_groups: co-resident clusters available for expert groups (1: none).
+inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePlan* p, bool allow_tc = true,
+                       int max_groups = 1) {
     if (M < 1 || M > (mode == 1 ? kRouteMaxM : kRouteGemvMaxM) || N < 8 || N > 1024 || N % 8 != 0) return false;
     if (K < 32 * cs || K % (32 * cs) != 0) return false;
     RoutePlan q{};
     q.cs = cs;
     q.kc = K / cs;
+    const int Ntot = N;
+    q.ng = 1;
+    // (the whole route splits one token group only: with several, the one
+    // merging CTA takes several tokens per warp and the split measured slower)
+    const int mcl = (M + kRouteRowsPerCluster - 1) / kRouteRowsPerCluster;
+    if (max_groups > 1 && !(mode == 0 && M > kRouteMaxM) && !(mode == 1 && mcl > 1) && N >= kRouteSplitMinN) {
+        int d = max_groups / mcl;
+        if (d > kRouteMaxGroups) d = kRouteMaxGroups;
+        for (; d >= 2; --d)
+            if ((N / 8) % d == 0 && N / d >= kRouteGroupMinN && topk <= N / d) break;
+        if (d >= 2) q.ng = d;
+    }
+    N = Ntot / q.ng;  // from here on: the experts of one cluster
+    q.nl = N;
     const int S = q.kc / 32, NT = N / 8;
     // k-parts per tile: a power of two (a warp keeps one part for all its
     // tiles) dividing S with at most kRouteSpwMax steps per part; more parts
@@ -124,7 +153,7 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     const bool big = mode == 0 && M > kRouteMaxM;
     if (big && !(allow_tc && N <= 128 && q.kc % 16 == 0)) return false;
     q.rpc = big ? kRouteGemvRowsPerCluster : kRouteRowsPerCluster;
-    q.clusters = (M + q.rpc - 1) / q.rpc;
+    q.clusters = (M + q.rpc - 1) / q.rpc * q.ng;
     const int Mc = M < q.rpc ? M : q.rpc;
     q.tok = 1;
     while (q.tok * cs < Mc) q.tok *= 2;
@@ -155,9 +184,12 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.off_ids = off;  // every token's ids in the CTA that sorts
     off = align_up(off + M * (mode == 1 ? topk : 0) * 4, 16);
     q.off_mask = off;
-    off = align_up(off + (mode == 1 ? N : 0) * 8, 16);
+    off = align_up(off + (mode == 1 ? Ntot : 0) * 8, 16);
     q.off_start = off;
-    off = align_up(off + (mode == 1 ? N + 32 : 0) * 4, 16);
+    off = align_up(off + (mode == 1 ? Ntot + 32 : 0) * 4, 16);
+    q.off_merge = off;  // ng > 1: the cluster's candidates as received (keys, then logits); in the
+                        // merging CTA all candidates [M][ng][k] (8 B keys, then logits)
+    if (mode == 1 && q.ng > 1) off = align_up(off + M * q.ng * topk * 12, 16);
     if (q.tc) {
         off = align_up(off, 128);
         q.off_a = off;  // weight tile, then (after the MMAs) the transposed accumulator

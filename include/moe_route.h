@@ -243,11 +243,17 @@ int mr_mxfp8_quant(const void *x, int64_t ldx, int M, int K, uint8_t *q,
  * mr_router_gemv -> mr_route_topk -> mr_moe_sort -> mr_mxfp8_quant on the
  * same inputs.  q and scale may both be NULL to skip the quantisation.
  * K % 512 == 0, N % 8 == 0, N <= 1024, topk <= 32.
- * One thread-block cluster per 16 tokens.  M <= 16 uses no scratch (scratch
+ * One thread-block cluster per 16 tokens.  M <= 16 needs no scratch (scratch
  * may be NULL).  M > 16: the clusters hand over through scratch by an atomic
  * last-arriver ticket (no spin-waits) and the last cluster sorts; scratch
  * must hold mr_scratch_bytes(M, N, K, topk) bytes (MR_ERR_INVALID_ARG if
  * NULL, MR_ERR_SCRATCH_TOO_SMALL if short).
+ * Many experts (N >= 512) with M <= 16: given a scratch of
+ * mr_scratch_bytes(M, N, K, topk) bytes, the experts are split into groups of
+ * >= 128, one cluster each, so that more SMs share the gate weight; each
+ * cluster's top-k candidates per token go through scratch to the cluster
+ * that takes the last ticket, which merges them and sorts.  Without that
+ * scratch the route runs unsplit.  The outputs are the same bits either way.
  */
 int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
                             int M, int N, int K, int topk, int scoring,
