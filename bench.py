@@ -709,6 +709,26 @@ def run_gemv_rows(ms):
     return 0
 
 
+def run_quant_rows(M):
+    """Three MXFP8 and three MXFP4 quantisations of the prefill x [M, 6144]
+    (two inputs, 50 MB each at M = 4096): a short program for a profiler to
+    capture the quantiser kernels."""
+    import torch
+    from decode_expert_routing_gb300 import build as mrbuild
+    mrbuild.build()
+    import decode_expert_routing_gb300 as mr
+    from decode_expert_routing_gb300 import inputs
+    mr.load_library()
+    xs = [torch.from_numpy(np.ascontiguousarray(inputs.prefill_x(M, K_HID, variant=v)).view(np.int16))
+          .view(torch.bfloat16).cuda() for v in range(2)]
+    for r in range(3):
+        mr.mxfp8_quant(xs[r % 2])
+    for r in range(3):
+        mr.mxfp4_quant(xs[r % 2])
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -716,12 +736,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--quant-rows", type=int, default=0,
+                    help="run three MXFP8 and three MXFP4 quantisations of x [M, 6144] (for a profiler) and exit")
     ap.add_argument("--gemv-rows", default="",
                     help="profiling aid: only run router_gemv three times at each of these M "
                          "(comma-separated) and exit, printing no JSON line")
     args = ap.parse_args()
     if args.gemv_rows:
         return run_gemv_rows([int(v) for v in args.gemv_rows.split(",")])
+    if args.quant_rows:
+        return run_quant_rows(args.quant_rows)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
