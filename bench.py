@@ -617,6 +617,41 @@ def run_ours(args):
                                     "GBs": round(s_bytes / (s_us * 1e-6) / 1e9, 1)}}
     del px, pq, pq4, ps, plog, psk, pids, psort, pssk
 
+    # decode batches past the one-launch route: the sort and the MXFP8 quant
+    # in one launch against the two separate launches
+    sortq = {}
+    for SM_ in (256, 1024):
+        sx = [dev_bf16(inputs.prefill_x(SM_, K_HID, variant=v)) for v in range(2)]
+        slog = torch.empty((SM_, N_EXP), dtype=torch.float32, device=dev)
+        ssk = mr.Scratch(512, N_EXP, K_HID, TOPK, device=dev)
+        with torch.cuda.stream(stream):
+            for r0 in range(0, SM_, 512):
+                mr.router_gemv(sx[0][r0:r0 + 512], ws[MS[0]][0], out=slog[r0:r0 + 512], scratch=ssk)
+            sids, _ = mr.route_topk(slog, TOPK)
+        torch.cuda.synchronize()
+        scap = mr.sort_capacity(SM_, TOPK, N_EXP, BLOCK)
+        sout = (torch.empty(scap, dtype=torch.int32, device=dev), torch.empty(scap // BLOCK, dtype=torch.int32, device=dev),
+                torch.empty(1, dtype=torch.int32, device=dev), torch.empty((SM_, K_HID), dtype=torch.uint8, device=dev),
+                torch.empty((SM_, K_HID // 32), dtype=torch.uint8, device=dev))
+        sssk = mr.Scratch(SM_, N_EXP, 512, TOPK, device=dev)
+
+        def body_one(sx=sx, sids=sids, sout=sout):
+            for r in range(16):
+                mr.moe_sort_quant(sids, sx[r % 2], N_EXP, BLOCK, "mxfp8", out=sout)
+
+        def body_two(sx=sx, sids=sids, sout=sout, sssk=sssk):
+            for r in range(16):
+                mr.moe_sort(sids, N_EXP, BLOCK, out=sout[:3], scratch=sssk)
+                mr.mxfp8_quant(sx[r % 2], out=sout[3:])
+        with torch.cuda.stream(stream):
+            body_one()
+            body_two()
+        u1, u2 = graph_us(body_one, 16), graph_us(body_two, 16)
+        sb = 4 * SM_ * TOPK + 4 * scap + 4 * (scap // BLOCK) + 4 + 2 * SM_ * K_HID + SM_ * K_HID + SM_ * K_HID // 32
+        sortq[str(SM_)] = {"us_per_call": round(u1, 3), "GBs": round(sb / (u1 * 1e-6) / 1e9, 1),
+                           "separate_sort_and_quant_us": round(u2, 3)}
+        del sx, slog, ssk, sids, sout, sssk
+
     # end to end through the public API: pinned host x in, outputs back out
     e2e_steps = min(args.steps, 2000)
     hx = {M: torch.from_numpy(np.ascontiguousarray(host[M][0][0]).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -670,6 +705,7 @@ def run_ours(args):
             "route_896_experts_sigmoid_top16": k3,
             "route_on_norm_scale_gemma": normed,
             "prefill_4096_rows": prefill,
+            "sort_quant_one_launch_block16": sortq,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -74,6 +74,7 @@ SIGNATURES = {
     "mr_norm_apply": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "mr_mxfp4_quant": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
     "mr_moe_route": (_I, [_P, _P]),
+    "mr_moe_sort_quant": (_I, [_P, _I, _I, _I, _I, _P, _I64, _I, _I, _P, _P, _P, _I64, _P, _P, _P]),
     "mr_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "mr_device_error": (_I, [_I]),
 }
@@ -496,3 +497,36 @@ def moe_route(x, w, topk: int, block: int, scoring: str = "softmax", bias=None, 
     p.scratch_bytes = scratch.nbytes
     _check(_load().mr_moe_route(ctypes.byref(p), _stream_ptr(stream)), "mr_moe_route")
     return out
+
+
+def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp8", out=None, stream=None):
+    """Sort and stage-1 quant in one launch (decode batches, M * topk <= 8192):
+    (sorted_token_ids, expert_ids, num_tokens_post_padded, q, scale)."""
+    torch = _torch()
+    if topk_ids.dim() != 2 or not topk_ids.is_contiguous():
+        raise ValueError("topk_ids must be contiguous [M, k]")
+    M, k = topk_ids.shape
+    ldx = _row_major_2d(x, "x")
+    if x.shape[0] != M:
+        raise ValueError("x must have the rows of topk_ids")
+    K = x.shape[1]
+    if quant not in ("mxfp8", "mxfp4"):
+        raise ValueError("quant must be mxfp8 or mxfp4")
+    cap = sort_capacity(M, k, num_experts, block)
+    if cap < 0:
+        raise MoeRouteUnsupported(MR_ERR_UNSUPPORTED, "mr_sort_capacity")
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(cap, dtype=torch.int32, device=dev), torch.empty(cap // block, dtype=torch.int32, device=dev),
+               torch.empty(1, dtype=torch.int32, device=dev),
+               torch.empty((M, K // 2 if quant == "mxfp4" else K), dtype=torch.uint8, device=dev),
+               torch.empty((M, K // 32), dtype=torch.uint8, device=dev))
+    st, ex, nt, q, s = out
+    _check(_load().mr_moe_sort_quant(_dev_ptr(topk_ids, "topk_ids", torch.int32), M, k, num_experts, block,
+                                     _dev_ptr(x, "x", torch.bfloat16), ldx, K, QUANT_FORMAT[quant],
+                                     _dev_ptr(st, "sorted_token_ids", torch.int32),
+                                     _dev_ptr(ex, "expert_ids", torch.int32),
+                                     _dev_ptr(nt, "num_tokens_post_padded", torch.int32), st.numel(),
+                                     _dev_ptr(q, "q", torch.uint8), _dev_ptr(s, "scale", torch.uint8),
+                                     _stream_ptr(stream)), "mr_moe_sort_quant")
+    return st, ex, nt, q, s

@@ -260,6 +260,24 @@ int mr_moe_sort(const int32_t* topk_ids, int M, int topk, int N, int block, int3
                                        num_tokens_post_padded, capacity, scratch, as_stream(stream)));
 }
 
+int mr_moe_sort_quant(const int32_t* topk_ids, int M, int topk, int N, int block, const void* x, int64_t ldx,
+                      int K, int quant_format, int32_t* sorted_token_ids, int32_t* expert_ids,
+                      int32_t* num_tokens_post_padded, int64_t capacity, uint8_t* q, uint8_t* scale, void* stream) {
+    int s = check_sort_args(M, topk, N, block, capacity);
+    if (s != MR_OK) return s;
+    if ((s = check_x(x, ldx, M, K)) != MR_OK) return s;
+    if (topk_ids == nullptr || !aligned(topk_ids, 4) || sorted_token_ids == nullptr ||
+        !aligned(sorted_token_ids, 4) || expert_ids == nullptr || !aligned(expert_ids, 4) ||
+        num_tokens_post_padded == nullptr || !aligned(num_tokens_post_padded, 4))
+        return MR_ERR_INVALID_ARG;
+    if (quant_format != MR_QUANT_MXFP8 && quant_format != MR_QUANT_MXFP4) return MR_ERR_INVALID_ARG;
+    if (q == nullptr || !aligned(q, 8) || scale == nullptr) return MR_ERR_INVALID_ARG;
+    if (K % 32 != 0 || (int64_t)M * topk > mr::kSortQuantMaxAssign) return MR_ERR_UNSUPPORTED;
+    return cuda_status(mr::launch_sort_quant(topk_ids, M, topk, N, block, sorted_token_ids, expert_ids,
+                                             num_tokens_post_padded, capacity, x, ldx, K, q, scale,
+                                             quant_format == MR_QUANT_MXFP4, as_stream(stream)));
+}
+
 int mr_mxfp8_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, void* stream) {
     int s = check_x(x, ldx, M, K);
     if (s != MR_OK) return s;

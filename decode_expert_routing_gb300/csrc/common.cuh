@@ -156,9 +156,21 @@ __device__ __forceinline__ int mx_scale_exponent(unsigned amax16, int emax) {
     return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 
-__device__ __forceinline__ unsigned max_mag16(uint32_t v) {
-    unsigned lo = v & 0x7FFFu, hi = (v >> 16) & 0x7FFFu;
-    return lo > hi ? lo : hi;
+// Largest |x| of a 32-block as a bf16 magnitude pattern: the 8 values of v
+// (this lane) and those of the other 3 lanes of its quad.  Non-negative bf16
+// patterns order like their values, so the maximum runs on packed 16-bit
+// integers (sign bits cleared).
+__device__ __forceinline__ unsigned vmax_u16x2(unsigned a, unsigned b) {
+    unsigned d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned quad_amax16(uint4 v) {
+    unsigned m = vmax_u16x2(vmax_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                            vmax_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    m = vmax_u16x2(m, __shfl_xor_sync(kFull, m, 1));
+    m = vmax_u16x2(m, __shfl_xor_sync(kFull, m, 2));
+    return max(m & 0xFFFFu, m >> 16);
 }
 
 // Quantise the 8 consecutive bf16 values of v (k = 8t .. 8t+7 of a 32-block
@@ -166,13 +178,7 @@ __device__ __forceinline__ unsigned max_mag16(uint32_t v) {
 // warp must call it together.  Returns the 8 e4m3 codes (lowest k in the
 // lowest byte) and writes the block's E8M0 byte to *scale_byte.
 __device__ __forceinline__ uint2 mx_quant_quad(uint4 v, unsigned* scale_byte) {
-    unsigned m = max_mag16(v.x);
-    m = max(m, max_mag16(v.y));
-    m = max(m, max_mag16(v.z));
-    m = max(m, max_mag16(v.w));
-    m = max(m, __shfl_xor_sync(kFull, m, 1));
-    m = max(m, __shfl_xor_sync(kFull, m, 2));
-    int X = mx_scale_exponent(m, 8);
+    int X = mx_scale_exponent(quad_amax16(v), 8);
     *scale_byte = (unsigned)(X + 127);
     // 2^-X is a normal fp32 for every X reachable from bf16 input (X <= 119).
     float inv = __uint_as_float((unsigned)(127 - X) << 23);
@@ -214,13 +220,7 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
 // (element i in nibble i: 4 bytes of the [M, K/2] output) and writes the
 // block's E8M0 byte X + 127, X = floor(log2(amax)) - 2.
 __device__ __forceinline__ uint32_t mx4_quant_quad(uint4 v, unsigned* scale_byte) {
-    unsigned m = max_mag16(v.x);
-    m = max(m, max_mag16(v.y));
-    m = max(m, max_mag16(v.z));
-    m = max(m, max_mag16(v.w));
-    m = max(m, __shfl_xor_sync(kFull, m, 1));
-    m = max(m, __shfl_xor_sync(kFull, m, 2));
-    int X = mx_scale_exponent(m, 2);
+    int X = mx_scale_exponent(quad_amax16(v), 2);
     *scale_byte = (unsigned)(X + 127);
     // X in [-127, 125] for bf16 input: 2^-X is a normal fp32, and x * 2^-X
     // is exact wherever it can round to a nonzero code

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_cta_kernel(SortArgs a) {
     RankSmem rs{sm, sm + nw * a.N, sm + nw * a.N + a.N};
     int* start = rs.lrank + a.n_assign;
     int* warp_tot = start + a.N;
-    cta_sort(a, a.ids, rs, start, warp_tot);
+    cta_sort(a, stage_ids(a.ids, a.n_assign, warp_tot + 32), rs, start, warp_tot);
 }
 
 struct SortWork {
@@ -99,9 +99,10 @@ __global__ void __launch_bounds__(kSortThreads) sort_count_kernel(SortArgs a, So
     const int C = gridDim.x, c = blockIdx.x, N = a.N;
     const int beg = c * kSortChunk, n = min(kSortChunk, a.n_assign - beg);
     RankSmem rs{sm, sm + nw * N, sm + nw * N + N};
-    const int seg = cta_rank(a.ids + beg, n, N, rs);
+    const int* ids = stage_ids(a.ids + beg, n, rs.lrank + kSortChunk);
+    const int seg = cta_rank(ids, n, N, rs);
     for (int i = tid; i < n; i += nthr) {
-        const int e = a.ids[beg + i];
+        const int e = ids[i];
         if (e >= 0 && e < N) w.lrank[beg + i] = rs.wcnt[(i / seg) * N + e] + rs.lrank[i];
     }
     for (int e = tid; e < N; e += nthr) w.chunk_cnt[(size_t)c * N + e] = rs.cnt[e];
@@ -112,10 +113,16 @@ __global__ void __launch_bounds__(kSortThreads) sort_count_kernel(SortArgs a, So
     const int B = a.block;
     for (int e = tid; e < N; e += nthr) {
         int run = 0;
-        for (int cc = 0; cc < C; ++cc) {
-            const int v = __ldcg(w.chunk_cnt + (size_t)cc * N + e);
-            w.chunk_off[(size_t)cc * N + e] = run;
-            run += v;
+        for (int c0 = 0; c0 < C; c0 += kLoadBatch) {  // chunk counts kLoadBatch at a time
+            int v[kLoadBatch];
+#pragma unroll
+            for (int u = 0; u < kLoadBatch; ++u)
+                v[u] = c0 + u < C ? __ldcg(w.chunk_cnt + (size_t)(c0 + u) * N + e) : 0;
+#pragma unroll
+            for (int u = 0; u < kLoadBatch; ++u) {
+                if (c0 + u < C) w.chunk_off[(size_t)(c0 + u) * N + e] = run;
+                run += v[u];
+            }
         }
         rs.cnt[e] = run;
         start[e] = (run + B - 1) / B * B;
@@ -144,10 +151,22 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(SortArgs a, 
     pdl_wait();
     const int tid = threadIdx.x, nthr = blockDim.x, c = blockIdx.x, N = a.N, B = a.block;
     const int beg = c * kSortChunk, n = min(kSortChunk, a.n_assign - beg);
-    for (int i = tid; i < n; i += nthr) {
-        const int e = a.ids[beg + i];
-        if (e < 0 || e >= N) continue;
-        a.sorted[w.start[e] + w.chunk_off[(size_t)c * N + e] + w.lrank[beg + i]] = beg + i;
+    for (int base = tid; base < n; base += nthr * kLoadBatch) {  // two dependent rounds per batch
+        int e[kLoadBatch], lr[kLoadBatch], pos[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int i = base + u * nthr;
+            e[u] = i < n ? a.ids[beg + i] : -1;
+            lr[u] = i < n ? w.lrank[beg + i] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const bool ok = e[u] >= 0 && e[u] < N;
+            pos[u] = ok ? w.start[e[u]] + w.chunk_off[(size_t)c * N + e[u]] + lr[u] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u)
+            if (pos[u] >= 0) a.sorted[pos[u]] = beg + base + u * nthr;
     }
     const int64_t gt = (int64_t)c * nthr + tid, T = (int64_t)gridDim.x * nthr;
     const int total = *w.total, sentinel = a.n_assign;
@@ -176,7 +195,7 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
     }
     const int C = (a.n_assign + kSortChunk - 1) / kSortChunk;
     SortWork w = sort_work(scratch, a.n_assign, N);
-    const int smem = 4 * (nw * N + N + kSortChunk);
+    const int smem = 4 * (nw * N + N + 2 * kSortChunk);
     cudaError_t e = ensure_smem((const void*)sort_count_kernel, smem, g_sort_count_smem);
     if (e != cudaSuccess) return e;
     unsigned* counter = static_cast<unsigned*>(scratch) + kSortCounterSlot;
@@ -194,22 +213,29 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;
 constexpr int kQuantTileVec = 32 * kQuantUnroll;
+constexpr int kSortQuantThreads = 512;
 
-// FP4: MXFP4 (E2M1 codes, two a byte, q [M, K/2]); else MXFP8 (E4M3, q [M, K]).
+// Tiles warp_id, warp_id + nwarps, ... of the quantisation of x [M, K]
+// (the whole warp takes part).  FP4: MXFP4 (E2M1 codes, two a byte,
+// q [M, K/2]); else MXFP8 (E4M3, q [M, K]).
 template <bool FP4>
-__global__ void __launch_bounds__(kQuantThreads) mx_quant_kernel(const uint16_t* x, int64_t ldx, int M, int K,
-                                                                 uint8_t* q, uint8_t* scale) {
-    pdl_trigger();
-    pdl_wait();
+__device__ __forceinline__ void quant_tiles(const uint16_t* x, int64_t ldx, int M, int K, uint8_t* q,
+                                            uint8_t* scale, int warp_id, int nwarps) {
     const int lane = threadIdx.x & 31;
     const int vpr = K / 8;                                   // vectors per row
     const int tpr = (vpr + kQuantTileVec - 1) / kQuantTileVec;  // tiles per row
-    const int tiles = M * tpr;                               // < 2^31: checked on the host
-    const int warp_id = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
     const int K32 = K / 32;
-    for (int tile = warp_id; tile < tiles; tile += nwarps) {
-        const int r = tile / tpr, c0 = (tile - r * tpr) * kQuantTileVec + lane;
+    // tile t = (row r, chunk ch) with t = r * tpr + ch; the stride nwarps
+    // advances (r, ch) by (dq, dr) with a carry: no division per tile
+    const int dq = nwarps / tpr, dr = nwarps - dq * tpr;
+    int r = warp_id / tpr, ch = warp_id - r * tpr;
+    for (; r < M; r += dq, ch += dr) {
+        if (ch >= tpr) {
+            ch -= tpr;
+            ++r;
+            if (r >= M) break;
+        }
+        const int c0 = ch * kQuantTileVec + lane;
         const uint16_t* xr = x + (int64_t)r * ldx;
         uint4 v[kQuantUnroll];
 #pragma unroll
@@ -231,6 +257,62 @@ __global__ void __launch_bounds__(kQuantThreads) mx_quant_kernel(const uint16_t*
             if (c < vpr && (lane & 3) == 0) scale[(int64_t)r * K32 + c / 4] = (uint8_t)sb;
         }
     }
+}
+
+template <bool FP4>
+__global__ void __launch_bounds__(kQuantThreads) mx_quant_kernel(const uint16_t* x, int64_t ldx, int M, int K,
+                                                                 uint8_t* q, uint8_t* scale) {
+    pdl_trigger();
+    pdl_wait();
+    quant_tiles<FP4>(x, ldx, M, K, q, scale, (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5),
+                     (int)((gridDim.x * blockDim.x) >> 5));
+}
+
+// ------------------------------------------------------------------ sort + quant
+
+// Sort and stage-1 quant in one launch (decode batches): CTA 0 sorts all
+// M*k <= kSortQuantMaxAssign assignments with the single-CTA sort while the
+// other CTAs quantise x; the two share nothing but the launch.
+template <bool FP4>
+__global__ void __launch_bounds__(kSortQuantThreads) sort_quant_kernel(SortArgs a, const uint16_t* x, int64_t ldx,
+                                                                       int M, int K, uint8_t* q, uint8_t* scale) {
+    extern __shared__ __align__(16) int sm[];
+    pdl_trigger();
+    pdl_wait();
+    if (blockIdx.x == 0) {
+        const int nw = blockDim.x >> 5;
+        RankSmem rs{sm, sm + nw * a.N, sm + nw * a.N + a.N};
+        int* start = rs.lrank + a.n_assign;
+        int* warp_tot = start + a.N;
+        cta_sort(a, stage_ids(a.ids, a.n_assign, warp_tot + 32), rs, start, warp_tot);
+        return;
+    }
+    quant_tiles<FP4>(x, ldx, M, K, q, scale, (int)(((blockIdx.x - 1) * blockDim.x + threadIdx.x) >> 5),
+                     (int)(((gridDim.x - 1) * blockDim.x) >> 5));
+}
+
+static int g_sort_quant_smem[2][64];
+
+cudaError_t launch_sort_quant(const int32_t* ids, int M, int topk, int N, int block, int32_t* sorted,
+                              int32_t* expert_ids, int32_t* ntpp, int64_t capacity, const void* x, int64_t ldx,
+                              int K, uint8_t* q, uint8_t* scale, bool fp4, cudaStream_t st) {
+    SortArgs a{ids, M * topk, N, block, sorted, expert_ids, ntpp, capacity};
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int nw = kSortQuantThreads / 32;
+    const int smem = 4 * cta_sort_smem_ints(nw, N, a.n_assign);
+    auto kernel = fp4 ? sort_quant_kernel<true> : sort_quant_kernel<false>;
+    e = ensure_smem((const void*)kernel, smem, g_sort_quant_smem[fp4 ? 1 : 0]);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (int64_t)M * ((K / 8 + kQuantTileVec - 1) / kQuantTileVec);
+    if (tiles >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+    int64_t qctas = (tiles + nw - 1) / nw;
+    const int64_t cap = (int64_t)sms * 2;  // two resident CTAs of 512 threads per SM, grid-stride beyond
+    if (qctas > cap) qctas = cap;
+    return launch_kernel(kernel, dim3((unsigned)(1 + qctas)), dim3(kSortQuantThreads), smem, st, a,
+                         static_cast<const uint16_t*>(x), ldx, M, K, q, scale);
 }
 
 cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, bool fp4,

@@ -146,9 +146,36 @@ __device__ __forceinline__ void cta_sort(const SortArgs& a, const int* ids_src, 
     if (tid == 0) *a.ntpp = total;
 }
 
-// Shared-memory ints the single-CTA sort needs for nwarps warps.
+// Shared-memory ints the single-CTA sort needs for nwarps warps (its tables,
+// then a copy of the ids: the ranking loop walks them in dependent steps, so
+// they are staged once with every load in flight instead of one L2 round
+// trip per step).
 __host__ __device__ constexpr int cta_sort_smem_ints(int nwarps, int N, int n_assign) {
-    return nwarps * N + 2 * N + n_assign + 32;
+    return nwarps * N + 2 * N + n_assign + 32 + n_assign;
+}
+
+// Loads issued in groups of kLoadBatch per thread before their uses, so
+// that a loop over global memory pays one L2 round trip per group.
+constexpr int kLoadBatch = 8;
+
+// ids[0..n) -> shared memory by the whole CTA (then a barrier).
+__device__ __forceinline__ const int* stage_ids(const int32_t* ids, int n, int* dst) {
+    const int nthr = blockDim.x;
+    for (int base = threadIdx.x; base < n; base += nthr * kLoadBatch) {
+        int v[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int i = base + u * nthr;
+            v[u] = i < n ? __ldg(ids + i) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int i = base + u * nthr;
+            if (i < n) dst[i] = v[u];
+        }
+    }
+    __syncthreads();
+    return dst;
 }
 
 }  // namespace mr

@@ -265,6 +265,25 @@ int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
                             void *scratch, size_t scratch_bytes, void *stream);
 
 /*
+ * a4 + a5 in ONE launch for decode batches [#46691 Summary: the MiniMax-M3.1
+ * sort and stage-1 quant run as one launch for decode batches and as four
+ * launches for prefill].  One CTA sorts topk_ids exactly as mr_moe_sort
+ * while the other CTAs of the launch quantise x exactly as mr_mxfp8_quant
+ * (quant_format MR_QUANT_MXFP8, q [M, K]) or mr_mxfp4_quant (MR_QUANT_MXFP4,
+ * q [M, K/2]); every output is bitwise equal to those calls.  Arguments and
+ * layouts as there; x is bf16 [M, ldx] with the rows of topk_ids.
+ * M * topk <= MR_SORT_QUANT_MAX_ASSIGN (1024 tokens at top-8) and K % 32 == 0,
+ * else MR_ERR_UNSUPPORTED; MR_QUANT_NONE or an unknown format, a NULL or
+ * misaligned (8 B) q, or a NULL scale returns MR_ERR_INVALID_ARG.  No scratch.
+ */
+#define MR_SORT_QUANT_MAX_ASSIGN 8192
+int mr_moe_sort_quant(const int32_t *topk_ids, int M, int topk, int N, int block,
+                      const void *x, int64_t ldx, int K, int quant_format,
+                      int32_t *sorted_token_ids, int32_t *expert_ids,
+                      int32_t *num_tokens_post_padded, int64_t capacity,
+                      uint8_t *q, uint8_t *scale, void *stream);
+
+/*
  * a5, MXFP4 variant [sglang #46691 Summary: the MiniMax-M3.1 sort kernels
  * MXFP4-quantise the stage-1 activations], per the OCP Microscaling Formats
  * v1.0 spec: for each row and block of 32 elements along K,

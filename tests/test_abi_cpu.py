@@ -191,4 +191,11 @@ def test_general_route_and_mxfp4_validation(lib):
     p.M, p.rstd, p.norm_weight, p.norm_kind = 4, 0x1000, 0x1000, 3   # unknown norm kind
     assert lib.mr_moe_route(ctypes.byref(p), None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_mxfp4_quant(fake, 48, 1, 40, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
+    # sort + quant in one launch: too many assignments, no quant format, misaligned q
+    assert lib.mr_moe_sort_quant(fake, 1025, 8, 128, 16, fake, 512, 512, 1, fake, fake, fake, 1 << 20, fake, fake,
+                                 None) == mr.MR_ERR_UNSUPPORTED
+    assert lib.mr_moe_sort_quant(fake, 4, 8, 128, 16, fake, 512, 512, 0, fake, fake, fake, 1 << 20, fake, fake,
+                                 None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_moe_sort_quant(fake, 4, 8, 128, 16, fake, 512, 512, 2, fake, fake, fake, 1 << 20, P(0x1004), fake,
+                                 None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_mxfp4_quant(fake, 64, 1, 64, P(0x1002), fake, None) == mr.MR_ERR_INVALID_ARG
