@@ -765,6 +765,34 @@ def run_quant_rows(M):
     return 0
 
 
+def run_route_896_rows(ms):
+    """Three one-launch routes at each M over 896 experts (K = 3584, sigmoid
+    + selection bias, top-16, block 16; expert groups for M <= 16): a short
+    program for a profiler to capture the route kernel in that shape."""
+    import torch
+    from decode_expert_routing_gb300 import build as mrbuild
+    mrbuild.build()
+    import decode_expert_routing_gb300 as mr
+    from decode_expert_routing_gb300 import inputs
+
+    mr.load_library()
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    K, N, k = 3584, 896, 16
+    wd = dev_bf16(inputs.router_inputs(1, K, N, 3)[1])
+    bd = torch.from_numpy(inputs.selection_bias(N)).cuda()
+    for M in ms:
+        xd = dev_bf16(inputs.router_inputs(M, K, N, 3)[0])
+        scratch = mr.Scratch(M, N, K, k)
+        out = mr.alloc_route_outputs(M, N, K, k, BLOCK, xd.device)
+        for _ in range(3):
+            mr.moe_route_sort_quant(xd, wd, k, BLOCK, "sigmoid", bd, out=out, scratch=scratch)
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -772,6 +800,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--route-896-rows", default="",
+                    help="run three 896-expert routes at each of these M (for a profiler) and exit")
     ap.add_argument("--quant-rows", type=int, default=0,
                     help="run three MXFP8 and three MXFP4 quantisations of x [M, 6144] (for a profiler) and exit")
     ap.add_argument("--gemv-rows", default="",
@@ -782,6 +812,8 @@ def main():
         return run_gemv_rows([int(v) for v in args.gemv_rows.split(",")])
     if args.quant_rows:
         return run_quant_rows(args.quant_rows)
+    if args.route_896_rows:
+        return run_route_896_rows([int(v) for v in args.route_896_rows.split(",")])
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
