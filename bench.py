@@ -225,6 +225,22 @@ def env_rank():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def reduce_max_ms(ms: float, world: int, device) -> float:
+    """The job's time: the slowest rank's (all-reduce MAX over the default
+    process group; the local time when there is one rank)."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the bytes every rank moved over the job's time."""
+    return bytes_per_rank_step * steps * world / (ms_max * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- oracle leg
 
 def oracle_workload_inputs():
@@ -404,13 +420,8 @@ def run_ours(args):
     clocks = sampler.summary(wall0 - 0.5, wall1)
     sampler.stop()
 
-    ms = start.elapsed_time(end)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    total_bytes = STEP_BYTES * args.steps * world
-    value = total_bytes / (ms_max * 1e-3) / 1e9
+    ms_max = reduce_max_ms(start.elapsed_time(end), world, dev)
+    value = job_gbs(STEP_BYTES, args.steps, world, ms_max)
 
     # dominant kernel: every launch of the step is the one-launch route
     # kernel, so its average launch duration is the timed region divided by
@@ -682,10 +693,7 @@ def run_ours(args):
             e2e_step(i)
         e1.record()
     torch.cuda.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = STEP_BYTES * e2e_steps * world / (float(e2e_ms.item()) * 1e-3) / 1e9
+    e2e_value = job_gbs(STEP_BYTES, e2e_steps, world, reduce_max_ms(e0.elapsed_time(e1), world, dev))
 
     cpu = cpu_baseline_leg() if (rank == 0 and world == 1) else None
 

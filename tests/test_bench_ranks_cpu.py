@@ -1,0 +1,60 @@
+"""bench.py's multi-rank plumbing on CPU: two gloo ranks agree on the job's
+time (the slowest rank's) and the whole-job throughput, and the reference
+arm runs on rank 0 only."""
+
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, times, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        dist.barrier()
+        ms_max = bench.reduce_max_ms(times[rank], world, "cpu")
+        out[rank] = (ms_max, bench.job_gbs(1000, 10, world, ms_max), bench.env_rank())
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    world, port = 2, _free_port()
+    times = [2.5, 4.0]
+    with mp.Manager() as man:
+        out = man.dict()
+        mp.start_processes(_rank_main, args=(world, port, times, out), nprocs=world, join=True,
+                           start_method="spawn")
+        res = dict(out)
+    for rank in range(world):
+        ms_max, gbs, env = res[rank]
+        assert ms_max == 4.0
+        assert gbs == pytest.approx(1000 * 10 * world / 4.0e-3 / 1e9)
+        assert env == (rank, rank, world)
+
+
+def test_single_rank_is_local_time():
+    assert bench.reduce_max_ms(3.25, 1, "cpu") == 3.25
+    assert bench.job_gbs(2000, 4, 1, 2.0) == pytest.approx(2000 * 4 / 2.0e-3 / 1e9)
+
+
+def test_reference_arm_runs_on_rank_0_only(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class Args:
+        steps, warmup, gpus = 1, 3, 2
+    assert bench.run_reference(Args()) == 0   # returns before loading the oracle or timing anything
