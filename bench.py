@@ -55,11 +55,6 @@ def algorithmic_bytes(M, K=K_HID, N=N_EXP, k=TOPK, B=BLOCK):
     return 2 * N * K + 2 * M * K + 4 * M * N + 8 * M * k + 4 * cap + 4 * (cap // B) + 4 + M * K + M * K // 32
 
 
-def output_bytes(M, K=K_HID, N=N_EXP, k=TOPK, B=BLOCK):
-    cap = sort_capacity(M, k, N, B)
-    return 4 * M * N + 8 * M * k + 4 * cap + 4 * (cap // B) + 4 + M * K + M * K // 32
-
-
 STEP_BYTES = sum(algorithmic_bytes(M) for M in MS)
 
 
@@ -665,20 +660,33 @@ def run_ours(args):
 
     # end to end through the public API: pinned host x in, outputs back out
     e2e_steps = min(args.steps, 2000)
-    hx = {M: torch.from_numpy(np.ascontiguousarray(host[M][0][0]).view(np.int16)).view(torch.bfloat16).pin_memory()
-          for M in MS}
-    hout = {M: {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs[M].items()} for M in MS}
-    h2d = sum(hx[M].numel() * 2 for M in MS)
-    d2h = sum(output_bytes(M) for M in MS)
-    xdev = {M: torch.empty_like(xs[M][0]) for M in MS}
+    # every M's x in one pinned buffer and every M's outputs in one arena:
+    # one host-to-device and one device-to-host copy per step
+    xoff, xo = {}, 0
+    for M in MS:
+        xoff[M] = xo
+        xo += M * K_HID
+    hx_all = torch.empty(xo, dtype=torch.bfloat16, pin_memory=True)
+    for M in MS:
+        hx_all[xoff[M]:xoff[M] + M * K_HID].view(torch.int16).copy_(
+            torch.from_numpy(np.ascontiguousarray(host[M][0][0]).view(np.int16)).reshape(-1))
+    dx_all = torch.empty_like(hx_all, device=dev)
+    xdev = {M: dx_all[xoff[M]:xoff[M] + M * K_HID].view(M, K_HID) for M in MS}
+    aoff, ao = {}, 0
+    for M in MS:
+        aoff[M] = ao
+        ao += mr.route_output_layout(M, N_EXP, K_HID, TOPK, BLOCK)[1]
+    arena = torch.empty(ao, dtype=torch.uint8, device=dev)
+    harena = torch.empty(ao, dtype=torch.uint8, pin_memory=True)
+    aouts = {M: mr.route_outputs_in(arena, M, N_EXP, K_HID, TOPK, BLOCK, offset=aoff[M]) for M in MS}
+    h2d, d2h = hx_all.numel() * 2, ao
 
     def e2e_step(i):
         s = i % SLOTS
+        dx_all.copy_(hx_all, non_blocking=True)
         for M in MS:
-            xdev[M].copy_(hx[M], non_blocking=True)
-            call(M, xdev[M], ws[M][s])
-            for k, v in outs[M].items():
-                hout[M][k].copy_(v, non_blocking=True)
+            mr.moe_route_sort_quant(xdev[M], ws[M][s], TOPK, BLOCK, out=aouts[M], scratch=scratch)
+        harena.copy_(arena, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -718,7 +726,8 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "path": "pinned host x -> device, Python binding per call, all outputs -> pinned host"},
+                    "path": "every M's x from one pinned host buffer to the device, one Python binding call "
+                            "per M, every output in one arena copied to pinned host"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "gpu": props.name, "sms": props.multi_processor_count,

@@ -307,6 +307,42 @@ def mxfp8_quant(x, out=None, stream=None):
     return q, s
 
 
+def route_output_layout(M: int, N: int, K: int, topk: int, block: int, quant=True):
+    """[(name, dtype, shape, byte offset)] of the one-launch route's outputs
+    packed into one buffer (each 16-byte aligned), and the buffer's bytes."""
+    torch = _torch()
+    cap = sort_capacity(M, topk, N, block)
+    items = [("logits", torch.float32, (M, N)), ("topk_ids", torch.int32, (M, topk)),
+             ("topk_weights", torch.float32, (M, topk)), ("sorted_token_ids", torch.int32, (cap,)),
+             ("expert_ids", torch.int32, (cap // block,)), ("num_tokens_post_padded", torch.int32, (1,))]
+    if quant:
+        items += [("q", torch.uint8, (M, K // 2 if quant == "mxfp4" else K)), ("scale", torch.uint8, (M, K // 32))]
+    layout, off = [], 0
+    for name, dt, shape in items:
+        n = 1
+        for d in shape:
+            n *= d
+        layout.append((name, dt, shape, off))
+        off += (n * torch.tensor([], dtype=dt).element_size() + 15) // 16 * 16
+    return layout, off
+
+
+def route_outputs_in(buf, M: int, N: int, K: int, topk: int, block: int, quant=True, offset: int = 0):
+    """Views of the route's outputs inside the uint8 buffer buf, from byte
+    offset (16-byte aligned) on: one copy of buf moves every output."""
+    layout, nbytes = route_output_layout(M, N, K, topk, block, quant)
+    if offset % 16 or buf.dtype != _torch().uint8 or buf.numel() < offset + nbytes:
+        raise ValueError("buf must be uint8 with room for the outputs at a 16-byte aligned offset")
+    out = {}
+    for name, dt, shape, off in layout:
+        n = 1
+        for d in shape:
+            n *= d
+        esz = _torch().tensor([], dtype=dt).element_size()
+        out[name] = buf[offset + off: offset + off + n * esz].view(dt).view(shape)
+    return out
+
+
 def mxfp4_quant(x, out=None, stream=None):
     """(q uint8 [M, K/2] packed e2m1 codes, element 2j in the low nibble;
     scale uint8 [M, K/32] e8m0)."""

@@ -199,3 +199,27 @@ def test_general_route_and_mxfp4_validation(lib):
     assert lib.mr_moe_sort_quant(fake, 4, 8, 128, 16, fake, 512, 512, 2, fake, fake, fake, 1 << 20, P(0x1004), fake,
                                  None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_mxfp4_quant(fake, 64, 1, 64, P(0x1002), fake, None) == mr.MR_ERR_INVALID_ARG
+
+
+def test_route_output_arena_layout():
+    import torch
+    for quant in (True, "mxfp4", None):
+        layout, nbytes = mr.route_output_layout(16, 128, 6144, 8, 16, quant)
+        names = [n for n, _, _, _ in layout]
+        assert names[:6] == ["logits", "topk_ids", "topk_weights", "sorted_token_ids", "expert_ids",
+                             "num_tokens_post_padded"]
+        assert ("q" in names) == bool(quant)
+        assert all(off % 16 == 0 for _, _, _, off in layout) and nbytes % 16 == 0
+        buf = torch.zeros(nbytes + 32, dtype=torch.uint8)
+        out = mr.route_outputs_in(buf, 16, 128, 6144, 8, 16, quant, offset=32)
+        cap = mr.sort_capacity(16, 8, 128, 16)
+        assert out["logits"].shape == (16, 128) and out["logits"].dtype == torch.float32
+        assert out["sorted_token_ids"].shape == (cap,) and out["expert_ids"].shape == (cap // 16,)
+        if quant:
+            assert out["q"].shape == (16, 6144 // 2 if quant == "mxfp4" else 6144)
+        # disjoint views inside the buffer
+        spans = sorted((t.data_ptr() - buf.data_ptr(), t.numel() * t.element_size()) for t in out.values())
+        assert spans[0][0] >= 32 and all(a + n <= b for (a, n), (b, _) in zip(spans, spans[1:]))
+        assert spans[-1][0] + spans[-1][1] <= buf.numel()
+    with pytest.raises(ValueError):
+        mr.route_outputs_in(torch.zeros(64, dtype=torch.uint8), 16, 128, 6144, 8, 16)

@@ -34,7 +34,7 @@ def _rank_main(rank, world, port, times, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world, port = 2, _free_port()
     times = [2.5, 4.0]
-    with mp.Manager() as man:
+    with mp.get_context("spawn").Manager() as man:
         out = man.dict()
         mp.start_processes(_rank_main, args=(world, port, times, out), nprocs=world, join=True,
                            start_method="spawn")
