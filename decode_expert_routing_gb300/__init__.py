@@ -486,6 +486,36 @@ def moe_route(x, w, topk: int, block: int, scoring: str = "softmax", bias=None, 
     """The one-launch route with every option (mr_moe_route): quant "mxfp8",
     "mxfp4" or None; with rstd (and norm_weight) x holds the residual rows
     and the route runs on the norm's scale.  Returns a dict of outputs."""
+    call = PreparedRoute(x, w, topk, block, scoring, bias, renormalize, quant, rstd, norm_weight, norm, out, scratch)
+    call(stream)
+    return call.out
+
+
+class PreparedRoute:
+    """The one-launch route over fixed buffers: the arguments are checked and
+    the mr_route_params block is built once; each call is one launch of
+    mr_moe_route on the given (or torch's current) stream.  The tensors are
+    referenced for the object's life; refill x (and rstd) in place between
+    calls.  Arguments as moe_route."""
+
+    def __init__(self, x, w, topk: int, block: int, scoring: str = "softmax", bias=None, renormalize: bool = True,
+                 quant="mxfp8", rstd=None, norm_weight=None, norm: str = "gemma", out=None,
+                 scratch: Scratch | None = None):
+        self.p, self.out, self._keep = _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd,
+                                                     norm_weight, norm, out, scratch)
+        self._ref = ctypes.byref(self.p)
+        self._fn = _load().mr_moe_route
+
+    def __call__(self, stream=None):
+        """Launch; stream: a torch stream, a raw cudaStream_t (int) or None."""
+        sp = stream if isinstance(stream, int) else _stream_ptr(stream)
+        status = self._fn(self._ref, sp)
+        if status != MR_OK:
+            _check(status, "mr_moe_route")
+        return self.out
+
+
+def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, norm_weight, norm, out, scratch):
     torch = _torch()
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
@@ -531,8 +561,7 @@ def moe_route(x, w, topk: int, block: int, scoring: str = "softmax", bias=None, 
         p.scale = _dev_ptr(st, "scale", torch.uint8)
     p.scratch = scratch.ptr
     p.scratch_bytes = scratch.nbytes
-    _check(_load().mr_moe_route(ctypes.byref(p), _stream_ptr(stream)), "mr_moe_route")
-    return out
+    return p, out, (x, w, bias, rstd, norm_weight, scratch)
 
 
 def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp8", out=None, stream=None):

@@ -100,3 +100,24 @@ def test_route_mxfp4_equals_standalone_and_oracle(mr, M, norm):
     for key in spec:
         assert np.array_equal(_bits(spec[key]), _bits(f8[key])), key
     assert int(scratch.counters().abs().sum()) == 0
+
+
+def test_prepared_route_equals_moe_route(mr):
+    import torch
+    M, K, N = 8, 6144, 128
+    x, w = inputs.router_inputs(M, K, N, 2)
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    call = mr.PreparedRoute(xd, wd, 8, 16, quant="mxfp4")
+    out = call()
+    ref = mr.moe_route(xd, wd, 8, 16, quant="mxfp4")
+    for key in ref:
+        assert np.array_equal(_bits(out[key]), _bits(ref[key])), key
+    # refill x in place and launch again on a raw stream handle
+    x2, _ = inputs.router_inputs(M, K, N, 2, variant=1)
+    xd.copy_(to_dev_bf16(x2))
+    s = torch.cuda.Stream()
+    call(s.cuda_stream)
+    s.synchronize()
+    ref2 = mr.moe_route(to_dev_bf16(x2), wd, 8, 16, quant="mxfp4")
+    for key in ref2:
+        assert np.array_equal(_bits(out[key]), _bits(ref2[key])), key
