@@ -1,0 +1,87 @@
+"""Host logic of the route kernel's plan (csrc/route_plan.h), compiled here
+with the host C++ compiler: for a grid of shapes every plan the kernel can
+receive keeps the invariants its index arithmetic relies on."""
+
+import os
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+PROBE = r'''
+#include <cstdio>
+#include <initializer_list>
+#include "route_plan.h"
+int main() {
+    const int Ms[] = {1, 2, 3, 4, 7, 8, 9, 15, 16, 17, 31, 32, 33, 47, 63, 64, 65, 100, 128, 200, 256, 257, 512};
+    const int Ns[] = {8, 40, 64, 128, 136, 256, 512, 640, 896, 1024};
+    const int Ks[] = {512, 1024, 3584, 6144, 7168};
+    const int topks[] = {1, 4, 8, 16, 32};
+    for (int mg : {1, 7, 9})
+    for (int mode = 0; mode < 2; ++mode)
+    for (int M : Ms) for (int N : Ns) for (int K : Ks) for (int k : topks) {
+        if (k > N) continue;
+        mr::RoutePlan p;
+        if (!mr::route_plan(M, N, K, k, mode, 16, &p, true, mg)) { printf("none %d %d %d %d %d %d\n", mg, mode, M, N, K, k); continue; }
+        printf("plan %d %d %d %d %d %d ng=%d nl=%d clusters=%d rpc=%d tok=%d wpt=%d spw=%d nslots=%d smem=%d tc=%d cs=%d kc=%d half=%d\n",
+               mg, mode, M, N, K, k, p.ng, p.nl, p.clusters, p.rpc, p.tok, p.wpt, p.spw, p.nslots, p.smem, p.tc, p.cs,
+               p.kc, (int)p.half);
+    }
+}
+'''
+
+
+@pytest.fixture(scope="module")
+def plans(tmp_path_factory):
+    d = tmp_path_factory.mktemp("plan")
+    src = d / "probe.cpp"
+    src.write_text(PROBE)
+    exe = d / "probe"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", os.path.join(ROOT, "decode_expert_routing_gb300", "csrc"),
+                    "-o", str(exe), str(src)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()
+    res = []
+    for line in out:
+        parts = line.split()
+        key = tuple(int(v) for v in parts[1:7])
+        if parts[0] == "none":
+            res.append((key, None))
+        else:
+            res.append((key, {kv.split("=")[0]: int(kv.split("=")[1]) for kv in parts[7:]}))
+    return res
+
+
+def test_plans_keep_the_kernel_invariants(plans):
+    pow2 = lambda v: v > 0 and (v & (v - 1)) == 0
+    n_plans = 0
+    for (mg, mode, M, N, K, k), p in plans:
+        if p is None:
+            continue
+        n_plans += 1
+        assert p["cs"] == 16 and p["kc"] * 16 == K and p["kc"] % 32 == 0
+        assert p["nl"] * p["ng"] == N and p["nl"] % 8 == 0
+        assert p["ng"] == 1 or (N >= 512 and p["nl"] >= 128 and k <= p["nl"] and mg > 1)
+        if mode == 1 and p["ng"] > 1:
+            assert M <= 16                       # the whole route splits one token group only
+        assert p["clusters"] == -(-M // p["rpc"]) * p["ng"]
+        assert p["ng"] == 1 or p["clusters"] <= max(mg, 1)
+        assert pow2(p["tok"]) and pow2(p["wpt"]) and p["tok"] * 16 >= min(M, p["rpc"])
+        assert p["wpt"] * p["spw"] * 32 == p["kc"] and p["spw"] <= 8
+        assert p["nslots"] % 8 == 0
+        assert p["smem"] <= (220 if p["tc"] else 200) * 1024 and p["smem"] % 16 == 0
+        assert p["tc"] == (1 if (mode == 0 and M > 64) else 0)
+        assert p["half"] == (1 if M <= 8 else 0)
+        if mode == 1:
+            assert M <= 64 and p["tok"] <= 16
+    assert n_plans > 1000
+
+
+def test_every_documented_decode_shape_has_a_plan(plans):
+    have = {key for key, p in plans if p is not None}
+    for M in (1, 2, 4, 8, 16, 32, 64):
+        assert (9, 1, M, 128, 6144, 8) in have
+    for M in (1, 8, 16, 32):
+        assert (9, 1, M, 896, 3584, 16) in have
+    for M in (128, 256, 512):
+        assert (9, 0, M, 128, 6144, 1) in have
