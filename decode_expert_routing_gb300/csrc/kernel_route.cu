@@ -1,5 +1,5 @@
 // The decode route in ONE launch for M <= 64: router GEMV, split-K
-// reduction, top-k gate, sort and MXFP8 quant.
+// reduction, top-k gate, sort and MXFP8 (or MXFP4) quant.
 //
 // The pages' one-launch decode router (sglang #46691 Summary: a router for
 // 1-16 tokens bitwise equal to router GEMV, gate and sort; sort + stage-1
@@ -29,11 +29,23 @@
 //   its rows; the sorting CTAs publish their ids and take a last-arriver
 //   ticket (the pages' hand-off), and the last one sorts every assignment.
 //
+// Variants of the same kernel:
+//   - GEMV alone (mode 0): what the standalone router GEMV runs for
+//     M <= 64, so the logits of the two are bitwise equal; above 64 rows
+//     (N <= 128) with 64 rows per cluster on tcgen05 (TC: the CTA's weight
+//     slice and x slice staged as K-major operand tiles, one thread issuing
+//     the MMAs into a TMEM accumulator, all warps reading it back).
+//   - Expert groups (GROUPS, N >= 512): the experts split into groups of
+//     >= 128, one cluster per group, so that more SMs share the gate weight;
+//     for the whole route each cluster's collector publishes its group's
+//     top-k candidates and the collector with the last ticket merges them.
+//   - Route on the norm's scale (rstd != nullptr): x holds the residual rows
+//     and each CTA forms bf16((x * rstd) * s) as it stages its slice.
+//   - MXFP4 instead of MXFP8 stage-1 codes (quant_fp4).
+//
 // Every wait for bytes from other CTAs is bounded in time and sets a device
 // flag when it runs out.  One cluster leaves nothing in scratch; several
-// clusters leave their ticket counter at zero again.  The GEMV alone (mode 0)
-// is what the standalone router GEMV runs for M <= 64, so the logits of the
-// two are bitwise equal.
+// clusters leave their ticket counter at zero again.
 #include "common.cuh"
 #include "internal.h"
 #include "route_plan.h"
