@@ -135,6 +135,13 @@ def _dev_ptr(t, name, dtype=None, allow_none=False):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _require_cuda(**tensors):
+    """Refuse host tensors up front: every step runs in the CUDA library."""
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
 def _row_major_2d(x, name):
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError(f"{name} must be 2-D with a contiguous last dimension")
@@ -211,6 +218,7 @@ class Scratch:
 
 def router_gemv(x, w, out=None, scratch: Scratch | None = None, stream=None):
     """fp32 logits [M, N] = x [M, K] (bf16) @ w [N, K]^T (bf16)."""
+    _require_cuda(x=x, w=w)
     torch = _torch()
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
@@ -381,6 +389,7 @@ def moe_route_sort_quant(x, w, topk: int, block: int, scoring: str = "softmax", 
                          renormalize: bool = True, quant: bool = True, out=None,
                          scratch: Scratch | None = None, stream=None):
     """The whole path for M <= 64 tokens in one launch; returns a dict of outputs."""
+    _require_cuda(x=x, w=w, bias=bias)
     torch = _torch()
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
@@ -410,6 +419,7 @@ def moe_route_sort_quant(x, w, topk: int, block: int, scoring: str = "softmax", 
 def norm_apply(sres, rstd, norm_weight, norm: str = "gemma", out=None, stream=None):
     """The router input on the norm's scale, written out: bf16 [M, K] with
     xn[m, k] = bf16((sres[m, k] * rstd[m]) * s[k]), s = g or 1 + g."""
+    _require_cuda(sres=sres, rstd=rstd, norm_weight=norm_weight)
     torch = _torch()
     ldx = _row_major_2d(sres, "sres")
     M, K = sres.shape
@@ -436,6 +446,7 @@ def moe_route_sort_quant_norm(sres, rstd, norm_weight, w, topk: int, block: int,
                               out=None, scratch: Scratch | None = None, stream=None):
     """The one-launch route with its input on the norm's scale (residual rows,
     per-token rstd, norm weight); returns a dict of outputs."""
+    _require_cuda(sres=sres, rstd=rstd, norm_weight=norm_weight, w=w, bias=bias)
     torch = _torch()
     ldx = _row_major_2d(sres, "sres")
     M, K = sres.shape
@@ -528,6 +539,7 @@ def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, no
         if norm_weight is None:
             raise ValueError("rstd needs norm_weight")
         _check_norm_args(rstd, norm_weight, M, K)
+    _require_cuda(x=x, w=w, bias=bias, rstd=rstd, norm_weight=norm_weight)
     if out is None:
         out = alloc_route_outputs(M, N, K, topk, block, x.device, quant)
     if scratch is None:
@@ -577,6 +589,7 @@ def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp
     K = x.shape[1]
     if quant not in ("mxfp8", "mxfp4"):
         raise ValueError("quant must be mxfp8 or mxfp4")
+    _require_cuda(topk_ids=topk_ids, x=x)
     cap = sort_capacity(M, k, num_experts, block)
     if cap < 0:
         raise MoeRouteUnsupported(MR_ERR_UNSUPPORTED, "mr_sort_capacity")

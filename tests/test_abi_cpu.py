@@ -223,3 +223,30 @@ def test_route_output_arena_layout():
         assert spans[-1][0] + spans[-1][1] <= buf.numel()
     with pytest.raises(ValueError):
         mr.route_outputs_in(torch.zeros(64, dtype=torch.uint8), 16, 128, 6144, 8, 16)
+
+
+def test_binding_rejects_bad_arguments_and_host_tensors():
+    # argument checks run before any launch; host tensors are refused (there
+    # is no CPU path behind the binding)
+    import torch
+    x = torch.zeros((4, 512), dtype=torch.bfloat16)
+    w = torch.zeros((128, 512), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="quant"):
+        mr.moe_route(x, w, 8, 16, quant="fp16")
+    with pytest.raises(ValueError, match="norm_weight"):
+        mr.moe_route(x, w, 8, 16, rstd=torch.ones(4))
+    with pytest.raises(ValueError, match="rstd"):
+        mr.moe_route(x, w, 8, 16, rstd=torch.ones(3), norm_weight=torch.zeros(512, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="CUDA"):
+        mr.moe_route(x, w, 8, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        mr.mxfp4_quant(x)
+    with pytest.raises(ValueError, match="CUDA"):
+        mr.router_gemv(x, w)
+    ids = torch.zeros((4, 8), dtype=torch.int32)
+    with pytest.raises(ValueError, match="quant"):
+        mr.moe_sort_quant(ids, x, 128, 16, quant="mxfp16")
+    with pytest.raises(ValueError, match="rows"):
+        mr.moe_sort_quant(ids, torch.zeros((5, 512), dtype=torch.bfloat16), 128, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        mr.moe_sort_quant(ids, x, 128, 16)
