@@ -320,10 +320,10 @@ def run_ours(args):
     import torch.distributed as dist
 
     rank, local_rank, world = env_rank()
+    torch.cuda.set_device(local_rank)  # before the process group: NCCL binds to the current device
+    dev = torch.device("cuda", local_rank)
     if world > 1:
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
 
     from decode_expert_routing_gb300 import build as mrbuild
     mrbuild.build()
