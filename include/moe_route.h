@@ -164,10 +164,18 @@ int mr_scratch_reset(void *scratch, size_t scratch_bytes, void *stream);
  * #46691 Summary: up to 512 rows].
  *   logits[m, n] = sum_k x[m, k] * w[n, k]   (fp32 accumulation)
  * x: bf16 [M, ldx]; w: bf16 [N, K] contiguous; logits: fp32 [M, N].
- * One launch.  The K range is split over CTAs; the last CTA to finish each
- * (n-block, row-tile) sums the fp32 partials in split order (deterministic)
- * and re-zeroes its counter.  Deterministic: the same inputs give the same
- * bits on every call.
+ * One launch.  The K range is split over CTAs and the partials are summed in
+ * split order (deterministic: the same inputs give the same bits on every
+ * call):
+ *  - whenever the cluster kernel's tiles fit (M <= 64; 64 < M <= 512 with
+ *    N <= 128 on tcgen05): one thread-block cluster per 16 rows (64 above
+ *    64 rows), each CTA a K slice, the partials summed by each row's owner
+ *    CTA over distributed shared memory; no scratch.  N >= 512 splits the
+ *    experts into groups of >= 128, one cluster each.  For M <= 64 these
+ *    are the logits of mr_moe_route_sort_quant, bit for bit;
+ *  - otherwise the split-K kernel: the last CTA to finish each (n-block,
+ *    row-tile) sums the fp32 partials and re-zeroes its counter (scratch
+ *    of mr_scratch_bytes bytes, else MR_ERR_INVALID_ARG / _SCRATCH_TOO_SMALL).
  */
 int mr_router_gemv(const void *x, int64_t ldx, const void *w, float *logits,
                    int M, int N, int K, void *scratch, size_t scratch_bytes,
