@@ -10,6 +10,8 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
+    if not config.option.basetemp:  # temporary files of the tests stay inside the repository
+        config.option.basetemp = os.path.join(ROOT, ".pytest_tmp")
 
 
 def gpu_available() -> bool:

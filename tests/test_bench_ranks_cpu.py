@@ -18,14 +18,14 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, times, out):
+def _rank_main(rank, world, port, times, q):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
                       LOCAL_RANK=str(rank))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         dist.barrier()
         ms_max = bench.reduce_max_ms(times[rank], world, "cpu")
-        out[rank] = (ms_max, bench.job_gbs(1000, 10, world, ms_max), bench.env_rank())
+        q.put((rank, ms_max, bench.job_gbs(1000, 10, world, ms_max), bench.env_rank()))
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -34,11 +34,13 @@ def _rank_main(rank, world, port, times, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world, port = 2, _free_port()
     times = [2.5, 4.0]
-    with mp.get_context("spawn").Manager() as man:
-        out = man.dict()
-        mp.start_processes(_rank_main, args=(world, port, times, out), nprocs=world, join=True,
-                           start_method="spawn")
-        res = dict(out)
+    q = mp.get_context("spawn").SimpleQueue()   # a pipe: no files, no manager process
+    mp.start_processes(_rank_main, args=(world, port, times, q), nprocs=world, join=True, start_method="spawn")
+    res = {}
+    while not q.empty():
+        rank, ms_max, gbs, env = q.get()
+        res[rank] = (ms_max, gbs, env)
+    assert sorted(res) == [0, 1]
     for rank in range(world):
         ms_max, gbs, env = res[rank]
         assert ms_max == 4.0
