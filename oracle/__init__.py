@@ -43,6 +43,7 @@ def _load():
         lib.oracle_topk_sigmoid.argtypes = [P, P, i32, i32, i32, i32, P, P]
         lib.oracle_sigmoid_f32.argtypes = [ctypes.c_float]
         lib.oracle_sigmoid_f32.restype = ctypes.c_float
+        lib.oracle_sigmoid_f32_array.argtypes = [P, i64, P]
         lib.oracle_sort_capacity.argtypes = [i32, i32, i32, i32]
         lib.oracle_sort_capacity.restype = i64
         lib.oracle_moe_sort.argtypes = [P, i32, i32, i32, i32, P, P, P, i64]
@@ -101,10 +102,11 @@ def route_topk(logits: np.ndarray, topk: int, scoring: str = "softmax", bias=Non
 
 
 def sigmoid_f32(values) -> np.ndarray:
-    """The fp32 sigmoid score recipe, element by element."""
-    v = np.asarray(values, dtype=np.float32).ravel()
-    f = _load().oracle_sigmoid_f32
-    return np.array([f(float(t)) for t in v], dtype=np.float32).reshape(np.shape(values))
+    """The correctly rounded fp32 sigmoid 1 / (1 + e^-l), element by element."""
+    v = _c(values, np.float32).ravel()
+    out = np.empty(v.shape[0], dtype=np.float32)
+    _load().oracle_sigmoid_f32_array(_ptr(v), v.shape[0], _ptr(out))
+    return out.reshape(np.shape(values))
 
 
 def sort_capacity(M: int, topk: int, N: int, block: int) -> int:

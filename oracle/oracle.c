@@ -6,8 +6,9 @@
  *
  * Plain, slow and single-threaded on purpose: every function is the written
  * definition of its step, with no blocking, fusion or reordering.  Floating
- * point is fp64 except where the method itself fixes fp32 (the sigmoid score
- * and the selection key of the sigmoid gate, see oracle_sigmoid_f32).
+ * point is fp64 except where the method itself fixes fp32 (the sigmoid score,
+ * evaluated in long double and rounded once to fp32, and the selection key
+ * of the sigmoid gate, see oracle_sigmoid_f32).
  *
  * Sources (GitHub PR pages about MoE decode routing):
  *  - sglang #36557 "MiniMax-M3: Triton split-K router GEMV with in-kernel
@@ -19,7 +20,7 @@
  *    review diff of the sort kernel: stable rank = number of earlier
  *    (token, slot) pairs on the same expert; MXFP8 stage-1 activations;
  *    896 experts, top-16, hidden 3584.
- * Where the pages are silent (sort layout, MX scale rule, sigmoid recipe,
+ * Where the pages are silent (sort layout, MX scale rule, sigmoid rounding,
  * tie order) the readings are stated at each function.
  *
  * Compile with -ffp-contract=off: a fused multiply-add may appear only where
@@ -118,44 +119,27 @@ void oracle_topk_softmax(const float *logits, int M, int N, int k, int renormali
 
 /*
  * fp32 sigmoid score.  The routing pages fix "fp32 sigmoid scores" for the
- * Kimi-K3-style gate but not how sigma is evaluated, and an fp32 sigma that
- * differs by one ulp between two libraries can swap two experts whose biased
- * scores are one ulp apart.  READING: the score is defined by one fully
- * specified fp32 recipe, so any implementation that follows it gets the same
- * bits:
- *   y  = clamp(-l, -87, 88)
- *   n  = rint(y * log2(e))                     (fp32 multiply, ties to even)
- *   r  = fma(-n, ln2_hi, y); r = fma(-n, ln2_lo, r)
- *        (Cody and Waite's argument reduction, "Software Manual for the
- *         Elementary Functions", 1980, with a two-part ln 2)
- *   p  = sum_{j=0..7} r^j / j!   by Horner's rule with fp32 fma
- *        (degree-7 Taylor polynomial of e^r on |r| <= ln2/2)
- *   e  = p * 2^n ;  s = 1 / (1 + e)            (fp32, round to nearest)
- * The tests pin s to within a few fp32 ulps of the exact sigma.
+ * Kimi-K3-style gate (sglang #46652, Modifications) but not how sigma is
+ * evaluated, and two fp32 evaluations that differ by one ulp can swap two
+ * experts whose biased scores are one ulp apart.  READING: the score is the
+ * plain definition sigma(l) = 1 / (1 + e^-l) of the fp32 logit l, rounded
+ * once to the nearest fp32 value (the correctly rounded sigmoid; a tie cannot
+ * occur, since sigma of a nonzero rational is irrational).  Evaluated here in
+ * long double (a 64-bit significand on x86-64, 113 bits on aarch64), whose
+ * relative error of a few 2^-64 is far below the distance of sigma from an
+ * fp32 rounding boundary, then rounded once to fp32.  Results below half the
+ * smallest fp32 subnormal round to +0; results within 2^-25 of 1 round to 1.
  */
 float oracle_sigmoid_f32(float l)
 {
-    const float log2e = 0x1.715476p+0f;
-    const float ln2_hi = 0x1.62e430p-1f;
-    const float ln2_lo = -0x1.05c610p-29f;
-    const float c[8] = {0x1p+0f, 0x1p+0f, 0x1p-1f, 0x1.555556p-3f,
-                        0x1.555556p-5f, 0x1.111112p-7f, 0x1.6c16c2p-10f, 0x1.a01a02p-13f};
-    float y = -l;
-    if (y < -87.0f) y = -87.0f;
-    if (y > 88.0f) y = 88.0f;
-    float t = y * log2e;
-    float n = rintf(t);
-    float r = fmaf(-n, ln2_hi, y);
-    r = fmaf(-n, ln2_lo, r);
-    float p = c[7];
-    for (int j = 6; j >= 0; --j) p = fmaf(p, r, c[j]);
-    int ni = (int)n;
-    uint32_t two_n_bits = (uint32_t)(ni + 127) << 23;
-    float two_n;
-    memcpy(&two_n, &two_n_bits, sizeof two_n);
-    float e = p * two_n;
-    float d = 1.0f + e;
-    return 1.0f / d;
+    long double e = expl(-(long double)l);
+    return (float)(1.0L / (1.0L + e));
+}
+
+/* Element-wise oracle_sigmoid_f32 of an array. */
+void oracle_sigmoid_f32_array(const float *l, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_sigmoid_f32(l[i]);
 }
 
 /*
