@@ -36,12 +36,22 @@ sys.path.insert(0, ROOT)
 
 METRIC = "router+topk+sort+quant µs/call and achieved HBM GB/s vs GB300 peak, M=1..64"
 K_HID, N_EXP, TOPK, BLOCK = 6144, 128, 8, 16
-MS = (2, 4, 8, 16, 32, 64)
+MS = (1, 2, 4, 8, 16, 32, 64)
+GEMV_ALONE_MS = (1, 2, 4, 8)
 FUSED_MAX_M = 64
 SLOTS = 32            # rotation slots (graphs); each holds its own x and W per M
 DISTINCT = 4          # distinct input draws, replicated over the slots
-WORKLOAD = ("decode batch buckets: M in {2,4,8,16,32,64}, K=6144, N=128, softmax top-8, "
+WORKLOAD = ("decode batch buckets: M in {1,2,4,8,16,32,64}, K=6144, N=128, softmax top-8, "
             "sort block 16, MXFP8 of x; one launch per M (router GEMV + gate + sort + quant)")
+
+
+def workload_config(world: int, pdl: bool = True) -> dict:
+    """The config dict both arms print (the same workload, the same words)."""
+    ring = sum(M * K_HID * 2 + N_EXP * K_HID * 2 for M in MS) * SLOTS
+    return {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2: {SLOTS} rotating slots of x and W, {ring / 1e6:.0f} MB resident "
+                  "(GPU arm: one CUDA graph per slot)",
+            "launch": "CUDA graph per step" + (", programmatic dependent launch" if pdl else "")}
 
 
 def sort_capacity(M, k, N, B):
@@ -263,7 +273,7 @@ def time_oracle(min_seconds: float, max_steps: int):
 def cpu_baseline_leg():
     steps, el = time_oracle(10.0, 40)
     return {"value": round(STEP_BYTES * steps / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} whole steps of the workload (all 6 M buckets) in {el:.1f} s, single thread"}
+            "sample": f"{steps} whole steps of the workload (all {len(MS)} M buckets) in {el:.1f} s, single thread"}
 
 
 def run_reference(args):
@@ -298,13 +308,13 @@ def run_reference(args):
             nbytes += algorithmic_bytes(M)
     el = time.perf_counter() - t0
     value = nbytes / el / 1e9
-    sample = ("whole steps of the workload (all 6 M buckets)" if whole else
-              "one M bucket of the workload per step, rotating over the 6 buckets")
+    sample = (f"whole steps of the workload (all {len(MS)} M buckets)" if whole else
+              f"one M bucket of the workload per step, rotating over the {len(MS)} buckets")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "n/a (host)"},
+        "data": "synthetic", "config": workload_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} steps, each {sample}; single thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -343,7 +353,6 @@ def run_ours(args):
     xs = {M: [base[M][s % DISTINCT][0].clone() for s in range(SLOTS)] for M in MS}
     ws = {M: [base[M][s % DISTINCT][1].clone() for s in range(SLOTS)] for M in MS}
     del base
-    ring_bytes = sum(xs[M][0].numel() * 2 + ws[M][0].numel() * 2 for M in MS) * SLOTS
 
     scratch = mr.Scratch(max(MS), N_EXP, K_HID, TOPK, device=dev)
     outs = {M: mr.alloc_route_outputs(M, N_EXP, K_HID, TOPK, BLOCK, dev) for M in MS}
@@ -432,6 +441,22 @@ def run_ours(args):
                 "avg_launch_us": round(avg_launch_us, 3),
                 "algorithmic_bytes_per_launch": round(STEP_BYTES / launches_per_step)}
 
+    def graph_us(body, calls, reps=10):
+        """Microseconds per call of body (calls launches) captured as one graph."""
+        with torch.cuda.stream(stream):
+            g = rt.capture(sp, body)
+        for _ in range(3):
+            rt.launch(g, sp)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(reps):
+                rt.launch(g, sp)
+            e1.record()
+        torch.cuda.synchronize()
+        rt.destroy(g)
+        return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
     # per-M microseconds per call (graph of 64 calls on rotating slots)
     per_m = {}
     for M in MS:
@@ -453,6 +478,23 @@ def run_ours(args):
         per_m[str(M)] = {"us_per_call": round(us, 3), "GBs": round(algorithmic_bytes(M) / (us * 1e-6) / 1e9, 1),
                          "launches_per_call": 1 if M <= FUSED_MAX_M else 4}
         rt.destroy(g)
+
+    # the router GEMV alone at decode sizes (N = 128, K = 6144, M <= 8): us
+    # per call and its fraction of the measured HBM bandwidth (graph of 64
+    # calls on the rotating slots, so the gate weight streams from HBM)
+    gemv_alone = {}
+    for M in GEMV_ALONE_MS:
+        lgm = torch.empty((M, N_EXP), dtype=torch.float32, device=dev)
+
+        def body(M=M, lgm=lgm):
+            for r in range(64):
+                mr.router_gemv(xs[M][r % SLOTS], ws[M][r % SLOTS], out=lgm, scratch=scratch)
+        with torch.cuda.stream(stream):
+            body()
+        us = graph_us(body, 64)
+        gb = (2 * N_EXP * K_HID + 2 * M * K_HID + 4 * M * N_EXP) / (us * 1e-6) / 1e9
+        gemv_alone[str(M)] = {"us_per_call": round(us, 3), "GBs": round(gb, 1), "frac_of_peak": round(gb / peak, 4)}
+        del lgm
 
     # the split-K GEMV with last-arriver fixup (64 < M <= 512): us per call
     split_k = {}
@@ -483,22 +525,6 @@ def run_ours(args):
         split_k[str(M)] = {"us_per_call": round(us, 3), "GBs": round(gb, 1)}
         rt.destroy(g)
         del xb, lg, sk
-
-    def graph_us(body, calls, reps=10):
-        """Microseconds per call of body (calls launches) captured as one graph."""
-        with torch.cuda.stream(stream):
-            g = rt.capture(sp, body)
-        for _ in range(3):
-            rt.launch(g, sp)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record()
-            for _ in range(reps):
-                rt.launch(g, sp)
-            e1.record()
-        torch.cuda.synchronize()
-        rt.destroy(g)
-        return e0.elapsed_time(e1) * 1e3 / (reps * calls)
 
     # A/B of the split-K hand-off: the one launch (partials summed in a fixed
     # order by the row's owner, then the gate) against the four-call chain
@@ -716,12 +742,10 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2: {SLOTS} rotating slots of x and W, "
-                             f"{ring_bytes / 1e6:.0f} MB resident, one CUDA graph per slot",
-                       "launch": "CUDA graph per step" + ("" if args.no_pdl else ", programmatic dependent launch")},
+            "config": workload_config(world, not args.no_pdl),
             "us_per_call": round(ms_max * 1e3 / args.steps / len(MS), 3),
             "per_m": per_m,
+            "router_gemv_alone_n128": gemv_alone,
             "split_k_gemv_rows_128_512": split_k,
             "route_896_experts_sigmoid_top16": k3,
             "route_on_norm_scale_gemma": normed,
@@ -743,78 +767,6 @@ def run_ours(args):
     return 0
 
 
-def run_gemv_rows(ms):
-    """Three router_gemv calls at each M (K = 6144, N = 128, the prefill x):
-    a short program for a profiler to capture the GEMV kernels."""
-    import torch
-    from decode_expert_routing_gb300 import build as mrbuild
-    mrbuild.build()
-    import decode_expert_routing_gb300 as mr
-    from decode_expert_routing_gb300 import inputs
-    mr.load_library()
-
-    def dev_bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-
-    wd = dev_bf16(inputs.router_inputs(2, K_HID, N_EXP, 2)[1])
-    for M in ms:
-        xd = dev_bf16(inputs.prefill_x(M, K_HID))
-        out = torch.empty((M, N_EXP), dtype=torch.float32, device="cuda")
-        scratch = mr.Scratch(M, N_EXP, K_HID, TOPK)
-        for _ in range(3):
-            mr.router_gemv(xd, wd, out=out, scratch=scratch)
-    torch.cuda.synchronize()
-    return 0
-
-
-def run_quant_rows(M):
-    """Three MXFP8 and three MXFP4 quantisations of the prefill x [M, 6144]
-    (two inputs, 50 MB each at M = 4096): a short program for a profiler to
-    capture the quantiser kernels."""
-    import torch
-    from decode_expert_routing_gb300 import build as mrbuild
-    mrbuild.build()
-    import decode_expert_routing_gb300 as mr
-    from decode_expert_routing_gb300 import inputs
-    mr.load_library()
-    xs = [torch.from_numpy(np.ascontiguousarray(inputs.prefill_x(M, K_HID, variant=v)).view(np.int16))
-          .view(torch.bfloat16).cuda() for v in range(2)]
-    for r in range(3):
-        mr.mxfp8_quant(xs[r % 2])
-    for r in range(3):
-        mr.mxfp4_quant(xs[r % 2])
-    torch.cuda.synchronize()
-    return 0
-
-
-def run_route_896_rows(ms):
-    """Three one-launch routes at each M over 896 experts (K = 3584, sigmoid
-    + selection bias, top-16, block 16; expert groups for M <= 16): a short
-    program for a profiler to capture the route kernel in that shape."""
-    import torch
-    from decode_expert_routing_gb300 import build as mrbuild
-    mrbuild.build()
-    import decode_expert_routing_gb300 as mr
-    from decode_expert_routing_gb300 import inputs
-
-    mr.load_library()
-
-    def dev_bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-
-    K, N, k = 3584, 896, 16
-    wd = dev_bf16(inputs.router_inputs(1, K, N, 3)[1])
-    bd = torch.from_numpy(inputs.selection_bias(N)).cuda()
-    for M in ms:
-        xd = dev_bf16(inputs.router_inputs(M, K, N, 3)[0])
-        scratch = mr.Scratch(M, N, K, k)
-        out = mr.alloc_route_outputs(M, N, K, k, BLOCK, xd.device)
-        for _ in range(3):
-            mr.moe_route_sort_quant(xd, wd, k, BLOCK, "sigmoid", bd, out=out, scratch=scratch)
-    torch.cuda.synchronize()
-    return 0
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -822,20 +774,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
-    ap.add_argument("--route-896-rows", default="",
-                    help="run three 896-expert routes at each of these M (for a profiler) and exit")
-    ap.add_argument("--quant-rows", type=int, default=0,
-                    help="run three MXFP8 and three MXFP4 quantisations of x [M, 6144] (for a profiler) and exit")
-    ap.add_argument("--gemv-rows", default="",
-                    help="profiling aid: only run router_gemv three times at each of these M "
-                         "(comma-separated) and exit, printing no JSON line")
     args = ap.parse_args()
-    if args.gemv_rows:
-        return run_gemv_rows([int(v) for v in args.gemv_rows.split(",")])
-    if args.quant_rows:
-        return run_quant_rows(args.quant_rows)
-    if args.route_896_rows:
-        return run_route_896_rows([int(v) for v in args.route_896_rows.split(",")])
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

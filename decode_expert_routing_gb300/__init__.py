@@ -18,7 +18,8 @@ import os
 
 __all__ = [
     "MoeRouteError", "MoeRouteUnsupported", "Scratch", "library_path", "load_library",
-    "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "LAUNCH_TEST_STALL", "LAUNCH_LEGACY_MMA", "set_wait_limit_ns",
+    "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "LAUNCH_TEST_STALL", "LAUNCH_LEGACY_MMA",
+    "LAUNCH_TEST_SLOW_SIGMOID", "LAUNCH_CHECK_SCRATCH", "set_wait_limit_ns",
     "device_error", "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
     "moe_sort", "mxfp8_quant", "moe_route_sort_quant", "router_gemv_noalloc",
 ]
@@ -27,7 +28,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libmoe_route.so")
 _lib = None
 
-MR_OK, MR_ERR_UNSUPPORTED, MR_ERR_INVALID_ARG, MR_ERR_SCRATCH_TOO_SMALL, MR_ERR_CUDA, MR_ERR_TIMEOUT = range(6)
+(MR_OK, MR_ERR_UNSUPPORTED, MR_ERR_INVALID_ARG, MR_ERR_SCRATCH_TOO_SMALL, MR_ERR_CUDA, MR_ERR_TIMEOUT,
+ MR_ERR_SCRATCH_DIRTY) = range(7)
 SCORING = {"softmax": 0, "sigmoid": 1}
 NORM_KIND = {"rms": 0, "gemma": 1}
 QUANT_FORMAT = {None: 0, "mxfp8": 1, "mxfp4": 2}
@@ -135,22 +137,64 @@ def _dev_ptr(t, name, dtype=None, allow_none=False):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _require_cuda(**tensors):
-    """Refuse host tensors up front: every step runs in the CUDA library."""
-    for name, t in tensors.items():
-        if t is not None and not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor")
-
-
 def _row_major_2d(x, name):
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError(f"{name} must be 2-D with a contiguous last dimension")
     return x.stride(0)
 
 
+def _one_device(**tensors):
+    """The one CUDA device of every given tensor (None entries skipped)."""
+    devs = {}
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        devs.setdefault(t.device, name)
+    if len(devs) != 1:
+        raise ValueError("tensors on different devices: " + ", ".join(f"{n} on {d}" for d, n in devs.items()))
+    return next(iter(devs))
+
+
+def _check_out(t, name, shape, dtype, device, min_numel=False):
+    """A caller-passed output: contiguous, of this dtype and shape (or at
+    least this many elements when min_numel), on this device."""
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if min_numel:
+        if t.numel() < shape:
+            raise ValueError(f"{name} needs at least {shape} elements, has {t.numel()}")
+    elif tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _check_scratch(scratch, device):
+    if scratch is not None and scratch.tensor.device != device:
+        raise ValueError(f"scratch must be on {device}")
+
+
+def _launch_ctx(device):
+    """The calling thread's current device set to device for the C call (the
+    library launches on the current device, on the given stream)."""
+    return _torch().cuda.device(device)
+
+
+def _stream_on(device, stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
 LAUNCH_PDL = 1
 LAUNCH_TEST_STALL = 2  # test hook: the cluster kernels' bounded waits run out
 LAUNCH_LEGACY_MMA = 4  # router GEMV of more than 64 rows: split-K mma.sync kernel instead of tcgen05
+LAUNCH_TEST_SLOW_SIGMOID = 8  # test hook: every exact sigmoid score through its double-double path
+LAUNCH_CHECK_SCRATCH = 16  # debug: calls that use scratch counters verify they are zero first (synchronous)
 
 
 def set_launch_flags(flags: int) -> None:
@@ -218,20 +262,23 @@ class Scratch:
 
 def router_gemv(x, w, out=None, scratch: Scratch | None = None, stream=None):
     """fp32 logits [M, N] = x [M, K] (bf16) @ w [N, K]^T (bf16)."""
-    _require_cuda(x=x, w=w)
     torch = _torch()
+    dev = _one_device(x=x, w=w, out=out)
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
     N = w.shape[0]
-    if not w.is_contiguous() or w.shape[1] != K:
+    if w.dim() != 2 or not w.is_contiguous() or w.shape[1] != K:
         raise ValueError("w must be contiguous [N, K]")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _check_out(out, "out", (M, N), torch.float32, dev)
     if scratch is None:
-        scratch = Scratch(M, N, K, 1, device=x.device)
-    _check(_load().mr_router_gemv(_dev_ptr(x, "x", torch.bfloat16), ldx, _dev_ptr(w, "w", torch.bfloat16),
-                                  _dev_ptr(out, "out", torch.float32), M, N, K, scratch.ptr,
-                                  scratch.nbytes, _stream_ptr(stream)), "mr_router_gemv")
+        scratch = Scratch(M, N, K, 1, device=dev)
+    _check_scratch(scratch, dev)
+    with _launch_ctx(dev):
+        _check(_load().mr_router_gemv(_dev_ptr(x, "x", torch.bfloat16), ldx, _dev_ptr(w, "w", torch.bfloat16),
+                                      _dev_ptr(out, "out", torch.float32), M, N, K, scratch.ptr,
+                                      scratch.nbytes, _stream_on(dev, stream)), "mr_router_gemv")
     return out
 
 
@@ -241,17 +288,20 @@ def router_gemv_noalloc(x, w, out=None, stream=None):
     cannot allocate; calls on one device share that scratch, so overlapping
     calls race.  The first call per device does a one-time set-up."""
     torch = _torch()
+    dev = _one_device(x=x, w=w, out=out)
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
     N = w.shape[0]
-    if not w.is_contiguous() or w.shape[1] != K:
+    if w.dim() != 2 or not w.is_contiguous() or w.shape[1] != K:
         raise ValueError("w must be contiguous [N, K]")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    _check(_load().mr_router_gemv_noalloc(_dev_ptr(x, "x", torch.bfloat16), ldx,
-                                          _dev_ptr(w, "w", torch.bfloat16),
-                                          _dev_ptr(out, "out", torch.float32), M, N, K,
-                                          _stream_ptr(stream)), "mr_router_gemv_noalloc")
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _check_out(out, "out", (M, N), torch.float32, dev)
+    with _launch_ctx(dev):
+        _check(_load().mr_router_gemv_noalloc(_dev_ptr(x, "x", torch.bfloat16), ldx,
+                                              _dev_ptr(w, "w", torch.bfloat16),
+                                              _dev_ptr(out, "out", torch.float32), M, N, K,
+                                              _stream_on(dev, stream)), "mr_router_gemv_noalloc")
     return out
 
 
@@ -259,17 +309,23 @@ def route_topk(logits, topk: int, scoring: str = "softmax", bias=None, renormali
                ids=None, weights=None, stream=None):
     """(topk_ids int32 [M, k], topk_weights fp32 [M, k])."""
     torch = _torch()
+    dev = _one_device(logits=logits, bias=bias, ids=ids, weights=weights)
     if logits.dim() != 2 or not logits.is_contiguous():
         raise ValueError("logits must be contiguous [M, N]")
     M, N = logits.shape
+    if bias is not None:
+        _check_out(bias, "bias", (N,), torch.float32, dev)
     if ids is None:
-        ids = torch.empty((M, topk), dtype=torch.int32, device=logits.device)
+        ids = torch.empty((M, topk), dtype=torch.int32, device=dev)
     if weights is None:
-        weights = torch.empty((M, topk), dtype=torch.float32, device=logits.device)
-    _check(_load().mr_route_topk(_dev_ptr(logits, "logits", torch.float32), M, N, topk, SCORING[scoring],
-                                 _dev_ptr(bias, "bias", torch.float32, allow_none=True), int(renormalize),
-                                 _dev_ptr(ids, "ids", torch.int32), _dev_ptr(weights, "weights", torch.float32),
-                                 _stream_ptr(stream)), "mr_route_topk")
+        weights = torch.empty((M, topk), dtype=torch.float32, device=dev)
+    _check_out(ids, "ids", (M, topk), torch.int32, dev)
+    _check_out(weights, "weights", (M, topk), torch.float32, dev)
+    with _launch_ctx(dev):
+        _check(_load().mr_route_topk(_dev_ptr(logits, "logits", torch.float32), M, N, topk, SCORING[scoring],
+                                     _dev_ptr(bias, "bias", torch.float32, allow_none=True), int(renormalize),
+                                     _dev_ptr(ids, "ids", torch.int32), _dev_ptr(weights, "weights", torch.float32),
+                                     _stream_on(dev, stream)), "mr_route_topk")
     return ids, weights
 
 
@@ -277,41 +333,64 @@ def moe_sort(topk_ids, num_experts: int, block: int, out=None, scratch: Scratch 
              stream=None):
     """(sorted_token_ids [cap], expert_ids [cap/block], num_tokens_post_padded [1]) int32."""
     torch = _torch()
+    st0, ex0, nt0 = out if out is not None else (None, None, None)
+    dev = _one_device(topk_ids=topk_ids, sorted_token_ids=st0, expert_ids=ex0, num_tokens_post_padded=nt0)
     if topk_ids.dim() != 2 or not topk_ids.is_contiguous():
         raise ValueError("topk_ids must be contiguous [M, k]")
     M, k = topk_ids.shape
     cap = sort_capacity(M, k, num_experts, block)
     if cap < 0:
         raise MoeRouteUnsupported(MR_ERR_UNSUPPORTED, "mr_sort_capacity")
-    dev = topk_ids.device
     if out is None:
         out = (torch.empty(cap, dtype=torch.int32, device=dev),
                torch.empty(cap // block, dtype=torch.int32, device=dev),
                torch.empty(1, dtype=torch.int32, device=dev))
     st, ex, nt = out
+    _check_sort_out(st, ex, nt, cap, block, dev)
+    _check_scratch(scratch, dev)
     sp, sb = (scratch.ptr, scratch.nbytes) if scratch is not None else (None, 0)
     if scratch is None and M * k > 2048:
         scratch = Scratch(M, num_experts, 512, k, device=dev)
         sp, sb = scratch.ptr, scratch.nbytes
-    _check(_load().mr_moe_sort(_dev_ptr(topk_ids, "topk_ids", torch.int32), M, k, num_experts, block,
-                               _dev_ptr(st, "sorted_token_ids", torch.int32),
-                               _dev_ptr(ex, "expert_ids", torch.int32),
-                               _dev_ptr(nt, "num_tokens_post_padded", torch.int32), st.numel(), sp, sb,
-                               _stream_ptr(stream)), "mr_moe_sort")
+    with _launch_ctx(dev):
+        _check(_load().mr_moe_sort(_dev_ptr(topk_ids, "topk_ids", torch.int32), M, k, num_experts, block,
+                                   _dev_ptr(st, "sorted_token_ids", torch.int32),
+                                   _dev_ptr(ex, "expert_ids", torch.int32),
+                                   _dev_ptr(nt, "num_tokens_post_padded", torch.int32), st.numel(), sp, sb,
+                                   _stream_on(dev, stream)), "mr_moe_sort")
     return st, ex, nt
+
+
+def _check_sort_out(st, ex, nt, cap, block, dev):
+    """The sort's outputs: st holds at least the capacity (its length is the
+    capacity passed on), ex one entry per block of it, nt one entry."""
+    torch = _torch()
+    _check_out(st, "sorted_token_ids", cap, torch.int32, dev, min_numel=True)
+    _check_out(ex, "expert_ids", st.numel() // block, torch.int32, dev, min_numel=True)
+    _check_out(nt, "num_tokens_post_padded", 1, torch.int32, dev, min_numel=True)
 
 
 def mxfp8_quant(x, out=None, stream=None):
     """(q uint8 [M, K] e4m3 codes, scale uint8 [M, K/32] e8m0)."""
+    return _mx_quant(x, out, stream, fp4=False)
+
+
+def _mx_quant(x, out, stream, fp4):
     torch = _torch()
+    dev = _one_device(x=x, **({} if out is None else dict(q=out[0], scale=out[1])))
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
+    qk = K // 2 if fp4 else K
     if out is None:
-        out = (torch.empty((M, K), dtype=torch.uint8, device=x.device),
-               torch.empty((M, K // 32), dtype=torch.uint8, device=x.device))
+        out = (torch.empty((M, qk), dtype=torch.uint8, device=dev),
+               torch.empty((M, K // 32), dtype=torch.uint8, device=dev))
     q, s = out
-    _check(_load().mr_mxfp8_quant(_dev_ptr(x, "x", torch.bfloat16), ldx, M, K, _dev_ptr(q, "q", torch.uint8),
-                                  _dev_ptr(s, "scale", torch.uint8), _stream_ptr(stream)), "mr_mxfp8_quant")
+    _check_out(q, "q", (M, qk), torch.uint8, dev)
+    _check_out(s, "scale", (M, K // 32), torch.uint8, dev)
+    fn, name = (_load().mr_mxfp4_quant, "mr_mxfp4_quant") if fp4 else (_load().mr_mxfp8_quant, "mr_mxfp8_quant")
+    with _launch_ctx(dev):
+        _check(fn(_dev_ptr(x, "x", torch.bfloat16), ldx, M, K, _dev_ptr(q, "q", torch.uint8),
+                  _dev_ptr(s, "scale", torch.uint8), _stream_on(dev, stream)), name)
     return q, s
 
 
@@ -354,16 +433,7 @@ def route_outputs_in(buf, M: int, N: int, K: int, topk: int, block: int, quant=T
 def mxfp4_quant(x, out=None, stream=None):
     """(q uint8 [M, K/2] packed e2m1 codes, element 2j in the low nibble;
     scale uint8 [M, K/32] e8m0)."""
-    torch = _torch()
-    ldx = _row_major_2d(x, "x")
-    M, K = x.shape
-    if out is None:
-        out = (torch.empty((M, K // 2), dtype=torch.uint8, device=x.device),
-               torch.empty((M, K // 32), dtype=torch.uint8, device=x.device))
-    q, s = out
-    _check(_load().mr_mxfp4_quant(_dev_ptr(x, "x", torch.bfloat16), ldx, M, K, _dev_ptr(q, "q", torch.uint8),
-                                  _dev_ptr(s, "scale", torch.uint8), _stream_ptr(stream)), "mr_mxfp4_quant")
-    return q, s
+    return _mx_quant(x, out, stream, fp4=True)
 
 
 def alloc_route_outputs(M: int, N: int, K: int, topk: int, block: int, device, quant=True):
@@ -385,24 +455,53 @@ def alloc_route_outputs(M: int, N: int, K: int, topk: int, block: int, device, q
     return out
 
 
+def _check_route_out(out, M, N, K, topk, block, quant, dev):
+    """Every output of the one-launch route: dtype, shape (the sort's at
+    least the capacity), contiguity and device."""
+    torch = _torch()
+    cap = sort_capacity(M, topk, N, block)
+    if cap < 0:
+        raise MoeRouteUnsupported(MR_ERR_UNSUPPORTED, "mr_sort_capacity")
+    _check_out(out["logits"], "logits", (M, N), torch.float32, dev)
+    _check_out(out["topk_ids"], "topk_ids", (M, topk), torch.int32, dev)
+    _check_out(out["topk_weights"], "topk_weights", (M, topk), torch.float32, dev)
+    _check_sort_out(out["sorted_token_ids"], out["expert_ids"], out["num_tokens_post_padded"], cap, block, dev)
+    if quant:
+        _check_out(out["q"], "q", (M, K // 2 if quant == "mxfp4" else K), torch.uint8, dev)
+        _check_out(out["scale"], "scale", (M, K // 32), torch.uint8, dev)
+
+
+def _check_w(w, K):
+    if w.dim() != 2 or not w.is_contiguous() or w.shape[1] != K:
+        raise ValueError("w must be contiguous [N, K]")
+
+
+def _check_bias(bias, N, dev):
+    if bias is not None:
+        _check_out(bias, "bias", (N,), _torch().float32, dev)
+
+
 def moe_route_sort_quant(x, w, topk: int, block: int, scoring: str = "softmax", bias=None,
                          renormalize: bool = True, quant: bool = True, out=None,
                          scratch: Scratch | None = None, stream=None):
     """The whole path for M <= 64 tokens in one launch; returns a dict of outputs."""
-    _require_cuda(x=x, w=w, bias=bias)
     torch = _torch()
+    dev = _one_device(x=x, w=w, bias=bias)
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
     N = w.shape[0]
-    if not w.is_contiguous() or w.shape[1] != K:
-        raise ValueError("w must be contiguous [N, K]")
+    _check_w(w, K)
+    _check_bias(bias, N, dev)
     if out is None:
-        out = alloc_route_outputs(M, N, K, topk, block, x.device, quant)
+        out = alloc_route_outputs(M, N, K, topk, block, dev, quant)
+    _check_route_out(out, M, N, K, topk, block, quant, dev)
     if scratch is None:
-        scratch = Scratch(M, N, K, topk, device=x.device)
+        scratch = Scratch(M, N, K, topk, device=dev)
+    _check_scratch(scratch, dev)
     q = out.get("q") if quant else None
     s = out.get("scale") if quant else None
-    _check(_load().mr_moe_route_sort_quant(
+    with _launch_ctx(dev):
+        st = _load().mr_moe_route_sort_quant(
         _dev_ptr(x, "x", torch.bfloat16), ldx, _dev_ptr(w, "w", torch.bfloat16), M, N, K, topk,
         SCORING[scoring], _dev_ptr(bias, "bias", torch.float32, allow_none=True), int(renormalize), block,
         _dev_ptr(out["logits"], "logits", torch.float32), _dev_ptr(out["topk_ids"], "topk_ids", torch.int32),
@@ -412,25 +511,28 @@ def moe_route_sort_quant(x, w, topk: int, block: int, scoring: str = "softmax", 
         _dev_ptr(out["num_tokens_post_padded"], "num_tokens_post_padded", torch.int32),
         out["sorted_token_ids"].numel(), _dev_ptr(q, "q", torch.uint8, allow_none=True),
         _dev_ptr(s, "scale", torch.uint8, allow_none=True), scratch.ptr, scratch.nbytes,
-        _stream_ptr(stream)), "mr_moe_route_sort_quant")
+        _stream_on(dev, stream))
+    _check(st, "mr_moe_route_sort_quant")
     return out
 
 
 def norm_apply(sres, rstd, norm_weight, norm: str = "gemma", out=None, stream=None):
     """The router input on the norm's scale, written out: bf16 [M, K] with
     xn[m, k] = bf16((sres[m, k] * rstd[m]) * s[k]), s = g or 1 + g."""
-    _require_cuda(sres=sres, rstd=rstd, norm_weight=norm_weight)
     torch = _torch()
+    dev = _one_device(sres=sres, rstd=rstd, norm_weight=norm_weight, out=out)
     ldx = _row_major_2d(sres, "sres")
     M, K = sres.shape
     _check_norm_args(rstd, norm_weight, M, K)
     if out is None:
-        out = torch.empty((M, K), dtype=torch.bfloat16, device=sres.device)
-    if not out.is_contiguous() or tuple(out.shape) != (M, K):
-        raise ValueError("out must be contiguous [M, K]")
-    _check(_load().mr_norm_apply(_dev_ptr(sres, "sres", torch.bfloat16), ldx, _dev_ptr(rstd, "rstd", torch.float32),
-                                 _dev_ptr(norm_weight, "norm_weight", torch.bfloat16), NORM_KIND[norm], M, K,
-                                 _dev_ptr(out, "out", torch.bfloat16), _stream_ptr(stream)), "mr_norm_apply")
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    _check_out(out, "out", (M, K), torch.bfloat16, dev)
+    with _launch_ctx(dev):
+        _check(_load().mr_norm_apply(_dev_ptr(sres, "sres", torch.bfloat16), ldx,
+                                     _dev_ptr(rstd, "rstd", torch.float32),
+                                     _dev_ptr(norm_weight, "norm_weight", torch.bfloat16), NORM_KIND[norm], M, K,
+                                     _dev_ptr(out, "out", torch.bfloat16), _stream_on(dev, stream)),
+               "mr_norm_apply")
     return out
 
 
@@ -446,21 +548,24 @@ def moe_route_sort_quant_norm(sres, rstd, norm_weight, w, topk: int, block: int,
                               out=None, scratch: Scratch | None = None, stream=None):
     """The one-launch route with its input on the norm's scale (residual rows,
     per-token rstd, norm weight); returns a dict of outputs."""
-    _require_cuda(sres=sres, rstd=rstd, norm_weight=norm_weight, w=w, bias=bias)
     torch = _torch()
+    dev = _one_device(sres=sres, rstd=rstd, norm_weight=norm_weight, w=w, bias=bias)
     ldx = _row_major_2d(sres, "sres")
     M, K = sres.shape
     N = w.shape[0]
-    if not w.is_contiguous() or w.shape[1] != K:
-        raise ValueError("w must be contiguous [N, K]")
+    _check_w(w, K)
+    _check_bias(bias, N, dev)
     _check_norm_args(rstd, norm_weight, M, K)
     if out is None:
-        out = alloc_route_outputs(M, N, K, topk, block, sres.device, quant)
+        out = alloc_route_outputs(M, N, K, topk, block, dev, quant)
+    _check_route_out(out, M, N, K, topk, block, quant, dev)
     if scratch is None:
-        scratch = Scratch(M, N, K, topk, device=sres.device)
+        scratch = Scratch(M, N, K, topk, device=dev)
+    _check_scratch(scratch, dev)
     q = out.get("q") if quant else None
     s = out.get("scale") if quant else None
-    _check(_load().mr_moe_route_sort_quant_norm(
+    with _launch_ctx(dev):
+        st = _load().mr_moe_route_sort_quant_norm(
         _dev_ptr(sres, "sres", torch.bfloat16), ldx, _dev_ptr(rstd, "rstd", torch.float32),
         _dev_ptr(norm_weight, "norm_weight", torch.bfloat16), NORM_KIND[norm],
         _dev_ptr(w, "w", torch.bfloat16), M, N, K, topk,
@@ -472,7 +577,8 @@ def moe_route_sort_quant_norm(sres, rstd, norm_weight, w, topk: int, block: int,
         _dev_ptr(out["num_tokens_post_padded"], "num_tokens_post_padded", torch.int32),
         out["sorted_token_ids"].numel(), _dev_ptr(q, "q", torch.uint8, allow_none=True),
         _dev_ptr(s, "scale", torch.uint8, allow_none=True), scratch.ptr, scratch.nbytes,
-        _stream_ptr(stream)), "mr_moe_route_sort_quant_norm")
+        _stream_on(dev, stream))
+    _check(st, "mr_moe_route_sort_quant_norm")
     return out
 
 
@@ -514,13 +620,26 @@ class PreparedRoute:
                  scratch: Scratch | None = None):
         self.p, self.out, self._keep = _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd,
                                                      norm_weight, norm, out, scratch)
+        self.device = x.device
         self._ref = ctypes.byref(self.p)
         self._fn = _load().mr_moe_route
 
     def __call__(self, stream=None):
-        """Launch; stream: a torch stream, a raw cudaStream_t (int) or None."""
-        sp = stream if isinstance(stream, int) else _stream_ptr(stream)
-        status = self._fn(self._ref, sp)
+        """Launch on the route's device; stream: a torch stream of that
+        device, a raw cudaStream_t (int) of that device, or None (torch's
+        current stream there)."""
+        torch = _torch()
+        if isinstance(stream, int):
+            sp = stream
+        else:
+            if stream is not None and stream.device != self.device:
+                raise ValueError(f"stream must be on {self.device}")
+            sp = _stream_on(self.device, stream)
+        if torch.cuda.current_device() == self.device.index:
+            status = self._fn(self._ref, sp)
+        else:
+            with _launch_ctx(self.device):
+                status = self._fn(self._ref, sp)
         if status != MR_OK:
             _check(status, "mr_moe_route")
         return self.out
@@ -531,19 +650,21 @@ def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, no
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
     N = w.shape[0]
-    if not w.is_contiguous() or w.shape[1] != K:
-        raise ValueError("w must be contiguous [N, K]")
+    _check_w(w, K)
     if quant not in QUANT_FORMAT:
         raise ValueError(f"quant must be one of {list(QUANT_FORMAT)}")
     if rstd is not None:
         if norm_weight is None:
             raise ValueError("rstd needs norm_weight")
         _check_norm_args(rstd, norm_weight, M, K)
-    _require_cuda(x=x, w=w, bias=bias, rstd=rstd, norm_weight=norm_weight)
+    dev = _one_device(x=x, w=w, bias=bias, rstd=rstd, norm_weight=norm_weight)
+    _check_bias(bias, N, dev)
     if out is None:
-        out = alloc_route_outputs(M, N, K, topk, block, x.device, quant)
+        out = alloc_route_outputs(M, N, K, topk, block, dev, quant)
+    _check_route_out(out, M, N, K, topk, block, quant, dev)
     if scratch is None:
-        scratch = Scratch(M, N, K, topk, device=x.device)
+        scratch = Scratch(M, N, K, topk, device=dev)
+    _check_scratch(scratch, dev)
     p = RouteParams()
     p.x = _dev_ptr(x, "x", torch.bfloat16)
     p.ldx = ldx
@@ -566,9 +687,6 @@ def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, no
     p.capacity = out["sorted_token_ids"].numel()
     if quant is not None:
         qt, st = out["q"], out["scale"]
-        want = K // 2 if quant == "mxfp4" else K
-        if tuple(qt.shape) != (M, want) or tuple(st.shape) != (M, K // 32):
-            raise ValueError(f"q must be [M, {want}] and scale [M, K/32] for {quant}")
         p.q = _dev_ptr(qt, "q", torch.uint8)
         p.scale = _dev_ptr(st, "scale", torch.uint8)
     p.scratch = scratch.ptr
@@ -589,22 +707,26 @@ def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp
     K = x.shape[1]
     if quant not in ("mxfp8", "mxfp4"):
         raise ValueError("quant must be mxfp8 or mxfp4")
-    _require_cuda(topk_ids=topk_ids, x=x)
+    dev = _one_device(topk_ids=topk_ids, x=x)
     cap = sort_capacity(M, k, num_experts, block)
     if cap < 0:
         raise MoeRouteUnsupported(MR_ERR_UNSUPPORTED, "mr_sort_capacity")
-    dev = topk_ids.device
     if out is None:
         out = (torch.empty(cap, dtype=torch.int32, device=dev), torch.empty(cap // block, dtype=torch.int32, device=dev),
                torch.empty(1, dtype=torch.int32, device=dev),
                torch.empty((M, K // 2 if quant == "mxfp4" else K), dtype=torch.uint8, device=dev),
                torch.empty((M, K // 32), dtype=torch.uint8, device=dev))
     st, ex, nt, q, s = out
-    _check(_load().mr_moe_sort_quant(_dev_ptr(topk_ids, "topk_ids", torch.int32), M, k, num_experts, block,
+    _check_sort_out(st, ex, nt, cap, block, dev)
+    _check_out(q, "q", (M, K // 2 if quant == "mxfp4" else K), torch.uint8, dev)
+    _check_out(s, "scale", (M, K // 32), torch.uint8, dev)
+    with _launch_ctx(dev):
+        status = _load().mr_moe_sort_quant(_dev_ptr(topk_ids, "topk_ids", torch.int32), M, k, num_experts, block,
                                      _dev_ptr(x, "x", torch.bfloat16), ldx, K, QUANT_FORMAT[quant],
                                      _dev_ptr(st, "sorted_token_ids", torch.int32),
                                      _dev_ptr(ex, "expert_ids", torch.int32),
                                      _dev_ptr(nt, "num_tokens_post_padded", torch.int32), st.numel(),
                                      _dev_ptr(q, "q", torch.uint8), _dev_ptr(s, "scale", torch.uint8),
-                                     _stream_ptr(stream)), "mr_moe_sort_quant")
+                                     _stream_on(dev, stream))
+    _check(status, "mr_moe_sort_quant")
     return st, ex, nt, q, s

@@ -55,6 +55,21 @@ namespace {
 bool allow_tc() { return (mr::launch_flags() & MR_LAUNCH_LEGACY_MMA) == 0; }
 }  // namespace
 namespace mr {
+int check_counters(const void* scratch, cudaStream_t st) {
+    if ((mr::launch_flags() & MR_LAUNCH_CHECK_SCRATCH) == 0) return MR_OK;
+    static thread_local unsigned host[MR_SCRATCH_COUNTER_BYTES / sizeof(unsigned)];
+    if (cudaMemcpyAsync(host, scratch, MR_SCRATCH_COUNTER_BYTES, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return MR_ERR_CUDA;
+    for (unsigned v : host)
+        if (v != 0u) return MR_ERR_SCRATCH_DIRTY;
+    return MR_OK;
+}
+}  // namespace mr
+namespace {
+using mr::check_counters;
+}  // namespace
+namespace mr {
 unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 void* trace_buffer() { return g_trace.load(std::memory_order_relaxed); }
 }  // namespace mr
@@ -62,7 +77,9 @@ void* trace_buffer() { return g_trace.load(std::memory_order_relaxed); }
 extern "C" {
 
 int mr_set_launch_flags(int flags) {
-    if (flags & ~(MR_LAUNCH_PDL | MR_LAUNCH_TEST_STALL | MR_LAUNCH_LEGACY_MMA)) return MR_ERR_INVALID_ARG;
+    if (flags & ~(MR_LAUNCH_PDL | MR_LAUNCH_TEST_STALL | MR_LAUNCH_LEGACY_MMA | MR_LAUNCH_TEST_SLOW_SIGMOID |
+                  MR_LAUNCH_CHECK_SCRATCH))
+        return MR_ERR_INVALID_ARG;
     g_launch_flags.store(flags, std::memory_order_relaxed);
     return MR_OK;
 }
@@ -97,6 +114,8 @@ const char* mr_status_string(int status) {
         case MR_ERR_SCRATCH_TOO_SMALL: return "MR_ERR_SCRATCH_TOO_SMALL: scratch_bytes below what the call needs";
         case MR_ERR_CUDA: return "MR_ERR_CUDA: the CUDA runtime reported an error";
         case MR_ERR_TIMEOUT: return "MR_ERR_TIMEOUT: a kernel's bounded wait for data from other CTAs ran out";
+        case MR_ERR_SCRATCH_DIRTY:
+            return "MR_ERR_SCRATCH_DIRTY: scratch counters not zero before the launch (never zeroed, or in use)";
         default: return "unknown mr_status";
     }
 }
@@ -226,6 +245,7 @@ int mr_router_gemv(const void* x, int64_t ldx, const void* w, float* logits, int
     GemvPlan p;
     if (!mr::gemv_plan(M, N, K, &p)) return MR_ERR_UNSUPPORTED;
     if (scratch_bytes < mr::kWorkOffset + mr::gemv_work_bytes(p, M, N)) return MR_ERR_SCRATCH_TOO_SMALL;
+    if ((s = check_counters(scratch, as_stream(stream))) != MR_OK) return s;
     return cuda_status(mr::launch_router_gemv(p, x, ldx, w, logits, M, N, K, scratch, as_stream(stream)));
 }
 
@@ -255,6 +275,7 @@ int mr_moe_sort(const int32_t* topk_ids, int M, int topk, int N, int block, int3
         if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;
         if (scratch_bytes < mr::kWorkOffset + mr::sort_work_bytes((int)n_assign, N))
             return MR_ERR_SCRATCH_TOO_SMALL;
+        if ((s = check_counters(scratch, as_stream(stream))) != MR_OK) return s;
     }
     return cuda_status(mr::launch_sort(topk_ids, M, topk, N, block, sorted_token_ids, expert_ids,
                                        num_tokens_post_padded, capacity, scratch, as_stream(stream)));
@@ -342,6 +363,7 @@ static int route_impl(const mr_route_params* p, void* stream) {
         a.cand_key = reinterpret_cast<unsigned long long*>(work);
         a.cand_val = reinterpret_cast<float*>(work + (size_t)M * rp.ng * topk * 8);
     }
+    if ((rp.clusters > 1 || rp.ng > 1) && (s = check_counters(p->scratch, as_stream(stream))) != MR_OK) return s;
     a.bias = scoring == MR_SCORE_SIGMOID ? p->sel_bias : nullptr;
     a.logits = p->logits;
     a.ids = p->topk_ids;

@@ -236,13 +236,27 @@ __device__ __forceinline__ uint32_t mx4_quant_quad(uint4 v, unsigned* scale_byte
 }
 
 // ---------------------------------------------------------------- sigmoid
+//
+// The sigmoid gate (sglang #46652, Modifications: fp32 sigmoid scores plus a
+// per-expert selection bias) scores expert n by s = sigma(l) = 1 / (1 + e^-l)
+// of its fp32 logit, rounded once to the nearest fp32 value (the correctly
+// rounded sigmoid), and selects by the fp32 sum s + bias.  Evaluating that
+// exactly for every expert would need fp64 throughout, which runs at a small
+// fraction of the fp32 rate here, so the gate works in two steps:
+//   1. sigmoid_approx (fp32, a few ulps) for every expert: selection keys good
+//      to well within kSigmoidKeyMargin, used only to find candidates;
+//   2. sigmoid_exact for the few candidates whose approximate key lies within
+//      the margin of the k-th largest: the correctly rounded score, from which
+//      the exact keys, the ranking and the weights are formed.
 
-// fp32 sigmoid score by a fixed recipe (every step correctly rounded, no
-// contraction), so that any implementation of the same steps gives the same
-// bits: y = clamp(-l, -87, 88); n = rint(y * log2 e); Cody-Waite reduction
-// r = y - n*ln2 with a two-part ln 2 (fused multiply-adds); e^r by the
-// degree-7 Taylor polynomial in Horner form; e = p * 2^n; s = 1 / (1 + e).
-__device__ __forceinline__ float sigmoid_score(float l) {
+// fp32 sigmoid good to a few ulps (every step rounded to nearest, no
+// contraction): y = clamp(-l, -87, 88); n = rint(y log2 e); Cody and Waite's
+// reduction r = y - n ln2 with a two-part ln 2; e^r by its degree-7 Taylor
+// polynomial in Horner form (truncation below 2^-27 on |r| <= ln2 / 2);
+// s = 1 / (1 + p 2^n).  Its absolute error is below 2^-21 for every l (below
+// 2^-37 once the clamp acts), so selection keys s + bias from it lie within
+// 2^-20 of the exact keys.
+__device__ __forceinline__ float sigmoid_approx(float l) {
     float y = -l;
     y = y < -87.0f ? -87.0f : y;
     y = y > 88.0f ? 88.0f : y;
@@ -260,6 +274,131 @@ __device__ __forceinline__ float sigmoid_score(float l) {
     float two_n = __uint_as_float((unsigned)((int)n + 127) << 23);
     float e = __fmul_rn(p, two_n);
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+}
+
+// Keys within this distance below the k-th largest approximate key are
+// re-scored exactly (four times the worst gap between approximate and exact
+// keys, so that every expert of the exact top-k is a candidate).
+constexpr float kSigmoidKeyMargin = 0x1p-18f;
+
+// Double-double arithmetic (a value is hi + lo, |lo| <= ulp(hi) / 2): the
+// error-free sum of Knuth and product via fma of Dekker, and the accurate
+// addition and division of Hida, Li and Bailey's double-double library
+// ("Algorithms for quad-double precision floating point arithmetic", 2001).
+// Every operation is an explicit round-to-nearest intrinsic (no contraction).
+struct ddouble {
+    double hi, lo;
+};
+__device__ __forceinline__ ddouble dd_two_sum(double a, double b) {
+    const double s = __dadd_rn(a, b), bb = __dsub_rn(s, a);
+    return {s, __dadd_rn(__dsub_rn(a, __dsub_rn(s, bb)), __dsub_rn(b, bb))};
+}
+__device__ __forceinline__ ddouble dd_quick_two_sum(double a, double b) {  // |a| >= |b|
+    const double s = __dadd_rn(a, b);
+    return {s, __dsub_rn(b, __dsub_rn(s, a))};
+}
+__device__ __forceinline__ ddouble dd_two_prod(double a, double b) {
+    const double p = __dmul_rn(a, b);
+    return {p, __fma_rn(a, b, -p)};
+}
+__device__ __forceinline__ ddouble dd_add(ddouble a, ddouble b) {
+    ddouble s = dd_two_sum(a.hi, b.hi);
+    const ddouble t = dd_two_sum(a.lo, b.lo);
+    s.lo = __dadd_rn(s.lo, t.hi);
+    s = dd_quick_two_sum(s.hi, s.lo);
+    s.lo = __dadd_rn(s.lo, t.lo);
+    return dd_quick_two_sum(s.hi, s.lo);
+}
+__device__ __forceinline__ ddouble dd_mul(ddouble a, ddouble b) {
+    ddouble p = dd_two_prod(a.hi, b.hi);
+    p.lo = __dadd_rn(p.lo, __dadd_rn(__dmul_rn(a.hi, b.lo), __dmul_rn(a.lo, b.hi)));
+    return dd_quick_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ ddouble dd_mul_d(ddouble a, double b) {
+    ddouble p = dd_two_prod(a.hi, b);
+    p.lo = __fma_rn(a.lo, b, p.lo);
+    return dd_quick_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ ddouble dd_div(ddouble a, ddouble b) {
+    // three quotient digits, each from the remainder of the previous ones
+    const double q1 = __ddiv_rn(a.hi, b.hi);
+    ddouble r = dd_add(a, dd_mul_d(b, -q1));
+    const double q2 = __ddiv_rn(r.hi, b.hi);
+    r = dd_add(r, dd_mul_d(b, -q2));
+    const double q3 = __ddiv_rn(r.hi, b.hi);
+    ddouble q = dd_quick_two_sum(q1, q2);
+    return dd_add(q, ddouble{q3, 0.0});
+}
+
+// sigma(l) correctly rounded to fp32, evaluated in double-double (relative
+// error far below 2^-90): ln 2 as three doubles (its value to 2^-160), n =
+// rint(y / ln2), r = y - n ln 2 (|r| <= ln2 / 2), e^r by its Taylor series to
+// degree 24 (truncation below 2^-115) in the nested form
+// 1 + r (1 + r/2 (1 + r/3 (...))), E = 2^n e^r, S = 1 / (1 + E); then the
+// one rounding of hi + lo to fp32.  Outside y = -l in (-20, 104) the result
+// is decided without evaluation: sigma < e^-104 < 2^-150 rounds to 0, and
+// 1 - sigma < e^-20 < 2^-25 rounds to 1.
+static __device__ __noinline__ float sigmoid_dd(float l) {
+    const double y = -(double)l;
+    if (y >= 104.0) return 0.0f;
+    if (y <= -20.0) return 1.0f;
+    constexpr double ln2_1 = 0x1.62e42fefa39efp-1, ln2_2 = 0x1.abc9e3b39803fp-56, ln2_3 = 0x1.7b57a079a1934p-111;
+    const double n = rint(__dmul_rn(y, 0x1.71547652b82fep+0));
+    const ddouble p1 = dd_two_prod(-n, ln2_1);  // -n ln2_1 exactly
+    ddouble r = dd_add(ddouble{y, 0.0}, p1);
+    r = dd_add(r, dd_two_prod(-n, ln2_2));
+    r = dd_add(r, ddouble{__dmul_rn(-n, ln2_3), 0.0});
+    ddouble p = {1.0, 0.0};
+    for (int j = 24; j >= 1; --j) {
+        const ddouble rj = dd_div(r, ddouble{(double)j, 0.0});
+        p = dd_add(ddouble{1.0, 0.0}, dd_mul(rj, p));
+    }
+    const double two_n = __longlong_as_double((long long)((int)n + 1023) << 52);  // n in [-29, 151]
+    const ddouble E = {__dmul_rn(p.hi, two_n), __dmul_rn(p.lo, two_n)};
+    const ddouble S = dd_div(ddouble{1.0, 0.0}, dd_add(ddouble{1.0, 0.0}, E));
+    // the fp32 value nearest to S.hi + S.lo: that of S.hi unless S.hi is
+    // exactly the midpoint between two fp32 values, where S.lo decides
+    const float c = __double2float_rn(S.hi);
+    const double cd = (double)c;
+    if (cd == S.hi) return c;
+    const float nb = S.hi > cd ? __uint_as_float(__float_as_uint(c) + 1u) : __uint_as_float(__float_as_uint(c) - 1u);
+    const double mid = __dmul_rn(0.5, __dadd_rn(cd, (double)nb));  // exact: a midpoint of fp32 values
+    if (S.hi != mid) return c;
+    return ((S.lo > 0.0) == (nb > c)) ? nb : c;
+}
+
+// sigma(l) correctly rounded to fp32.  Fast path in fp64: the CUDA Math API
+// documents exp (double) to within 1 ulp, and the addition and the division
+// each round once, so s = sigma (1 + d) with |d| <= 2^-51.  Rounding is
+// monotone: if s (1 - 2^-48) and s (1 + 2^-48) round to the same fp32 value,
+// so does sigma (Ziv's rounding test, "Fast evaluation of elementary
+// mathematical functions with correctly rounded last bit", 1991).  Otherwise
+// (about one logit in 10^7, or every call when slow is set, a test hook) the
+// double-double evaluation decides.  Non-negative result; +0 when sigma is
+// below half the smallest fp32 subnormal.
+__device__ __forceinline__ float sigmoid_exact(float l, bool slow) {
+    const double e = exp(-(double)l);
+    const double s = __ddiv_rn(1.0, __dadd_rn(1.0, e));
+    const double m = __dmul_rn(s, 0x1p-48);
+    const float lo = __double2float_rn(__dsub_rn(s, m)), hi = __double2float_rn(__dadd_rn(s, m));
+    if (lo == hi && !slow) return lo;
+    return sigmoid_dd(l);
+}
+
+// Inverse of ordered_key (the canonical fp32 value of a key).
+__device__ __forceinline__ float key_value(unsigned key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Selection key of a sigmoid-gate candidate: exact score plus bias (fp32).
+__device__ __forceinline__ unsigned sigmoid_key_exact(float logit, float bias, bool slow) {
+    return ordered_key(__fadd_rn(sigmoid_exact(logit, slow), bias));
+}
+
+// The lowest approximate key that can still belong to the exact top-k, given
+// the k-th largest approximate key kth (an ordered key).
+__device__ __forceinline__ unsigned sigmoid_candidate_floor(unsigned kth) {
+    return ordered_key(__fsub_rn(key_value(kth), kSigmoidKeyMargin));
 }
 
 }  // namespace mr

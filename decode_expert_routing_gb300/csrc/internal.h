@@ -69,6 +69,10 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
 
 // Launch options (MR_LAUNCH_* bits of mr_set_launch_flags).
 int launch_flags();
+// With MR_LAUNCH_CHECK_SCRATCH: MR_ERR_SCRATCH_DIRTY unless every counter of
+// the scratch prefix is zero (copied to the host on st and waited for);
+// MR_OK when the check is off.
+int check_counters(const void* scratch, cudaStream_t st);
 // Device buffer for phase stamps of tracing builds (nullptr otherwise).
 void* trace_buffer();
 

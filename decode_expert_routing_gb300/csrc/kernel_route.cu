@@ -198,7 +198,7 @@ __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* ro
     const bool live = lane < a.topk;
     float num, den;
     if (a.scoring == 1) {
-        num = live ? sigmoid_score(my_val) : 0.0f;
+        num = live ? sigmoid_exact(my_val, (a.flags & 8) != 0) : 0.0f;
         den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
         return a.renormalize ? __fdiv_rn(num, den) : num;
     }
@@ -614,9 +614,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         }
         if (a.mode == 0) continue;
         float sel0 = sum0, sel1 = sum1;
-        if (a.scoring == 1) {
-            sel0 = __fadd_rn(sigmoid_score(sum0), bpre0);
-            sel1 = __fadd_rn(sigmoid_score(sum1), bpre1);
+        if (a.scoring == 1) {  // approximate keys: they only pick the candidates
+            sel0 = __fadd_rn(sigmoid_approx(sum0), bpre0);
+            sel1 = __fadd_rn(sigmoid_approx(sum1), bpre1);
         }
         const unsigned long long c0 = h0 ? composite(ordered_key(sel0), e_off + n0) : 0ull;
         const unsigned long long c1 = h1 ? composite(ordered_key(sel1), e_off + n1) : 0ull;
@@ -628,7 +628,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         MR_TRACE_CLK(a.trace, 1);
         __syncthreads();  // s_wmin; rowbuf of this row
         MR_TRACE_CLK(a.trace, 3);
-        const unsigned T = __reduce_min_sync(kFull, lane < kRouteWarps ? s_wmin[lane] : 0xFFFFFFFFu);
+        unsigned T = __reduce_min_sync(kFull, lane < kRouteWarps ? s_wmin[lane] : 0xFFFFFFFFu);
+        // sigmoid gate: every expert of the exact top-k has an approximate
+        // key within the margin of the k-th largest (>= T), so the
+        // candidates reach that far down
+        if (a.scoring == 1) T = sigmoid_candidate_floor(T);
         MR_TRACE_CLK(a.trace, 4);
         const bool p0 = h0 && k0 >= T, p1 = h1 && k1 >= T;
         const unsigned b0 = __ballot_sync(kFull, p0), b1 = __ballot_sync(kFull, p1);
@@ -644,6 +648,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         // PR adjacent lanes per candidate, each counting the beaters among
         // candidates part, part + PR, ...; a segmented reduction adds them
         const int C = s_ccount;
+        if (a.scoring == 1) {  // the candidates' exact keys (correctly rounded sigmoid + bias)
+            for (int i = tid; i < C; i += kRouteThreads) {
+                const int id = 0x7FFFFFFF - (int)(unsigned)(ccand[i] & 0xFFFFFFFFull);
+                const float b = a.bias != nullptr ? __ldg(a.bias + id) : 0.0f;
+                ccand[i] = composite(sigmoid_key_exact(rowbuf[rl * N + id - e_off], b, (a.flags & 8) != 0), id);
+            }
+            __syncthreads();
+        }
         int prs = 5;
         while (prs > 0 && (C << prs) > kRouteThreads) --prs;
         const int PR = 1 << prs;

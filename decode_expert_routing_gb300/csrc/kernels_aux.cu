@@ -22,7 +22,8 @@ int topk_npl(int N) { return N <= 128 ? 4 : N <= 256 ? 8 : N <= 512 ? 16 : 32; }
 cudaError_t launch_topk(const float* logits, int M, int N, int topk, int scoring,
                         const float* bias, int renormalize, int32_t* ids, float* weights,
                         cudaStream_t st) {
-    TopkArgs a{logits, bias, ids, weights, M, N, topk, scoring, renormalize};
+    TopkArgs a{logits, bias, ids, weights, M, N, topk, scoring, renormalize,
+               (launch_flags() & 8) ? 1 : 0};
     dim3 grid((M + kTopkWarps - 1) / kTopkWarps);
     const dim3 block(32 * kTopkWarps);
     switch (topk_npl(N)) {

@@ -18,24 +18,54 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MR_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[64];  // per device: device address of g_noalloc_scratch, or nullptr
 
-// Once per device, with that device current: fetch the array's device address
-// and zero its counter prefix (the split-K counters must start at zero; every
-// later call leaves them at zero again).
-int scratch_for_current_device(void** out) {
+// Per device: the array's device address and the context it was looked up
+// in, as of the last set-up.
+struct Placement {
+    void* ptr;
+    void* ctx;
+};
+Placement g_placement[64];
+
+// The calling thread's current CUDA context (a driver handle), or nullptr if
+// the driver entry point is unavailable.  A context that is destroyed and
+// created again (cudaDeviceReset) loads this module again, possibly at
+// another address and with its contents undefined.
+void* current_context() {
+    using GetCtx = int (*)(void**);
+    static GetCtx fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<GetCtx>(f);
+    }();
+    void* ctx = nullptr;
+    if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
+
+// The array's device address for the current device, looked up on every
+// call (host code only sees a stand-in under its name).  The first call in a
+// context, or one that finds the array at a new address, zeroes the counter
+// prefix on the call's stream (the split-K counters must start at zero;
+// every later call leaves them at zero again).
+int scratch_for_current_device(cudaStream_t st, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MR_ERR_CUDA;
     if (dev < 0 || dev >= 64) return MR_ERR_UNSUPPORTED;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MR_ERR_CUDA;
+    void* ctx = current_context();
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MR_ERR_CUDA;
-        if (cudaMemset(p, 0, MR_SCRATCH_COUNTER_BYTES) != cudaSuccess) return MR_ERR_CUDA;
-        if (cudaDeviceSynchronize() != cudaSuccess) return MR_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+    Placement& pl = g_placement[dev];
+    if (pl.ptr != p || pl.ctx != ctx || ctx == nullptr) {  // (no context handle: zero on every call)
+        if (cudaMemsetAsync(p, 0, MR_SCRATCH_COUNTER_BYTES, st) != cudaSuccess) return MR_ERR_CUDA;
+        pl.ptr = p;
+        pl.ctx = ctx;
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return MR_OK;
 }
 
@@ -53,10 +83,11 @@ extern "C" int mr_router_gemv_noalloc(const void* x, int64_t ldx, const void* w,
     // the built-in scratch has a fixed size: larger problems are refused
     if (mr::kWorkOffset + mr::gemv_work_bytes(p, M, N) > (size_t)MR_NOALLOC_SCRATCH_BYTES)
         return MR_ERR_UNSUPPORTED;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
     void* scratch = nullptr;
-    const int s = scratch_for_current_device(&scratch);
+    int s = scratch_for_current_device(st, &scratch);
     if (s != MR_OK) return s;
-    const cudaError_t e =
-        mr::launch_router_gemv(p, x, ldx, w, logits, M, N, K, scratch, static_cast<cudaStream_t>(stream));
+    if ((s = mr::check_counters(scratch, st)) != MR_OK) return s;
+    const cudaError_t e = mr::launch_router_gemv(p, x, ldx, w, logits, M, N, K, scratch, st);
     return e == cudaSuccess ? MR_OK : MR_ERR_CUDA;
 }

@@ -22,6 +22,10 @@ constexpr int kRouteGemvMaxM = 512;
 constexpr int kRouteSplitMinN = 512;
 constexpr int kRouteGroupMinN = 128;
 constexpr int kRouteMaxGroups = 8;
+// The router GEMV alone (no gate to merge) splits any N >= 32 into groups of
+// >= 16 experts (two 8-expert MMA tiles), so that a 1.6 MB gate weight
+// streams through up to 8 clusters instead of one.
+constexpr int kRouteGemvGroupMinN = 16;
 
 struct RouteArgs {
     const uint16_t* x;
@@ -121,11 +125,13 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     // (the whole route splits one token group only: with several, the one
     // merging CTA takes several tokens per warp and the split measured slower)
     const int mcl = (M + kRouteRowsPerCluster - 1) / kRouteRowsPerCluster;
-    if (max_groups > 1 && !(mode == 0 && M > kRouteMaxM) && !(mode == 1 && mcl > 1) && N >= kRouteSplitMinN) {
+    const int split_min = mode == 0 ? 2 * kRouteGemvGroupMinN : kRouteSplitMinN;
+    const int group_min = mode == 0 ? kRouteGemvGroupMinN : kRouteGroupMinN;
+    if (max_groups > 1 && !(mode == 0 && M > kRouteMaxM) && !(mode == 1 && mcl > 1) && N >= split_min) {
         int d = max_groups / mcl;
         if (d > kRouteMaxGroups) d = kRouteMaxGroups;
         for (; d >= 2; --d)
-            if ((N / 8) % d == 0 && N / d >= kRouteGroupMinN && topk <= N / d) break;
+            if ((N / 8) % d == 0 && N / d >= group_min && topk <= N / d) break;
         if (d >= 2) q.ng = d;
     }
     N = Ntot / q.ng;  // from here on: the experts of one cluster
@@ -133,7 +139,10 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     const int S = q.kc / 32, NT = N / 8;
     // k-parts per tile: a power of two (a warp keeps one part for all its
     // tiles) dividing S with at most kRouteSpwMax steps per part; more parts
-    // while the CTA has fewer tiles than warps
+    // while the CTA would have fewer tiles than warps WITHOUT expert groups
+    // (the same split with and without groups: every logit then sums the
+    // same partials in the same order, so the GEMV alone and the whole route
+    // give the same bits however the experts are grouped)
     int w = 0;
     for (int d = 1; d <= kRouteWarps && d <= S; d *= 2)
         if (S % d == 0 && S / d <= kRouteSpwMax) {
@@ -141,7 +150,8 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
             break;
         }
     if (w == 0) return false;
-    while (NT * w < kRouteWarps && 2 * w <= kRouteWarps && S % (2 * w) == 0) w *= 2;
+    const int NTall = Ntot / 8;
+    while (NTall * w < kRouteWarps && 2 * w <= kRouteWarps && S % (2 * w) == 0) w *= 2;
     if ((cs * w) % 8 != 0) return false;  // the owner sums split-K slots in groups of 8
     q.wpt = w;
     q.spw = S / w;

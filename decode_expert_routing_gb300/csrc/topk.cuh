@@ -4,8 +4,10 @@
 // pick the k experts with the largest selection key and weight them.
 //   softmax: key = logit; weights = softmax of the selected logits
 //            (renormalised) or the full softmax probabilities.
-//   sigmoid: s = sigmoid(logit) (fixed fp32 recipe), key = s + bias;
-//            weights = s of the selected, renormalised or not.
+//   sigmoid: s = sigmoid(logit) correctly rounded to fp32, key = s + bias;
+//            weights = s of the selected, renormalised or not.  Approximate
+//            fp32 keys find the k-th largest key; only experts within
+//            kSigmoidKeyMargin of it are re-scored exactly, then selected.
 // Ties go to the lower expert id.
 //
 // GB300 design: one warp per token.  Lane l holds the keys of experts
@@ -29,7 +31,42 @@ struct TopkArgs {
     int M, N, k;
     int scoring;           // 0 softmax, 1 sigmoid
     int renormalize;
+    int slow_sigmoid;      // test hook: every exact sigmoid through double-double
 };
+
+// k rounds of the warp's largest key (ties to the lower id): slot r's id and
+// logit go to lane r (my_id, my_val); the winners' keys are cleared.  Returns
+// the k-th largest key.
+template <int NPL>
+__device__ __forceinline__ unsigned warp_select(unsigned (&key)[NPL], const float (&val)[NPL], int k, int* my_id,
+                                                float* my_val) {
+    const int lane = threadIdx.x & 31;
+    unsigned best = 0u;
+    int bestj = 0;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+        if (key[j] > best) { best = key[j]; bestj = j; }
+    unsigned kmax = 0u;
+    for (int r = 0; r < k; ++r) {
+        kmax = __reduce_max_sync(kFull, best);
+        const unsigned cand = (best == kmax) ? (unsigned)(lane + 32 * bestj) : 0xFFFFFFFFu;
+        const unsigned win = __reduce_min_sync(kFull, cand);
+        const int owner = (int)(win & 31u), wj = (int)(win >> 5);
+        float wv = 0.0f;
+        if (lane == owner) {
+            best = 0u;
+            bestj = 0;
+#pragma unroll
+            for (int j = 0; j < NPL; ++j) {
+                if (j == wj) { wv = val[j]; key[j] = 0u; }
+                if (key[j] > best) { best = key[j]; bestj = j; }
+            }
+        }
+        wv = __shfl_sync(kFull, wv, owner);
+        if (lane == r) { *my_id = (int)win; *my_val = wv; }
+    }
+    return kmax;
+}
 
 // Gate of one token (row m) by one warp.  If ids_smem != nullptr the chosen
 // ids are also written there (slot order).  Reads the logits through L2 so
@@ -45,49 +82,42 @@ __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids
         const int id = lane + 32 * j;
         val[j] = id < a.N ? __ldcg(row + id) : 0.0f;
     }
+    // keys: the logit (softmax), else the approximate sigmoid + bias
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
         const int id = lane + 32 * j;
         unsigned kv = 0u;  // below every real key: never selected while real keys remain
         if (id < a.N) {
             float sel = val[j];
-            if (a.scoring == 1) sel = __fadd_rn(sigmoid_score(val[j]), a.bias ? __ldg(a.bias + id) : 0.0f);
+            if (a.scoring == 1) sel = __fadd_rn(sigmoid_approx(val[j]), a.bias ? __ldg(a.bias + id) : 0.0f);
             kv = ordered_key(sel);
         }
         key[j] = kv;
     }
-    unsigned best = 0u;
-    int bestj = 0;
-#pragma unroll
-    for (int j = 0; j < NPL; ++j)
-        if (key[j] > best) { best = key[j]; bestj = j; }
-
     int my_id = 0;
     float my_val = 0.0f;
-    for (int r = 0; r < a.k; ++r) {
-        const unsigned kmax = __reduce_max_sync(kFull, best);
-        const unsigned cand = (best == kmax) ? (unsigned)(lane + 32 * bestj) : 0xFFFFFFFFu;
-        const unsigned win = __reduce_min_sync(kFull, cand);
-        const int owner = (int)(win & 31u), wj = (int)(win >> 5);
-        float wv = 0.0f;
-        if (lane == owner) {
-            best = 0u;
-            bestj = 0;
+    if (a.scoring == 1) {
+        // the k-th largest approximate key bounds the candidates; they are
+        // re-scored exactly, the others drop out, and the selection runs again
+        unsigned probe[NPL];
 #pragma unroll
-            for (int j = 0; j < NPL; ++j) {
-                if (j == wj) { wv = val[j]; key[j] = 0u; }
-                if (key[j] > best) { best = key[j]; bestj = j; }
-            }
+        for (int j = 0; j < NPL; ++j) probe[j] = key[j];
+        const unsigned floor_key = sigmoid_candidate_floor(warp_select<NPL>(probe, val, a.k, &my_id, &my_val));
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) {
+            const int id = lane + 32 * j;
+            key[j] = (id < a.N && key[j] >= floor_key)
+                         ? sigmoid_key_exact(val[j], a.bias ? __ldg(a.bias + id) : 0.0f, a.slow_sigmoid != 0)
+                         : 0u;
         }
-        wv = __shfl_sync(kFull, wv, owner);
-        if (lane == r) { my_id = (int)win; my_val = wv; }
     }
+    warp_select<NPL>(key, val, a.k, &my_id, &my_val);
 
     // weights: lane r < k owns slot r
     const bool live = lane < a.k;
     float num = 0.0f, den;
     if (a.scoring == 1) {
-        num = live ? sigmoid_score(my_val) : 0.0f;
+        num = live ? sigmoid_exact(my_val, a.slow_sigmoid != 0) : 0.0f;
         den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
     } else {
         const float lmax = __shfl_sync(kFull, my_val, 0);  // slot 0 holds the largest logit

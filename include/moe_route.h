@@ -70,7 +70,8 @@ typedef enum mr_status {
     MR_ERR_INVALID_ARG = 2,      /* null or misaligned pointer, bad size       */
     MR_ERR_SCRATCH_TOO_SMALL = 3,/* scratch_bytes below what the call needs    */
     MR_ERR_CUDA = 4,             /* the CUDA runtime reported an error         */
-    MR_ERR_TIMEOUT = 5           /* mr_device_error: a bounded wait ran out    */
+    MR_ERR_TIMEOUT = 5,          /* mr_device_error: a bounded wait ran out    */
+    MR_ERR_SCRATCH_DIRTY = 6     /* debug check: scratch counters not zero     */
 } mr_status;
 
 typedef enum mr_scoring {
@@ -93,6 +94,8 @@ typedef enum mr_quant_format {
 #define MR_LAUNCH_PDL 1         /* programmatic dependent launch, see below */
 #define MR_LAUNCH_TEST_STALL 2  /* test hook for the timeout path, see below */
 #define MR_LAUNCH_LEGACY_MMA 4  /* router GEMV on mma.sync instead of tcgen05 */
+#define MR_LAUNCH_TEST_SLOW_SIGMOID 8  /* test hook: exact sigmoid always by its slow path */
+#define MR_LAUNCH_CHECK_SCRATCH 16   /* debug: verify scratch counters before a launch */
 
 /*
  * Sets the launch options of every later call in this process; returns
@@ -107,6 +110,20 @@ typedef enum mr_quant_format {
  * mma.sync instead of the tcgen05 cluster kernel (the two sum the split-K
  * partials in different orders, so their logits agree within fp32 rounding,
  * not bit for bit); up to 64 rows it always runs on mma.sync.
+ * MR_LAUNCH_TEST_SLOW_SIGMOID (a test of the sigmoid gate, never for
+ * production): every exact sigmoid score takes its double-double path
+ * instead of the fp64 fast path with its rounding test; the outputs are the
+ * same bits, only slower.
+ * MR_LAUNCH_CHECK_SCRATCH (a debug check): a call that is about to launch a
+ * kernel that uses the scratch counters (the split-K GEMV's last-arriver
+ * fixup [#36557 description: the last CTA re-zeroes its counter slot], the
+ * sort of more than 2048 assignments, the one-launch route over several
+ * clusters or expert groups) first copies the counter prefix to the host on
+ * its stream and waits for it; if any counter is not zero (a scratch buffer
+ * that was never zeroed, was written by someone else, or is in use by a
+ * call on another stream) it returns MR_ERR_SCRATCH_DIRTY and launches
+ * nothing.  It makes those calls synchronous: do not use it under stream
+ * capture or in production.
  * Default: 0 (plain stream order, tcgen05 where the weight tile fits).
  */
 int mr_set_launch_flags(int flags);
@@ -187,10 +204,13 @@ int mr_router_gemv(const void *x, int64_t ldx, const void *w, float *logits,
  *   MR_SCORE_SOFTMAX: selection key = the logit; weights = softmax
  *     probabilities of the selected experts (divided by their sum when
  *     renormalize != 0).
- *   MR_SCORE_SIGMOID: s = sigmoid(logit) by a fixed fp32 recipe (Cody-Waite
- *     reduction + degree-7 Taylor polynomial, fp32 fma; within 3 ulp of the
- *     exact sigmoid); key = s + sel_bias[n] in fp32; weights = the unbiased
- *     s of the selected (divided by their sum when renormalize != 0).
+ *   MR_SCORE_SIGMOID: s = sigmoid(logit) = 1 / (1 + e^-logit) rounded once
+ *     to the nearest fp32 value (correctly rounded: an fp64 evaluation with a
+ *     rounding test, double-double where that test cannot decide); key =
+ *     s + sel_bias[n] in fp32; weights = the unbiased s of the selected
+ *     (divided by their sum when renormalize != 0).  Only experts whose fp32
+ *     approximate key is near the k-th largest are scored exactly; the ids
+ *     are those of the exact keys.
  * Ties: the lower expert id wins; -0 and +0 tie.  Slot j of a token is its
  * j-th best expert.  logits: fp32 [M, N]; sel_bias: fp32 [N] or NULL
  * (sigmoid only); topk_ids: int32 [M, topk]; topk_weights: fp32 [M, topk].
@@ -402,9 +422,15 @@ int mr_norm_apply(const void *sres, int64_t ldx, const float *rstd, const void *
  * for bit).  The scratch is MR_NOALLOC_SCRATCH_BYTES of device memory that
  * this library declares at file scope; every GPU that loads the library
  * holds it until the process exits.
- *  - The FIRST call on each device does the set-up (looks up the array's
- *    device address and zeroes its counters, synchronously on that device);
- *    make that first call before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (host code cannot use the array's name as an address).  The FIRST call
+ *    in a device's context -- including the first after that context was
+ *    destroyed and created again, e.g. by cudaDeviceReset, which reloads the
+ *    library's device code -- zeroes the array's counters with one
+ *    cudaMemsetAsync on the call's stream before its launch; make that first
+ *    call before any stream capture.
+ *  - With MR_LAUNCH_CHECK_SCRATCH set, each call verifies that the array's
+ *    counters are zero before it launches (see mr_set_launch_flags).
  *  - Every call on a device shares the one array, and the array keeps the
  *    last call's contents: calls that can overlap on the GPU (different
  *    streams, concurrent threads) race and corrupt each other's results.

@@ -44,8 +44,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.mr_abi_version() == 1
-    for s in range(6):
+    for s in range(7):
         assert lib.mr_status_string(s).startswith(b"MR_")
+    assert b"SCRATCH_DIRTY" in lib.mr_status_string(mr.MR_ERR_SCRATCH_DIRTY)
     assert lib.mr_status_string(99) == b"unknown mr_status"
 
 
@@ -133,7 +134,9 @@ def test_validation_returns_before_any_launch(lib):
     assert lib.mr_norm_apply(fake, 48, fake, fake, 0, 2, 48, None, None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_norm_apply(fake, 48, fake, fake, 5, 2, 48, fake, None) == mr.MR_ERR_INVALID_ARG
     # launch options and the wait limit (host-only settings)
-    assert lib.mr_set_launch_flags(8) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_set_launch_flags(32) == mr.MR_ERR_INVALID_ARG
+    for f in (mr.LAUNCH_TEST_SLOW_SIGMOID, mr.LAUNCH_CHECK_SCRATCH):
+        assert lib.mr_set_launch_flags(f) == mr.MR_OK and lib.mr_get_launch_flags() == f
     assert lib.mr_set_launch_flags(mr.LAUNCH_LEGACY_MMA) == mr.MR_OK
     assert lib.mr_get_launch_flags() == mr.LAUNCH_LEGACY_MMA
     assert lib.mr_set_launch_flags(0) == mr.MR_OK
@@ -250,3 +253,99 @@ def test_binding_rejects_bad_arguments_and_host_tensors():
         mr.moe_sort_quant(ids, torch.zeros((5, 512), dtype=torch.bfloat16), 128, 16)
     with pytest.raises(ValueError, match="CUDA"):
         mr.moe_sort_quant(ids, x, 128, 16)
+
+
+class _FakeCuda:
+    """Stands in for a CUDA tensor in host-side argument checks (no GPU
+    here): device, dtype, shape, strides and contiguity only.  Any use of
+    its data would fail (data_ptr raises), so a check that lets a bad
+    argument through to the library shows up as an error of the wrong kind."""
+
+    def __init__(self, shape, dtype, device=0, contiguous=True):
+        import torch
+        self.shape = torch.Size(shape)
+        self.dtype = dtype
+        self.device = torch.device("cuda", device)
+        self.is_cuda = True
+        self._contig = contiguous
+
+    def dim(self):
+        return len(self.shape)
+
+    def numel(self):
+        n = 1
+        for d in self.shape:
+            n *= d
+        return n
+
+    def stride(self, i=None):
+        st, acc = [], 1
+        for d in reversed(self.shape):
+            st.append(acc)
+            acc *= d
+        st = tuple(reversed(st))
+        if not self._contig and len(st) == 2:
+            st = (st[0] * 2, 1)
+        return st if i is None else st[i]
+
+    def is_contiguous(self):
+        return self._contig
+
+    def data_ptr(self):
+        raise AssertionError("the library was reached with an argument the binding should have refused")
+
+
+def test_binding_refuses_bad_outputs_and_mixed_devices():
+    """Caller-passed outputs of the wrong shape, dtype or layout, and tensors
+    on different devices, are refused before any launch (a short or strided
+    output would be written out of bounds, a pointer of another device used
+    on the current one)."""
+    import torch
+    bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+    x, w = _FakeCuda((4, 512), bf), _FakeCuda((128, 512), bf)
+    for fn in (mr.router_gemv, mr.router_gemv_noalloc):
+        with pytest.raises(ValueError, match="shape"):
+            fn(x, w, out=_FakeCuda((4, 64), f32))
+        with pytest.raises(ValueError, match="contiguous"):
+            fn(x, w, out=_FakeCuda((4, 128), f32, contiguous=False))
+        with pytest.raises(ValueError, match="float32"):
+            fn(x, w, out=_FakeCuda((4, 128), bf))
+        with pytest.raises(ValueError, match="devices"):
+            fn(x, _FakeCuda((128, 512), bf, device=1))
+        with pytest.raises(ValueError, match="devices"):
+            fn(x, w, out=_FakeCuda((4, 128), f32, device=1))
+    lg = _FakeCuda((4, 128), f32)
+    with pytest.raises(ValueError, match="ids"):
+        mr.route_topk(lg, 8, ids=_FakeCuda((4, 4), i32), weights=_FakeCuda((4, 8), f32))
+    with pytest.raises(ValueError, match="bias"):
+        mr.route_topk(lg, 8, "sigmoid", bias=_FakeCuda((64,), f32),
+                      ids=_FakeCuda((4, 8), i32), weights=_FakeCuda((4, 8), f32))
+    cap = mr.sort_capacity(4, 8, 128, 16)
+    ids = _FakeCuda((4, 8), i32)
+    with pytest.raises(ValueError, match="sorted_token_ids"):
+        mr.moe_sort(ids, 128, 16, out=(_FakeCuda((cap - 16,), i32), _FakeCuda((cap // 16,), i32), _FakeCuda((1,), i32)))
+    with pytest.raises(ValueError, match="expert_ids"):
+        mr.moe_sort(ids, 128, 16, out=(_FakeCuda((cap,), i32), _FakeCuda((cap // 16 - 1,), i32), _FakeCuda((1,), i32)))
+    with pytest.raises(ValueError, match="q"):
+        mr.mxfp8_quant(x, out=(_FakeCuda((4, 256), u8), _FakeCuda((4, 16), u8)))
+    with pytest.raises(ValueError, match="q"):
+        mr.mxfp4_quant(x, out=(_FakeCuda((4, 512), u8), _FakeCuda((4, 16), u8)))
+    route_out = dict(logits=_FakeCuda((4, 128), f32), topk_ids=_FakeCuda((4, 8), i32),
+                     topk_weights=_FakeCuda((4, 8), f32), sorted_token_ids=_FakeCuda((cap,), i32),
+                     expert_ids=_FakeCuda((cap // 16,), i32), num_tokens_post_padded=_FakeCuda((1,), i32),
+                     q=_FakeCuda((4, 512), u8), scale=_FakeCuda((4, 16), u8))
+    for name, bad in (("logits", _FakeCuda((4, 127), f32)), ("topk_weights", _FakeCuda((4, 8), bf)),
+                      ("q", _FakeCuda((4, 256), u8)), ("scale", _FakeCuda((4, 16), u8, device=1))):
+        o = dict(route_out, **{name: bad})
+        with pytest.raises(ValueError, match=name):
+            mr.moe_route_sort_quant(x, w, 8, 16, out=o)
+        with pytest.raises(ValueError, match=name):
+            mr.moe_route(x, w, 8, 16, out=o)
+    with pytest.raises(ValueError, match="devices"):
+        mr.moe_route(x, w, 8, 16, out=route_out, bias=_FakeCuda((128,), f32, device=1), scoring="sigmoid")
+    with pytest.raises(ValueError, match="scale"):
+        mr.moe_sort_quant(ids, x, 128, 16, out=(_FakeCuda((cap,), i32), _FakeCuda((cap // 16,), i32),
+                                                _FakeCuda((1,), i32), _FakeCuda((4, 512), u8),
+                                                _FakeCuda((4, 8), u8)))
+    with pytest.raises(ValueError, match="out"):
+        mr.norm_apply(x, _FakeCuda((4,), f32), _FakeCuda((512,), bf), out=_FakeCuda((4, 256), bf))

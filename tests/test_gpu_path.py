@@ -12,7 +12,7 @@ import pytest
 import oracle
 from decode_expert_routing_gb300 import inputs
 from tests.gpu_util import (assert_logits_close, check_gate, check_quant, check_sort, host,
-                            to_dev, to_dev_bf16)
+                            to_dev, to_dev_bf16, torch_mod)
 
 pytestmark = pytest.mark.gpu
 
@@ -139,15 +139,111 @@ def test_gate_modes_and_edges(mr, scoring, renorm):
         check_gate(lg, host(ids), host(wts), k, scoring, bias if scoring == "sigmoid" else None, renorm)
 
 
-def test_sigmoid_recipe_bitwise(mr):
-    """The kernel's fp32 sigmoid equals the oracle's recipe bit for bit: with
-    k = N every score appears (non-renormalised weights are the scores)."""
-    N = 1024
-    lg = np.linspace(-30, 30, 31 * N).astype(np.float32).reshape(31, N)
+def _hard_sigmoid_logits():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "sigmoid_hard_cases.txt")
+    rows = [ln.split() for ln in open(path) if not ln.startswith("#")]
+    return np.array([int(r[0], 16) for r in rows], dtype=np.uint32).view(np.float32)
+
+
+def _sigmoid_scores_on_gpu(mr, lg):
+    """The kernel's sigmoid score of every logit: with k = N = 32 every expert
+    is selected, and the weights without renormalisation are the scores."""
     ids, wts = mr.route_topk(to_dev(lg), 32, "sigmoid", None, renormalize=False)
     ids, wts = host(ids), host(wts)
-    want = oracle.sigmoid_f32(np.take_along_axis(lg, ids, 1))
-    assert np.array_equal(wts.view(np.uint32), want.view(np.uint32))
+    return wts, np.take_along_axis(lg, ids, 1)
+
+
+def _sigmoid_sweep(n_rows):
+    rng = np.random.default_rng(17)
+    vals = np.concatenate([np.linspace(-88, 88, n_rows * 32 - 4096), rng.uniform(-110, -87, 2048),
+                           rng.uniform(15, 40, 2048)]).astype(np.float32)
+    rng.shuffle(vals)
+    hard = _hard_sigmoid_logits()
+    vals[: hard.size] = hard
+    return vals.reshape(n_rows, 32)
+
+
+@pytest.mark.parametrize("slow", [False, True])
+def test_sigmoid_scores_correctly_rounded_bitwise(mr, slow):
+    """The kernel's sigmoid scores equal the oracle's correctly rounded fp32
+    sigmoid bit for bit: over 2^20 logits in [-88, 88] plus the subnormal and
+    near-one ranges and the stored hard cases (within ~1e-14 of an fp32
+    rounding boundary, where the fp64 path's rounding test fails and the
+    double-double path decides).  slow: the test hook that sends every score
+    through the double-double path (a smaller sweep)."""
+    lg = _sigmoid_sweep(1 << 10 if slow else 1 << 15)
+    prev = mr.get_launch_flags()
+    mr.set_launch_flags(prev | (mr.LAUNCH_TEST_SLOW_SIGMOID if slow else 0))
+    try:
+        wts, picked = _sigmoid_scores_on_gpu(mr, lg)
+    finally:
+        mr.set_launch_flags(prev)
+    want = oracle.sigmoid_f32(picked)
+    bad = np.flatnonzero(wts.view(np.uint32).ravel() != want.view(np.uint32).ravel())
+    assert bad.size == 0, [(float(picked.ravel()[i]), float(wts.ravel()[i]), float(want.ravel()[i])) for i in bad[:5]]
+
+
+def _near_tie_bias(lg_rows, bias, k, offset_ulps):
+    """Bias of the expert ranked k+1 on row 0 moved so that its exact key
+    (oracle sigmoid + bias, fp32) sits offset_ulps from the k-th key: 0 is an
+    exact tie (the lower id wins), +-1 one ulp above or below.  The
+    approximate fp32 scores cannot order such keys; only exact ones can."""
+    s = oracle.sigmoid_f32(lg_rows[0])
+    t = (s + bias).astype(np.float32)
+    order = np.lexsort((np.arange(t.size), -t.astype(np.float64)))
+    i, j = int(order[k - 1]), int(order[k])
+    target = t[i]
+    for _ in range(abs(offset_ulps)):
+        target = np.nextafter(target, np.float32(np.inf if offset_ulps > 0 else -np.inf))
+    b = bias.copy()
+    bj = np.float32(np.float64(target) - np.float64(s[j]))
+    for _ in range(64):  # nearest bias with s_j + b_j == target in fp32
+        got = np.float32(s[j] + bj)
+        if got == target:
+            break
+        bj = np.nextafter(bj, np.float32(np.inf if got < target else -np.inf))
+    assert np.float32(s[j] + bj) == target
+    b[j] = bj
+    return b
+
+
+@pytest.mark.parametrize("offset", [-1, 0, 1])
+def test_sigmoid_near_ties_decided_by_exact_scores(mr, offset):
+    """Keys one ulp apart or tied (the k-th and (k+1)-th of a token, built by
+    moving one bias): the standalone gate and the one-launch route pick the
+    oracle's ids, bit for bit, on the GPU's logits."""
+    K, N, k, B = 3584, 896, 16, 16
+    for M in (1, 8):
+        x, w = inputs.router_inputs(M, K, N, 3)
+        xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+        lh = host(mr.router_gemv(xd, wd))
+        bias = _near_tie_bias(lh, inputs.selection_bias(N), k, offset)
+        ids, wts = mr.route_topk(to_dev(lh), k, "sigmoid", to_dev(bias))
+        check_gate(lh, host(ids), host(wts), k, "sigmoid", bias)
+        out = mr.moe_route_sort_quant(xd, wd, k, B, "sigmoid", to_dev(bias))
+        assert np.array_equal(host(out["logits"]).view(np.uint32), lh.view(np.uint32))
+        check_gate(lh, host(out["topk_ids"]), host(out["topk_weights"]), k, "sigmoid", bias)
+
+
+def test_route_sigmoid_slow_path_same_bits(mr):
+    """The one-launch route over 896 experts with every exact score taken by
+    the double-double path gives the same bits as the normal path."""
+    K, N, k, B = 3584, 896, 16, 16
+    x, w = inputs.router_inputs(8, K, N, 3)
+    bias = to_dev(inputs.selection_bias(N))
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    ref = mr.moe_route_sort_quant(xd, wd, k, B, "sigmoid", bias)
+    prev = mr.get_launch_flags()
+    mr.set_launch_flags(prev | mr.LAUNCH_TEST_SLOW_SIGMOID)
+    try:
+        got = mr.moe_route_sort_quant(xd, wd, k, B, "sigmoid", bias)
+        torch_mod().cuda.synchronize()
+    finally:
+        mr.set_launch_flags(prev)
+    for name in ("logits", "topk_ids", "topk_weights", "sorted_token_ids", "expert_ids", "q", "scale"):
+        a, b = host(ref[name]), host(got[name])
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), name
 
 
 # ------------------------------------------------------------------ sort
@@ -284,3 +380,39 @@ def test_adversarial_skew_ties_and_quant_edges(mr):
     q, s = mr.mxfp8_quant(xd)
     check_quant(x, host(q), host(s))
     torch.cuda.synchronize()
+
+
+def test_scratch_dirty_check_refuses_before_launch(mr):
+    """With the debug scratch check on, a call whose scratch counters are not
+    zero (one slot corrupted from the host) returns MR_ERR_SCRATCH_DIRTY and
+    launches nothing (its output keeps its sentinel); after a reset the same
+    calls succeed.  Covers the split-K GEMV, the multi-CTA sort and the
+    one-launch route over several clusters."""
+    torch = torch_mod()
+    N, K, k, B = 128, 6144, 8, 16
+    prev = mr.get_launch_flags()
+    x, w = inputs.router_inputs(128, K, N, 2)
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    scratch = mr.Scratch(512, N, K, k)
+    ids = to_dev(np.random.default_rng(1).integers(0, N, (512, k)).astype(np.int32))
+    calls = {
+        "gemv": lambda: mr.router_gemv(xd, wd, out=lg, scratch=scratch),
+        "sort": lambda: mr.moe_sort(ids, N, B, scratch=scratch),
+        "route": lambda: mr.moe_route_sort_quant(xd[:32], wd, k, B, scratch=scratch),
+    }
+    lg = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda")
+    try:
+        mr.set_launch_flags(prev | mr.LAUNCH_CHECK_SCRATCH | mr.LAUNCH_LEGACY_MMA)
+        for name, fn in calls.items():
+            scratch.counters()[4097 if name == "sort" else 17] = 5
+            torch.cuda.synchronize()
+            with pytest.raises(mr.MoeRouteError) as ei:
+                fn()
+            assert ei.value.status == mr.MR_ERR_SCRATCH_DIRTY, name
+            scratch.reset()
+            fn()
+            torch.cuda.synchronize()
+            assert int(scratch.counters().abs().sum()) == 0, name
+    finally:
+        mr.set_launch_flags(prev)
+    assert_logits_close(host(lg), oracle.router_gemv(x, w))

@@ -61,7 +61,8 @@ def test_plans_keep_the_kernel_invariants(plans):
         n_plans += 1
         assert p["cs"] == 16 and p["kc"] * 16 == K and p["kc"] % 32 == 0
         assert p["nl"] * p["ng"] == N and p["nl"] % 8 == 0
-        assert p["ng"] == 1 or (N >= 512 and p["nl"] >= 128 and k <= p["nl"] and mg > 1)
+        if p["ng"] > 1:  # expert groups: >= 128 experts for the whole route, >= 16 for the GEMV alone
+            assert mg > 1 and (N >= 512 and p["nl"] >= 128 and k <= p["nl"] if mode == 1 else p["nl"] >= 16)
         if mode == 1 and p["ng"] > 1:
             assert M <= 16                       # the whole route splits one token group only
         assert p["clusters"] == -(-M // p["rpc"]) * p["ng"]
@@ -85,3 +86,21 @@ def test_every_documented_decode_shape_has_a_plan(plans):
         assert (9, 1, M, 896, 3584, 16) in have
     for M in (128, 256, 512):
         assert (9, 0, M, 128, 6144, 1) in have
+
+
+def test_expert_groups_keep_the_split_k_of_the_unsplit_plan(plans):
+    """Every logit sums the same split-K partials in the same order whether
+    or not the experts are split into groups, and in the GEMV alone as in the
+    whole route (M <= 64): the k-parts per tile, the k-steps per part and the
+    slots per logit agree, so the logits are the same bits."""
+    by_key = {key: p for key, p in plans if p is not None}
+    n = 0
+    for (mg, mode, M, N, K, k), p in by_key.items():
+        ref = by_key.get((1, mode, M, N, K, k))
+        if ref is not None and not p["tc"]:
+            assert (p["wpt"], p["spw"], p["nslots"]) == (ref["wpt"], ref["spw"], ref["nslots"])
+            n += p["ng"] > 1
+        route = by_key.get((mg, 1, M, N, K, k))
+        if mode == 0 and route is not None and not p["tc"]:
+            assert (p["wpt"], p["spw"], p["nslots"]) == (route["wpt"], route["spw"], route["nslots"])
+    assert n > 100
