@@ -58,6 +58,7 @@ def _load():
         lib.oracle_e2m1_encode.restype = ctypes.c_uint8
         lib.oracle_e2m1_encode_array.argtypes = [P, i64, P]
         lib.oracle_mxfp4_quant.argtypes = [P, i64, i32, i32, P, P]
+        lib.oracle_sorted_quant.argtypes = [P, i64, i32, i32, i32, P, i32, i32, P, P]
         _lib = lib
     return _lib
 
@@ -206,4 +207,20 @@ def mxfp4_quant(x_bf16: np.ndarray):
     q = np.empty((M, K // 2), dtype=np.uint8)
     s = np.empty((M, K // 32), dtype=np.uint8)
     _load().oracle_mxfp4_quant(_ptr(x), K, M, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def sorted_quant(x_bf16: np.ndarray, topk: int, sorted_token_ids: np.ndarray, num_tokens_post_padded: int,
+                 fmt: str = "mxfp8"):
+    """Stage-1 activations in sorted order: (q uint8 [ntpp, K] or [ntpp, K/2],
+    scale uint8 [ntpp, K/32]); row p quantises x[sorted_token_ids[p] // topk],
+    padding rows are zero."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    st = _c(sorted_token_ids, np.int32)
+    n = int(num_tokens_post_padded)
+    fp4 = {"mxfp8": 0, "mxfp4": 1}[fmt]
+    q = np.empty((n, K // 2 if fp4 else K), dtype=np.uint8)
+    s = np.empty((n, K // 32), dtype=np.uint8)
+    _load().oracle_sorted_quant(_ptr(x), K, M, K, topk, _ptr(st), n, fp4, _ptr(q), _ptr(s))
     return q, s

@@ -428,3 +428,39 @@ void oracle_mxfp4_quant(const uint16_t *x, int64_t ldx, int M, int K,
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Next row: stage-1 activations written in sorted order.              */
+/* sglang #46691, Summary ("MoE sorting + quant": the sort kernels     */
+/* quantise the stage-1 activations) and "Changes to existing          */
+/* kernels" (the sort and the stage-1 quant in one launch for decode   */
+/* batches).  READING: the grouped expert GEMM reads its A operand     */
+/* row by row in the sorted order, so row p of the output, for         */
+/* p < num_tokens_post_padded, is the MX quantisation of the token of  */
+/* the assignment at sorted position p: x[f / k] with                  */
+/* f = sorted_token_ids[p] < M k; a padding position (f = M k) gives   */
+/* an all-zero row (codes 0, scale bytes 0: the quantisation of a row  */
+/* of zeros).  Rows at or past num_tokens_post_padded are not part of  */
+/* the output.  Formats as oracle_mxfp8_quant (fp4 = 0: q [rows, K])   */
+/* and oracle_mxfp4_quant (fp4 = 1: q [rows, K/2]); scale [rows, K/32].*/
+/* ------------------------------------------------------------------ */
+void oracle_sorted_quant(const uint16_t *x, int64_t ldx, int M, int K, int k,
+                         const int32_t *sorted_token_ids, int32_t num_tokens_post_padded,
+                         int fp4, uint8_t *q, uint8_t *scale)
+{
+    const int64_t qk = fp4 ? K / 2 : K, sk = K / 32;
+    for (int64_t p = 0; p < num_tokens_post_padded; ++p) {
+        const int64_t f = sorted_token_ids[p];
+        uint8_t *qrow = q + p * qk, *srow = scale + p * sk;
+        if (f >= 0 && f < (int64_t)M * k) {
+            const uint16_t *xrow = x + (f / k) * ldx;
+            if (fp4)
+                oracle_mxfp4_quant(xrow, ldx, 1, K, qrow, srow);
+            else
+                oracle_mxfp8_quant(xrow, ldx, 1, K, qrow, srow);
+        } else {
+            memset(qrow, 0, (size_t)qk);
+            memset(srow, 0, (size_t)sk);
+        }
+    }
+}
