@@ -34,6 +34,8 @@ SCORING = {"softmax": 0, "sigmoid": 1}
 NORM_KIND = {"rms": 0, "gemma": 1}
 QUANT_FORMAT = {None: 0, "mxfp8": 1, "mxfp4": 2}
 SCRATCH_COUNTER_BYTES = 32768
+PSORT_MAX_ASSIGN = 65536   # mr_moe_sort: one launch, no scratch, up to this many assignments
+QUANT_SORTED_ROWS = 0x100  # mr_moe_sort_quant: quantised rows in sorted order
 
 
 class MoeRouteError(RuntimeError):
@@ -349,7 +351,7 @@ def moe_sort(topk_ids, num_experts: int, block: int, out=None, scratch: Scratch 
     _check_sort_out(st, ex, nt, cap, block, dev)
     _check_scratch(scratch, dev)
     sp, sb = (scratch.ptr, scratch.nbytes) if scratch is not None else (None, 0)
-    if scratch is None and M * k > 2048:
+    if scratch is None and M * k > PSORT_MAX_ASSIGN:
         scratch = Scratch(M, num_experts, 512, k, device=dev)
         sp, sb = scratch.ptr, scratch.nbytes
     with _launch_ctx(dev):
@@ -694,9 +696,14 @@ def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, no
     return p, out, (x, w, bias, rstd, norm_weight, scratch)
 
 
-def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp8", out=None, stream=None):
-    """Sort and stage-1 quant in one launch (decode batches, M * topk <= 8192):
-    (sorted_token_ids, expert_ids, num_tokens_post_padded, q, scale)."""
+def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp8", out=None, stream=None,
+                   sorted_rows: bool = False):
+    """Sort and stage-1 quant in one launch (decode batches, M * topk <= 65536):
+    (sorted_token_ids, expert_ids, num_tokens_post_padded, q, scale).  q and
+    scale are in token order ([M, K or K/2], [M, K/32]), or with sorted_rows
+    in sorted order ([capacity, ...] rows: row p quantises the token of the
+    assignment at sorted position p, padding rows are zero, rows past
+    num_tokens_post_padded are left as they were)."""
     torch = _torch()
     if topk_ids.dim() != 2 or not topk_ids.is_contiguous():
         raise ValueError("topk_ids must be contiguous [M, k]")
@@ -711,22 +718,26 @@ def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp
     cap = sort_capacity(M, k, num_experts, block)
     if cap < 0:
         raise MoeRouteUnsupported(MR_ERR_UNSUPPORTED, "mr_sort_capacity")
+    rows = cap if sorted_rows else M
+    qk = K // 2 if quant == "mxfp4" else K
     if out is None:
         out = (torch.empty(cap, dtype=torch.int32, device=dev), torch.empty(cap // block, dtype=torch.int32, device=dev),
-               torch.empty(1, dtype=torch.int32, device=dev),
-               torch.empty((M, K // 2 if quant == "mxfp4" else K), dtype=torch.uint8, device=dev),
-               torch.empty((M, K // 32), dtype=torch.uint8, device=dev))
+               torch.empty(1, dtype=torch.int32, device=dev), torch.empty((rows, qk), dtype=torch.uint8, device=dev),
+               torch.empty((rows, K // 32), dtype=torch.uint8, device=dev))
     st, ex, nt, q, s = out
     _check_sort_out(st, ex, nt, cap, block, dev)
-    _check_out(q, "q", (M, K // 2 if quant == "mxfp4" else K), torch.uint8, dev)
-    _check_out(s, "scale", (M, K // 32), torch.uint8, dev)
+    if sorted_rows and st.numel() != cap:
+        raise ValueError("sorted rows: sorted_token_ids must hold exactly the capacity (its rows index q)")
+    _check_out(q, "q", (rows, qk), torch.uint8, dev)
+    _check_out(s, "scale", (rows, K // 32), torch.uint8, dev)
+    fmt = QUANT_FORMAT[quant] | (QUANT_SORTED_ROWS if sorted_rows else 0)
     with _launch_ctx(dev):
         status = _load().mr_moe_sort_quant(_dev_ptr(topk_ids, "topk_ids", torch.int32), M, k, num_experts, block,
-                                     _dev_ptr(x, "x", torch.bfloat16), ldx, K, QUANT_FORMAT[quant],
-                                     _dev_ptr(st, "sorted_token_ids", torch.int32),
-                                     _dev_ptr(ex, "expert_ids", torch.int32),
-                                     _dev_ptr(nt, "num_tokens_post_padded", torch.int32), st.numel(),
-                                     _dev_ptr(q, "q", torch.uint8), _dev_ptr(s, "scale", torch.uint8),
-                                     _stream_on(dev, stream))
+                                           _dev_ptr(x, "x", torch.bfloat16), ldx, K, fmt,
+                                           _dev_ptr(st, "sorted_token_ids", torch.int32),
+                                           _dev_ptr(ex, "expert_ids", torch.int32),
+                                           _dev_ptr(nt, "num_tokens_post_padded", torch.int32), st.numel(),
+                                           _dev_ptr(q, "q", torch.uint8), _dev_ptr(s, "scale", torch.uint8),
+                                           _stream_on(dev, stream))
     _check(status, "mr_moe_sort_quant")
     return st, ex, nt, q, s

@@ -7,6 +7,7 @@
 #include "../../include/moe_route.h"
 #include "internal.h"
 #include "route_plan.h"
+#include "sort.cuh"
 
 namespace {
 
@@ -162,7 +163,7 @@ size_t mr_scratch_bytes(int M_max, int N, int K, int topk) {
         if (b > work) work = b;
     }
     const int64_t n_assign = (int64_t)M_max * topk;
-    if (n_assign > mr::kSortChunk && n_assign < ((int64_t)1 << 30)) {
+    if (n_assign > mr::kPSortMaxAssign && n_assign < ((int64_t)1 << 30)) {
         const size_t b = mr::sort_work_bytes((int)n_assign, N);
         if (b > work) work = b;
     }
@@ -270,7 +271,7 @@ int mr_moe_sort(const int32_t* topk_ids, int M, int topk, int N, int block, int3
         num_tokens_post_padded == nullptr || !aligned(num_tokens_post_padded, 4))
         return MR_ERR_INVALID_ARG;
     const int64_t n_assign = (int64_t)M * topk;
-    if (n_assign > mr::kSortChunk) {
+    if (n_assign > mr::kPSortMaxAssign) {
         if (n_assign >= ((int64_t)1 << 30)) return MR_ERR_UNSUPPORTED;
         if (scratch == nullptr || !aligned(scratch, 256)) return MR_ERR_INVALID_ARG;
         if (scratch_bytes < mr::kWorkOffset + mr::sort_work_bytes((int)n_assign, N))
@@ -291,12 +292,14 @@ int mr_moe_sort_quant(const int32_t* topk_ids, int M, int topk, int N, int block
         !aligned(sorted_token_ids, 4) || expert_ids == nullptr || !aligned(expert_ids, 4) ||
         num_tokens_post_padded == nullptr || !aligned(num_tokens_post_padded, 4))
         return MR_ERR_INVALID_ARG;
-    if (quant_format != MR_QUANT_MXFP8 && quant_format != MR_QUANT_MXFP4) return MR_ERR_INVALID_ARG;
+    const int fmt = quant_format & ~MR_QUANT_SORTED_ROWS;
+    const bool sorted_rows = (quant_format & MR_QUANT_SORTED_ROWS) != 0;
+    if (fmt != MR_QUANT_MXFP8 && fmt != MR_QUANT_MXFP4) return MR_ERR_INVALID_ARG;
     if (q == nullptr || !aligned(q, 8) || scale == nullptr) return MR_ERR_INVALID_ARG;
-    if (K % 32 != 0 || (int64_t)M * topk > mr::kSortQuantMaxAssign) return MR_ERR_UNSUPPORTED;
-    return cuda_status(mr::launch_sort_quant(topk_ids, M, topk, N, block, sorted_token_ids, expert_ids,
-                                             num_tokens_post_padded, capacity, x, ldx, K, q, scale,
-                                             quant_format == MR_QUANT_MXFP4, as_stream(stream)));
+    if (K % 32 != 0 || (int64_t)M * topk > MR_SORT_QUANT_MAX_ASSIGN) return MR_ERR_UNSUPPORTED;
+    const mr::SortArgs a{topk_ids, M * topk, N, block, sorted_token_ids, expert_ids, num_tokens_post_padded, capacity};
+    return cuda_status(mr::launch_psort(a, M, topk, x, ldx, K, q, scale, fmt == MR_QUANT_MXFP4 ? 2 : 1, sorted_rows,
+                                        as_stream(stream)));
 }
 
 int mr_mxfp8_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, void* stream) {

@@ -49,11 +49,15 @@ cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, i
                         cudaStream_t st);
 cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, bool fp4,
                          cudaStream_t st);
-// Sort (CTA 0) and stage-1 quant (the other CTAs) in one launch, M*topk <= kSortQuantMaxAssign.
-constexpr int kSortQuantMaxAssign = 8192;
-cudaError_t launch_sort_quant(const int32_t* ids, int M, int topk, int N, int block, int32_t* sorted,
-                              int32_t* expert_ids, int32_t* ntpp, int64_t capacity, const void* x, int64_t ldx,
-                              int K, uint8_t* q, uint8_t* scale, bool fp4, cudaStream_t st);
+// One-launch parallel sort (every CTA counts every id): up to this many
+// assignments, at most kPSortMaxOwn placed by one CTA.
+constexpr int kPSortMaxAssign = 65536;
+constexpr int kPSortMaxOwn = 2048;
+struct SortArgs;
+// fmt: 0 sort only, 1 MXFP8, 2 MXFP4 of x; sorted_rows: q and scale hold the
+// quantised rows at the sorted positions (capacity rows) instead of token order.
+cudaError_t launch_psort(const SortArgs& s, int M, int topk, const void* x, int64_t ldx, int K, uint8_t* q,
+                         uint8_t* scale, int fmt, bool sorted_rows, cudaStream_t st);
 cudaError_t launch_norm_apply(const void* x, int64_t ldx, const float* rstd, const void* g, int gemma, int M,
                               int K, void* xn, cudaStream_t st);
 struct RoutePlan;

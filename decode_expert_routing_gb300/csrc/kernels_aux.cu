@@ -48,18 +48,6 @@ cudaError_t ensure_smem(const void* func, int bytes, int* done_per_device) {
     return e;
 }
 
-// Whole sort of <= kSortChunk assignments by one CTA.
-__global__ void __launch_bounds__(kSortThreads) sort_cta_kernel(SortArgs a) {
-    extern __shared__ __align__(16) int sm[];
-    pdl_trigger();
-    pdl_wait();
-    const int nw = blockDim.x >> 5;
-    RankSmem rs{sm, sm + nw * a.N, sm + nw * a.N + a.N};
-    int* start = rs.lrank + a.n_assign;
-    int* warp_tot = start + a.N;
-    cta_sort(a, stage_ids(a.ids, a.n_assign, warp_tot + 32), rs, start, warp_tot);
-}
-
 struct SortWork {
     int* chunk_cnt;   // [C][N]
     int* chunk_off;   // [C][N]
@@ -180,20 +168,15 @@ __global__ void __launch_bounds__(kSortThreads) sort_scatter_kernel(SortArgs a, 
     for (int64_t b = total / B + gt; b < a.capacity / B; b += T) a.expert_ids[b] = -1;
 }
 
-static int g_sort_cta_smem[64];
 static int g_sort_count_smem[64];
 
 cudaError_t launch_sort(const int32_t* ids, int M, int topk, int N, int block, int32_t* sorted,
                         int32_t* expert_ids, int32_t* ntpp, int64_t capacity, void* scratch,
                         cudaStream_t st) {
     SortArgs a{ids, M * topk, N, block, sorted, expert_ids, ntpp, capacity};
+    if (a.n_assign <= kPSortMaxAssign)
+        return launch_psort(a, M, topk, nullptr, 0, 0, nullptr, nullptr, 0, false, st);
     const int nw = kSortThreads / 32;
-    if (a.n_assign <= kSortChunk) {
-        const int smem = 4 * cta_sort_smem_ints(nw, N, a.n_assign);
-        cudaError_t e = ensure_smem((const void*)sort_cta_kernel, smem, g_sort_cta_smem);
-        if (e != cudaSuccess) return e;
-        return launch_kernel(sort_cta_kernel, dim3(1), dim3(kSortThreads), smem, st, a);
-    }
     const int C = (a.n_assign + kSortChunk - 1) / kSortChunk;
     SortWork w = sort_work(scratch, a.n_assign, N);
     const int smem = 4 * (nw * N + N + 2 * kSortChunk);
@@ -269,51 +252,215 @@ __global__ void __launch_bounds__(kQuantThreads) mx_quant_kernel(const uint16_t*
                      (int)((gridDim.x * blockDim.x) >> 5));
 }
 
-// ------------------------------------------------------------------ sort + quant
+// ------------------------------------------------------------------ parallel sort (+ quant)
+//
+// The sort of up to kPSortMaxAssign assignments in ONE launch over many CTAs
+// with no hand-off between them: every CTA counts the assignments of every
+// expert (all ids, read through L2) and those of the rows before its own
+// block, so it knows the padded start of each expert and the final position
+// of each of its own assignments without waiting for another CTA.  CTA c
+// places the assignments of its token rows [c R, (c + 1) R), writes the
+// padding and the block ids of experts c, c + G, ..., its share of the tail
+// and of num_tokens_post_padded, and (with a format) the MX quantisation of
+// its rows: in token order, or at the sorted positions of the rows'
+// assignments (the zero rows of the padding by the CTA of their expert).
 
-// Sort and stage-1 quant in one launch (decode batches): CTA 0 sorts all
-// M*k <= kSortQuantMaxAssign assignments with the single-CTA sort while the
-// other CTAs quantise x; the two share nothing but the launch.
+// hist[e] += number of ids[beg, end) equal to e (ids outside [0, N) are
+// skipped): each warp takes 32-id chunks, kPSortUnroll of them with their
+// loads in flight, and adds the peers of a chunk with one shared atomic.
+constexpr int kPSortUnroll = 4;
+__device__ __forceinline__ void psort_hist(const int32_t* ids, int beg, int end, int N, int* hist) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int base = beg + warp * 32 * kPSortUnroll; base < end; base += nw * 32 * kPSortUnroll) {
+        int e[kPSortUnroll];
+#pragma unroll
+        for (int u = 0; u < kPSortUnroll; ++u) {
+            const int i = base + u * 32 + lane;
+            e[u] = i < end ? __ldg(ids + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kPSortUnroll; ++u) {
+            const bool valid = e[u] >= 0 && e[u] < N;
+            const unsigned peers = __match_any_sync(kFull, valid ? e[u] : (int)(0x40000000u | (unsigned)lane));
+            if (valid && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[e[u]], __popc(peers));
+        }
+    }
+}
+
+// MX quantisation of rows x[0, rows) written to the sorted positions of their
+// assignments: pos[r * k + j] (or -1: not placed).  The same tile walk and
+// arithmetic as quant_tiles; each tile's codes and scales go to k rows.
 template <bool FP4>
-__global__ void __launch_bounds__(kSortQuantThreads) sort_quant_kernel(SortArgs a, const uint16_t* x, int64_t ldx,
-                                                                       int M, int K, uint8_t* q, uint8_t* scale) {
+__device__ __forceinline__ void quant_rows_to_positions(const uint16_t* x, int64_t ldx, int rows, int K,
+                                                        const int* pos, int k, uint8_t* q, uint8_t* scale,
+                                                        int warp_id, int nwarps) {
+    const int lane = threadIdx.x & 31;
+    const int vpr = K / 8, tpr = (vpr + kQuantTileVec - 1) / kQuantTileVec, K32 = K / 32;
+    const int64_t qk = FP4 ? K / 2 : K;
+    for (int t = warp_id; t < rows * tpr; t += nwarps) {
+        const int r = t / tpr, c0 = (t - r * tpr) * kQuantTileVec + lane;
+        const uint16_t* xr = x + (int64_t)r * ldx;
+        uint4 v[kQuantUnroll];
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int c = c0 + u * 32;
+            v[u] = c < vpr ? ld_ro_v4(xr + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int c = c0 + u * 32;
+            unsigned sb;
+            uint2 q8 = make_uint2(0u, 0u);
+            uint32_t q4 = 0u;
+            if constexpr (FP4)
+                q4 = mx4_quant_quad(v[u], &sb);
+            else
+                q8 = mx_quant_quad(v[u], &sb);
+            if (c >= vpr) continue;
+            for (int j = 0; j < k; ++j) {
+                const int p = pos[r * k + j];
+                if (p < 0) continue;
+                if constexpr (FP4)
+                    *reinterpret_cast<uint32_t*>(q + (int64_t)p * qk + c * 4) = q4;
+                else
+                    *reinterpret_cast<uint2*>(q + (int64_t)p * qk + c * 8) = q8;
+                if ((lane & 3) == 0) scale[(int64_t)p * K32 + c / 4] = (uint8_t)sb;
+            }
+        }
+    }
+}
+
+struct PSortArgs {
+    SortArgs s;
+    int M, k, rows_per;   // token rows per CTA
+    const uint16_t* x;    // stage-1 activations [M, ldx] (FMT != 0)
+    int64_t ldx;
+    int K;
+    uint8_t* q;           // [M or capacity rows, K or K/2]
+    uint8_t* scale;       // [M or capacity rows, K/32]
+};
+
+// Shared-memory ints of one CTA: pre, tot, start [N] each, 32 scan slots, own
+// ids and positions [own], the ranking tables (warps x N, N, own).
+__host__ __device__ constexpr int psort_smem_ints(int nwarps, int N, int own) {
+    return 3 * N + 32 + 2 * own + nwarps * N + N + own;
+}
+
+// FMT: 0 sort only, 1 MXFP8, 2 MXFP4; SORTED: quantised rows at the sorted
+// positions (q, scale with capacity rows) instead of token order.
+template <int FMT, bool SORTED>
+__global__ void __launch_bounds__(kSortQuantThreads) psort_kernel(PSortArgs a) {
     extern __shared__ __align__(16) int sm[];
     pdl_trigger();
     pdl_wait();
-    if (blockIdx.x == 0) {
-        const int nw = blockDim.x >> 5;
-        RankSmem rs{sm, sm + nw * a.N, sm + nw * a.N + a.N};
-        int* start = rs.lrank + a.n_assign;
-        int* warp_tot = start + a.N;
-        cta_sort(a, stage_ids(a.ids, a.n_assign, warp_tot + 32), rs, start, warp_tot);
-        return;
+    const int tid = threadIdx.x, nthr = blockDim.x, nw = nthr >> 5, warp = tid >> 5;
+    const int N = a.s.N, B = a.s.block, k = a.k, G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int n_all = a.s.n_assign, sentinel = n_all;
+    const int m0 = min(c * a.rows_per, a.M), m1 = min(m0 + a.rows_per, a.M);
+    const int f0 = m0 * k, n_own = (m1 - m0) * k, own_max = a.rows_per * k;
+    int* pre = sm;                   // assignments per expert in rows [0, m0)
+    int* tot = pre + N;              // assignments per expert, all rows
+    int* start = tot + N;            // padded start of each expert's run
+    int* warp_tot = start + N;       // scan slots
+    int* own_ids = warp_tot + 32;    // this CTA's ids
+    int* own_pos = own_ids + own_max;  // their sorted positions (-1: not placed)
+    RankSmem rs{own_pos + own_max, own_pos + own_max + nw * N, own_pos + own_max + nw * N + N};
+    for (int e = tid; e < N; e += nthr) {
+        pre[e] = 0;
+        tot[e] = 0;
     }
-    quant_tiles<FP4>(x, ldx, M, K, q, scale, (int)(((blockIdx.x - 1) * blockDim.x + threadIdx.x) >> 5),
-                     (int)(((gridDim.x - 1) * blockDim.x) >> 5));
+    for (int i = tid; i < n_own; i += nthr) own_ids[i] = __ldg(a.s.ids + f0 + i);
+    __syncthreads();
+    psort_hist(a.s.ids, 0, f0, N, pre);
+    psort_hist(a.s.ids, f0, n_all, N, tot);
+    __syncthreads();
+    for (int e = tid; e < N; e += nthr) {
+        const int t = tot[e] + pre[e];
+        tot[e] = t;
+        start[e] = (t + B - 1) / B * B;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan(start, N, warp_tot);
+    // stable ranks inside this CTA's block, offset by the rows before it
+    const int seg = cta_rank(own_ids, n_own, N, rs);
+    for (int i = tid; i < n_own; i += nthr) {
+        const int e = own_ids[i];
+        int p = -1;
+        if (e >= 0 && e < N) {
+            p = start[e] + pre[e] + rs.wcnt[(i / seg) * N + e] + rs.lrank[i];
+            a.s.sorted[p] = f0 + i;
+        }
+        own_pos[i] = p;
+    }
+    // padding and block ids of experts c, c + G, ...; the tail past the total
+    for (int e = c; e < N; e += G) {
+        const int st = start[e], t = tot[e], pd = (t + B - 1) / B * B;
+        for (int i = t + tid; i < pd; i += nthr) a.s.sorted[st + i] = sentinel;
+        for (int b = st / B + tid; b < (st + pd) / B; b += nthr) a.s.expert_ids[b] = e;
+    }
+    {
+        const int64_t gt = (int64_t)c * nthr + tid, T = (int64_t)G * nthr;
+        for (int64_t i = total + gt; i < a.s.capacity; i += T) a.s.sorted[i] = sentinel;
+        for (int64_t b = total / B + gt; b < a.s.capacity / B; b += T) a.s.expert_ids[b] = -1;
+    }
+    if (c == 0 && tid == 0) *a.s.ntpp = total;
+    if constexpr (FMT != 0) {
+        constexpr bool FP4 = FMT == 2;
+        const int K = a.K;
+        const int64_t qk = FP4 ? K / 2 : K, K32 = K / 32;
+        if constexpr (!SORTED) {
+            quant_tiles<FP4>(a.x + (int64_t)m0 * a.ldx, a.ldx, m1 - m0, K, a.q + (int64_t)m0 * qk,
+                             a.scale + (int64_t)m0 * K32, warp, nw);
+        } else {
+            __syncthreads();  // own_pos complete
+            quant_rows_to_positions<FP4>(a.x + (int64_t)m0 * a.ldx, a.ldx, m1 - m0, K, own_pos, k, a.q, a.scale,
+                                         warp, nw);
+            // zero rows at the padding positions of experts c, c + G, ...
+            for (int e = c; e < N; e += G) {
+                const int st = start[e], t = tot[e], pd = (t + B - 1) / B * B;
+                const int64_t nq = (int64_t)(pd - t) * (qk / 8);  // 8-byte words (qk % 16 == 0)
+                uint2* qz = reinterpret_cast<uint2*>(a.q + (int64_t)(st + t) * qk);
+                for (int64_t i = tid; i < nq; i += nthr) qz[i] = make_uint2(0u, 0u);
+                const int64_t ns = (int64_t)(pd - t) * K32;
+                uint8_t* sz = a.scale + (int64_t)(st + t) * K32;
+                for (int64_t i = tid; i < ns; i += nthr) sz[i] = 0;
+            }
+        }
+    }
 }
 
-static int g_sort_quant_smem[2][64];
+static int g_psort_smem[6][64];
 
-cudaError_t launch_sort_quant(const int32_t* ids, int M, int topk, int N, int block, int32_t* sorted,
-                              int32_t* expert_ids, int32_t* ntpp, int64_t capacity, const void* x, int64_t ldx,
-                              int K, uint8_t* q, uint8_t* scale, bool fp4, cudaStream_t st) {
-    SortArgs a{ids, M * topk, N, block, sorted, expert_ids, ntpp, capacity};
+cudaError_t launch_psort(const SortArgs& s, int M, int topk, const void* x, int64_t ldx, int K, uint8_t* q,
+                         uint8_t* scale, int fmt, bool sorted_rows, cudaStream_t st) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // rows per CTA: at most one CTA per SM (each counts every id), and at
+    // most kPSortMaxOwn assignments placed by one CTA
+    int rows_per = (M + sms - 1) / sms;
+    if (rows_per * topk > kPSortMaxOwn) rows_per = kPSortMaxOwn / topk;
+    if (rows_per < 1) rows_per = 1;
+    const int G = (M + rows_per - 1) / rows_per;
+    PSortArgs a{s, M, topk, rows_per, static_cast<const uint16_t*>(x), ldx, K, q, scale};
     const int nw = kSortQuantThreads / 32;
-    const int smem = 4 * cta_sort_smem_ints(nw, N, a.n_assign);
-    auto kernel = fp4 ? sort_quant_kernel<true> : sort_quant_kernel<false>;
-    e = ensure_smem((const void*)kernel, smem, g_sort_quant_smem[fp4 ? 1 : 0]);
+    const int smem = 4 * psort_smem_ints(nw, s.N, rows_per * topk);
+    void (*kernel)(PSortArgs) = nullptr;
+    int slot = 0;
+    if (fmt == 0) {
+        kernel = psort_kernel<0, false>;
+    } else if (fmt == 1) {
+        kernel = sorted_rows ? psort_kernel<1, true> : psort_kernel<1, false>;
+        slot = sorted_rows ? 2 : 1;
+    } else {
+        kernel = sorted_rows ? psort_kernel<2, true> : psort_kernel<2, false>;
+        slot = sorted_rows ? 4 : 3;
+    }
+    e = ensure_smem((const void*)kernel, smem, g_psort_smem[slot]);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (int64_t)M * ((K / 8 + kQuantTileVec - 1) / kQuantTileVec);
-    if (tiles >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
-    int64_t qctas = (tiles + nw - 1) / nw;
-    const int64_t cap = (int64_t)sms * 2;  // two resident CTAs of 512 threads per SM, grid-stride beyond
-    if (qctas > cap) qctas = cap;
-    return launch_kernel(kernel, dim3((unsigned)(1 + qctas)), dim3(kSortQuantThreads), smem, st, a,
-                         static_cast<const uint16_t*>(x), ldx, M, K, q, scale);
+    return launch_kernel(kernel, dim3((unsigned)G), dim3(kSortQuantThreads), smem, st, a);
 }
 
 cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t* scale, bool fp4,

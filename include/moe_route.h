@@ -242,8 +242,10 @@ int64_t mr_sort_capacity(int M, int topk, int N, int block);
  * topk_ids: int32 [M, topk]; sorted_token_ids: int32 [capacity];
  * expert_ids: int32 [capacity / block]; num_tokens_post_padded: int32 [1].
  * capacity must be >= mr_sort_capacity(M, topk, N, block).  1 <= block <=
- * 1024.  One launch up to 2048 assignments; two launches above (scratch
- * used).  Output bits are unique (no freedom in the layout).
+ * 1024.  One launch up to 65536 assignments (over up to one CTA per SM, each
+ * CTA counting every id and placing the assignments of its own token rows;
+ * scratch unused, may be NULL); two launches above (scratch used).  Output
+ * bits are unique (no freedom in the layout).
  */
 int mr_moe_sort(const int32_t *topk_ids, int M, int topk, int N, int block,
                 int32_t *sorted_token_ids, int32_t *expert_ids,
@@ -295,16 +297,26 @@ int mr_moe_route_sort_quant(const void *x, int64_t ldx, const void *w,
 /*
  * a4 + a5 in ONE launch for decode batches [#46691 Summary: the MiniMax-M3.1
  * sort and stage-1 quant run as one launch for decode batches and as four
- * launches for prefill].  One CTA sorts topk_ids exactly as mr_moe_sort
- * while the other CTAs of the launch quantise x exactly as mr_mxfp8_quant
- * (quant_format MR_QUANT_MXFP8, q [M, K]) or mr_mxfp4_quant (MR_QUANT_MXFP4,
- * q [M, K/2]); every output is bitwise equal to those calls.  Arguments and
- * layouts as there; x is bf16 [M, ldx] with the rows of topk_ids.
- * M * topk <= MR_SORT_QUANT_MAX_ASSIGN (1024 tokens at top-8) and K % 32 == 0,
+ * launches for prefill].  The sort outputs are bitwise equal to mr_moe_sort.
+ * The quantisation, exactly as mr_mxfp8_quant (quant_format MR_QUANT_MXFP8)
+ * or mr_mxfp4_quant (MR_QUANT_MXFP4), is written
+ *  - in token order: q [M, K] (MXFP8) or [M, K/2] (MXFP4), scale [M, K/32],
+ *    bitwise equal to those calls; or
+ *  - with MR_QUANT_SORTED_ROWS or-ed into quant_format, in sorted order for
+ *    the grouped expert GEMM [#46691 Summary "MoE sorting + quant"]: q has
+ *    capacity rows of K (MXFP8) or K/2 (MXFP4) bytes and scale capacity rows
+ *    of K/32 bytes; for p < *num_tokens_post_padded, row p is the
+ *    quantisation of x[sorted_token_ids[p] / topk] and a padding position
+ *    (sentinel M*topk) is a row of zero codes and zero scale bytes.  Rows at
+ *    or past *num_tokens_post_padded are not written.
+ * Arguments and layouts as there; x is bf16 [M, ldx] with the rows of
+ * topk_ids.  One launch over up to one CTA per SM, no scratch.
+ * M * topk <= MR_SORT_QUANT_MAX_ASSIGN (8192 tokens at top-8) and K % 32 == 0,
  * else MR_ERR_UNSUPPORTED; MR_QUANT_NONE or an unknown format, a NULL or
- * misaligned (8 B) q, or a NULL scale returns MR_ERR_INVALID_ARG.  No scratch.
+ * misaligned (8 B) q, or a NULL scale returns MR_ERR_INVALID_ARG.
  */
-#define MR_SORT_QUANT_MAX_ASSIGN 8192
+#define MR_SORT_QUANT_MAX_ASSIGN 65536
+#define MR_QUANT_SORTED_ROWS 0x100
 int mr_moe_sort_quant(const int32_t *topk_ids, int M, int topk, int N, int block,
                       const void *x, int64_t ldx, int K, int quant_format,
                       int32_t *sorted_token_ids, int32_t *expert_ids,

@@ -105,7 +105,8 @@ def test_validation_returns_before_any_launch(lib):
     # sort: capacity too small
     assert lib.mr_moe_sort(fake, 1, 8, 128, 16, fake, fake, fake, 64, None, 0, None) == mr.MR_ERR_INVALID_ARG
     # sort of a large batch without scratch
-    assert lib.mr_moe_sort(fake, 4096, 8, 128, 64, fake, fake, fake, 40832, None, 0, None) == mr.MR_ERR_INVALID_ARG
+    assert mr.sort_capacity(9000, 8, 128, 64) == 80064
+    assert lib.mr_moe_sort(fake, 9000, 8, 128, 64, fake, fake, fake, 80064, None, 0, None) == mr.MR_ERR_INVALID_ARG
     # quant: K % 32
     assert lib.mr_mxfp8_quant(fake, 48, 1, 40, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
     # fused: M > 64
@@ -195,7 +196,7 @@ def test_general_route_and_mxfp4_validation(lib):
     assert lib.mr_moe_route(ctypes.byref(p), None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_mxfp4_quant(fake, 48, 1, 40, fake, fake, None) == mr.MR_ERR_UNSUPPORTED
     # sort + quant in one launch: too many assignments, no quant format, misaligned q
-    assert lib.mr_moe_sort_quant(fake, 1025, 8, 128, 16, fake, 512, 512, 1, fake, fake, fake, 1 << 20, fake, fake,
+    assert lib.mr_moe_sort_quant(fake, 8193, 8, 128, 16, fake, 512, 512, 1, fake, fake, fake, 1 << 20, fake, fake,
                                  None) == mr.MR_ERR_UNSUPPORTED
     assert lib.mr_moe_sort_quant(fake, 4, 8, 128, 16, fake, 512, 512, 0, fake, fake, fake, 1 << 20, fake, fake,
                                  None) == mr.MR_ERR_INVALID_ARG

@@ -251,7 +251,8 @@ def test_route_sigmoid_slow_path_same_bits(mr):
 
 @pytest.mark.parametrize("M,k,N,B", [(1, 8, 128, 16), (2, 8, 128, 16), (16, 8, 128, 16), (64, 8, 128, 16),
                                      (32, 16, 896, 16), (16, 16, 896, 16), (256, 8, 128, 16), (4096, 8, 128, 64),
-                                     (257, 8, 128, 64), (7, 3, 9, 1), (100, 32, 1024, 128), (333, 7, 50, 32)])
+                                     (257, 8, 128, 64), (7, 3, 9, 1), (100, 32, 1024, 128), (333, 7, 50, 32),
+                                     (8192, 8, 128, 64), (9000, 8, 128, 16), (2100, 32, 1024, 16)])
 def test_sort_matches_oracle(mr, M, k, N, B):
     rng = np.random.default_rng(M * 7 + k)
     ids = np.stack([rng.permutation(N)[:k] for _ in range(M)]).astype(np.int32)
@@ -387,14 +388,15 @@ def test_scratch_dirty_check_refuses_before_launch(mr):
     zero (one slot corrupted from the host) returns MR_ERR_SCRATCH_DIRTY and
     launches nothing (its output keeps its sentinel); after a reset the same
     calls succeed.  Covers the split-K GEMV, the multi-CTA sort and the
-    one-launch route over several clusters."""
+    one-launch route over several clusters (the sort above 65536
+    assignments, where it takes two launches)."""
     torch = torch_mod()
     N, K, k, B = 128, 6144, 8, 16
     prev = mr.get_launch_flags()
     x, w = inputs.router_inputs(128, K, N, 2)
     xd, wd = to_dev_bf16(x), to_dev_bf16(w)
     scratch = mr.Scratch(512, N, K, k)
-    ids = to_dev(np.random.default_rng(1).integers(0, N, (512, k)).astype(np.int32))
+    ids = to_dev(np.random.default_rng(1).integers(0, N, (9000, k)).astype(np.int32))  # > 65536: two launches
     calls = {
         "gemv": lambda: mr.router_gemv(xd, wd, out=lg, scratch=scratch),
         "sort": lambda: mr.moe_sort(ids, N, B, scratch=scratch),
