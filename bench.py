@@ -675,14 +675,26 @@ def run_ours(args):
             for r in range(16):
                 mr.moe_sort(sids, N_EXP, BLOCK, out=sout[:3], scratch=sssk)
                 mr.mxfp8_quant(sx[r % 2], out=sout[3:])
+        # the stage-1 activations written in sorted order (capacity rows)
+        srows = (sout[0], sout[1], sout[2], torch.empty((scap, K_HID), dtype=torch.uint8, device=dev),
+                 torch.empty((scap, K_HID // 32), dtype=torch.uint8, device=dev))
+
+        def body_sorted(sx=sx, sids=sids, srows=srows):
+            for r in range(16):
+                mr.moe_sort_quant(sids, sx[r % 2], N_EXP, BLOCK, "mxfp8", out=srows, sorted_rows=True)
         with torch.cuda.stream(stream):
             body_one()
             body_two()
-        u1, u2 = graph_us(body_one, 16), graph_us(body_two, 16)
+            body_sorted()
+        u1, u2, u3 = graph_us(body_one, 16), graph_us(body_two, 16), graph_us(body_sorted, 16)
+        ntpp = int(srows[2].item())
         sb = 4 * SM_ * TOPK + 4 * scap + 4 * (scap // BLOCK) + 4 + 2 * SM_ * K_HID + SM_ * K_HID + SM_ * K_HID // 32
+        sb_sorted = 4 * SM_ * TOPK + 4 * scap + 4 * (scap // BLOCK) + 4 + 2 * SM_ * K_HID + ntpp * (K_HID + K_HID // 32)
         sortq[str(SM_)] = {"us_per_call": round(u1, 3), "GBs": round(sb / (u1 * 1e-6) / 1e9, 1),
-                           "separate_sort_and_quant_us": round(u2, 3)}
-        del sx, slog, ssk, sids, sout, sssk
+                           "separate_sort_and_quant_us": round(u2, 3),
+                           "sorted_rows": {"us_per_call": round(u3, 3), "rows_written": ntpp,
+                                           "GBs": round(sb_sorted / (u3 * 1e-6) / 1e9, 1)}}
+        del sx, slog, ssk, sids, sout, sssk, srows
 
     # end to end through the public API: pinned host x in, outputs back out
     e2e_steps = min(args.steps, 2000)

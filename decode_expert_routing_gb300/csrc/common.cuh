@@ -330,6 +330,11 @@ __device__ __forceinline__ ddouble dd_div(ddouble a, ddouble b) {
     return dd_add(q, ddouble{q3, 0.0});
 }
 
+// The fp64 level with its rounding test, then double-double (see
+// sigmoid_exact): out of line, since the float-float level decides almost
+// every call.
+static __device__ __noinline__ float sigmoid_exact_wide(float l, bool slow);
+
 // sigma(l) correctly rounded to fp32, evaluated in double-double (relative
 // error far below 2^-90): ln 2 as three doubles (its value to 2^-160), n =
 // rint(y / ln2), r = y - n ln 2 (|r| <= ln2 / 2), e^r by its Taylor series to
@@ -367,16 +372,7 @@ static __device__ __noinline__ float sigmoid_dd(float l) {
     return ((S.lo > 0.0) == (nb > c)) ? nb : c;
 }
 
-// sigma(l) correctly rounded to fp32.  Fast path in fp64: the CUDA Math API
-// documents exp (double) to within 1 ulp, and the addition and the division
-// each round once, so s = sigma (1 + d) with |d| <= 2^-51.  Rounding is
-// monotone: if s (1 - 2^-48) and s (1 + 2^-48) round to the same fp32 value,
-// so does sigma (Ziv's rounding test, "Fast evaluation of elementary
-// mathematical functions with correctly rounded last bit", 1991).  Otherwise
-// (about one logit in 10^7, or every call when slow is set, a test hook) the
-// double-double evaluation decides.  Non-negative result; +0 when sigma is
-// below half the smallest fp32 subnormal.
-__device__ __forceinline__ float sigmoid_exact(float l, bool slow) {
+static __device__ __noinline__ float sigmoid_exact_wide(float l, bool slow) {
     const double e = exp(-(double)l);
     const double s = __ddiv_rn(1.0, __dadd_rn(1.0, e));
     const double m = __dmul_rn(s, 0x1p-48);
@@ -385,14 +381,111 @@ __device__ __forceinline__ float sigmoid_exact(float l, bool slow) {
     return sigmoid_dd(l);
 }
 
+// Float-float arithmetic (a value is hi + lo in fp32, |lo| <= ulp(hi) / 2):
+// the same error-free transformations and accurate addition and division as
+// the double-double ones above, on fp32 FMA pipes (which run at many times
+// the fp64 rate here); relative error of an operation a few 2^-48.
+struct ffloat {
+    float hi, lo;
+};
+__device__ __forceinline__ ffloat ff_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b), bb = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ ffloat ff_quick_two_sum(float a, float b) {  // |a| >= |b|
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ ffloat ff_two_prod(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ ffloat ff_add(ffloat a, ffloat b) {
+    ffloat s = ff_two_sum(a.hi, b.hi);
+    const ffloat t = ff_two_sum(a.lo, b.lo);
+    s.lo = __fadd_rn(s.lo, t.hi);
+    s = ff_quick_two_sum(s.hi, s.lo);
+    s.lo = __fadd_rn(s.lo, t.lo);
+    return ff_quick_two_sum(s.hi, s.lo);
+}
+__device__ __forceinline__ ffloat ff_mul(ffloat a, ffloat b) {
+    ffloat p = ff_two_prod(a.hi, b.hi);
+    p.lo = __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo));
+    return ff_quick_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ ffloat ff_div(ffloat a, ffloat b) {
+    const float q1 = __fdiv_rn(a.hi, b.hi);
+    ffloat r = ff_add(a, ff_mul(b, ffloat{-q1, 0.0f}));
+    const float q2 = __fdiv_rn(r.hi, b.hi);
+    r = ff_add(r, ff_mul(b, ffloat{-q2, 0.0f}));
+    const float q3 = __fdiv_rn(r.hi, b.hi);
+    return ff_add(ff_quick_two_sum(q1, q2), ffloat{q3, 0.0f});
+}
+
+// sigma(l) in float-float for |l| <= 69, with Ziv's rounding test: *done
+// is set when the fp32 value returned is sigma correctly rounded.  With
+// a = |l| and z = e^-a = 2^-n e^u, n = rint(a log2 e), u = n ln2 - a in
+// [-ln2/2, ln2/2] (ln 2 as three floats, good to 2^-72): e^u by its Taylor
+// series to degree 11 (truncation below 2^-47), degrees 7-11 in fp32 on
+// u.hi (below 2^-47 of the sum), degrees 6..0 as float-float Horner steps;
+// sigma = 1 / (1 + z) for l >= 0, z / (1 + z) for l < 0 (no overflow, and z
+// >= e^-69 stays a normal fp32).  The evaluation's relative error is below
+// 2^-42; sigma rounds to s.hi when both s (1 -+ 2^-39) lie inside s.hi's
+// rounding interval (the margin also covers the rounding of the test).
+__device__ __forceinline__ float sigmoid_ff(float l, bool* done) {
+    const float a = fabsf(l);
+    *done = false;
+    if (!(a <= 69.0f)) return 0.0f;
+    const float n = rintf(__fmul_rn(a, 0x1.715476p+0f));
+    ffloat u = ff_add(ff_two_prod(n, 0x1.62e430p-1f), ffloat{-a, 0.0f});
+    u = ff_add(u, ff_two_prod(n, -0x1.05c610p-29f));
+    u = ff_add(u, ffloat{__fmul_rn(n, -0x1.950d88p-54f), 0.0f});
+    float t = 0x1.ae6456p-26f;  // 1/11!, then 1/10! .. 1/7!
+    t = __fmaf_rn(t, u.hi, 0x1.27e4fcp-22f);
+    t = __fmaf_rn(t, u.hi, 0x1.71de3ap-19f);
+    t = __fmaf_rn(t, u.hi, 0x1.a01a02p-16f);
+    t = __fmaf_rn(t, u.hi, 0x1.a01a02p-13f);
+    ffloat p = {t, 0.0f};
+    p = ff_add(ffloat{0x1.6c16c2p-10f, -0x1.27d27ep-35f}, ff_mul(u, p));  // 1/6!
+    p = ff_add(ffloat{0x1.111112p-7f, -0x1.dddddep-32f}, ff_mul(u, p));   // 1/5!
+    p = ff_add(ffloat{0x1.555556p-5f, -0x1.555556p-30f}, ff_mul(u, p));   // 1/4!
+    p = ff_add(ffloat{0x1.555556p-3f, -0x1.555556p-28f}, ff_mul(u, p));   // 1/3!
+    p = ff_add(ffloat{0x1p-1f, 0.0f}, ff_mul(u, p));
+    p = ff_add(ffloat{1.0f, 0.0f}, ff_mul(u, p));
+    p = ff_add(ffloat{1.0f, 0.0f}, ff_mul(u, p));
+    const float two_mn = __uint_as_float((unsigned)(127 - (int)n) << 23);  // n in [0, 100]
+    const ffloat z = {__fmul_rn(p.hi, two_mn), __fmul_rn(p.lo, two_mn)};
+    const ffloat s = ff_div(l >= 0.0f ? ffloat{1.0f, 0.0f} : z, ff_add(ffloat{1.0f, 0.0f}, z));
+    const float c = s.hi;  // in [e^-69 / 2, 1]: normal, positive
+    const float up = __fsub_rn(__uint_as_float(__float_as_uint(c) + 1u), c);
+    const float dn = __fsub_rn(c, __uint_as_float(__float_as_uint(c) - 1u));
+    const float m = __fmul_rn(c, 0x1p-39f);
+    *done = __fadd_rn(s.lo, m) < __fmul_rn(0.5f, up) && __fsub_rn(s.lo, m) > -__fmul_rn(0.5f, dn);
+    return c;
+}
+
+// sigma(l) correctly rounded to fp32.  First the float-float evaluation with
+// its rounding test (decides all but about one logit in 10^4).  Then fp64:
+// the CUDA Math API documents exp (double) to within 1 ulp, and the addition
+// and the division each round once, so s = sigma (1 + d) with |d| <= 2^-51;
+// rounding is monotone, so if s (1 - 2^-48) and s (1 + 2^-48) round to the
+// same fp32 value, so does sigma (Ziv's rounding test, "Fast evaluation of
+// elementary mathematical functions with correctly rounded last bit", 1991).
+// Otherwise (about one logit in 10^7, or every call when slow is set, a
+// test hook) the double-double evaluation decides.  Non-negative result; +0
+// when sigma is below half the smallest fp32 subnormal.
+__device__ __forceinline__ float sigmoid_exact(float l, bool slow) {
+    if (!slow) {
+        bool done;
+        const float r = sigmoid_ff(l, &done);
+        if (done) return r;
+    }
+    return sigmoid_exact_wide(l, slow);
+}
+
 // Inverse of ordered_key (the canonical fp32 value of a key).
 __device__ __forceinline__ float key_value(unsigned key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-
-// Selection key of a sigmoid-gate candidate: exact score plus bias (fp32).
-__device__ __forceinline__ unsigned sigmoid_key_exact(float logit, float bias, bool slow) {
-    return ordered_key(__fadd_rn(sigmoid_exact(logit, slow), bias));
 }
 
 // The lowest approximate key that can still belong to the exact top-k, given

@@ -188,17 +188,18 @@ __device__ __forceinline__ unsigned long long composite(unsigned key, int id) {
     return ((unsigned long long)key << 32) | (unsigned)(0x7FFFFFFF - id);
 }
 
-// Weight of slot r = lane (lane < k holds (val) of slot r): the same
-// arithmetic as the standalone gate kernel.  row: the token's n_row logits
-// (only the full-softmax denominator reads it), in shared memory, or in
-// global memory written by other CTAs (read through L2).
+// Weight of slot r = lane (lane < k holds (val) of slot r: its logit, or
+// for the sigmoid gate its exact score): the same arithmetic as the
+// standalone gate kernel.  row: the token's n_row logits (only the
+// full-softmax denominator reads it), in shared memory, or in global memory
+// written by other CTAs (read through L2).
 __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* row, int n_row, bool global_row,
                                              float my_val) {
     const int lane = threadIdx.x & 31;
     const bool live = lane < a.topk;
     float num, den;
     if (a.scoring == 1) {
-        num = live ? sigmoid_exact(my_val, (a.flags & 8) != 0) : 0.0f;
+        num = live ? my_val : 0.0f;
         den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
         return a.renormalize ? __fdiv_rn(num, den) : num;
     }
@@ -557,7 +558,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const float* recv = reinterpret_cast<const float*>(sm + a.off_recv);
     float* rowbuf = reinterpret_cast<float*>(sm + a.off_row);
     unsigned long long* ccand = reinterpret_cast<unsigned long long*>(sm + a.off_cand);
-    float* oval = reinterpret_cast<float*>(ccand + N);
+    float* oval = reinterpret_cast<float*>(ccand + N);  // per owned row: the k winners' values
+    float* cscore = oval + tok * k;                     // sigmoid gate: exact score of candidate i
     const int grow = row0 + c * tok;  // global index of this CTA's first row
     const int plane = tok * N;        // floats between two slots of the receive buffer
     const int n0 = tid, n1 = tid + kRouteThreads;
@@ -648,11 +650,13 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         // PR adjacent lanes per candidate, each counting the beaters among
         // candidates part, part + PR, ...; a segmented reduction adds them
         const int C = s_ccount;
-        if (a.scoring == 1) {  // the candidates' exact keys (correctly rounded sigmoid + bias)
+        if (a.scoring == 1) {  // the candidates' exact scores and keys (correctly rounded sigmoid + bias)
             for (int i = tid; i < C; i += kRouteThreads) {
                 const int id = 0x7FFFFFFF - (int)(unsigned)(ccand[i] & 0xFFFFFFFFull);
                 const float b = a.bias != nullptr ? __ldg(a.bias + id) : 0.0f;
-                ccand[i] = composite(sigmoid_key_exact(rowbuf[rl * N + id - e_off], b, (a.flags & 8) != 0), id);
+                const float sc = sigmoid_exact(rowbuf[rl * N + id - e_off], (a.flags & 8) != 0);
+                cscore[i] = sc;
+                ccand[i] = composite(ordered_key(__fadd_rn(sc, b)), id);
             }
             __syncthreads();
         }
@@ -673,14 +677,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                     const uint32_t cb = smem_u32(sm + a.off_merge), sbar = map_rank(bar1, (unsigned)sorter);
                     st_async_f2(map_rank(cb + (uint32_t)((ml * k + r) * 8), (unsigned)sorter),
                                 __uint_as_float((unsigned)cn), __uint_as_float((unsigned)(cn >> 32)), sbar);
+                    const float v = a.scoring == 1 ? cscore[ci] : rowbuf[rl * N + id - e_off];
                     st_async_s32(map_rank(cb + (uint32_t)(Mq * k * 8 + (ml * k + r) * 4), (unsigned)sorter),
-                                 __float_as_int(rowbuf[rl * N + id - e_off]), sbar);
+                                 __float_as_int(v), sbar);
                 } else if (part == 0 && r < k) {
                     const int id = 0x7FFFFFFF - (int)(unsigned)(cn & 0xFFFFFFFFull);
                     st_async_s32(map_rank(smem_u32(sm + a.off_ids) + (uint32_t)((ml * k + r) * 4), (unsigned)sorter),
                                  id, map_rank(bar1, (unsigned)sorter));
                     a.ids[(int64_t)m * k + r] = id;
-                    oval[rl * k + r] = rowbuf[rl * N + id];
+                    oval[rl * k + r] = a.scoring == 1 ? cscore[ci] : rowbuf[rl * N + id];
                 }
             }
         }

@@ -189,8 +189,8 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.off_row = off;
     off = align_up(off + q.tok * N * 4, 16);
     q.off_key = off;  // (unused: the selection keys stay in registers)
-    q.off_cand = off;  // N candidate composites (one row at a time); per row k values
-    off = align_up(off + (mode == 1 ? N * 8 + q.tok * topk * 8 : 0), 16);
+    q.off_cand = off;  // N candidate composites (one row at a time); per row k values; N exact scores
+    off = align_up(off + (mode == 1 ? N * 12 + q.tok * topk * 8 : 0), 16);
     q.off_ids = off;  // every token's ids in the CTA that sorts
     off = align_up(off + M * (mode == 1 ? topk : 0) * 4, 16);
     q.off_mask = off;

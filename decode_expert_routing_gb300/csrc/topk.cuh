@@ -95,29 +95,32 @@ __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids
         key[j] = kv;
     }
     int my_id = 0;
-    float my_val = 0.0f;
+    float my_val = 0.0f;  // slot lane's logit, or for the sigmoid gate its exact score
     if (a.scoring == 1) {
         // the k-th largest approximate key bounds the candidates; they are
         // re-scored exactly, the others drop out, and the selection runs again
         unsigned probe[NPL];
+        float score[NPL];
 #pragma unroll
         for (int j = 0; j < NPL; ++j) probe[j] = key[j];
         const unsigned floor_key = sigmoid_candidate_floor(warp_select<NPL>(probe, val, a.k, &my_id, &my_val));
 #pragma unroll
         for (int j = 0; j < NPL; ++j) {
             const int id = lane + 32 * j;
-            key[j] = (id < a.N && key[j] >= floor_key)
-                         ? sigmoid_key_exact(val[j], a.bias ? __ldg(a.bias + id) : 0.0f, a.slow_sigmoid != 0)
-                         : 0u;
+            const bool cand = id < a.N && key[j] >= floor_key;
+            score[j] = cand ? sigmoid_exact(val[j], a.slow_sigmoid != 0) : 0.0f;
+            key[j] = cand ? ordered_key(__fadd_rn(score[j], a.bias ? __ldg(a.bias + id) : 0.0f)) : 0u;
         }
+        warp_select<NPL>(key, score, a.k, &my_id, &my_val);
+    } else {
+        warp_select<NPL>(key, val, a.k, &my_id, &my_val);
     }
-    warp_select<NPL>(key, val, a.k, &my_id, &my_val);
 
     // weights: lane r < k owns slot r
     const bool live = lane < a.k;
     float num = 0.0f, den;
     if (a.scoring == 1) {
-        num = live ? sigmoid_exact(my_val, a.slow_sigmoid != 0) : 0.0f;
+        num = live ? my_val : 0.0f;
         den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
     } else {
         const float lmax = __shfl_sync(kFull, my_val, 0);  // slot 0 holds the largest logit
