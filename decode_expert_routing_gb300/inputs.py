@@ -90,6 +90,7 @@ def bf16_bits_to_f32(b) -> np.ndarray:
 # Tensor tags inside one workload's key space.
 TAG_X, TAG_W, TAG_BIAS, TAG_ROWS, TAG_EDGE, TAG_VARIANT = 1, 2, 3, 4, 5, 6
 TAG_RMS, TAG_NORMW = 7, 8
+TAG_SH_CODE, TAG_SH_SCALE = 9, 10
 
 
 def normal_bf16(shape, std: float, config_id: int, tag: int, seed: int = 0) -> np.ndarray:
@@ -165,6 +166,26 @@ def norm_inputs(M: int, K: int, config_id: int = 6, seed: int = 0, variant: int 
     rstd = (1.0 / amp).astype(np.float32)
     g = normal_bf16((K,), 0.1, config_id, TAG_NORMW | vtag, seed)
     return sres, rstd, g
+
+
+def shared_expert_weights(I: int, K: int, config_id: int = 7, seed: int = 0, variant: int = 0):
+    """Synthetic MXFP8 gate/up weights of a shared expert: E4M3 codes
+    [2I, K] (rows [0, I) gate, [I, 2I) up) and E8M0 scale bytes [2I, K/32].
+
+    Codes are drawn as bit fields: a random sign, an exponent field uniform
+    in 4..11 and a mantissa uniform in 0..7 (magnitudes 2^-3 .. 30, never the
+    NaN code); scale bytes 127 + X with X uniform in -12..-8, so that a
+    weight is about 3e-5 .. 0.12, the size of the gate weights here.
+    """
+    vtag = variant << 8
+    d = draws_u64(stream_key(config_id, TAG_SH_CODE | vtag, seed), 2 * I * K)
+    sign = (d & np.uint64(1)).astype(np.uint8) << 7
+    expo = (4 + ((d >> np.uint64(8)) % np.uint64(8))).astype(np.uint8)
+    mant = ((d >> np.uint64(16)) & np.uint64(7)).astype(np.uint8)
+    codes = (sign | (expo << 3) | mant).reshape(2 * I, K)
+    ds = draws_u64(stream_key(config_id, TAG_SH_SCALE | vtag, seed), 2 * I * (K // 32))
+    scale = (127 - 12 + (ds % np.uint64(5))).astype(np.uint8).reshape(2 * I, K // 32)
+    return codes, scale
 
 
 def tied_gate(w: np.ndarray, pairs=((10, 11), (50, 51))) -> np.ndarray:

@@ -59,6 +59,11 @@ def _load():
         lib.oracle_e2m1_encode_array.argtypes = [P, i64, P]
         lib.oracle_mxfp4_quant.argtypes = [P, i64, i32, i32, P, P]
         lib.oracle_sorted_quant.argtypes = [P, i64, i32, i32, i32, P, i32, i32, P, P]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        lib.oracle_shared_gate_up.argtypes = [P, i64, P, P, i32, i32, i32, P, P]
         _lib = lib
     return _lib
 
@@ -224,3 +229,29 @@ def sorted_quant(x_bf16: np.ndarray, topk: int, sorted_token_ids: np.ndarray, nu
     s = np.empty((n, K // 32), dtype=np.uint8)
     _load().oracle_sorted_quant(_ptr(x), K, M, K, topk, _ptr(st), n, fp4, _ptr(q), _ptr(s))
     return q, s
+
+
+def e4m3_decode(code: int) -> float:
+    """Exact value of an E4M3 code (NaN for S.1111.111)."""
+    return float(_load().oracle_e4m3_decode(int(code)))
+
+
+def bf16_from_double(v: float) -> int:
+    """bf16 bits of the bf16 value nearest to the double v (ties to even)."""
+    return int(_load().oracle_bf16_from_double(float(v)))
+
+
+def shared_gate_up(x_bf16: np.ndarray, w13_codes: np.ndarray, w13_scale: np.ndarray):
+    """The shared expert's gate/up projection and SwiGLU: (act bf16 bits
+    [M, I], h float64 [M, 2I]) for x [M, K] (bf16 bits), w13 E4M3 codes
+    [2I, K] (gate rows first) and E8M0 scale bytes [2I, K/32]."""
+    x = _c(x_bf16, np.uint16)
+    w = _c(w13_codes, np.uint8)
+    sc = _c(w13_scale, np.uint8)
+    M, K = x.shape
+    R, K2 = w.shape
+    assert K == K2 and R % 2 == 0 and sc.shape == (R, K // 32)
+    act = np.empty((M, R // 2), dtype=np.uint16)
+    h = np.empty((M, R), dtype=np.float64)
+    _load().oracle_shared_gate_up(_ptr(x), K, _ptr(w), _ptr(sc), M, K, R // 2, _ptr(act), _ptr(h))
+    return act, h

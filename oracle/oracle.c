@@ -464,3 +464,73 @@ void oracle_sorted_quant(const uint16_t *x, int64_t ldx, int M, int K, int k,
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Next row: the shared expert's gate/up projection fused into the     */
+/* router launch.  sglang #46691, Summary: the router GEMV's split-K   */
+/* partials fuse with the shared expert's fp8 SwiGLU in one launch,    */
+/* and the MiniMax-M3.1 shared expert's gate_up is 1536 x 6144;        */
+/* sgl-amd-mono #56 page, Modifications: the shared expert runs on     */
+/* the checkpoint's MXFP8 values (E4M3 elements, one scale per 32      */
+/* along K) with bf16 activations.                                     */
+/* ------------------------------------------------------------------ */
+
+/* Exact value of an E4M3 code (OCP FP8: bias 7, subnormals m 2^-9, no
+ * infinities; S.1111.111 is NaN). */
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (c & 0x80) ? -v : v;
+}
+
+/* bf16 bits of the bf16 value nearest to the finite double v (ties to the
+ * even code): the significand at bf16's 8 bits, rint (round to nearest
+ * even), subnormals below 2^-126 on the fixed quantum 2^-133. */
+uint16_t oracle_bf16_from_double(double v)
+{
+    const uint16_t sign = signbit(v) ? 0x8000 : 0;
+    if (v == 0.0) return sign;
+    const double a = fabs(v);
+    int e2;
+    frexp(a, &e2);
+    int ex = e2 - 1;                       /* floor(log2 a) */
+    if (ex < -126) ex = -126;
+    const double q = rint(ldexp(a, 7 - ex)); /* units of 2^(ex - 7) */
+    const float f = (float)ldexp(q, ex - 7); /* exact: at most 9 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)((u >> 16) | sign);
+}
+
+/*
+ * READING: w13 holds 2I rows of K E4M3 codes, rows [0, I) the gate
+ * projection and rows [I, 2I) the up projection (the fused "w13" of a
+ * gated MLP), with E8M0 scale bytes w13_scale [2I, K/32]:
+ *   W[r, k] = e4m3(w13[r, k]) * 2^(w13_scale[r, k / 32] - 127)
+ *   h[m, r] = sum_k x[m, k] W[r, k]                 (fp64, k order)
+ *   act[m, i] = silu(h[m, i]) * h[m, I + i],  silu(v) = v / (1 + e^-v)
+ * act rounded once to bf16 (nearest even): the input of the shared expert's
+ * down projection.  h [M, 2I] is returned as well (the tests derive their
+ * tolerance from it).
+ */
+void oracle_shared_gate_up(const uint16_t *x, int64_t ldx, const uint8_t *w13, const uint8_t *w13_scale,
+                           int M, int K, int I, uint16_t *act, double *h)
+{
+    for (int m = 0; m < M; ++m) {
+        for (int r = 0; r < 2 * I; ++r) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const double w = ldexp(oracle_e4m3_decode(w13[(int64_t)r * K + k]),
+                                       (int)w13_scale[(int64_t)r * (K / 32) + k / 32] - 127);
+                acc += bf16_value(x[(int64_t)m * ldx + k]) * w;
+            }
+            h[(int64_t)m * 2 * I + r] = acc;
+        }
+        for (int i = 0; i < I; ++i) {
+            const double g = h[(int64_t)m * 2 * I + i], u = h[(int64_t)m * 2 * I + I + i];
+            act[(int64_t)m * I + i] = oracle_bf16_from_double(g / (1.0 + exp(-g)) * u);
+        }
+    }
+}
