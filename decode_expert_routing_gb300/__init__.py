@@ -21,7 +21,8 @@ __all__ = [
     "set_launch_flags", "get_launch_flags", "LAUNCH_PDL", "LAUNCH_TEST_STALL", "LAUNCH_LEGACY_MMA",
     "LAUNCH_TEST_SLOW_SIGMOID", "LAUNCH_CHECK_SCRATCH", "set_wait_limit_ns",
     "device_error", "router_gemv_supported", "scratch_bytes", "sort_capacity", "router_gemv", "route_topk",
-    "moe_sort", "mxfp8_quant", "moe_route_sort_quant", "router_gemv_noalloc",
+    "moe_sort", "mxfp8_quant", "moe_route_sort_quant", "router_gemv_noalloc", "shared_gate_up", "moe_route",
+    "PreparedRoute", "moe_sort_quant", "mxfp4_quant", "norm_apply", "moe_route_sort_quant_norm",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +82,7 @@ SIGNATURES = {
     "mr_moe_sort_quant": (_I, [_P, _I, _I, _I, _I, _P, _I64, _I, _I, _P, _P, _P, _I64, _P, _P, _P]),
     "mr_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "mr_device_error": (_I, [_I]),
+    "mr_shared_gate_up": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
 }
 
 
@@ -595,19 +597,55 @@ class RouteParams(ctypes.Structure):
         ("topk_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p), ("sorted_token_ids", ctypes.c_void_p),
         ("expert_ids", ctypes.c_void_p), ("num_tokens_post_padded", ctypes.c_void_p), ("capacity", ctypes.c_int64),
         ("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("scratch", ctypes.c_void_p),
-        ("scratch_bytes", ctypes.c_size_t),
+        ("scratch_bytes", ctypes.c_size_t), ("shared_w13", ctypes.c_void_p), ("shared_w13_scale", ctypes.c_void_p),
+        ("shared_inter", ctypes.c_int), ("shared_act", ctypes.c_void_p),
     ]
 
 
 def moe_route(x, w, topk: int, block: int, scoring: str = "softmax", bias=None, renormalize: bool = True,
               quant="mxfp8", rstd=None, norm_weight=None, norm: str = "gemma", out=None,
-              scratch: Scratch | None = None, stream=None):
+              scratch: Scratch | None = None, stream=None, shared=None):
     """The one-launch route with every option (mr_moe_route): quant "mxfp8",
     "mxfp4" or None; with rstd (and norm_weight) x holds the residual rows
-    and the route runs on the norm's scale.  Returns a dict of outputs."""
-    call = PreparedRoute(x, w, topk, block, scoring, bias, renormalize, quant, rstd, norm_weight, norm, out, scratch)
+    and the route runs on the norm's scale; shared = (w13 E4M3 codes [2I, K],
+    scale bytes [2I, K/32]) adds the shared expert's gate/up + SwiGLU to the
+    launch (out["shared_act"], bf16 [M, I]).  Returns a dict of outputs."""
+    call = PreparedRoute(x, w, topk, block, scoring, bias, renormalize, quant, rstd, norm_weight, norm, out, scratch,
+                         shared)
     call(stream)
     return call.out
+
+
+def _check_shared(shared, M, K, dev):
+    """(w13, w13_scale) of the shared expert: uint8 [2I, K] and [2I, K/32]; returns I."""
+    torch = _torch()
+    w13, sc = shared
+    if w13.dim() != 2 or w13.shape[1] != K or w13.shape[0] % 2:
+        raise ValueError("w13 must be [2I, K]")
+    R = w13.shape[0]
+    _check_out(w13, "w13", (R, K), torch.uint8, dev)
+    _check_out(sc, "w13_scale", (R, K // 32), torch.uint8, dev)
+    return R // 2
+
+
+def shared_gate_up(x, w13, w13_scale, out=None, stream=None):
+    """The shared expert's gate/up projection and SwiGLU (mr_shared_gate_up):
+    bf16 [M, I] = silu(x . gate^T) * (x . up^T) with MXFP8 w13 (E4M3 codes
+    [2I, K], gate rows first, E8M0 scales [2I, K/32]); M <= 16."""
+    torch = _torch()
+    dev = _one_device(x=x, w13=w13, w13_scale=w13_scale, out=out)
+    ldx = _row_major_2d(x, "x")
+    M, K = x.shape
+    I = _check_shared((w13, w13_scale), M, K, dev)
+    if out is None:
+        out = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+    _check_out(out, "out", (M, I), torch.bfloat16, dev)
+    with _launch_ctx(dev):
+        _check(_load().mr_shared_gate_up(_dev_ptr(x, "x", torch.bfloat16), ldx, _dev_ptr(w13, "w13", torch.uint8),
+                                         _dev_ptr(w13_scale, "w13_scale", torch.uint8), M, K, I,
+                                         _dev_ptr(out, "out", torch.bfloat16), _stream_on(dev, stream)),
+               "mr_shared_gate_up")
+    return out
 
 
 class PreparedRoute:
@@ -619,9 +657,9 @@ class PreparedRoute:
 
     def __init__(self, x, w, topk: int, block: int, scoring: str = "softmax", bias=None, renormalize: bool = True,
                  quant="mxfp8", rstd=None, norm_weight=None, norm: str = "gemma", out=None,
-                 scratch: Scratch | None = None):
+                 scratch: Scratch | None = None, shared=None):
         self.p, self.out, self._keep = _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd,
-                                                     norm_weight, norm, out, scratch)
+                                                     norm_weight, norm, out, scratch, shared)
         self.device = x.device
         self._ref = ctypes.byref(self.p)
         self._fn = _load().mr_moe_route
@@ -647,7 +685,8 @@ class PreparedRoute:
         return self.out
 
 
-def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, norm_weight, norm, out, scratch):
+def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, norm_weight, norm, out, scratch,
+                  shared=None):
     torch = _torch()
     ldx = _row_major_2d(x, "x")
     M, K = x.shape
@@ -693,7 +732,16 @@ def _route_params(x, w, topk, block, scoring, bias, renormalize, quant, rstd, no
         p.scale = _dev_ptr(st, "scale", torch.uint8)
     p.scratch = scratch.ptr
     p.scratch_bytes = scratch.nbytes
-    return p, out, (x, w, bias, rstd, norm_weight, scratch)
+    if shared is not None:
+        I = _check_shared(shared, M, K, dev)
+        if "shared_act" not in out:
+            out["shared_act"] = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+        _check_out(out["shared_act"], "shared_act", (M, I), torch.bfloat16, dev)
+        p.shared_w13 = _dev_ptr(shared[0], "w13", torch.uint8)
+        p.shared_w13_scale = _dev_ptr(shared[1], "w13_scale", torch.uint8)
+        p.shared_inter = I
+        p.shared_act = _dev_ptr(out["shared_act"], "shared_act", torch.bfloat16)
+    return p, out, (x, w, bias, rstd, norm_weight, scratch, shared)
 
 
 def moe_sort_quant(topk_ids, x, num_experts: int, block: int, quant: str = "mxfp8", out=None, stream=None,

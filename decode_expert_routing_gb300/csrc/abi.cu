@@ -322,6 +322,31 @@ int mr_mxfp4_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, uint8_t
 
 static int check_norm(const float* rstd, const void* norm_w, int norm_kind);
 
+// Validates the shared expert's arguments and adds its clusters to the
+// launch: a's sh_* fields, rp's cluster count and shared memory.
+static int shared_args(const uint8_t* w13, const uint8_t* w13_scale, int I, void* act, int M, int K, int cs,
+                       mr::RouteArgs* a, mr::RoutePlan* rp) {
+    if (w13 == nullptr || !aligned(w13, 8) || w13_scale == nullptr || act == nullptr || !aligned(act, 4) || I < 1)
+        return MR_ERR_INVALID_ARG;
+    mr::SharedPlan sp;
+    if (!mr::shared_plan(M, K, I, cs, &sp)) return MR_ERR_UNSUPPORTED;
+    a->sh_w = w13;
+    a->sh_scale = w13_scale;
+    a->sh_out = static_cast<uint16_t*>(act);
+    a->sh_I = I;
+    a->sh_clusters = sp.clusters;
+    a->sh_pairs = sp.pairs;
+    a->sh_wpt = sp.wpt;
+    a->sh_spw = sp.spw;
+    a->sh_units = sp.units;
+    a->sh_nslots = sp.nslots;
+    a->sh_off_x = sp.off_x;
+    a->sh_off_recv = sp.off_recv;
+    rp->sh_clusters = sp.clusters;
+    if (sp.smem > rp->smem) rp->smem = sp.smem;
+    return MR_OK;
+}
+
 // The one-launch route.  p->rstd != nullptr puts the router input on the
 // norm's scale (residual rows x rstd x norm weight, rounded to bf16 in the
 // kernel); p->quant_format picks the stage-1 activation format.
@@ -395,6 +420,11 @@ static int route_impl(const mr_route_params* p, void* stream) {
     a.rstd = p->rstd;
     a.norm_w = static_cast<const uint16_t*>(p->norm_weight);
     a.norm_gemma = p->norm_kind == MR_NORM_GEMMA ? 1 : 0;
+    if (p->shared_w13 != nullptr) {  // the shared expert's clusters join the launch
+        if ((s = shared_args(p->shared_w13, p->shared_w13_scale, p->shared_inter, p->shared_act, M, K, cs, &a,
+                             &rp)) != MR_OK)
+            return s;
+    }
     return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
 }
 
@@ -480,6 +510,38 @@ int mr_norm_apply(const void* sres, int64_t ldx, const float* rstd, const void* 
     if (xn == nullptr || !aligned(xn, 16)) return MR_ERR_INVALID_ARG;
     return cuda_status(mr::launch_norm_apply(sres, ldx, rstd, norm_weight, norm_kind == MR_NORM_GEMMA ? 1 : 0, M,
                                              K, xn, as_stream(stream)));
+}
+
+int mr_shared_gate_up(const void* x, int64_t ldx, const uint8_t* w13, const uint8_t* w13_scale, int M, int K,
+                      int I, void* act, void* stream) {
+    int s = check_x(x, ldx, M, K);
+    if (s != MR_OK) return s;
+    if (K % MR_GEMV_K_MULTIPLE != 0 || M > mr::kShMaxM) return MR_ERR_UNSUPPORTED;
+    const int cs = mr::route_cluster_size();
+    mr::RoutePlan rp{};
+    rp.cs = cs;
+    rp.kc = K / cs;
+    rp.clusters = 0;
+    rp.ng = 1;
+    rp.nl = 0;
+    mr::RouteArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.ldx = ldx;
+    a.M = M;
+    a.K = K;
+    a.cs = cs;
+    a.cs_shift = mr::ilog2_exact(cs);
+    a.kc = K / cs;
+    a.clusters = 0;
+    a.flags = mr::launch_flags();
+    a.wait_ns = mr::wait_limit_ns();
+    if ((s = shared_args(w13, w13_scale, I, act, M, K, cs, &a, &rp)) != MR_OK) return s;
+    mr::SharedPlan sp;
+    mr::shared_plan(M, K, I, cs, &sp);
+    a.tok = sp.tok;
+    a.tok_shift = mr::ilog2_exact(sp.tok);
+    a.xpitch = sp.xpitch;
+    return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
 }
 
 }  // extern "C"

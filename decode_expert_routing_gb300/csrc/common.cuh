@@ -197,6 +197,24 @@ __device__ __forceinline__ uint2 mx_quant_quad(uint4 v, unsigned* scale_byte) {
     return make_uint2(out[0], out[1]);
 }
 
+// Two E4M3 codes (lower k in the low byte) -> two bf16 values (lower k in
+// the low half), exactly: every E4M3 value is a normal f16 or zero (the
+// conversion to f16 is exact), and its three mantissa bits sit at the top of
+// the f16 mantissa, so the bf16 code is the f16 magnitude shifted right by 3
+// with the exponent rebiased by 127 - 15 = 112; zeros stay zero.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    const uint32_t h = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
+    const uint32_t mag = h & 0x7FFF7FFFu;
+    const uint32_t sh = (mag >> 3) & 0x0FFF0FFFu;
+    return (h & 0x80008000u) | (sh + (0x38003800u & __vcmpne2(mag, 0u)));
+}
+
+// 2^(byte - 127) as fp32 for an E8M0 scale byte < 255 (byte 0: the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(unsigned byte) {
+    return byte != 0u ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
 // ---------------------------------------------------------------- MXFP4
 
 // Eight fp32 values -> eight E2M1 codes (round to nearest even, saturating

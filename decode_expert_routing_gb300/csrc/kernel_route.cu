@@ -287,6 +287,142 @@ __device__ __forceinline__ void row_weights(const RouteArgs& a, const float* row
     }
 }
 
+// Shared expert's gate/up projection and SwiGLU, run by the clusters after
+// the route's in the same launch (sglang #46691 Summary: the router fused
+// with the shared expert's fp8 SwiGLU; sgl-amd-mono #56: the shared expert
+// on its MXFP8 values with bf16 activations).  Cluster sc takes pairs
+// [sc P, (sc + 1) P): local rows [0, P) are gate rows pair0 + i, rows
+// [P, 2P) the up rows I + pair0 + i.  CTA c takes the K slice c for all of
+// them, as the route does for the experts: warps run m16n8k16 bf16 MMAs on
+// (8-row tile, k-part) units, the E4M3 weights converted to bf16 exactly
+// and each 32-wide k step (one MX block) scaled by its E8M0 factor after
+// its two MMAs (acc += block sum * 2^X, one fused multiply-add).  Partial
+// sums go by st.async to the CTA that owns the token row, which adds the
+// split-K partials in a fixed order and writes bf16(silu(gate) * up).
+static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int sc) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    __shared__ __align__(8) unsigned long long s_shbar;
+    __shared__ int s_shok;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+    const int c = (int)cluster_rank();
+    const int Mq = a.M, K = a.K, kc = a.kc, P = a.sh_pairs, R = 2 * P, I = a.sh_I;
+    const int tok = a.tok, wpt = a.sh_wpt, spw = a.sh_spw, nslots = a.sh_nslots;
+    const int my_rows = max(0, min(tok, Mq - c * tok));
+    const int pair0 = sc * P;
+    const uint32_t bar = smem_u32(&s_shbar);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const unsigned stall = (a.flags & 2) ? 16u : 0u;  // test hook: bytes that never come
+        if (my_rows > 0) mbar_expect_tx(bar, (unsigned)(my_rows * nslots * R * 4) + stall);
+    }
+    cluster_arrive_relaxed();
+    pdl_trigger();
+    const int64_t kslice = (int64_t)c * kc;
+    const int K32 = K / 32;
+    // this warp's units u = warp, warp + 16, ...: tile j = u / wpt, part p = u % wpt
+    // weights and scales are parameters: loaded before the dependency wait
+    uint2 wv[kShUnitsPerWarp][kRouteSpwMax];
+    uint32_t sv[kShUnitsPerWarp][kRouteSpwMax];  // scale bytes of rows 2t, 2t + 1 of the tile
+#pragma unroll
+    for (int uu = 0; uu < kShUnitsPerWarp; ++uu) {
+        const int u = warp + kRouteWarps * uu;
+        const bool ok = u < a.sh_units;
+        const int j = ok ? u / wpt : 0, p = ok ? u - j * wpt : 0;
+        const int lr = j * 8 + g, lc0 = j * 8 + 2 * t;
+        const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
+        const int64_t gc0 = lc0 < P ? pair0 + lc0 : I + pair0 + (lc0 - P);  // rows 2t, 2t + 1 stay in one half
+        const uint8_t* wp = a.sh_w + gr * K + kslice + (int64_t)p * spw * 32 + 8 * t;
+        const uint8_t* sp = a.sh_scale + gc0 * K32 + kslice / 32 + (int64_t)p * spw;
+#pragma unroll
+        for (int s = 0; s < kRouteSpwMax; ++s) {
+            const bool live = ok && s < spw;
+            wv[uu][s] = live ? __ldg(reinterpret_cast<const uint2*>(wp + s * 32)) : make_uint2(0u, 0u);
+            sv[uu][s] = live ? ((uint32_t)__ldg(sp + s) | ((uint32_t)__ldg(sp + K32 + s) << 8)) : 0u;
+        }
+    }
+    pdl_wait();
+    // the x slice -> shared memory (on the norm's scale when rstd is given)
+    unsigned char* xs = sm + a.sh_off_x;
+    const int vpr = kc / 8;
+    for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
+        const int r = v / vpr, cv = v - r * vpr;
+        uint4 d = ld_ro_v4(a.x + (int64_t)r * a.ldx + kslice + cv * 8);
+        if (a.rstd != nullptr)
+            d = norm_chunk(d, ld_ro_v4(a.norm_w + kslice + cv * 8), __ldg(a.rstd + r), a.norm_gemma != 0);
+        *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
+    }
+    __syncthreads();
+    cluster_wait();  // every CTA of the cluster is running: DSMEM is live
+    const uint32_t recv_local = smem_u32(sm + a.sh_off_recv);
+    uint32_t owner_bar[2] = {0u, 0u};
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        if (g + 8 * h < Mq) owner_bar[h] = map_rank(bar, (unsigned)((g + 8 * h) >> a.tok_shift));
+#pragma unroll
+    for (int uu = 0; uu < kShUnitsPerWarp; ++uu) {
+        const int u = warp + kRouteWarps * uu;
+        if (u >= a.sh_units) break;
+        const int j = u / wpt, p = u - j * wpt;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int s = 0; s < kRouteSpwMax; ++s) {
+            if (s < spw) {
+                const int kk = (p * spw + s) * 32 + 8 * t;
+                const uint4 xa = g < Mq ? lds128(xs + g * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 xb = g + 8 < Mq ? lds128(xs + (g + 8) * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t b0 = e4m3x2_to_bf16x2(wv[uu][s].x), b1 = e4m3x2_to_bf16x2(wv[uu][s].x >> 16);
+                const uint32_t b2 = e4m3x2_to_bf16x2(wv[uu][s].y), b3 = e4m3x2_to_bf16x2(wv[uu][s].y >> 16);
+                float blk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                mma_bf16_m16n8k16(blk, xa.x, xb.x, xa.y, xb.y, b0, b1);
+                mma_bf16_m16n8k16(blk, xa.z, xb.z, xa.w, xb.w, b2, b3);
+                const float s0 = e8m0_value(sv[uu][s] & 0xFFu), s1 = e8m0_value(sv[uu][s] >> 8);
+                acc[0] = __fmaf_rn(blk[0], s0, acc[0]);
+                acc[1] = __fmaf_rn(blk[1], s1, acc[1]);
+                acc[2] = __fmaf_rn(blk[2], s0, acc[2]);
+                acc[3] = __fmaf_rn(blk[3], s1, acc[3]);
+            }
+        }
+        const int col = j * 8 + 2 * t, slot = c * wpt + p;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = g + 8 * h;
+            if (r < Mq) {
+                const int own = r >> a.tok_shift, rl = r & (tok - 1);
+                const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * R + col) * 4);
+                st_async_f2(map_rank(la, (unsigned)own), acc[2 * h], acc[2 * h + 1], owner_bar[h]);
+            }
+        }
+    }
+    if (my_rows == 0) return;
+    if (!cta_wait_bytes(bar, a.wait_ns, &s_shok)) return;
+    // owner: pair i of each owned row; partials added in slot order
+    const float* recv = reinterpret_cast<const float*>(sm + a.sh_off_recv);
+    const int plane = tok * R;
+    for (int idx = tid; idx < my_rows * P; idx += kRouteThreads) {
+        const int rl = idx / P, i = idx - rl * P;
+        const float* pg = recv + rl * R + i;
+        float gs = 0.0f, us = 0.0f;
+        for (int sl = 0; sl < nslots; sl += 8) {
+            float vg[8], vu[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                vg[q] = pg[(sl + q) * plane];
+                vu[q] = pg[(sl + q) * plane + P];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                gs = __fadd_rn(gs, vg[q]);
+                us = __fadd_rn(us, vu[q]);
+            }
+        }
+        const float act = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs))), us);
+        uint16_t b;
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(act));
+        a.sh_out[(int64_t)(c * tok + rl) * I + pair0 + i] = b;
+    }
+}
+
 // HALF: at most 8 token rows (half of the m16 tile live).  TC: the router
 // GEMV on tcgen05 (GEMV alone, 64-row clusters) instead of mma.sync.
 // GROUPS: the experts are split into a.ng groups, one cluster per group.
@@ -300,6 +436,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     __shared__ __align__(16) unsigned s_wmin[kRouteWarps];  // gate: per warp, smallest group maximum
     __shared__ int s_ccount;                                  // gate: candidates so far
     __shared__ __align__(16) int s_wtot[2 * kRouteWarps];     // sort: blocks per warp (experts t, t + 512)
+    if ((int)(blockIdx.x >> a.cs_shift) >= a.clusters) {  // the shared expert's clusters
+        shared_gate_up_cta(a, (int)(blockIdx.x >> a.cs_shift) - a.clusters);
+        return;
+    }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int c = (int)cluster_rank();
@@ -1000,7 +1140,7 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.cs * p.clusters);
+    cfg.gridDim = dim3(p.cs * (p.clusters + p.sh_clusters));
     cfg.blockDim = dim3(kRouteThreads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = st;

@@ -80,6 +80,14 @@ struct RouteArgs {
     const uint16_t* norm_w;
     int norm_gemma;
     int quant_fp4;  // q holds MXFP4 ([M, K/2]) instead of MXFP8 ([M, K])
+    // shared expert's gate/up projection + SwiGLU in the same launch
+    // (sh_clusters > 0): the clusters after the route's each take sh_pairs
+    // (gate row, up row) pairs of w13 (E4M3 [2 sh_I, K], rows [0, sh_I) gate)
+    // with E8M0 scales [2 sh_I, K/32]; act = silu(gate) * up -> bf16 [M, sh_I]
+    const uint8_t* sh_w;
+    const uint8_t* sh_scale;
+    uint16_t* sh_out;
+    int sh_I, sh_clusters, sh_pairs, sh_wpt, sh_spw, sh_units, sh_nslots, sh_off_x, sh_off_recv;
 };
 
 // Multiplier for division by d (1 <= d <= 2^11) of dividends below 2^21:
@@ -95,6 +103,7 @@ inline int ilog2_exact(int v) {
 
 struct RoutePlan {
     int cs, kc, spw, wpt, units, tok, xpitch, clusters, rpc;
+    int sh_clusters;  // shared-expert clusters after the route's (0: none)
     int ng, nl, off_merge;  // expert groups, experts per group, merge buffers
     int tc, nmma, tmem_cols, nslots, off_a, off_b, off_dst;
     bool half;
@@ -216,6 +225,61 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     }
     q.smem = off;
     if (q.smem > (q.tc ? kRouteSmemMaxTc : kRouteSmemMax)) return false;
+    *p = q;
+    return true;
+}
+
+// Shared expert's gate/up projection in the route launch (M <= 16 token rows,
+// one cluster of cs CTAs per group of pairs, CTA c the K slice c as the
+// route's): at most kShUnitsPerWarp (8-row tile, k-part) units per warp.
+constexpr int kShUnitsPerWarp = 3;
+constexpr int kShMaxClusters = 16;  // (clusters never wait on each other: more than fit at once is fine)
+constexpr int kShMaxM = 16;
+
+struct SharedPlan {
+    int clusters, pairs, wpt, spw, units, nslots, tok, xpitch, off_x, off_recv, smem;
+};
+
+// Returns false when (M, K, I) is outside what the shared-expert CTAs cover.
+inline bool shared_plan(int M, int K, int I, int cs, SharedPlan* p) {
+    if (M < 1 || M > kShMaxM || I < 8 || I % 8 != 0 || K < 32 * cs || K % (32 * cs) != 0) return false;
+    SharedPlan q{};
+    const int kc = K / cs, S = kc / 32;
+    int w = 0;
+    for (int d = 1; d <= kRouteWarps && d <= S; d *= 2)
+        if (S % d == 0 && S / d <= kRouteSpwMax) {
+            w = d;
+            break;
+        }
+    if (w == 0 || (cs * w) % 8 != 0) return false;
+    // as many clusters as divide the 8-pair groups, up to kShMaxClusters,
+    // with at most kShUnitsPerWarp units per warp
+    int sc = 0;
+    for (int d = kShMaxClusters; d >= 1; --d) {
+        if ((I / 8) % d != 0) continue;
+        const int units = (2 * (I / d) / 8) * w;
+        if (units <= kShUnitsPerWarp * kRouteWarps) {
+            sc = d;
+            break;
+        }
+    }
+    if (sc == 0) return false;
+    q.clusters = sc;
+    q.pairs = I / sc;
+    q.wpt = w;
+    q.spw = S / w;
+    q.units = (2 * q.pairs / 8) * w;
+    q.nslots = cs * w;
+    q.tok = 1;
+    while (q.tok * cs < M) q.tok *= 2;
+    q.xpitch = kc * 2 + (((kc * 2) % 128 == 0) ? 64 : 0);
+    int off = 0;
+    q.off_x = off;
+    off = align_up(off + M * q.xpitch, 16);
+    q.off_recv = off;
+    off = align_up(off + q.nslots * q.tok * 2 * q.pairs * 4, 16);
+    q.smem = off;
+    if (q.smem > kRouteSmemMax) return false;
     *p = q;
     return true;
 }

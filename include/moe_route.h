@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MR_ABI_VERSION 1
+#define MR_ABI_VERSION 2
 
 /* Bytes at the start of every scratch buffer that hold the launch counters. */
 #define MR_SCRATCH_COUNTER_BYTES 32768
@@ -347,10 +347,18 @@ int mr_mxfp4_quant(const void *x, int64_t ldx, int M, int K, uint8_t *q,
  *  - quant_format: MR_QUANT_NONE (q and scale ignored), MR_QUANT_MXFP8
  *    (q [M, K]) or MR_QUANT_MXFP4 (q [M, K/2], as mr_mxfp4_quant); q must be
  *    8-byte aligned.  An unknown format returns MR_ERR_INVALID_ARG.
+ *  - shared_w13 != NULL: the shared expert's gate/up projection and SwiGLU
+ *    run in the same launch, on extra clusters beside the route's (sglang
+ *    #46691 Summary: the router fused with the shared expert's fp8 SwiGLU,
+ *    the one-launch decode router running the shared expert's gate_up),
+ *    writing shared_act exactly as mr_shared_gate_up (on the norm's scale
+ *    too when rstd != NULL: the shared expert reads the norm's output).
+ *    M <= 16, else MR_ERR_UNSUPPORTED.
  * Every output is bitwise equal to the unfused calls on the same input
  * (mr_norm_apply first when rstd != NULL; mr_mxfp8_quant or mr_mxfp4_quant
- * for the quant).  The caller owns the struct; it is read during the call
- * only.
+ * for the quant; mr_shared_gate_up for the shared expert).  The caller owns
+ * the struct; it is read during the call only.  (ABI version 2 appended the
+ * shared_* fields.)
  */
 typedef struct mr_route_params {
     const void *x;               /* bf16 [M, ldx] */
@@ -375,6 +383,12 @@ typedef struct mr_route_params {
     uint8_t *scale;              /* uint8 [M, K/32] */
     void *scratch;
     size_t scratch_bytes;
+    /* the shared expert's gate/up projection + SwiGLU in the same launch
+     * (shared_w13 == NULL: none); see mr_shared_gate_up.  M <= 16. */
+    const uint8_t *shared_w13;        /* E4M3 [2 * shared_inter, K] */
+    const uint8_t *shared_w13_scale;  /* E8M0 [2 * shared_inter, K / 32] */
+    int shared_inter;                 /* I */
+    void *shared_act;                 /* bf16 [M, shared_inter] */
 } mr_route_params;
 
 int mr_moe_route(const mr_route_params *params, void *stream);
@@ -417,6 +431,31 @@ int mr_moe_route_sort_quant_norm(const void *sres, int64_t ldx, const float *rst
  */
 int mr_norm_apply(const void *sres, int64_t ldx, const float *rstd, const void *norm_weight,
                   int norm_kind, int M, int K, void *xn, void *stream);
+
+/*
+ * The shared expert's gate/up projection and SwiGLU [sglang #46691 Summary:
+ * the router GEMV fused with the shared expert's fp8 SwiGLU, the MiniMax-M3.1
+ * shared expert's 1536 x 6144 gate_up; sgl-amd-mono #56 page, Modifications:
+ * the shared expert on its MXFP8 values with bf16 activations]:
+ *   W[r, k]   = E4M3(w13[r, k]) * 2^(w13_scale[r, k / 32] - 127)
+ *   h[m, r]   = sum_k x[m, k] W[r, k]          (fp32 accumulation)
+ *   act[m, i] = silu(h[m, i]) * h[m, I + i],   silu(v) = v / (1 + e^-v)
+ * rounded to bf16 (nearest even).  x: bf16 [M, ldx]; w13: E4M3 codes
+ * [2I, K] row-major, rows [0, I) the gate projection and [I, 2I) the up
+ * projection (8-byte aligned); w13_scale: E8M0 bytes [2I, K / 32] (below
+ * 255, NaN); act: bf16 [M, I] (4-byte aligned).  Each 32-wide block of a
+ * row is summed in fp32 (products exact) and scaled by its factor with one
+ * fused multiply-add; the K range is split over the CTAs of a cluster as in
+ * the router GEMV and the partial sums are added in a fixed order, so the
+ * result is deterministic.  The output keeps finite values when the
+ * weights' scale bytes are at most 246 (|W| below 2^128).  1 <= M <= 16,
+ * K % 512 == 0, I % 8 == 0, and I up to 1536 at K = 6144 (at most 48 row
+ * tiles x k-parts per CTA over at most 16 clusters), else
+ * MR_ERR_UNSUPPORTED.  One launch.  In mr_moe_route (mr_route_params.shared_w13) the same work
+ * joins the routing launch.
+ */
+int mr_shared_gate_up(const void *x, int64_t ldx, const uint8_t *w13, const uint8_t *w13_scale, int M, int K,
+                      int I, void *act, void *stream);
 
 /* Bytes of the library-owned scratch of mr_router_gemv_noalloc (8 MiB). */
 #define MR_NOALLOC_SCRATCH_BYTES 8388608

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mr_abi_version() == 1
+    assert lib.mr_abi_version() == 2
     for s in range(7):
         assert lib.mr_status_string(s).startswith(b"MR_")
     assert b"SCRATCH_DIRTY" in lib.mr_status_string(mr.MR_ERR_SCRATCH_DIRTY)
@@ -350,3 +350,26 @@ def test_binding_refuses_bad_outputs_and_mixed_devices():
                                                 _FakeCuda((4, 8), u8)))
     with pytest.raises(ValueError, match="out"):
         mr.norm_apply(x, _FakeCuda((4,), f32), _FakeCuda((512,), bf), out=_FakeCuda((4, 256), bf))
+
+
+def test_shared_gate_up_validation(lib):
+    """Host checks of the shared expert's entry point (nothing launches)."""
+    fake = ctypes.c_void_p(0x1000)
+    P = ctypes.c_void_p
+    # M above 16, K not a multiple of 512, I not a multiple of 8
+    assert lib.mr_shared_gate_up(fake, 6144, fake, fake, 17, 6144, 768, fake, None) == mr.MR_ERR_UNSUPPORTED
+    assert lib.mr_shared_gate_up(fake, 6144, fake, fake, 4, 6000, 768, fake, None) == mr.MR_ERR_UNSUPPORTED
+    assert lib.mr_shared_gate_up(fake, 6144, fake, fake, 4, 6144, 100, fake, None) == mr.MR_ERR_UNSUPPORTED
+    # null or misaligned weights / output
+    assert lib.mr_shared_gate_up(fake, 6144, None, fake, 4, 6144, 768, fake, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_shared_gate_up(fake, 6144, P(0x1004), fake, 4, 6144, 768, fake, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_shared_gate_up(fake, 6144, fake, None, 4, 6144, 768, fake, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_shared_gate_up(fake, 6144, fake, fake, 4, 6144, 768, P(0x1002), None) == mr.MR_ERR_INVALID_ARG
+    # the route with a shared expert: more than 16 tokens is outside its cover
+    p = mr.RouteParams()
+    p.x, p.ldx, p.w, p.M, p.N, p.K, p.topk, p.block = fake, 6144, fake, 32, 128, 6144, 8, 16
+    for f in ("logits", "topk_ids", "topk_weights", "sorted_token_ids", "expert_ids", "num_tokens_post_padded",
+              "scratch", "shared_w13", "shared_w13_scale", "shared_act"):
+        setattr(p, f, fake)
+    p.capacity, p.scratch_bytes, p.shared_inter = 4096, 1 << 20, 768
+    assert lib.mr_moe_route(ctypes.byref(p), None) == mr.MR_ERR_UNSUPPORTED

@@ -104,3 +104,56 @@ def test_expert_groups_keep_the_split_k_of_the_unsplit_plan(plans):
         if mode == 0 and route is not None and not p["tc"]:
             assert (p["wpt"], p["spw"], p["nslots"]) == (route["wpt"], route["spw"], route["nslots"])
     assert n > 100
+
+
+SHARED_PROBE = r"""
+#include <cstdio>
+#include <initializer_list>
+#include "route_plan.h"
+int main() {
+    for (int cs : {8, 16})
+    for (int M = 1; M <= 17; ++M)
+    for (int K : {512, 3584, 6144, 7168})
+    for (int I : {8, 64, 96, 256, 768, 1024, 1536, 2048, 100}) {
+        mr::SharedPlan p;
+        if (!mr::shared_plan(M, K, I, cs, &p)) { printf("none %d %d %d %d\n", cs, M, K, I); continue; }
+        printf("plan %d %d %d %d %d %d %d %d %d %d %d %d\n", cs, M, K, I, p.clusters, p.pairs, p.wpt, p.spw,
+               p.units, p.nslots, p.tok, p.smem);
+    }
+}
+"""
+
+
+def test_shared_plan_invariants(tmp_path):
+    """Every shared-expert plan keeps what the kernel's indexing relies on:
+    pairs in whole 8-row tiles split evenly over the clusters, at most three
+    units per warp, the K slice covered by the parts, the owners' token rows,
+    split-K slots in groups of 8, shared memory within the route kernel's."""
+    src = tmp_path / "probe.cpp"
+    src.write_text(SHARED_PROBE)
+    exe = tmp_path / "probe"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", os.path.join(ROOT, "decode_expert_routing_gb300", "csrc"),
+                    "-o", str(exe), str(src)], check=True)
+    lines = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()
+    n = 0
+    for line in lines:
+        f = line.split()
+        cs, M, K, I = (int(v) for v in f[1:5])
+        S = K // cs // 32 if K % (32 * cs) == 0 else 0
+        w = next((d for d in (1, 2, 4, 8, 16) if S and S % d == 0 and S // d <= 8), 0)
+        fits = [d for d in range(1, 17) if I % 8 == 0 and (I // 8) % d == 0 and (2 * (I // d) // 8) * w <= 48]
+        if f[0] == "none":
+            assert M > 16 or I % 8 or not S or not w or not fits
+            continue
+        sc, P, w2, spw, units, nslots, tok, smem = (int(v) for v in f[5:])
+        n += 1
+        assert w2 == w and sc == max(fits)
+        assert sc * P == I and P % 8 == 0 and 1 <= sc <= 16
+        assert units == (2 * P // 8) * w and units <= 3 * 16
+        assert w * spw * 32 * cs == K and spw <= 8 and nslots == cs * w and nslots % 8 == 0
+        assert tok * cs >= M and tok & (tok - 1) == 0
+        assert smem <= 200 * 1024
+    assert n > 300
+    have = {tuple(int(v) for v in line.split()[1:5]) for line in lines if line.startswith("plan")}
+    for M in range(1, 17):
+        assert (16, M, 6144, 768) in have and (16, M, 6144, 1536) in have and (8, M, 6144, 768) in have
