@@ -569,6 +569,51 @@ def run_ours(args):
         del k3x, k3o
     del k3w, k3scratch
 
+    # the shared expert's gate/up + SwiGLU (MXFP8 w13 [1536, 6144], the
+    # MiniMax-M3.1 shape) fused into the route's launch, against the route
+    # and a separate shared-expert launch; and the shared expert alone (its
+    # 9.7 MB weight stream against the HBM roofline).  16 rotating copies of
+    # w13 (151 MB) keep it out of L2.
+    shared = {}
+    SH_I, SH_COPIES = 768, 16
+    sh_host = [inputs.shared_expert_weights(SH_I, K_HID, variant=v) for v in range(2)]
+    sh_w = [torch.from_numpy(sh_host[v % 2][0]).to(dev) for v in range(SH_COPIES)]
+    sh_s = [torch.from_numpy(sh_host[v % 2][1]).to(dev) for v in range(SH_COPIES)]
+    sh_bytes_w = 2 * SH_I * K_HID + 2 * SH_I * (K_HID // 32)
+    for M in (1, 8, 16):
+        o = outs[M]
+        sh_out = torch.empty((M, SH_I), dtype=torch.bfloat16, device=dev)
+        o_sh = dict(o, shared_act=sh_out)
+        calls = [mr.PreparedRoute(xs[M][r % SLOTS], ws[M][r % SLOTS], TOPK, BLOCK, out=o_sh, scratch=scratch,
+                                  shared=(sh_w[r % SH_COPIES], sh_s[r % SH_COPIES])) for r in range(32)]
+        plain = [mr.PreparedRoute(xs[M][r % SLOTS], ws[M][r % SLOTS], TOPK, BLOCK, out=o, scratch=scratch)
+                 for r in range(32)]
+
+        def body_fused(calls=calls):
+            for c_ in calls:
+                c_(sp)
+
+        def body_sep(M=M, plain=plain, sh_out=sh_out):
+            for r, c_ in enumerate(plain):
+                c_(sp)
+                mr.shared_gate_up(xs[M][r % SLOTS], sh_w[r % SH_COPIES], sh_s[r % SH_COPIES], out=sh_out)
+
+        def body_alone(M=M, sh_out=sh_out):
+            for r in range(32):
+                mr.shared_gate_up(xs[M][r % SLOTS], sh_w[r % SH_COPIES], sh_s[r % SH_COPIES], out=sh_out)
+        with torch.cuda.stream(stream):
+            body_fused()
+            body_sep()
+            body_alone()
+        uf, us_, ua = graph_us(body_fused, 32), graph_us(body_sep, 32), graph_us(body_alone, 32)
+        ab = sh_bytes_w + 2 * M * K_HID + 2 * M * SH_I
+        shared[str(M)] = {"one_launch_us": round(uf, 3), "route_then_shared_us": round(us_, 3),
+                          "shared_alone_us": round(ua, 3), "shared_alone_GBs": round(ab / (ua * 1e-6) / 1e9, 1),
+                          "shared_alone_frac_of_peak": round(ab / (ua * 1e-6) / 1e9 / peak, 4),
+                          "one_launch_GBs": round((ab + algorithmic_bytes(M)) / (uf * 1e-6) / 1e9, 1)}
+        del calls, plain, sh_out
+    del sh_w, sh_s
+
     # the route on the norm's scale (residual rows, per-token rstd, Gemma
     # norm weight normalised inside the route kernel) against the norm's
     # output written out by its own launch and routed after it
@@ -761,6 +806,7 @@ def run_ours(args):
             "split_k_gemv_rows_128_512": split_k,
             "route_896_experts_sigmoid_top16": k3,
             "route_on_norm_scale_gemma": normed,
+            "route_with_shared_expert_1536x6144_mxfp8": shared,
             "prefill_4096_rows": prefill,
             "sort_quant_one_launch_block16": sortq,
             "roofline": roofline,

@@ -266,25 +266,35 @@ __global__ void __launch_bounds__(kQuantThreads) mx_quant_kernel(const uint16_t*
 // assignments (the zero rows of the padding by the CTA of their expert).
 
 // hist[e] += number of ids[beg, end) equal to e (ids outside [0, N) are
-// skipped): each warp takes 32-id chunks, kPSortUnroll of them with their
-// loads in flight, and adds the peers of a chunk with one shared atomic.
-constexpr int kPSortUnroll = 4;
-__device__ __forceinline__ void psort_hist(const int32_t* ids, int beg, int end, int N, int* hist) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int base = beg + warp * 32 * kPSortUnroll; base < end; base += nw * 32 * kPSortUnroll) {
-        int e[kPSortUnroll];
+// skipped).  Each warp counts into its own row of warp_hist ([warps][N],
+// zero on entry and on return) with shared atomics, kLoadBatch coalesced
+// loads in flight per thread; the rows are then added into hist.  (Warp-wide
+// peer matching per 32 ids ran on a low-throughput pipe and made the count
+// the long pole of the sort.)
+__device__ __forceinline__ void psort_hist(const int32_t* ids, int beg, int end, int N, int* warp_hist, int* hist) {
+    const int tid = threadIdx.x, nthr = blockDim.x, nw = nthr >> 5;
+    int* my = warp_hist + (tid >> 5) * N;
+    for (int base = beg + tid; base < end; base += nthr * kLoadBatch) {
+        int e[kLoadBatch];
 #pragma unroll
-        for (int u = 0; u < kPSortUnroll; ++u) {
-            const int i = base + u * 32 + lane;
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int i = base + u * nthr;
             e[u] = i < end ? __ldg(ids + i) : -1;
         }
 #pragma unroll
-        for (int u = 0; u < kPSortUnroll; ++u) {
-            const bool valid = e[u] >= 0 && e[u] < N;
-            const unsigned peers = __match_any_sync(kFull, valid ? e[u] : (int)(0x40000000u | (unsigned)lane));
-            if (valid && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[e[u]], __popc(peers));
-        }
+        for (int u = 0; u < kLoadBatch; ++u)
+            if (e[u] >= 0 && e[u] < N) atomicAdd(&my[e[u]], 1);
     }
+    __syncthreads();
+    for (int e = tid; e < N; e += nthr) {
+        int sum = 0;
+        for (int w = 0; w < nw; ++w) {
+            sum += warp_hist[w * N + e];
+            warp_hist[w * N + e] = 0;
+        }
+        hist[e] += sum;
+    }
+    __syncthreads();
 }
 
 // MX quantisation of rows x[0, rows) written to the sorted positions of their
@@ -369,11 +379,11 @@ __global__ void __launch_bounds__(kSortQuantThreads) psort_kernel(PSortArgs a) {
         pre[e] = 0;
         tot[e] = 0;
     }
+    for (int i = tid; i < nw * N; i += nthr) rs.wcnt[i] = 0;  // the per-warp counts of psort_hist
     for (int i = tid; i < n_own; i += nthr) own_ids[i] = __ldg(a.s.ids + f0 + i);
     __syncthreads();
-    psort_hist(a.s.ids, 0, f0, N, pre);
-    psort_hist(a.s.ids, f0, n_all, N, tot);
-    __syncthreads();
+    psort_hist(a.s.ids, 0, f0, N, rs.wcnt, pre);
+    psort_hist(a.s.ids, f0, n_all, N, rs.wcnt, tot);
     for (int e = tid; e < N; e += nthr) {
         const int t = tot[e] + pre[e];
         tot[e] = t;
