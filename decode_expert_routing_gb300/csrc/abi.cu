@@ -326,10 +326,11 @@ static int check_norm(const float* rstd, const void* norm_w, int norm_kind);
 // launch: a's sh_* fields, rp's cluster count and shared memory.
 static int shared_args(const uint8_t* w13, const uint8_t* w13_scale, int I, void* act, int M, int K, int cs,
                        mr::RouteArgs* a, mr::RoutePlan* rp) {
-    if (w13 == nullptr || !aligned(w13, 8) || w13_scale == nullptr || act == nullptr || !aligned(act, 4) || I < 1)
+    if (w13 == nullptr || !aligned(w13, 16) || w13_scale == nullptr || act == nullptr || !aligned(act, 4) || I < 1)
         return MR_ERR_INVALID_ARG;
     mr::SharedPlan sp;
-    if (!mr::shared_plan(M, K, I, cs, &sp)) return MR_ERR_UNSUPPORTED;
+    const int fit = mr::route_max_clusters() - rp->clusters;
+    if (!mr::shared_plan(M, K, I, cs, &sp, fit > 1 ? fit : 1)) return MR_ERR_UNSUPPORTED;
     a->sh_w = w13;
     a->sh_scale = w13_scale;
     a->sh_out = static_cast<uint16_t*>(act);
@@ -342,6 +343,9 @@ static int shared_args(const uint8_t* w13, const uint8_t* w13_scale, int I, void
     a->sh_nslots = sp.nslots;
     a->sh_off_x = sp.off_x;
     a->sh_off_recv = sp.off_recv;
+    a->sh_off_w = sp.off_w;
+    a->sh_off_s = sp.off_s;
+    a->sh_spitch = sp.spitch;
     rp->sh_clusters = sp.clusters;
     if (sp.smem > rp->smem) rp->smem = sp.smem;
     return MR_OK;
@@ -537,7 +541,7 @@ int mr_shared_gate_up(const void* x, int64_t ldx, const uint8_t* w13, const uint
     a.wait_ns = mr::wait_limit_ns();
     if ((s = shared_args(w13, w13_scale, I, act, M, K, cs, &a, &rp)) != MR_OK) return s;
     mr::SharedPlan sp;
-    mr::shared_plan(M, K, I, cs, &sp);
+    mr::shared_plan(M, K, I, cs, &sp, mr::route_max_clusters());
     a.tok = sp.tok;
     a.tok_shift = mr::ilog2_exact(sp.tok);
     a.xpitch = sp.xpitch;

@@ -320,25 +320,33 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
     pdl_trigger();
     const int64_t kslice = (int64_t)c * kc;
     const int K32 = K / 32;
-    // this warp's units u = warp, warp + 16, ...: tile j = u / wpt, part p = u % wpt
-    // weights and scales are parameters: loaded before the dependency wait
-    uint2 wv[kShUnitsPerWarp][kRouteSpwMax];
-    uint32_t sv[kShUnitsPerWarp][kRouteSpwMax];  // scale bytes of rows 2t, 2t + 1 of the tile
-#pragma unroll
-    for (int uu = 0; uu < kShUnitsPerWarp; ++uu) {
-        const int u = warp + kRouteWarps * uu;
-        const bool ok = u < a.sh_units;
-        const int j = ok ? u / wpt : 0, p = ok ? u - j * wpt : 0;
-        const int lr = j * 8 + g, lc0 = j * 8 + 2 * t;
+    // The CTA's weight slice (R rows x kc E4M3 bytes, rows padded by 16 B
+    // against bank conflicts) and its scale bytes go to shared memory by
+    // cp.async, all issued before the dependency wait (they are parameters);
+    // then units u = warp, warp + 16, ... (tile j = u / wpt, k-part p =
+    // u % wpt) read them from there in a rolled loop (a CTA runs it once, from
+    // a cold instruction cache).
+    unsigned char* ws = sm + a.sh_off_w;
+    unsigned char* ss = sm + a.sh_off_s;
+    const int wpitch = kc + 16, spitch = a.sh_spitch, cpr = kc / 16, spr = kc / 32;
+    for (int i = tid; i < R * cpr; i += kRouteThreads) {
+        const int lr = i / cpr, cc = i - lr * cpr;
         const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
-        const int64_t gc0 = lc0 < P ? pair0 + lc0 : I + pair0 + (lc0 - P);  // rows 2t, 2t + 1 stay in one half
-        const uint8_t* wp = a.sh_w + gr * K + kslice + (int64_t)p * spw * 32 + 8 * t;
-        const uint8_t* sp = a.sh_scale + gc0 * K32 + kslice / 32 + (int64_t)p * spw;
+        cp_async16(smem_u32(ws + lr * wpitch + cc * 16), a.sh_w + gr * K + kslice + cc * 16);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int i0 = tid; i0 < R * spr; i0 += kRouteThreads * kShScaleBatch) {  // scale bytes, loads batched
+        uint8_t v[kShScaleBatch];
 #pragma unroll
-        for (int s = 0; s < kRouteSpwMax; ++s) {
-            const bool live = ok && s < spw;
-            wv[uu][s] = live ? __ldg(reinterpret_cast<const uint2*>(wp + s * 32)) : make_uint2(0u, 0u);
-            sv[uu][s] = live ? ((uint32_t)__ldg(sp + s) | ((uint32_t)__ldg(sp + K32 + s) << 8)) : 0u;
+        for (int b = 0; b < kShScaleBatch; ++b) {
+            const int i = i0 + b * kRouteThreads, lr = i / spr, cc = i - lr * spr;
+            const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
+            v[b] = i < R * spr ? __ldg(a.sh_scale + gr * K32 + kslice / 32 + cc) : 0;
+        }
+#pragma unroll
+        for (int b = 0; b < kShScaleBatch; ++b) {
+            const int i = i0 + b * kRouteThreads, lr = i / spr, cc = i - lr * spr;
+            if (i < R * spr) ss[lr * spitch + cc] = v[b];
         }
     }
     pdl_wait();
@@ -352,6 +360,7 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
             d = norm_chunk(d, ld_ro_v4(a.norm_w + kslice + cv * 8), __ldg(a.rstd + r), a.norm_gemma != 0);
         *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
     const uint32_t recv_local = smem_u32(sm + a.sh_off_recv);
@@ -359,11 +368,11 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
 #pragma unroll
     for (int h = 0; h < 2; ++h)
         if (g + 8 * h < Mq) owner_bar[h] = map_rank(bar, (unsigned)((g + 8 * h) >> a.tok_shift));
-#pragma unroll
-    for (int uu = 0; uu < kShUnitsPerWarp; ++uu) {
-        const int u = warp + kRouteWarps * uu;
-        if (u >= a.sh_units) break;
+#pragma unroll 1
+    for (int u = warp; u < a.sh_units; u += kRouteWarps) {
         const int j = u / wpt, p = u - j * wpt;
+        const unsigned char* wrow = ws + (j * 8 + g) * wpitch + p * spw * 32 + 8 * t;
+        const unsigned char* srow0 = ss + (j * 8 + 2 * t) * spitch + p * spw;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int s = 0; s < kRouteSpwMax; ++s) {
@@ -371,12 +380,13 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
                 const int kk = (p * spw + s) * 32 + 8 * t;
                 const uint4 xa = g < Mq ? lds128(xs + g * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
                 const uint4 xb = g + 8 < Mq ? lds128(xs + (g + 8) * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t b0 = e4m3x2_to_bf16x2(wv[uu][s].x), b1 = e4m3x2_to_bf16x2(wv[uu][s].x >> 16);
-                const uint32_t b2 = e4m3x2_to_bf16x2(wv[uu][s].y), b3 = e4m3x2_to_bf16x2(wv[uu][s].y >> 16);
+                const uint2 w8 = *reinterpret_cast<const uint2*>(wrow + s * 32);
+                const uint32_t b0 = e4m3x2_to_bf16x2(w8.x), b1 = e4m3x2_to_bf16x2(w8.x >> 16);
+                const uint32_t b2 = e4m3x2_to_bf16x2(w8.y), b3 = e4m3x2_to_bf16x2(w8.y >> 16);
                 float blk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 mma_bf16_m16n8k16(blk, xa.x, xb.x, xa.y, xb.y, b0, b1);
                 mma_bf16_m16n8k16(blk, xa.z, xb.z, xa.w, xb.w, b2, b3);
-                const float s0 = e8m0_value(sv[uu][s] & 0xFFu), s1 = e8m0_value(sv[uu][s] >> 8);
+                const float s0 = e8m0_value(srow0[s]), s1 = e8m0_value(srow0[spitch + s]);
                 acc[0] = __fmaf_rn(blk[0], s0, acc[0]);
                 acc[1] = __fmaf_rn(blk[1], s1, acc[1]);
                 acc[2] = __fmaf_rn(blk[2], s0, acc[2]);
@@ -626,8 +636,48 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int nb = (my_tiles + kRouteBatch - 1) / kRouteBatch;
     const int slot = c * wpt + p;
     const int r0 = g, r1 = g + 8;  // one m16 tile: at most 16 token rows per cluster here
+    uint32_t tok_bar[2] = {0u, 0u};  // at most 8 rows: mbarrier of the owner of tokens 2t and 2t + 1
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        if (2 * t + h < Mq) tok_bar[h] = map_rank(bar0, (unsigned)((2 * t + h) >> a.tok_shift));
     for (int b = 0; b < nb; ++b) {
         if (b > 0) load_w_batch(a, wg, kslice, warp, g, t, b, wv);
+        if constexpr (HALF) {
+            // At most 8 token rows: the experts take the MMA's 16-row side
+            // (the batch's two 8-expert tiles, rows 0-7 and 8-15) and the
+            // tokens its 8 columns, so one pair of MMAs per 32-wide k step
+            // covers both tiles (half the MMAs of tokens on the 16-row side,
+            // where 8 of the 16 rows are empty).
+            static_assert(kRouteBatch == 2, "two 8-expert tiles make the 16 rows");
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int s = 0; s < kRouteSpwMax; ++s) {
+                if (s < a.spw) {
+                    const int kk = (p * a.spw + s) * 32 + 8 * t;
+                    const uint4 xa = g < Mq ? lds128(xs + g * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
+                    mma_bf16_m16n8k16(acc, wv[0][s].x, wv[1][s].x, wv[0][s].y, wv[1][s].y, xa.x, xa.y);
+                    mma_bf16_m16n8k16(acc2, wv[0][s].z, wv[1][s].z, wv[0][s].w, wv[1][s].w, xa.z, xa.w);
+                }
+            }
+            MR_TRACE_WARP(a.trace, 4);
+            // acc[2 uu + h]: the expert of row g of unit uu's tile, token 2t + h
+#pragma unroll
+            for (int uu = 0; uu < 2; ++uu) {
+                const int j = j0 + tiles_per_pass * (b * 2 + uu);
+                if (j >= NT) break;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = 2 * t + h;
+                    if (r < Mq) {
+                        const int own = r >> a.tok_shift, rl = r & (tok - 1);
+                        const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * N + j * 8 + g) * 4);
+                        st_async_s32(map_rank(la, (unsigned)own),
+                                     __float_as_int(__fadd_rn(acc[2 * uu + h], acc2[2 * uu + h])), tok_bar[h]);
+                    }
+                }
+            }
+            continue;
+        }
         float acc[kRouteBatch][4];
 #pragma unroll
         for (int uu = 0; uu < kRouteBatch; ++uu) acc[uu][0] = acc[uu][1] = acc[uu][2] = acc[uu][3] = 0.0f;
@@ -673,8 +723,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // done once its slice is quantised: nothing is ever sent to it.  Owners
     // quantise later, off the path of the gate.
     // (On the tensor-core path every CTA has quantised during its MMAs.)
-    if (sorts) {
-        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
+    if (sorts) {  // (a sorting CTA that owns rows quantises after the sort, off its path)
+        if (!TC && quants && my_rows == 0) quant_slice(a, xs, Mq, row0, kslice);
         if (a.clusters == 1) fill_sort_padding(a, a.M * k);
     } else if (my_rows == 0) {
         if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
@@ -840,6 +890,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     MR_TRACE_WARP(a.trace, 7);
     int* ids_all = reinterpret_cast<int*>(sm + a.off_ids);
     const int M = a.M, MK = M * k, B = a.block, NS = a.ldn;
+    // what a sorting CTA that owns rows still owes for them once the sort no
+    // longer waits on it: their weights (not with expert groups: the merge
+    // weighs every token) and its x slice's quantisation
+    auto finish_sorter_rows = [&]() {
+        if (my_rows == 0) return;
+        if (!GROUPS) row_weights(a, rowbuf, oval, my_rows, grow);
+        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
+    };
     if constexpr (GROUPS) {
         // ---- expert groups: the owners have sent their rows' group
         //      candidates (k per row, in rank order) to the cluster's
@@ -866,7 +924,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
         }
         const unsigned ticket = cta_ticket(a.counter, &s_ticket);
-        if (ticket != (unsigned)(a.clusters - 1)) return;
+        if (ticket != (unsigned)(a.clusters - 1)) {
+            finish_sorter_rows();
+            return;
+        }
         // one warp per token: its ng lists of k candidates (each descending)
         // go to shared memory; lane g < ng holds the head of list g, and k
         // rounds each take the largest head (two redux.sync maximums: the
@@ -938,7 +999,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         if (!TC) quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
-    row_weights(a, rowbuf, oval, my_rows, grow);
     if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
     MR_TRACE_STAMP(a.trace, 5);
     MR_TRACE_WARP(a.trace, 9);
@@ -950,7 +1010,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     if (a.clusters > 1) {
         for (int f = tid; f < Mq * k; f += kRouteThreads) a.ids_scratch[row0 * k + f] = ids_all[f];
         const unsigned ticket = cta_ticket(a.counter, &s_ticket);
-        if (ticket != (unsigned)(a.clusters - 1)) return;
+        if (ticket != (unsigned)(a.clusters - 1)) {
+            finish_sorter_rows();
+            return;
+        }
         // every row from scratch (this cluster's own ids sit at local offsets)
         for (int f = tid; f < MK; f += kRouteThreads) ids_all[f] = __ldcg(a.ids_scratch + f);
         if (tid == 0) *a.counter = 0u;
@@ -1035,6 +1098,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     if (tid == 0 && a.trace) a.trace[blockIdx.x * 512 + 25] = clock64();
 #endif
     MR_TRACE_STAMP(a.trace, 7);
+    finish_sorter_rows();
 }
 
 // ------------------------------------------------------------------ host

@@ -402,11 +402,12 @@ __global__ void __launch_bounds__(kSortQuantThreads) psort_kernel(PSortArgs a) {
         }
         own_pos[i] = p;
     }
-    // padding and block ids of experts c, c + G, ...; the tail past the total
-    for (int e = c; e < N; e += G) {
+    // padding and block ids of experts c, c + G, ... (a thread per expert);
+    // the tail past the total
+    for (int e = c + G * tid; e < N; e += G * nthr) {
         const int st = start[e], t = tot[e], pd = (t + B - 1) / B * B;
-        for (int i = t + tid; i < pd; i += nthr) a.s.sorted[st + i] = sentinel;
-        for (int b = st / B + tid; b < (st + pd) / B; b += nthr) a.s.expert_ids[b] = e;
+        for (int i = t; i < pd; ++i) a.s.sorted[st + i] = sentinel;
+        for (int b = st / B; b < (st + pd) / B; ++b) a.s.expert_ids[b] = e;
     }
     {
         const int64_t gt = (int64_t)c * nthr + tid, T = (int64_t)G * nthr;

@@ -88,6 +88,7 @@ struct RouteArgs {
     const uint8_t* sh_scale;
     uint16_t* sh_out;
     int sh_I, sh_clusters, sh_pairs, sh_wpt, sh_spw, sh_units, sh_nslots, sh_off_x, sh_off_recv;
+    int sh_off_w, sh_off_s, sh_spitch;  // the CTA's weight slice and scale bytes in shared memory
 };
 
 // Multiplier for division by d (1 <= d <= 2^11) of dividends below 2^21:
@@ -232,16 +233,19 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
 // Shared expert's gate/up projection in the route launch (M <= 16 token rows,
 // one cluster of cs CTAs per group of pairs, CTA c the K slice c as the
 // route's): at most kShUnitsPerWarp (8-row tile, k-part) units per warp.
-constexpr int kShUnitsPerWarp = 3;
+constexpr int kShUnitsPerWarp = 4;
 constexpr int kShMaxClusters = 16;  // (clusters never wait on each other: more than fit at once is fine)
 constexpr int kShMaxM = 16;
+constexpr int kShScaleBatch = 8;  // scale-byte loads a thread keeps in flight
 
 struct SharedPlan {
-    int clusters, pairs, wpt, spw, units, nslots, tok, xpitch, off_x, off_recv, smem;
+    int clusters, pairs, wpt, spw, units, nslots, tok, xpitch, off_x, off_recv, off_w, off_s, spitch, smem;
 };
 
 // Returns false when (M, K, I) is outside what the shared-expert CTAs cover.
-inline bool shared_plan(int M, int K, int I, int cs, SharedPlan* p) {
+// fit: clusters that can run beside the route's at once; the plan takes the
+// most clusters up to fit (one wave), else the fewest beyond it.
+inline bool shared_plan(int M, int K, int I, int cs, SharedPlan* p, int fit = kShMaxClusters) {
     if (M < 1 || M > kShMaxM || I < 8 || I % 8 != 0 || K < 32 * cs || K % (32 * cs) != 0) return false;
     SharedPlan q{};
     const int kc = K / cs, S = kc / 32;
@@ -252,17 +256,14 @@ inline bool shared_plan(int M, int K, int I, int cs, SharedPlan* p) {
             break;
         }
     if (w == 0 || (cs * w) % 8 != 0) return false;
-    // as many clusters as divide the 8-pair groups, up to kShMaxClusters,
-    // with at most kShUnitsPerWarp units per warp
+    // clusters: a divisor of the 8-pair groups with at most kShUnitsPerWarp
+    // units per warp; the most that fit at once, else the fewest that work
+    auto ok = [&](int d) { return (I / 8) % d == 0 && (2 * (I / d) / 8) * w <= kShUnitsPerWarp * kRouteWarps; };
     int sc = 0;
-    for (int d = kShMaxClusters; d >= 1; --d) {
-        if ((I / 8) % d != 0) continue;
-        const int units = (2 * (I / d) / 8) * w;
-        if (units <= kShUnitsPerWarp * kRouteWarps) {
-            sc = d;
-            break;
-        }
-    }
+    for (int d = fit < kShMaxClusters ? fit : kShMaxClusters; d >= 1 && sc == 0; --d)
+        if (ok(d)) sc = d;
+    for (int d = (fit < kShMaxClusters ? fit : kShMaxClusters) + 1; d <= kShMaxClusters && sc == 0; ++d)
+        if (ok(d)) sc = d;
     if (sc == 0) return false;
     q.clusters = sc;
     q.pairs = I / sc;
@@ -278,6 +279,11 @@ inline bool shared_plan(int M, int K, int I, int cs, SharedPlan* p) {
     off = align_up(off + M * q.xpitch, 16);
     q.off_recv = off;
     off = align_up(off + q.nslots * q.tok * 2 * q.pairs * 4, 16);
+    q.off_w = off;  // 2P rows of kc weight bytes, 16 bytes of padding a row
+    off = align_up(off + 2 * q.pairs * (kc + 16), 16);
+    q.spitch = align_up(kc / 32, 4);
+    q.off_s = off;  // 2P rows of kc / 32 scale bytes
+    off = align_up(off + 2 * q.pairs * q.spitch, 16);
     q.smem = off;
     if (q.smem > kRouteSmemMax) return false;
     *p = q;

@@ -442,12 +442,15 @@ int mr_norm_apply(const void *sres, int64_t ldx, const float *rstd, const void *
  *   act[m, i] = silu(h[m, i]) * h[m, I + i],   silu(v) = v / (1 + e^-v)
  * rounded to bf16 (nearest even).  x: bf16 [M, ldx]; w13: E4M3 codes
  * [2I, K] row-major, rows [0, I) the gate projection and [I, 2I) the up
- * projection (8-byte aligned); w13_scale: E8M0 bytes [2I, K / 32] (below
+ * projection (16-byte aligned); w13_scale: E8M0 bytes [2I, K / 32] (below
  * 255, NaN); act: bf16 [M, I] (4-byte aligned).  Each 32-wide block of a
  * row is summed in fp32 (products exact) and scaled by its factor with one
  * fused multiply-add; the K range is split over the CTAs of a cluster as in
  * the router GEMV and the partial sums are added in a fixed order, so the
- * result is deterministic.  The output keeps finite values when the
+ * result is deterministic.  Each CTA stages its K slice of the weights in
+ * shared memory (cp.async, issued before it waits on the previous kernel);
+ * the number of clusters is the most that run beside the route's at once.
+ * The output keeps finite values when the
  * weights' scale bytes are at most 246 (|W| below 2^128).  1 <= M <= 16,
  * K % 512 == 0, I % 8 == 0, and I up to 1536 at K = 6144 (at most 48 row
  * tiles x k-parts per CTA over at most 16 clusters), else

@@ -362,7 +362,7 @@ def test_shared_gate_up_validation(lib):
     assert lib.mr_shared_gate_up(fake, 6144, fake, fake, 4, 6144, 100, fake, None) == mr.MR_ERR_UNSUPPORTED
     # null or misaligned weights / output
     assert lib.mr_shared_gate_up(fake, 6144, None, fake, 4, 6144, 768, fake, None) == mr.MR_ERR_INVALID_ARG
-    assert lib.mr_shared_gate_up(fake, 6144, P(0x1004), fake, 4, 6144, 768, fake, None) == mr.MR_ERR_INVALID_ARG
+    assert lib.mr_shared_gate_up(fake, 6144, P(0x1008), fake, 4, 6144, 768, fake, None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_shared_gate_up(fake, 6144, fake, None, 4, 6144, 768, fake, None) == mr.MR_ERR_INVALID_ARG
     assert lib.mr_shared_gate_up(fake, 6144, fake, fake, 4, 6144, 768, P(0x1002), None) == mr.MR_ERR_INVALID_ARG
     # the route with a shared expert: more than 16 tokens is outside its cover
