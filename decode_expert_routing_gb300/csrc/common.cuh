@@ -206,8 +206,9 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
     const uint32_t h = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
     const uint32_t mag = h & 0x7FFF7FFFu;
-    const uint32_t sh = (mag >> 3) & 0x0FFF0FFFu;
-    return (h & 0x80008000u) | (sh + (0x38003800u & __vcmpne2(mag, 0u)));
+    uint32_t nz;  // 1 in each half whose magnitude is nonzero
+    asm("min.u16x2 %0, %1, %2;" : "=r"(nz) : "r"(mag), "r"(0x00010001u));
+    return (h & 0x80008000u) | (((mag >> 3) & 0x0FFF0FFFu) + nz * 0x3800u);
 }
 
 // 2^(byte - 127) as fp32 for an E8M0 scale byte < 255 (byte 0: the subnormal 2^-127).

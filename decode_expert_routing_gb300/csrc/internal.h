@@ -53,6 +53,7 @@ cudaError_t launch_quant(const void* x, int64_t ldx, int M, int K, uint8_t* q, u
 // assignments, at most kPSortMaxOwn placed by one CTA.
 constexpr int kPSortMaxAssign = 65536;
 constexpr int kPSortMaxOwn = 2048;
+constexpr int kPSortStageMax = 16384;  // ids staged in shared memory up to here (64 KiB)
 struct SortArgs;
 // fmt: 0 sort only, 1 MXFP8, 2 MXFP4 of x; sorted_rows: q and scale hold the
 // quantised rows at the sorted positions (capacity rows) instead of token order.

@@ -329,24 +329,32 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
     unsigned char* ws = sm + a.sh_off_w;
     unsigned char* ss = sm + a.sh_off_s;
     const int wpitch = kc + 16, spitch = a.sh_spitch, cpr = kc / 16, spr = kc / 32;
-    for (int i = tid; i < R * cpr; i += kRouteThreads) {
-        const int lr = i / cpr, cc = i - lr * cpr;
-        const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
-        cp_async16(smem_u32(ws + lr * wpitch + cc * 16), a.sh_w + gr * K + kslice + cc * 16);
+    // 16-byte chunk cc of local row lr: thread tid takes chunk tid % cpr of
+    // rows tid / cpr, + 512 / cpr, ... when cpr divides 512 (kc = 384:
+    // cpr = 24 does not, so the (row, chunk) pair advances with a carry)
+    {
+        const int dr = kRouteThreads / cpr, dc = kRouteThreads - dr * cpr;
+        int lr = tid / cpr, cc = tid - lr * cpr;
+        for (; lr < R; lr += dr, cc += dc) {
+            if (cc >= cpr) {
+                cc -= cpr;
+                if (++lr >= R) break;
+            }
+            const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
+            cp_async16(smem_u32(ws + lr * wpitch + cc * 16), a.sh_w + gr * K + kslice + cc * 16);
+        }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int i0 = tid; i0 < R * spr; i0 += kRouteThreads * kShScaleBatch) {  // scale bytes, loads batched
-        uint8_t v[kShScaleBatch];
+    if (tid < R) {  // a thread per row: its kc / 32 scale bytes, 8 loads in flight at a time
+        const int64_t gr = tid < P ? pair0 + tid : I + pair0 + (tid - P);
+        const uint8_t* src = a.sh_scale + gr * K32 + kslice / 32;
+        for (int b0 = 0; b0 < spr; b0 += 8) {
+            uint8_t v[8];
 #pragma unroll
-        for (int b = 0; b < kShScaleBatch; ++b) {
-            const int i = i0 + b * kRouteThreads, lr = i / spr, cc = i - lr * spr;
-            const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
-            v[b] = i < R * spr ? __ldg(a.sh_scale + gr * K32 + kslice / 32 + cc) : 0;
-        }
+            for (int b = 0; b < 8; ++b) v[b] = b0 + b < spr ? __ldg(src + b0 + b) : 0;
 #pragma unroll
-        for (int b = 0; b < kShScaleBatch; ++b) {
-            const int i = i0 + b * kRouteThreads, lr = i / spr, cc = i - lr * spr;
-            if (i < R * spr) ss[lr * spitch + cc] = v[b];
+            for (int b = 0; b < 8; ++b)
+                if (b0 + b < spr) ss[tid * spitch + b0 + b] = v[b];
         }
     }
     pdl_wait();
@@ -723,8 +731,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // done once its slice is quantised: nothing is ever sent to it.  Owners
     // quantise later, off the path of the gate.
     // (On the tensor-core path every CTA has quantised during its MMAs.)
-    if (sorts) {  // (a sorting CTA that owns rows quantises after the sort, off its path)
-        if (!TC && quants && my_rows == 0) quant_slice(a, xs, Mq, row0, kslice);
+    if (sorts) {
+        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
         if (a.clusters == 1) fill_sort_padding(a, a.M * k);
     } else if (my_rows == 0) {
         if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
@@ -890,14 +898,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     MR_TRACE_WARP(a.trace, 7);
     int* ids_all = reinterpret_cast<int*>(sm + a.off_ids);
     const int M = a.M, MK = M * k, B = a.block, NS = a.ldn;
-    // what a sorting CTA that owns rows still owes for them once the sort no
-    // longer waits on it: their weights (not with expert groups: the merge
-    // weighs every token) and its x slice's quantisation
-    auto finish_sorter_rows = [&]() {
-        if (my_rows == 0) return;
-        if (!GROUPS) row_weights(a, rowbuf, oval, my_rows, grow);
-        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
-    };
     if constexpr (GROUPS) {
         // ---- expert groups: the owners have sent their rows' group
         //      candidates (k per row, in rank order) to the cluster's
@@ -924,10 +924,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
         }
         const unsigned ticket = cta_ticket(a.counter, &s_ticket);
-        if (ticket != (unsigned)(a.clusters - 1)) {
-            finish_sorter_rows();
-            return;
-        }
+        if (ticket != (unsigned)(a.clusters - 1)) return;
         // one warp per token: its ng lists of k candidates (each descending)
         // go to shared memory; lane g < ng holds the head of list g, and k
         // rounds each take the largest head (two redux.sync maximums: the
@@ -999,6 +996,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         if (!TC) quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
+    row_weights(a, rowbuf, oval, my_rows, grow);
     if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
     MR_TRACE_STAMP(a.trace, 5);
     MR_TRACE_WARP(a.trace, 9);
@@ -1010,10 +1008,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     if (a.clusters > 1) {
         for (int f = tid; f < Mq * k; f += kRouteThreads) a.ids_scratch[row0 * k + f] = ids_all[f];
         const unsigned ticket = cta_ticket(a.counter, &s_ticket);
-        if (ticket != (unsigned)(a.clusters - 1)) {
-            finish_sorter_rows();
-            return;
-        }
+        if (ticket != (unsigned)(a.clusters - 1)) return;
         // every row from scratch (this cluster's own ids sit at local offsets)
         for (int f = tid; f < MK; f += kRouteThreads) ids_all[f] = __ldcg(a.ids_scratch + f);
         if (tid == 0) *a.counter = 0u;
@@ -1098,7 +1093,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     if (tid == 0 && a.trace) a.trace[blockIdx.x * 512 + 25] = clock64();
 #endif
     MR_TRACE_STAMP(a.trace, 7);
-    finish_sorter_rows();
 }
 
 // ------------------------------------------------------------------ host

@@ -279,7 +279,7 @@ __device__ __forceinline__ void psort_hist(const int32_t* ids, int beg, int end,
 #pragma unroll
         for (int u = 0; u < kLoadBatch; ++u) {
             const int i = base + u * nthr;
-            e[u] = i < end ? __ldg(ids + i) : -1;
+            e[u] = i < end ? ids[i] : -1;
         }
 #pragma unroll
         for (int u = 0; u < kLoadBatch; ++u)
@@ -343,6 +343,7 @@ __device__ __forceinline__ void quant_rows_to_positions(const uint16_t* x, int64
 struct PSortArgs {
     SortArgs s;
     int M, k, rows_per;   // token rows per CTA
+    int staged;           // 1: every id staged in shared memory (n_assign <= kPSortStageMax)
     const uint16_t* x;    // stage-1 activations [M, ldx] (FMT != 0)
     int64_t ldx;
     int K;
@@ -380,10 +381,20 @@ __global__ void __launch_bounds__(kSortQuantThreads) psort_kernel(PSortArgs a) {
         tot[e] = 0;
     }
     for (int i = tid; i < nw * N; i += nthr) rs.wcnt[i] = 0;  // the per-warp counts of psort_hist
-    for (int i = tid; i < n_own; i += nthr) own_ids[i] = __ldg(a.s.ids + f0 + i);
+    // up to kPSortStageMax ids: all of them to shared memory in one round of
+    // loads, counted from there (and this CTA's own ids are a slice of them)
+    const int32_t* ids = a.s.ids;
+    if (a.staged) {
+        int* all = own_pos + own_max + nw * N + N + own_max;
+        stage_ids(a.s.ids, n_all, all);
+        ids = all;
+        for (int i = tid; i < n_own; i += nthr) own_ids[i] = all[f0 + i];
+    } else {
+        for (int i = tid; i < n_own; i += nthr) own_ids[i] = __ldg(a.s.ids + f0 + i);
+    }
     __syncthreads();
-    psort_hist(a.s.ids, 0, f0, N, rs.wcnt, pre);
-    psort_hist(a.s.ids, f0, n_all, N, rs.wcnt, tot);
+    psort_hist(ids, 0, f0, N, rs.wcnt, pre);
+    psort_hist(ids, f0, n_all, N, rs.wcnt, tot);
     for (int e = tid; e < N; e += nthr) {
         const int t = tot[e] + pre[e];
         tot[e] = t;
@@ -455,9 +466,10 @@ cudaError_t launch_psort(const SortArgs& s, int M, int topk, const void* x, int6
     if (rows_per * topk > kPSortMaxOwn) rows_per = kPSortMaxOwn / topk;
     if (rows_per < 1) rows_per = 1;
     const int G = (M + rows_per - 1) / rows_per;
-    PSortArgs a{s, M, topk, rows_per, static_cast<const uint16_t*>(x), ldx, K, q, scale};
+    const int staged = s.n_assign <= kPSortStageMax ? 1 : 0;
+    PSortArgs a{s, M, topk, rows_per, staged, static_cast<const uint16_t*>(x), ldx, K, q, scale};
     const int nw = kSortQuantThreads / 32;
-    const int smem = 4 * psort_smem_ints(nw, s.N, rows_per * topk);
+    const int smem = 4 * (psort_smem_ints(nw, s.N, rows_per * topk) + (staged ? s.n_assign : 0));
     void (*kernel)(PSortArgs) = nullptr;
     int slot = 0;
     if (fmt == 0) {

@@ -258,7 +258,10 @@ inline bool shared_plan(int M, int K, int I, int cs, SharedPlan* p, int fit = kS
     if (w == 0 || (cs * w) % 8 != 0) return false;
     // clusters: a divisor of the 8-pair groups with at most kShUnitsPerWarp
     // units per warp; the most that fit at once, else the fewest that work
-    auto ok = [&](int d) { return (I / 8) % d == 0 && (2 * (I / d) / 8) * w <= kShUnitsPerWarp * kRouteWarps; };
+    auto ok = [&](int d) {
+        return (I / 8) % d == 0 && (2 * (I / d) / 8) * w <= kShUnitsPerWarp * kRouteWarps &&
+               2 * (I / d) <= kRouteThreads;  // a thread per row loads the scales
+    };
     int sc = 0;
     for (int d = fit < kShMaxClusters ? fit : kShMaxClusters; d >= 1 && sc == 0; --d)
         if (ok(d)) sc = d;

@@ -144,7 +144,8 @@ def test_shared_plan_invariants(tmp_path):
         cs, M, K, I = (int(v) for v in f[1:5])
         S = K // cs // 32 if K % (32 * cs) == 0 else 0
         w = next((d for d in (1, 2, 4, 8, 16) if S and S % d == 0 and S // d <= 8), 0)
-        fits = [d for d in range(1, 17) if I % 8 == 0 and (I // 8) % d == 0 and (2 * (I // d) // 8) * w <= 64]
+        fits = [d for d in range(1, 17) if I % 8 == 0 and (I // 8) % d == 0 and (2 * (I // d) // 8) * w <= 64
+                and 2 * (I // d) <= 512]
         if f[0] == "none":
             assert M > 16 or I % 8 or not S or not w or not fits
             continue
