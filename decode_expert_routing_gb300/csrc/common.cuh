@@ -10,12 +10,15 @@ namespace mr {
 constexpr unsigned kFull = 0xffffffffu;
 
 // 16-byte streaming load of data read once per launch (the gate weight):
-// read-only path, no L1 allocation.
+// read-only path, no L1 allocation.  volatile: the load is issued where it
+// is written, so loads of parameters placed before the programmatic-
+// dependent-launch wait are in flight while the kernel waits (a plain asm
+// without memory operands may be sunk to its first use, after the wait).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
     return r;
 }
 
