@@ -44,7 +44,10 @@ class MoeRouteError(RuntimeError):
 
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {_load().mr_status_string(status).decode()}")
+        msg = f"{what}: {_load().mr_status_string(status).decode()}"
+        if status == MR_ERR_CUDA:
+            msg += f" (cudaError_t {_load().mr_last_cuda_error()})"
+        super().__init__(msg)
 
 
 class MoeRouteUnsupported(MoeRouteError):
@@ -83,6 +86,7 @@ SIGNATURES = {
     "mr_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "mr_device_error": (_I, [_I]),
     "mr_shared_gate_up": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
+    "mr_last_cuda_error": (_I, []),
 }
 
 

@@ -15,7 +15,13 @@ using mr::GemvPlan;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? MR_OK : MR_ERR_CUDA; }
+thread_local int g_last_cuda_error = 0;  // behind this thread's last MR_ERR_CUDA
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MR_OK;
+    g_last_cuda_error = (int)e;
+    return MR_ERR_CUDA;
+}
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
@@ -94,8 +100,8 @@ int mr_set_wait_limit_ns(uint64_t ns) {
 }
 
 int mr_device_error(int clear) {
-    const int v = mr::route_device_error(clear);
-    return v < 0 ? MR_ERR_CUDA : v ? MR_ERR_TIMEOUT : MR_OK;
+    const int v = mr::route_device_error(clear), t = mr::tc_gemv_device_error(clear);
+    return (v < 0 || t < 0) ? MR_ERR_CUDA : (v || t) ? MR_ERR_TIMEOUT : MR_OK;
 }
 
 #ifdef MR_TRACE
@@ -123,10 +129,13 @@ const char* mr_status_string(int status) {
 
 int mr_abi_version(void) { return MR_ABI_VERSION; }
 
+int mr_last_cuda_error(void) { return g_last_cuda_error; }
+
 int mr_router_gemv_supported(int M, int N, int K, int64_t ldx) {
     if (ldx < K || ldx % 8 != 0 || K % MR_GEMV_K_MULTIPLE != 0) return 0;
     mr::RoutePlan rp;
-    if (mr::route_plan(M, N, K, 1, 0, 16, &rp)) return 1;
+    mr::TcGemvPlan tp;
+    if (mr::route_plan(M, N, K, 1, 0, 16, &rp) || mr::tc_gemv_plan(M, N, K, 16, 1, &tp)) return 1;
     if (M <= mr::kRouteMaxM) return 0;
     GemvPlan p;
     return mr::gemv_plan(M, N, K, &p) ? 1 : 0;
@@ -212,13 +221,7 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.mag_n = mr::div_magic(p.nl);
     a.mag_vpr = mr::div_magic(p.kc / 8);
     a.mag_n4 = mr::div_magic(N / 4 > 0 ? N / 4 : 1);
-    a.tc = p.tc;
-    a.nmma = p.nmma;
-    a.tmem_cols = p.tmem_cols;
     a.nslots = p.nslots;
-    a.off_a = p.off_a;
-    a.off_b = p.off_b;
-    a.off_dst = p.off_dst;
     a.trace = static_cast<unsigned long long*>(mr::trace_buffer());
     a.flags = mr::launch_flags();
     a.wait_ns = mr::wait_limit_ns();
@@ -232,10 +235,19 @@ int mr_router_gemv(const void* x, int64_t ldx, const void* w, float* logits, int
     if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) || N < 1)
         return MR_ERR_INVALID_ARG;
     if (K % MR_GEMV_K_MULTIPLE != 0) return MR_ERR_UNSUPPORTED;
+    if (M > mr::kRouteMaxM && allow_tc()) {  // above 64 rows: tcgen05 when its plan fits
+        mr::TcGemvPlan tp;
+        if (mr::tc_gemv_plan(M, N, K, mr::route_cluster_size(), mr::route_max_clusters(), &tp))
+        {
+            cudaError_t e = cudaSuccess;
+            const int st = mr::launch_tc_gemv(tp, x, ldx, w, logits, M, N, K, as_stream(stream), &e);
+            return st == MR_ERR_CUDA ? cuda_status(e) : st;
+        }
+    }
     {   // the cluster kernel (no scratch) whenever its plan fits; above 64 rows
         // the split-K GEMV with last-arriver fixup takes the rest
         mr::RoutePlan rp;
-        if (mr::route_plan(M, N, K, 1, 0, mr::route_cluster_size(), &rp, allow_tc(), mr::route_max_clusters())) {
+        if (mr::route_plan(M, N, K, 1, 0, mr::route_cluster_size(), &rp, mr::route_max_clusters())) {
             mr::RouteArgs a = route_args(rp, x, ldx, w, M, N, K, 0);
             a.logits = logits;
             return cuda_status(mr::launch_route_cluster(rp, a, as_stream(stream)));
@@ -378,10 +390,10 @@ static int route_impl(const mr_route_params* p, void* stream) {
     // expert groups need scratch for their candidates: without it (or with
     // too little) the route runs its experts in one cluster per 16 tokens
     const bool have_scratch = p->scratch != nullptr && aligned(p->scratch, 256);
-    if (!mr::route_plan(M, N, K, topk, 1, cs, &rp, allow_tc(), have_scratch ? mr::route_max_clusters() : 1))
+    if (!mr::route_plan(M, N, K, topk, 1, cs, &rp, have_scratch ? mr::route_max_clusters() : 1))
         return MR_ERR_UNSUPPORTED;
     if (rp.ng > 1 && p->scratch_bytes < mr::kWorkOffset + (size_t)M * rp.ng * topk * 12 &&
-        !mr::route_plan(M, N, K, topk, 1, cs, &rp, allow_tc(), 1))
+        !mr::route_plan(M, N, K, topk, 1, cs, &rp, 1))
         return MR_ERR_UNSUPPORTED;
     mr::RouteArgs a = route_args(rp, p->x, p->ldx, p->w, M, N, K, 1);
     if (rp.clusters > 1) {  // the clusters meet in scratch: a ticket and every token's ids

@@ -31,10 +31,8 @@
 //
 // Variants of the same kernel:
 //   - GEMV alone (mode 0): what the standalone router GEMV runs for
-//     M <= 64, so the logits of the two are bitwise equal; above 64 rows
-//     (N <= 128) with 64 rows per cluster on tcgen05 (TC: the CTA's weight
-//     slice and x slice staged as K-major operand tiles, one thread issuing
-//     the MMAs into a TMEM accumulator, all warps reading it back).
+//     M <= 64, so the logits of the two are bitwise equal (above 64 rows the
+//     tensor-core GEMV of kernel_tc_gemv.cu takes over).
 //   - Expert groups (GROUPS, N >= 512): the experts split into groups of
 //     >= 128, one cluster per group, so that more SMs share the gate weight;
 //     for the whole route each cluster's collector publishes its group's
@@ -46,98 +44,12 @@
 // Every wait for bytes from other CTAs is bounded in time and sets a device
 // flag when it runs out.  One cluster leaves nothing in scratch; several
 // clusters leave their ticket counter at zero again.
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "route_plan.h"
 
 namespace mr {
-
-__device__ __forceinline__ unsigned cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint32_t map_rank(uint32_t local, unsigned rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Hand-offs between the CTAs of a cluster: the sender writes with st.async,
-// which also counts the bytes on an mbarrier in the receiving CTA; the
-// receiver has announced the bytes it expects, so the barrier's phase 0
-// completes when the last byte has landed.  No release fence on either side.
-__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait0(uint32_t bar) {
-    unsigned ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void st_async_f2(uint32_t addr, float a, float b, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
-                 "f"(a), "f"(b), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void st_async_s32(uint32_t addr, int v, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.s32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
-                 "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// ---- tcgen05 (5th-generation tensor core, accumulator in tensor memory)
-// Shared-memory matrix descriptor of a K-major tile without swizzle: start
-// address, leading (k) and stride (8-row group) byte offsets, each >> 4, and
-// the fixed descriptor version bit.
-__device__ __forceinline__ unsigned long long tc_desc(uint32_t addr) {
-    return (unsigned long long)((addr >> 4) & 0x3FFFu) | ((unsigned long long)(kTcLbo >> 4) << 16) |
-           ((unsigned long long)(kTcSbo >> 4) << 32) | (1ull << 46);
-}
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N >> 3 and M >> 4.
-__device__ __forceinline__ uint32_t tc_idesc(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-// Byte offset of 16-byte chunk cc (k elements 8 cc .. 8 cc + 7) of row r in a
-// K-major tile whose 16-wide k-steps lie `step` bytes apart.
-__device__ __forceinline__ uint32_t tc_off(int r, int cc, int step) {
-    return (uint32_t)((cc >> 1) * step + (r >> 3) * kTcSbo + (cc & 1) * kTcLbo + (r & 7) * 16);
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // Set when a bounded wait of the route kernel ran out (read by the host).
 __device__ int g_route_timeout;
@@ -441,15 +353,13 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
     }
 }
 
-// HALF: at most 8 token rows (half of the m16 tile live).  TC: the router
-// GEMV on tcgen05 (GEMV alone, 64-row clusters) instead of mma.sync.
+// HALF: at most 8 token rows (half of the m16 tile live).
 // GROUPS: the experts are split into a.ng groups, one cluster per group.
-template <bool HALF, bool TC, bool GROUPS>
+template <bool HALF, bool GROUPS>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) unsigned long long s_bar[3];  // [0] partial logits in, [1] ids in, [2] MMAs done
     __shared__ int s_ok[3];
-    __shared__ uint32_t s_tmem;  // tcgen05: base address of the accumulator
     __shared__ unsigned s_ticket;
     __shared__ __align__(16) unsigned s_wmin[kRouteWarps];  // gate: per warp, smallest group maximum
     __shared__ int s_ccount;                                  // gate: candidates so far
@@ -517,22 +427,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      precede the wait
     uint4 wv[kRouteBatch][kRouteSpwMax];
     const int vpr = a.kc / 8;  // 16-byte chunks per row of the CTA's K slice
-    if constexpr (TC) {
-        if (warp == 0) {  // accumulator columns in tensor memory (one CTA per SM: never contended)
-            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                         "r"(a.tmem_cols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
-        const uint32_t at = smem_u32(sm + a.off_a);
-        for (int i = tid; i < N * vpr; i += kRouteThreads) {
-            const int e = fdiv(i, a.mag_vpr), cc = i - e * vpr;
-            cp_async16(at + tc_off(e, cc, kTcAStep), a.w + (int64_t)e * K + kslice + cc * 8);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    } else {
-        load_w_batch(a, wg, kslice, warp, g, t, 0, wv);
-    }
+    load_w_batch(a, wg, kslice, warp, g, t, 0, wv);
     float bpre0 = 0.0f, bpre1 = 0.0f;  // selection bias of this thread's experts t and t + 512
     if (a.bias != nullptr) {
         if (tid < N) bpre0 = __ldg(a.bias + e_off + tid);
@@ -547,93 +442,22 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      residual rows times rstd and the norm weight, rounded to bf16 as
     //      the norm would store them)
     unsigned char* xs = sm + a.off_x;
-    const bool keep_xs = !(TC && a.mode == 0);  // row-major copy for mma.sync / the quantiser
     const bool norm = a.rstd != nullptr;
     for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
         const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
         uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
         if (norm)
             d = norm_chunk(d, ld_ro_v4(a.norm_w + kslice + cv * 8), __ldg(a.rstd + row0 + r), a.norm_gemma != 0);
-        if (keep_xs) *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
-        if constexpr (TC) *reinterpret_cast<uint4*>(sm + a.off_b + tc_off(r, cv, a.nmma * 32)) = d;
+        *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
     }
     MR_TRACE_WARP(a.trace, 0);
-    if constexpr (TC) {  // the weight tile has landed; both tiles are visible to the tensor core
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-    }
     __syncthreads();
-    if constexpr (TC) tc_fence_after();
     MR_TRACE_STAMP(a.trace, 1);
 
     // ---- MMA: batches of units sharing one k-part; partial tiles go
     //      straight to the receive buffers of the rows' owners
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
     const uint32_t recv_local = smem_u32(sm + a.off_recv);
-    if constexpr (TC) {
-        // one thread issues the K slice's MMAs: D[128 experts x NMMA tokens]
-        // += W tile [128 x 16] . x tile [NMMA x 16]^T per 16-wide k-step
-        const uint32_t tmem = s_tmem;
-        if (tid == 0) {
-            const unsigned long long ad0 = tc_desc(smem_u32(sm + a.off_a)), bd0 = tc_desc(smem_u32(sm + a.off_b));
-            const uint32_t idesc = tc_idesc(128, a.nmma);
-            const int nq = a.kc / 16;
-            const unsigned long long bstep = (unsigned long long)((a.nmma * 32) >> 4);
-            for (int q = 0; q < nq; ++q) {
-                const unsigned long long ad = ad0 + (unsigned long long)q * (kTcAStep >> 4), bd = bd0 + (unsigned long long)q * bstep;
-                asm volatile(
-                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-                    "l"(ad), "l"(bd), "r"(idesc), "r"((uint32_t)(q > 0))
-                    : "memory");
-            }
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar2)
-                         : "memory");
-        }
-        if (quants) quant_slice(a, xs, Mq, row0, kslice);  // while the tensor core works
-        const bool ok = cta_wait_bytes(bar2, a.wait_ns, &s_ok[2]);
-        MR_TRACE_STAMP(a.trace, 9);
-        tc_fence_after();
-        // warp w reads accumulator lanes (experts) 32 (w % 4) .. + 31, column
-        // blocks w / 4, w / 4 + 4, ... (a warp may touch only its lane quarter)
-        if (ok) {
-            float* dst = reinterpret_cast<float*>(sm + a.off_dst);  // [token][expert]
-            const int q4 = warp & 3, e = q4 * 32 + lane;
-            for (int cb = warp >> 2; cb < a.nmma / 16; cb += kRouteWarps / 4) {
-                uint32_t v[16];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-                    : "r"(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(cb * 16)));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (e < N) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (cb * 16 + j < Mq) dst[(cb * 16 + j) * N + e] = __uint_as_float(v[j]);
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) {
-            tc_fence_after();
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
-        }
-        if (!ok) return;
-        MR_TRACE_STAMP(a.trace, 10);
-        // 16-byte messages: row r's N partial logits to the row's owner
-        const float* dsrc = reinterpret_cast<const float*>(sm + a.off_dst);
-        const int n4 = N >> 2;
-        for (int item = tid; item < Mq * n4; item += kRouteThreads) {
-            const int r = fdiv(item, a.mag_n4), c4 = item - r * n4;
-            const int own = r >> a.tok_shift, rl = r & (tok - 1);
-            const uint32_t la = recv_local + (uint32_t)(((c * tok + rl) * N + 4 * c4) * 4);
-            st_async_f4(map_rank(la, (unsigned)own), *reinterpret_cast<const float4*>(dsrc + r * N + 4 * c4),
-                        map_rank(bar0, (unsigned)own));
-        }
-    } else {
     uint32_t owner_bar[2] = {0u, 0u};  // mbarrier of the owner of rows g and g + 8
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -722,7 +546,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
         }
     }
-    }  // mma.sync path
     MR_TRACE_WARP(a.trace, 1);
     MR_TRACE_WARP(a.trace, 2);
     // The sorter quantises its slice now (and, with one cluster, fills the
@@ -730,12 +553,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // barriers of this CTA).  A CTA that owns no rows and does not sort is
     // done once its slice is quantised: nothing is ever sent to it.  Owners
     // quantise later, off the path of the gate.
-    // (On the tensor-core path every CTA has quantised during its MMAs.)
     if (sorts) {
-        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
+        if (quants) quant_slice(a, xs, Mq, row0, kslice);
         if (a.clusters == 1) fill_sort_padding(a, a.M * k);
     } else if (my_rows == 0) {
-        if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
+        if (quants) quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
     if (my_rows > 0 && !cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
@@ -779,6 +601,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
             a.logits[(int64_t)(grow + rl) * a.ldn + e_off + n] = sum;
         }
+        MR_TRACE_STAMP(a.trace, 3);
         return;  // nothing else reads this CTA's shared memory
     }
     for (int rl = 0; rl < my_rows; ++rl) {
@@ -908,7 +731,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         //      candidates that beat it (a binary search: each list is
         //      descending; the composites are unique).
         if (!sorts) {
-            if (!TC && quants) quant_slice(a, xs, Mq, row0, kslice);
+            if (quants) quant_slice(a, xs, Mq, row0, kslice);
             return;
         }
         if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
@@ -993,7 +816,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     } else {
     if (!sorts) {  // the weights and the quantisation finish this CTA
         row_weights(a, rowbuf, oval, my_rows, grow);
-        if (!TC) quant_slice(a, xs, Mq, row0, kslice);
+        quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
     row_weights(a, rowbuf, oval, my_rows, grow);
@@ -1108,15 +931,14 @@ int route_device_error(int clear) {
 }
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
-static int g_attr_done[64][8];  // per device and instantiation
+static int g_attr_done[64][4];  // per device and instantiation
 
-template <bool HALF, bool TC, bool GROUPS>
+template <bool HALF, bool GROUPS>
 static cudaError_t prepare(int dev) {
-    const int slot = (HALF ? 1 : 0) + (TC ? 2 : 0) + (GROUPS ? 4 : 0);
+    const int slot = (HALF ? 1 : 0) + (GROUPS ? 2 : 0);
     if (g_attr_done[dev][slot]) return cudaSuccess;
-    auto k = route_cluster_kernel<HALF, TC, GROUPS>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TC ? kRouteSmemMaxTc : kRouteSmemMax);
+    auto k = route_cluster_kernel<HALF, GROUPS>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) g_attr_done[dev][slot] = 1;
     return e;
@@ -1126,7 +948,7 @@ int route_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (g_cluster16[dev] == 0) {
-        cudaError_t e = prepare<false, false, false>(dev);
+        cudaError_t e = prepare<false, false>(dev);
         int n = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -1140,7 +962,7 @@ int route_cluster_size() {
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false>, &cfg);
         }
         g_cluster16[dev] = (e == cudaSuccess && n >= 1) ? 1 : -1;
         cudaGetLastError();  // a refused query leaves no sticky error
@@ -1167,7 +989,7 @@ int route_max_clusters() {
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false>, &cfg);
         g_max_clusters[dev] = (e == cudaSuccess && n >= 1) ? n : 1;
         cudaGetLastError();
     }
@@ -1180,21 +1002,18 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     void (*kernel)(RouteArgs) = nullptr;
-    if (p.tc) {
-        e = prepare<false, true, false>(dev);
-        kernel = route_cluster_kernel<false, true, false>;
-    } else if (p.ng > 1 && p.half) {
-        e = prepare<true, false, true>(dev);
-        kernel = route_cluster_kernel<true, false, true>;
+    if (p.ng > 1 && p.half) {
+        e = prepare<true, true>(dev);
+        kernel = route_cluster_kernel<true, true>;
     } else if (p.ng > 1) {
-        e = prepare<false, false, true>(dev);
-        kernel = route_cluster_kernel<false, false, true>;
+        e = prepare<false, true>(dev);
+        kernel = route_cluster_kernel<false, true>;
     } else if (p.half) {
-        e = prepare<true, false, false>(dev);
-        kernel = route_cluster_kernel<true, false, false>;
+        e = prepare<true, false>(dev);
+        kernel = route_cluster_kernel<true, false>;
     } else {
-        e = prepare<false, false, false>(dev);
-        kernel = route_cluster_kernel<false, false, false>;
+        e = prepare<false, false>(dev);
+        kernel = route_cluster_kernel<false, false>;
     }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -10,12 +10,10 @@ constexpr int kRouteThreads = 512;        // 16 warps per CTA
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteBatch = 2;            // (tile, k-part) units whose loads a warp keeps in flight
 constexpr int kRouteSpwMax = 8;           // 32-wide k steps per unit, at most
-constexpr int kRouteSmemMax = 200 * 1024;    // dynamic shared memory, at most (mma.sync kernels)
-constexpr int kRouteSmemMaxTc = 220 * 1024;  // the tcgen05 kernel (weight and x tiles)
+constexpr int kRouteSmemMax = 200 * 1024;    // dynamic shared memory, at most
 constexpr int kRouteMaxM = 64;
 constexpr int kRouteRowsPerCluster = 16;  // token rows per cluster of the whole route (one m16 MMA tile)
-constexpr int kRouteGemvRowsPerCluster = 64;  // GEMV-only launches of more than 64 rows (four m16 tiles)
-constexpr int kRouteGemvMaxM = 512;
+constexpr int kRouteGemvMaxM = 512;        // the router GEMV alone (above kRouteMaxM: tcgen05)
 // Expert groups: routes over many experts split them across clusters (each
 // cluster a group of >= kRouteGroupMinN experts) so that more SMs share the
 // gate weight; the groups' top-k candidates meet in scratch.
@@ -56,11 +54,7 @@ struct RouteArgs {
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
     int tok_shift, wpt_shift;  // log2 of tok and wpt (both powers of two)
     int gs_shift;    // gate threshold: log2 of the lane-group size (<= 32 threads)
-    int tc;          // 1: the GEMV runs on tcgen05 (TMEM accumulator), 0: on mma.sync
-    int nmma;        // tcgen05: token columns of the MMA (16..64, multiple of 16)
-    int tmem_cols;   // tcgen05: TMEM columns allocated (power of two >= 32)
     int nslots;      // split-K partials per logit at the owner
-    int off_a, off_b, off_dst;  // tcgen05: weight tile, x tile, transposed accumulator
     // q = (x * magic) >> 32 equals x / d for 0 <= x < 2^21, d <= 1024
     unsigned long long mag_n, mag_k, mag_block, mag_vpr, mag_n4;
     unsigned long long* trace;
@@ -106,7 +100,7 @@ struct RoutePlan {
     int cs, kc, spw, wpt, units, tok, xpitch, clusters, rpc;
     int sh_clusters;  // shared-expert clusters after the route's (0: none)
     int ng, nl, off_merge;  // expert groups, experts per group, merge buffers
-    int tc, nmma, tmem_cols, nslots, off_a, off_b, off_dst;
+    int nslots;
     bool half;
     int smem;
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
@@ -115,17 +109,10 @@ struct RoutePlan {
 inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Returns false when (M, N, K, topk) is outside what the cluster kernel
-// covers with cluster size cs.
-// tcgen05 operand tiles (K-major, no swizzle): core matrices of 8 rows x 16 B;
-// inside one 16-wide k-step, core matrix (row group rg, k half kh) sits at
-// rg * kTcSbo + kh * kTcLbo.  The weight tile always spans 128 rows (the MMA's M).
-constexpr int kTcLbo = 128, kTcSbo = 256;
-constexpr int kTcAStep = 128 * 16 * 2;  // bytes of the weight tile per 16-wide k-step
-
+// covers with cluster size cs (at most kRouteMaxM rows, in both modes).
 // max_groups: co-resident clusters available for expert groups (1: none).
-inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePlan* p, bool allow_tc = true,
-                       int max_groups = 1) {
-    if (M < 1 || M > (mode == 1 ? kRouteMaxM : kRouteGemvMaxM) || N < 8 || N > 1024 || N % 8 != 0) return false;
+inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePlan* p, int max_groups = 1) {
+    if (M < 1 || M > kRouteMaxM || N < 8 || N > 1024 || N % 8 != 0) return false;
     if (K < 32 * cs || K % (32 * cs) != 0) return false;
     RoutePlan q{};
     q.cs = cs;
@@ -137,7 +124,7 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     const int mcl = (M + kRouteRowsPerCluster - 1) / kRouteRowsPerCluster;
     const int split_min = mode == 0 ? 2 * kRouteGemvGroupMinN : kRouteSplitMinN;
     const int group_min = mode == 0 ? kRouteGemvGroupMinN : kRouteGroupMinN;
-    if (max_groups > 1 && !(mode == 0 && M > kRouteMaxM) && !(mode == 1 && mcl > 1) && N >= split_min) {
+    if (max_groups > 1 && !(mode == 1 && mcl > 1) && N >= split_min) {
         int d = max_groups / mcl;
         if (d > kRouteMaxGroups) d = kRouteMaxGroups;
         for (; d >= 2; --d)
@@ -166,13 +153,9 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.wpt = w;
     q.spw = S / w;
     q.units = NT * w;
-    // one cluster per 16 token rows (GEMV alone above 64 rows: per 64 rows);
-    // rows owned per CTA: a power of two covering ceil(rows of a cluster / cs)
-    // (64-row clusters only on tcgen05: without it more than 64 rows take the
-    // split-K GEMV with last-arriver fixup)
-    const bool big = mode == 0 && M > kRouteMaxM;
-    if (big && !(allow_tc && N <= 128 && q.kc % 16 == 0)) return false;
-    q.rpc = big ? kRouteGemvRowsPerCluster : kRouteRowsPerCluster;
+    // one cluster per 16 token rows; rows owned per CTA: a power of two
+    // covering ceil(rows of a cluster / cs)
+    q.rpc = kRouteRowsPerCluster;
     q.clusters = (M + q.rpc - 1) / q.rpc * q.ng;
     const int Mc = M < q.rpc ? M : q.rpc;
     q.tok = 1;
@@ -181,19 +164,14 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     if (ilog2_exact(q.tok) < 0 || ilog2_exact(w) < 0 || ilog2_exact(cs) < 0) return false;
     q.half = M <= 8;
     q.xpitch = q.kc * 2 + (((q.kc * 2) % 128 == 0) ? 64 : 0);
-    // tcgen05 for the GEMV alone above 64 rows (64 token columns per MMA) when
-    // the CTA's weight slice fits one 128-row tile.  At 16 rows its chain of
-    // K/16 dependent MMAs issued by one thread plus the accumulator read-back
-    // is slower than 16 warps of mma.sync (measured), so the decode route
-    // keeps mma.sync.
-    q.tc = big ? 1 : 0;
-    q.nmma = (Mc + 15) / 16 * 16;
-    q.tmem_cols = q.nmma <= 32 ? 32 : 64;
-    q.nslots = q.tc ? cs : cs * w;
+    // (tcgen05 at 16 rows: a chain of K/16 dependent MMAs issued by one
+    // thread plus the accumulator read-back measured slower than 16 warps of
+    // mma.sync, so the decode route keeps mma.sync)
+    q.nslots = cs * w;
 
     int off = 0;
     q.off_x = off;  // row-major x slice (MMA operand of mma.sync; quantiser input)
-    off = align_up(off + ((q.tc && mode == 0) ? 0 : Mc * q.xpitch), 16);
+    off = align_up(off + Mc * q.xpitch, 16);
     q.off_recv = off;
     off = align_up(off + q.nslots * q.tok * N * 4, 16);
     q.off_row = off;
@@ -210,22 +188,58 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.off_merge = off;  // ng > 1: the cluster's candidates as received (keys, then logits); in the
                         // merging CTA all candidates [M][ng][k] (8 B keys, then logits)
     if (mode == 1 && q.ng > 1) off = align_up(off + M * q.ng * topk * 12, 16);
-    if (q.tc) {
-        off = align_up(off, 128);
-        q.off_a = off;  // weight tile, then (after the MMAs) the transposed accumulator
-        const int a_bytes = (q.kc / 16) * kTcAStep, d_bytes = q.nmma * N * 4;
-        off = align_up(off + a_bytes, 128);
-        q.off_b = off;
-        off = align_up(off + (q.kc / 16) * q.nmma * 32, 128);
-        if (d_bytes <= a_bytes) {
-            q.off_dst = q.off_a;
-        } else {
-            q.off_dst = off;
-            off = align_up(off + d_bytes, 16);
-        }
-    }
     q.smem = off;
-    if (q.smem > (q.tc ? kRouteSmemMaxTc : kRouteSmemMax)) return false;
+    if (q.smem > kRouteSmemMax) return false;
+    *p = q;
+    return true;
+}
+
+// Router GEMV alone for kRouteMaxM < M <= kRouteGemvMaxM rows on tcgen05:
+// one cluster of cs CTAs per rpc token rows, CTA c the K slice c.  The
+// slice arrives in stages of kTcStageK k (one 128-byte swizzled row per
+// token or expert), all resident at once: per stage an rpc-row x tile (the
+// MMA's N side) and a 128-row weight tile (its M side; rows past N are never
+// written).  After the CTA's MMAs the weight stages hold the accumulator as
+// [token][expert] rows (when it fits there; else after), and the owners'
+// receive buffers take the x stages' place once every CTA of the cluster has
+// finished its MMAs (or follow the rest when the x stages are smaller).
+// Offsets are from a 1024-byte aligned base inside the dynamic shared memory
+// (1024 bytes of slack).
+constexpr int kTcStageK = 64;
+constexpr int kTcWStageBytes = 128 * 128;
+constexpr int kTcMaxStages = 8;
+constexpr int kTcSmemMax = 226 * 1024;  // dynamic (the per-block maximum is 227 KiB with the static part)
+
+struct TcGemvPlan {
+    int cs, kc, nq, nstage, rpc, tok, clusters, tmem_cols, off_w, off_stage, off_recv, smem;
+};
+
+// fit: clusters resident at once; 64-row clusters when that many cover M,
+// else 128-row clusters.  Returns false outside what the kernel covers.
+inline bool tc_gemv_plan(int M, int N, int K, int cs, int fit, TcGemvPlan* p) {
+    if (M <= kRouteMaxM || M > kRouteGemvMaxM || N < 8 || N > 128 || N % 8 != 0) return false;
+    if (cs < 1 || K < cs || K % cs != 0 || (K / cs) % 16 != 0) return false;
+    TcGemvPlan q{};
+    q.cs = cs;
+    q.kc = K / cs;
+    q.nq = q.kc / 16;
+    q.nstage = (q.kc + kTcStageK - 1) / kTcStageK;
+    if (q.nstage > kTcMaxStages) return false;
+    q.rpc = (M + 63) / 64 <= fit ? 64 : 128;
+    q.clusters = (M + q.rpc - 1) / q.rpc;
+    q.tok = 1;
+    while (q.tok * cs < q.rpc) q.tok *= 2;
+    q.tmem_cols = q.rpc;  // fp32 accumulator: 128 lanes (experts) x rpc columns (tokens)
+    const int xbytes = q.nstage * q.rpc * 128, wbytes = q.nstage * kTcWStageBytes;
+    const int sbytes = q.rpc * N * 4, rbytes = cs * q.tok * N * 4;
+    q.off_w = xbytes;
+    int end = xbytes + wbytes;
+    q.off_stage = sbytes <= wbytes ? q.off_w : end;
+    if (sbytes > wbytes) end += sbytes;
+    q.off_recv = rbytes <= xbytes ? 0 : end;
+    if (rbytes > xbytes) end += rbytes;
+    q.smem = 1024 + end;
+    if (q.smem > kTcSmemMax) return false;
     *p = q;
     return true;
 }

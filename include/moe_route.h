@@ -152,6 +152,10 @@ int mr_device_error(int clear);
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mr_status_string(int status);
 
+/* The cudaError_t value behind the calling thread's most recent
+ * MR_ERR_CUDA (0 when no call of this thread has returned MR_ERR_CUDA). */
+int mr_last_cuda_error(void);
+
 /* MR_ABI_VERSION of the loaded library. */
 int mr_abi_version(void);
 

@@ -56,9 +56,9 @@ def test_router_gemv_matches_oracle(mr, cid, M):
 
 @pytest.mark.parametrize("M,legacy", [(65, 0), (100, 0), (129, 0), (200, 0), (512, 0), (100, 1), (512, 1)])
 def test_router_gemv_rows_past_64(mr, M, legacy):
-    """More than 64 rows: cluster split-K over 64-row clusters on tcgen05
-    (ragged last cluster), or with the legacy launch option the split-K
-    mma.sync GEMV with last-arriver fixup."""
+    """More than 64 rows: the tensor-core GEMV (ragged last cluster), or with
+    the legacy launch option the split-K mma.sync GEMV with last-arriver
+    fixup."""
     x, w = inputs.router_inputs(M, 6144, 128, 7)
     scratch = mr.Scratch(M, 128, 6144, 8)
     flags = mr.get_launch_flags()

@@ -14,7 +14,7 @@ PROBE = r'''
 #include <initializer_list>
 #include "route_plan.h"
 int main() {
-    const int Ms[] = {1, 2, 3, 4, 7, 8, 9, 15, 16, 17, 31, 32, 33, 47, 63, 64, 65, 100, 128, 200, 256, 257, 512};
+    const int Ms[] = {1, 2, 3, 4, 7, 8, 9, 15, 16, 17, 31, 32, 33, 47, 63, 64, 65, 100};
     const int Ns[] = {8, 40, 64, 128, 136, 256, 512, 640, 896, 1024};
     const int Ks[] = {512, 1024, 3584, 6144, 7168};
     const int topks[] = {1, 4, 8, 16, 32};
@@ -23,9 +23,9 @@ int main() {
     for (int M : Ms) for (int N : Ns) for (int K : Ks) for (int k : topks) {
         if (k > N) continue;
         mr::RoutePlan p;
-        if (!mr::route_plan(M, N, K, k, mode, 16, &p, true, mg)) { printf("none %d %d %d %d %d %d\n", mg, mode, M, N, K, k); continue; }
-        printf("plan %d %d %d %d %d %d ng=%d nl=%d clusters=%d rpc=%d tok=%d wpt=%d spw=%d nslots=%d smem=%d tc=%d cs=%d kc=%d half=%d\n",
-               mg, mode, M, N, K, k, p.ng, p.nl, p.clusters, p.rpc, p.tok, p.wpt, p.spw, p.nslots, p.smem, p.tc, p.cs,
+        if (!mr::route_plan(M, N, K, k, mode, 16, &p, mg)) { printf("none %d %d %d %d %d %d\n", mg, mode, M, N, K, k); continue; }
+        printf("plan %d %d %d %d %d %d ng=%d nl=%d clusters=%d rpc=%d tok=%d wpt=%d spw=%d nslots=%d smem=%d cs=%d kc=%d half=%d\n",
+               mg, mode, M, N, K, k, p.ng, p.nl, p.clusters, p.rpc, p.tok, p.wpt, p.spw, p.nslots, p.smem, p.cs,
                p.kc, (int)p.half);
     }
 }
@@ -70,11 +70,11 @@ def test_plans_keep_the_kernel_invariants(plans):
         assert pow2(p["tok"]) and pow2(p["wpt"]) and p["tok"] * 16 >= min(M, p["rpc"])
         assert p["wpt"] * p["spw"] * 32 == p["kc"] and p["spw"] <= 8
         assert p["nslots"] % 8 == 0
-        assert p["smem"] <= (220 if p["tc"] else 200) * 1024 and p["smem"] % 16 == 0
-        assert p["tc"] == (1 if (mode == 0 and M > 64) else 0)
+        assert p["smem"] <= 200 * 1024 and p["smem"] % 16 == 0
         assert p["half"] == (1 if M <= 8 else 0)
+        assert M <= 64 and p["rpc"] == 16          # above 64 rows: the tensor-core GEMV's own plan
         if mode == 1:
-            assert M <= 64 and p["tok"] <= 16
+            assert p["tok"] <= 16
     assert n_plans > 1000
 
 
@@ -84,8 +84,7 @@ def test_every_documented_decode_shape_has_a_plan(plans):
         assert (9, 1, M, 128, 6144, 8) in have
     for M in (1, 8, 16, 32):
         assert (9, 1, M, 896, 3584, 16) in have
-    for M in (128, 256, 512):
-        assert (9, 0, M, 128, 6144, 1) in have
+    assert not any(key[2] > 64 for key in have)
 
 
 def test_expert_groups_keep_the_split_k_of_the_unsplit_plan(plans):
@@ -97,11 +96,11 @@ def test_expert_groups_keep_the_split_k_of_the_unsplit_plan(plans):
     n = 0
     for (mg, mode, M, N, K, k), p in by_key.items():
         ref = by_key.get((1, mode, M, N, K, k))
-        if ref is not None and not p["tc"]:
+        if ref is not None:
             assert (p["wpt"], p["spw"], p["nslots"]) == (ref["wpt"], ref["spw"], ref["nslots"])
             n += p["ng"] > 1
         route = by_key.get((mg, 1, M, N, K, k))
-        if mode == 0 and route is not None and not p["tc"]:
+        if mode == 0 and route is not None:
             assert (p["wpt"], p["spw"], p["nslots"]) == (route["wpt"], route["spw"], route["nslots"])
     assert n > 100
 
@@ -162,3 +161,78 @@ def test_shared_plan_invariants(tmp_path):
     have = {tuple(int(v) for v in line.split()[1:5]) for line in lines if line.startswith("plan")}
     for M in range(1, 17):
         assert (16, M, 6144, 768) in have and (16, M, 6144, 1536) in have and (8, M, 6144, 768) in have
+
+
+TC_PROBE = r"""
+#include <cstdio>
+#include <initializer_list>
+#include "route_plan.h"
+int main() {
+    for (int cs : {8, 16})
+    for (int fit : {1, 4, 7, 8, 16})
+    for (int M : {1, 64, 65, 100, 128, 129, 200, 256, 300, 448, 449, 512, 513})
+    for (int N : {8, 40, 64, 120, 128, 136, 1024})
+    for (int K : {512, 1024, 3584, 6144, 7168, 8192}) {
+        mr::TcGemvPlan p;
+        if (!mr::tc_gemv_plan(M, N, K, cs, fit, &p)) { printf("none %d %d %d %d %d\n", cs, fit, M, N, K); continue; }
+        printf("plan %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d\n", cs, fit, M, N, K, p.kc, p.nq, p.nstage,
+               p.rpc, p.tok, p.clusters, p.tmem_cols, p.off_w, p.off_stage, p.off_recv, p.smem, p.cs);
+    }
+}
+"""
+
+
+def test_tc_gemv_plan_invariants(tmp_path):
+    """Every plan of the tensor-core GEMV (64 < M <= 512, N <= 128) keeps
+    what the kernel relies on: whole 16-wide k-steps per CTA, at most 8
+    resident 64-wide stages, 1024-byte aligned swizzled stage tiles, 64-row
+    clusters exactly when that many are resident at once (else 128-row), the
+    owners' token rows, the accumulator's columns, and the transposed rows
+    and receive buffers inside the dead stages or after them, disjoint."""
+    src = tmp_path / "probe.cpp"
+    src.write_text(TC_PROBE)
+    exe = tmp_path / "probe"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", os.path.join(ROOT, "decode_expert_routing_gb300", "csrc"),
+                    "-o", str(exe), str(src)], check=True)
+    lines = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()
+    pow2 = lambda v: v > 0 and (v & (v - 1)) == 0
+    have = {}
+    for line in lines:
+        f = line.split()
+        cs, fit, M, N, K = (int(v) for v in f[1:6])
+        if f[0] == "none":
+            kc = K // cs
+            rpc = 64 if -(-M // 64) <= fit else 128
+            assert (M <= 64 or M > 512 or N > 128 or N % 8 or K % cs or kc % 16
+                    or -(-kc // 64) > 8 or 1024 + (rpc * 128 + 16384) * -(-kc // 64) > 226 * 1024)
+            continue
+        kc, nq, nstage, rpc, tok, clusters, tcols, off_w, off_stage, off_recv, smem, pcs = (int(v) for v in f[6:])
+        have[(cs, fit, M, N, K)] = dict(rpc=rpc, clusters=clusters, smem=smem)
+        assert 64 < M <= 512 and N <= 128 and N % 8 == 0 and pcs == cs
+        assert kc * cs == K and kc % 16 == 0 and nq == kc // 16 and nstage == -(-kc // 64) <= 8
+        assert rpc == (64 if -(-M // 64) <= fit else 128) and clusters == -(-M // rpc)
+        assert pow2(tok) and tok * cs >= rpc and tok * cs < 2 * rpc
+        assert tcols == rpc
+        xbytes, wbytes = nstage * rpc * 128, nstage * 16384
+        assert off_w == xbytes and off_w % 1024 == 0 and (rpc * 128) % 1024 == 0
+        regions = [(0, xbytes), (off_w, off_w + wbytes)]
+        sbytes, rbytes = rpc * N * 4, cs * tok * N * 4
+        if sbytes <= wbytes:
+            assert off_stage == off_w
+        else:
+            assert off_stage >= off_w + wbytes
+            regions.append((off_stage, off_stage + sbytes))
+        if rbytes <= xbytes:
+            assert off_recv == 0
+        else:
+            assert off_recv >= off_w + wbytes
+            regions.append((off_recv, off_recv + rbytes))
+        regions.sort()
+        assert all(a[1] <= b[0] for a, b in zip(regions, regions[1:]))
+        assert off_stage % 16 == 0 and off_recv % 16 == 0
+        assert smem == 1024 + regions[-1][1] and smem <= 226 * 1024
+    big = have[(16, 7, 512, 128, 6144)]
+    assert big["rpc"] == 128 and big["clusters"] == 4          # one wave where 64-row clusters would need 8
+    assert have[(16, 7, 448, 128, 6144)]["clusters"] == 7
+    for M in (65, 128, 256, 512):
+        assert (16, 7, M, 128, 6144) in have and (16, 7, M, 128, 7168) in have
