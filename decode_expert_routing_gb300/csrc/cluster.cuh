@@ -75,9 +75,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 
 // Another CTA's mbarrier of the same cluster (address from map_rank): one
-// arrival, ordered after this thread's earlier memory operations.
+// relaxed arrival.  A release at cluster scope would first wait for every
+// earlier write of the thread, global ones included, to be performed (some
+// hundreds of cycles); callers arrive after a wait whose outcome the
+// receiver relies on, and the arrival cannot be performed before that wait
+// has returned.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // One arrival on a local mbarrier.
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {

@@ -91,9 +91,10 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
 
 // Optional phase stamps (compile with -DMR_TRACE), 512 u64 per CTA at
 // trace + (blockIdx.y * gridDim.x + blockIdx.x) * 512.  %globaltimer (ns):
-// MR_TRACE_STAMP: thread 0 writes slot (< 32); MR_TRACE_WARP: lane 0 of every
-// warp writes slot 32 + 16 * phase + warp (phase < 14, 16 warps at most).
-// %clock64 (SM cycles): MR_TRACE_CLK: thread 0 writes slot 256 + slot.
+// MR_TRACE_STAMP: thread 0 writes slot (< 32), and %clock64 (SM cycles) at
+// slot 288 + slot; MR_TRACE_WARP: lane 0 of every warp writes slot
+// 32 + 16 * phase + warp (phase < 14, 16 warps at most).
+// MR_TRACE_CLK: thread 0 writes %clock64 at slot 256 + slot (< 32).
 #ifdef MR_TRACE
 #define MR_TRACE_AT(trace, slot)                                                     \
     do {                                                                             \
@@ -103,7 +104,10 @@ __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_sl
     } while (0)
 #define MR_TRACE_STAMP(trace, slot)                                                  \
     do {                                                                             \
-        if (threadIdx.x == 0 && (trace) != nullptr) MR_TRACE_AT(trace, slot);        \
+        if (threadIdx.x == 0 && (trace) != nullptr) {                                \
+            MR_TRACE_AT(trace, slot);                                                \
+            (trace)[(blockIdx.y * gridDim.x + blockIdx.x) * 512 + 288 + (slot)] = clock64(); \
+        }                                                                            \
     } while (0)
 #define MR_TRACE_WARP(trace, phase)                                                  \
     do {                                                                             \

@@ -4,8 +4,8 @@
 // The pages' router GEMV (sglang #36557, description: split-K partial dots
 // with an in-kernel fixup) at prefill-sized row counts is a small GEMM:
 // D[M x N] = x[M x K] . W[N x K]^T with K = 6144.  Here one cluster of CS
-// CTAs takes RPC token rows (64, or 128 when the 64-row clusters would not
-// all be resident at once) and CTA c the K slice [c*K/CS, (c+1)*K/CS):
+// CTAs takes RPC token rows (M spread over the clusters resident at once, a
+// multiple of 16) and CTA c the K slice [c*K/CS, (c+1)*K/CS):
 //
 //   1. The tensor memory accelerator copies the slice in stages of 64 k, one
 //      128-byte swizzled row per expert or token: every weight stage before
@@ -44,7 +44,6 @@ struct TcGemvArgs {
     unsigned long long* trace;
     unsigned long long wait_ns;
     int M, N, kc, nq, nstage, rpc, tok, tok_shift, cs, tmem_cols, off_w, off_stage, off_recv;
-    int stage_bytes;  // bytes one stage's two copies bring (rpc + N rows of 128 bytes)
     int flags;        // launch options (bit 1: a test stall, bytes that never come)
 };
 
@@ -86,7 +85,8 @@ __device__ __forceinline__ uint32_t bf16_idesc(int m, int n) {
 
 __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_constant__ TcGemvArgs a) {
     extern __shared__ unsigned char dsm[];
-    __shared__ __align__(8) unsigned long long s_full[kTcMaxStages];  // stage s landed
+    __shared__ __align__(8) unsigned long long s_full[kTcMaxStages];   // x stage s landed
+    __shared__ __align__(8) unsigned long long s_wfull[kTcMaxStages];  // weight stage s landed
     // [0] MMAs done, [1] the cluster's MMAs done, [2] partials in, [3] this CTA's copies landed
     __shared__ __align__(8) unsigned long long s_bar[4];
     __shared__ int s_ok[4];
@@ -107,7 +107,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
     const uint32_t xstage = (uint32_t)rpc * 128u;
     MR_TRACE_STAMP(a.trace, 0);
     if (tid == 0) {
-        for (int s = 0; s < a.nstage; ++s) mbar_init(smem_u32(&s_full[s]), 1);
+        for (int s = 0; s < a.nstage; ++s) {
+            mbar_init(smem_u32(&s_full[s]), 1);
+            mbar_init(smem_u32(&s_wfull[s]), 1);
+        }
         mbar_init(bar_mma, 1);
         mbar_init(bar_done, (unsigned)a.cs);
         mbar_init(bar_recv, 1);
@@ -118,8 +121,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
         tma_prefetch_map(&a.tm_w);
         tma_prefetch_map(&a.tm_x);
         for (int s = 0; s < a.nstage; ++s) {
-            const uint32_t full = smem_u32(&s_full[s]);
-            mbar_expect_tx(full, (unsigned)a.stage_bytes);
+            const uint32_t full = smem_u32(&s_wfull[s]);
+            mbar_expect_tx(full, (unsigned)(N * kTcStageK * 2));
             tma_load_2d(ws + (uint32_t)(s * kTcWStageBytes), &a.tm_w, kslice + s * kTcStageK, 0, full);
         }
     }
@@ -134,8 +137,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
     pdl_wait();
     MR_TRACE_STAMP(a.trace, 8);
     if (tid == 0)
-        for (int s = 0; s < a.nstage; ++s)
-            tma_load_2d(xs + (uint32_t)s * xstage, &a.tm_x, kslice + s * kTcStageK, row0, smem_u32(&s_full[s]));
+        for (int s = 0; s < a.nstage; ++s) {
+            const uint32_t full = smem_u32(&s_full[s]);
+            mbar_expect_tx(full, (unsigned)(rpc * kTcStageK * 2));
+            tma_load_2d(xs + (uint32_t)s * xstage, &a.tm_x, kslice + s * kTcStageK, row0, full);
+        }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -148,6 +154,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
         for (int s = 0; s < a.nstage; ++s) {
             // (after a wait that ran out, the later stages are still waited
             // for, bounded, so that no copy is left in flight)
+            if (!tc_wait0(smem_u32(&s_wfull[s]), a.wait_ns)) fail = 1;
+            MR_TRACE_STAMP(a.trace, 22 + s);
             if (!tc_wait0(smem_u32(&s_full[s]), a.wait_ns)) fail = 1;
             MR_TRACE_STAMP(a.trace, 16 + s);
             if (fail) continue;
@@ -234,8 +242,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
         if (tid < a.cs) mbar_arrive_remote(map_rank(bar_fin, (unsigned)tid));
         const float* rv = reinterpret_cast<const float*>(dsm + (recv - smem_u32(dsm)));
         const int plane = tok * N;  // floats between two slices' partials
-        for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
-            const int rl = idx / N, n = idx - rl * N;
+        const int n = tid & 127;    // expert n (N <= 128) of rows tid / 128, + 4, ...
+        for (int rl = tid >> 7; rl < my_rows && n < N; rl += kRouteThreads / 128) {
             const float* pp = rv + rl * N + n;
             float sum = 0.0f;
             for (int sl = 0; sl < a.cs; sl += 8) {  // cs is 8 or 16: loads first, then the adds in order
@@ -316,7 +324,6 @@ int launch_tc_gemv(const TcGemvPlan& p, const void* x, int64_t ldx, const void* 
     a.off_w = p.off_w;
     a.off_stage = p.off_stage;
     a.off_recv = p.off_recv;
-    a.stage_bytes = (p.rpc + N) * kTcStageK * 2;
     a.flags = launch_flags();
     if (!g_prepared[dev]) {
         if ((*err = cudaFuncSetAttribute(tc_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemMax)) !=

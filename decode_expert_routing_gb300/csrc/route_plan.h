@@ -214,8 +214,11 @@ struct TcGemvPlan {
     int cs, kc, nq, nstage, rpc, tok, clusters, tmem_cols, off_w, off_stage, off_recv, smem;
 };
 
-// fit: clusters resident at once; 64-row clusters when that many cover M,
-// else 128-row clusters.  Returns false outside what the kernel covers.
+// fit: clusters resident at once.  Rows per cluster: M spread over fit
+// clusters, rounded up to a multiple of 16 (the MMA's N), 16 to 128: the
+// fewer rows a cluster takes, the fewer bytes of x each CTA loads and of
+// partials it sends (rpc x N fp32); the MMAs per CTA stay K / (16 cs).
+// Returns false outside what the kernel covers.
 inline bool tc_gemv_plan(int M, int N, int K, int cs, int fit, TcGemvPlan* p) {
     if (M <= kRouteMaxM || M > kRouteGemvMaxM || N < 8 || N > 128 || N % 8 != 0) return false;
     if (cs < 1 || K < cs || K % cs != 0 || (K / cs) % 16 != 0) return false;
@@ -225,11 +228,15 @@ inline bool tc_gemv_plan(int M, int N, int K, int cs, int fit, TcGemvPlan* p) {
     q.nq = q.kc / 16;
     q.nstage = (q.kc + kTcStageK - 1) / kTcStageK;
     if (q.nstage > kTcMaxStages) return false;
-    q.rpc = (M + 63) / 64 <= fit ? 64 : 128;
+    const int f = fit < 1 ? 1 : fit;
+    q.rpc = ((M + f - 1) / f + 15) / 16 * 16;
+    if (q.rpc < 16) q.rpc = 16;
+    if (q.rpc > 128) q.rpc = 128;
     q.clusters = (M + q.rpc - 1) / q.rpc;
     q.tok = 1;
     while (q.tok * cs < q.rpc) q.tok *= 2;
-    q.tmem_cols = q.rpc;  // fp32 accumulator: 128 lanes (experts) x rpc columns (tokens)
+    q.tmem_cols = 32;  // fp32 accumulator: 128 lanes (experts) x rpc columns (tokens)
+    while (q.tmem_cols < q.rpc) q.tmem_cols *= 2;
     const int xbytes = q.nstage * q.rpc * 128, wbytes = q.nstage * kTcWStageBytes;
     const int sbytes = q.rpc * N * 4, rbytes = cs * q.tok * N * 4;
     q.off_w = xbytes;

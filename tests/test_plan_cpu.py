@@ -185,10 +185,11 @@ int main() {
 def test_tc_gemv_plan_invariants(tmp_path):
     """Every plan of the tensor-core GEMV (64 < M <= 512, N <= 128) keeps
     what the kernel relies on: whole 16-wide k-steps per CTA, at most 8
-    resident 64-wide stages, 1024-byte aligned swizzled stage tiles, 64-row
-    clusters exactly when that many are resident at once (else 128-row), the
-    owners' token rows, the accumulator's columns, and the transposed rows
-    and receive buffers inside the dead stages or after them, disjoint."""
+    resident 64-wide stages, 1024-byte aligned swizzled stage tiles, rows per
+    cluster a multiple of 16 spreading M over the resident clusters (one
+    wave), the owners' token rows, the accumulator's columns, and the
+    transposed rows and receive buffers inside the dead stages or after them,
+    disjoint."""
     src = tmp_path / "probe.cpp"
     src.write_text(TC_PROBE)
     exe = tmp_path / "probe"
@@ -202,7 +203,7 @@ def test_tc_gemv_plan_invariants(tmp_path):
         cs, fit, M, N, K = (int(v) for v in f[1:6])
         if f[0] == "none":
             kc = K // cs
-            rpc = 64 if -(-M // 64) <= fit else 128
+            rpc = min(128, max(16, -(-(-(-M // fit)) // 16) * 16))
             assert (M <= 64 or M > 512 or N > 128 or N % 8 or K % cs or kc % 16
                     or -(-kc // 64) > 8 or 1024 + (rpc * 128 + 16384) * -(-kc // 64) > 226 * 1024)
             continue
@@ -210,9 +211,10 @@ def test_tc_gemv_plan_invariants(tmp_path):
         have[(cs, fit, M, N, K)] = dict(rpc=rpc, clusters=clusters, smem=smem)
         assert 64 < M <= 512 and N <= 128 and N % 8 == 0 and pcs == cs
         assert kc * cs == K and kc % 16 == 0 and nq == kc // 16 and nstage == -(-kc // 64) <= 8
-        assert rpc == (64 if -(-M // 64) <= fit else 128) and clusters == -(-M // rpc)
-        assert pow2(tok) and tok * cs >= rpc and tok * cs < 2 * rpc
-        assert tcols == rpc
+        assert rpc == min(128, max(16, -(-(-(-M // fit)) // 16) * 16)) and clusters == -(-M // rpc)
+        assert clusters <= fit or rpc == 128                       # one wave whenever 128-row clusters allow it
+        assert pow2(tok) and tok * cs >= rpc and (tok == 1 or tok * cs < 2 * rpc)
+        assert pow2(tcols) and tcols >= max(32, rpc) and tcols < 2 * max(32, rpc)
         xbytes, wbytes = nstage * rpc * 128, nstage * 16384
         assert off_w == xbytes and off_w % 1024 == 0 and (rpc * 128) % 1024 == 0
         regions = [(0, xbytes), (off_w, off_w + wbytes)]
@@ -232,7 +234,7 @@ def test_tc_gemv_plan_invariants(tmp_path):
         assert off_stage % 16 == 0 and off_recv % 16 == 0
         assert smem == 1024 + regions[-1][1] and smem <= 226 * 1024
     big = have[(16, 7, 512, 128, 6144)]
-    assert big["rpc"] == 128 and big["clusters"] == 4          # one wave where 64-row clusters would need 8
-    assert have[(16, 7, 448, 128, 6144)]["clusters"] == 7
+    assert big["rpc"] == 80 and big["clusters"] == 7           # one wave where 64-row clusters would need 8
+    assert have[(16, 7, 448, 128, 6144)]["rpc"] == 64 and have[(16, 7, 128, 128, 6144)]["clusters"] == 4
     for M in (65, 128, 256, 512):
         assert (16, 7, M, 128, 6144) in have and (16, 7, M, 128, 7168) in have
