@@ -211,23 +211,40 @@ __device__ __forceinline__ void row_weights(const RouteArgs& a, const float* row
 // its two MMAs (acc += block sum * 2^X, one fused multiply-add).  Partial
 // sums go by st.async to the CTA that owns the token row, which adds the
 // split-K partials in a fixed order and writes bf16(silu(gate) * up).
-// Inlined at its one call site: as an out-of-line function reading the
-// launch's parameters through a reference it measured 1.8 us slower.
-static __device__ __forceinline__ void shared_gate_up_cta(const RouteArgs& a, int sc) {
+// Out of line (inlined, it made every cold launch of the route ~2 us
+// slower); it reads each launch value it needs once, on entry.
+static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int sc) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) unsigned long long s_shbar;
     __shared__ int s_shok;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c = (int)cluster_rank();
+    // every launch value this function uses, read once here (through the
+    // reference the compiler would read some again after every store)
     const int Mq = a.M, K = a.K, kc = a.kc, P = a.sh_pairs, R = 2 * P, I = a.sh_I;
     const int tok = a.tok, wpt = a.sh_wpt, spw = a.sh_spw, nslots = a.sh_nslots;
+    const int xpitch = a.xpitch, units = a.sh_units, tok_shift = a.tok_shift, spitch = a.sh_spitch;
+    const int flags = a.flags;
+    const unsigned long long wait_ns = a.wait_ns;
+    const int64_t ldx = a.ldx;
+    const uint16_t* const xg = a.x;
+    const uint16_t* const norm_w = a.norm_w;
+    const float* const rstd = a.rstd;
+    const bool gemma = a.norm_gemma != 0;
+    const uint8_t* const wg8 = a.sh_w;
+    const uint8_t* const sg8 = a.sh_scale;
+    uint16_t* const out = a.sh_out;
+    unsigned char* const ws = sm + a.sh_off_w;
+    unsigned char* const ss = sm + a.sh_off_s;
+    unsigned char* const xs = sm + a.sh_off_x;
+    const uint32_t recv_local = smem_u32(sm + a.sh_off_recv);
     const int my_rows = max(0, min(tok, Mq - c * tok));
     const int pair0 = sc * P;
     const uint32_t bar = smem_u32(&s_shbar);
     if (tid == 0) {
         mbar_init(bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const unsigned stall = (a.flags & 2) ? 16u : 0u;  // test hook: bytes that never come
+        const unsigned stall = (flags & 2) ? 16u : 0u;  // test hook: bytes that never come
         if (my_rows > 0) mbar_expect_tx(bar, (unsigned)(my_rows * nslots * R * 4) + stall);
     }
     cluster_arrive_relaxed();
@@ -240,9 +257,7 @@ static __device__ __forceinline__ void shared_gate_up_cta(const RouteArgs& a, in
     // then units u = warp, warp + 16, ... (tile j = u / wpt, k-part p =
     // u % wpt) read them from there in a rolled loop (a CTA runs it once, from
     // a cold instruction cache).
-    unsigned char* ws = sm + a.sh_off_w;
-    unsigned char* ss = sm + a.sh_off_s;
-    const int wpitch = kc + 16, spitch = a.sh_spitch, cpr = kc / 16, spr = kc / 32;
+    const int wpitch = kc + 16, cpr = kc / 16, spr = kc / 32;
     // 16-byte chunk cc of local row lr: thread tid takes chunk tid % cpr of
     // rows tid / cpr, + 512 / cpr, ... when cpr divides 512 (kc = 384:
     // cpr = 24 does not, so the (row, chunk) pair advances with a carry)
@@ -255,13 +270,13 @@ static __device__ __forceinline__ void shared_gate_up_cta(const RouteArgs& a, in
                 if (++lr >= R) break;
             }
             const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
-            cp_async16(smem_u32(ws + lr * wpitch + cc * 16), a.sh_w + gr * K + kslice + cc * 16);
+            cp_async16(smem_u32(ws + lr * wpitch + cc * 16), wg8 + gr * K + kslice + cc * 16);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid < R) {  // a thread per row: its kc / 32 scale bytes, 8 loads in flight at a time
         const int64_t gr = tid < P ? pair0 + tid : I + pair0 + (tid - P);
-        const uint8_t* src = a.sh_scale + gr * K32 + kslice / 32;
+        const uint8_t* src = sg8 + gr * K32 + kslice / 32;
         for (int b0 = 0; b0 < spr; b0 += 8) {
             uint8_t v[8];
 #pragma unroll
@@ -273,25 +288,22 @@ static __device__ __forceinline__ void shared_gate_up_cta(const RouteArgs& a, in
     }
     pdl_wait();
     // the x slice -> shared memory (on the norm's scale when rstd is given)
-    unsigned char* xs = sm + a.sh_off_x;
     const int vpr = kc / 8;
     for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
         const int r = v / vpr, cv = v - r * vpr;
-        uint4 d = ld_ro_v4(a.x + (int64_t)r * a.ldx + kslice + cv * 8);
-        if (a.rstd != nullptr)
-            d = norm_chunk(d, ld_ro_v4(a.norm_w + kslice + cv * 8), __ldg(a.rstd + r), a.norm_gemma != 0);
-        *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
+        uint4 d = ld_ro_v4(xg + (int64_t)r * ldx + kslice + cv * 8);
+        if (rstd != nullptr) d = norm_chunk(d, ld_ro_v4(norm_w + kslice + cv * 8), __ldg(rstd + r), gemma);
+        *reinterpret_cast<uint4*>(xs + r * xpitch + cv * 16) = d;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
-    const uint32_t recv_local = smem_u32(sm + a.sh_off_recv);
     uint32_t owner_bar[2] = {0u, 0u};
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-        if (g + 8 * h < Mq) owner_bar[h] = map_rank(bar, (unsigned)((g + 8 * h) >> a.tok_shift));
+        if (g + 8 * h < Mq) owner_bar[h] = map_rank(bar, (unsigned)((g + 8 * h) >> tok_shift));
 #pragma unroll 1
-    for (int u = warp; u < a.sh_units; u += kRouteWarps) {
+    for (int u = warp; u < units; u += kRouteWarps) {
         const int j = u / wpt, p = u - j * wpt;
         const unsigned char* wrow = ws + (j * 8 + g) * wpitch + p * spw * 32 + 8 * t;
         const unsigned char* srow0 = ss + (j * 8 + 2 * t) * spitch + p * spw;
@@ -300,8 +312,8 @@ static __device__ __forceinline__ void shared_gate_up_cta(const RouteArgs& a, in
         for (int s = 0; s < kRouteSpwMax; ++s) {
             if (s < spw) {
                 const int kk = (p * spw + s) * 32 + 8 * t;
-                const uint4 xa = g < Mq ? lds128(xs + g * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
-                const uint4 xb = g + 8 < Mq ? lds128(xs + (g + 8) * a.xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 xa = g < Mq ? lds128(xs + g * xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 xb = g + 8 < Mq ? lds128(xs + (g + 8) * xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
                 const uint2 w8 = *reinterpret_cast<const uint2*>(wrow + s * 32);
                 const uint32_t b0 = e4m3x2_to_bf16x2(w8.x), b1 = e4m3x2_to_bf16x2(w8.x >> 16);
                 const uint32_t b2 = e4m3x2_to_bf16x2(w8.y), b3 = e4m3x2_to_bf16x2(w8.y >> 16);
@@ -320,16 +332,16 @@ static __device__ __forceinline__ void shared_gate_up_cta(const RouteArgs& a, in
         for (int h = 0; h < 2; ++h) {
             const int r = g + 8 * h;
             if (r < Mq) {
-                const int own = r >> a.tok_shift, rl = r & (tok - 1);
+                const int own = r >> tok_shift, rl = r & (tok - 1);
                 const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * R + col) * 4);
                 st_async_f2(map_rank(la, (unsigned)own), acc[2 * h], acc[2 * h + 1], owner_bar[h]);
             }
         }
     }
     if (my_rows == 0) return;
-    if (!cta_wait_bytes(bar, a.wait_ns, &s_shok)) return;
+    if (!cta_wait_bytes(bar, wait_ns, &s_shok)) return;
     // owner: pair i of each owned row; partials added in slot order
-    const float* recv = reinterpret_cast<const float*>(sm + a.sh_off_recv);
+    const float* recv = reinterpret_cast<const float*>(sm + (recv_local - smem_u32(sm)));
     const int plane = tok * R;
     for (int idx = tid; idx < my_rows * P; idx += kRouteThreads) {
         const int rl = idx / P, i = idx - rl * P;
@@ -351,7 +363,7 @@ static __device__ __forceinline__ void shared_gate_up_cta(const RouteArgs& a, in
         const float act = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs))), us);
         uint16_t b;
         asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(act));
-        a.sh_out[(int64_t)(c * tok + rl) * I + pair0 + i] = b;
+        out[(int64_t)(c * tok + rl) * I + pair0 + i] = b;
     }
 }
 
