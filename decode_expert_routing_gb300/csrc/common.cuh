@@ -152,15 +152,13 @@ __device__ __forceinline__ float warp_sum_fixed(float v) {
 
 // E8M0 exponent X of a 32-block from the largest |x| as a bf16 magnitude
 // pattern (sign cleared): X = floor(log2(amax)) - emax (8 for E4M3, 2 for
-// E2M1), clamped to [-127, 127]; amax == 0 gives -127.  Integer-exact:
-// normal bf16 -> exponent field - 127, subnormal bf16 (value = mant * 2^-133)
-// -> msb(mant) - 133.
+// E2M1), clamped to [-127, 127]; amax == 0 gives -127.  For a normal bf16
+// floor(log2(amax)) is its exponent field e minus 127; a subnormal or zero
+// amax (e = 0) has floor(log2) <= -127, so X <= -129 clamps to -127, as
+// e - 127 - emax does; e <= 255 keeps X <= 128 - emax < 127.  So X is
+// max(e - 127 - emax, -127) for every pattern.
 __device__ __forceinline__ int mx_scale_exponent(unsigned amax16, int emax) {
-    if (amax16 == 0u) return -127;
-    unsigned e = amax16 >> 7;
-    int fl = (e != 0u) ? (int)e - 127 : (31 - __clz((int)(amax16 & 0x7Fu))) - 133;
-    int X = fl - emax;
-    return X < -127 ? -127 : (X > 127 ? 127 : X);
+    return max((int)(amax16 >> 7) - 127 - emax, -127);
 }
 
 // Largest |x| of a 32-block as a bf16 magnitude pattern: the 8 values of v
