@@ -48,6 +48,7 @@ def test_version_and_status_strings(lib):
         assert lib.mr_status_string(s).startswith(b"MR_")
     assert b"SCRATCH_DIRTY" in lib.mr_status_string(mr.MR_ERR_SCRATCH_DIRTY)
     assert lib.mr_status_string(99) == b"unknown mr_status"
+    assert lib.mr_last_cuda_error() == 0  # no call of this thread has returned MR_ERR_CUDA
 
 
 def test_shape_predicate(lib):
