@@ -160,6 +160,11 @@ size_t mr_scratch_bytes(int M_max, int N, int K, int topk) {
             const size_t b = mr::gemv_work_bytes(p, M, N);
             if (b > work) work = b;
         }
+        mr::TcGemvPlan tp;  // the tensor-core GEMV's partials (a bound over every resident-cluster count)
+        if (mr::tc_gemv_plan(M, N, K, 16, 1, &tp)) {
+            const size_t b = (size_t)mr::tc_gemv_part_bound(M, N);
+            if (b > work) work = b;
+        }
     }
     if (M_max > mr::kRouteRowsPerCluster) {  // fused route over several clusters: every token's ids
         const int Mf = M_max < mr::kRouteMaxM ? M_max : mr::kRouteMaxM;
@@ -235,12 +240,14 @@ int mr_router_gemv(const void* x, int64_t ldx, const void* w, float* logits, int
     if (w == nullptr || !aligned(w, 16) || logits == nullptr || !aligned(logits, 8) || N < 1)
         return MR_ERR_INVALID_ARG;
     if (K % MR_GEMV_K_MULTIPLE != 0) return MR_ERR_UNSUPPORTED;
-    if (M > mr::kRouteMaxM && allow_tc()) {  // above 64 rows: tcgen05 when its plan fits
+    if (M > mr::kRouteMaxM && allow_tc()) {  // above 64 rows: tcgen05 when its plan and the scratch fit
         mr::TcGemvPlan tp;
-        if (mr::tc_gemv_plan(M, N, K, mr::route_cluster_size(), mr::route_max_clusters(), &tp))
-        {
+        if (mr::tc_gemv_plan(M, N, K, mr::route_cluster_size(), mr::route_max_clusters(), &tp) &&
+            scratch != nullptr && aligned(scratch, 256) &&
+            scratch_bytes >= mr::kWorkOffset + (size_t)tp.part_bytes) {
             cudaError_t e = cudaSuccess;
-            const int st = mr::launch_tc_gemv(tp, x, ldx, w, logits, M, N, K, as_stream(stream), &e);
+            void* part = static_cast<unsigned char*>(scratch) + mr::kWorkOffset;
+            const int st = mr::launch_tc_gemv(tp, x, ldx, w, logits, M, N, K, part, as_stream(stream), &e);
             return st == MR_ERR_CUDA ? cuda_status(e) : st;
         }
     }

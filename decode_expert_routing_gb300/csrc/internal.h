@@ -71,12 +71,13 @@ int route_max_clusters();  // clusters of route_cluster_size() CTAs that fit on 
 int route_device_error(int clear);
 unsigned long long wait_limit_ns();
 cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStream_t st);
-// Router GEMV alone above 64 rows on tcgen05 (tensor maps encoded here);
-// returns an mr_status, with the CUDA error in *err on MR_ERR_CUDA.
+// Router GEMV alone above 64 rows on tcgen05 (tensor maps encoded here),
+// its split-K partials in part (p.part_bytes, 16-byte aligned); returns an
+// mr_status, with the CUDA error in *err on MR_ERR_CUDA.
 // tc_gemv_device_error: as route_device_error, for its bounded waits.
 struct TcGemvPlan;
 int launch_tc_gemv(const TcGemvPlan& p, const void* x, int64_t ldx, const void* w, float* logits, int M, int N,
-                   int K, cudaStream_t st, cudaError_t* err);
+                   int K, void* part, cudaStream_t st, cudaError_t* err);
 int tc_gemv_device_error(int clear);
 
 // Launch options (MR_LAUNCH_* bits of mr_set_launch_flags).

@@ -15,18 +15,19 @@
 //      D[128 expert rows x RPC tokens] += W stage . x stage^T in 16-wide
 //      k-steps (weight rows past N are never written and their accumulator
 //      lanes never read).
-//   3. Each warp reads its quarter of the accumulator lanes (32 experts) back,
-//      16 tokens per load, and writes them transposed, [token][expert], into
-//      the dead weight stages (a warp's stores cover whole 128-byte rows).
-//   4. Split-K reduction over distributed shared memory: every CTA tells
-//      every other one when its MMAs are done (a remote mbarrier arrival);
-//      once all have, each CTA sends every owner its rows with one bulk copy
-//      into the owner's x stages (token r of the cluster belongs to CTA
-//      r / TOK), counted on the owner's mbarrier.  The owner sums the CS
-//      partials of each logit in CTA order, and tells every CTA its copy has
-//      landed (a sender stays resident until then).
+//   3. Each warp reads its quarter of the accumulator lanes (32 experts)
+//      back, 16 tokens per load, and stores the partial sums to scratch as
+//      [token][expert] rows of its slice (a warp's stores cover 128
+//      consecutive bytes).
+//   4. Split-K reduction through L2: after one cluster barrier (release /
+//      acquire: every slice is in place), CTA c sums the CS slices of the
+//      logits of its TOK rows of the cluster, in CTA order, and writes them.
+//      (Exchanging the partials over distributed shared memory instead was
+//      bound by the cluster's DSMEM fabric, about 90 bytes per cycle for all
+//      16 CTAs together.)
 //
-// Every wait is bounded in time and sets a device flag when it runs out.
+// Every mbarrier wait is bounded in time and sets a device flag when it runs
+// out; every CTA reaches the cluster barrier (no CTA returns before it).
 #include <cuda.h>
 
 #include "../../include/moe_route.h"
@@ -41,10 +42,11 @@ struct TcGemvArgs {
     CUtensorMap tm_x;  // x [M rows][K] (row pitch ldx), bf16; box 64 k x rpc rows, 128-byte swizzle
     CUtensorMap tm_w;  // W [N rows][K], bf16; box 64 k x N rows, 128-byte swizzle
     float* logits;     // [M][N] fp32
+    float* part;       // scratch: split-K partials [clusters][cs][rpc][N] fp32
     unsigned long long* trace;
     unsigned long long wait_ns;
-    int M, N, kc, nq, nstage, rpc, tok, tok_shift, cs, tmem_cols, off_w, off_stage, off_recv;
-    int flags;        // launch options (bit 1: a test stall, bytes that never come)
+    int M, N, kc, nq, nstage, rpc, tok, cs, tmem_cols, off_w;
+    int flags;  // launch options (bit 1: a test stall, 16 bytes of the first x stage that never come)
 };
 
 // Set when a bounded wait of the tensor-core GEMV ran out (read by the host).
@@ -87,9 +89,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
     extern __shared__ unsigned char dsm[];
     __shared__ __align__(8) unsigned long long s_full[kTcMaxStages];   // x stage s landed
     __shared__ __align__(8) unsigned long long s_wfull[kTcMaxStages];  // weight stage s landed
-    // [0] MMAs done, [1] the cluster's MMAs done, [2] partials in, [3] this CTA's copies landed
-    __shared__ __align__(8) unsigned long long s_bar[4];
-    __shared__ int s_ok[4];
+    __shared__ __align__(8) unsigned long long s_mma;                  // the CTA's MMAs done
+    __shared__ int s_ok[2];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned c = cluster_rank();
@@ -97,12 +98,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
     const int row0 = cl * a.rpc, Mq = min(a.rpc, a.M - row0);
     const int N = a.N, tok = a.tok, rpc = a.rpc;
     const int my_rows = max(0, min(tok, Mq - (int)c * tok));
-    const int nown = (Mq + tok - 1) / tok;  // CTAs of the cluster that own rows
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
-    const uint32_t xs = base, ws = base + (uint32_t)a.off_w, stg = base + (uint32_t)a.off_stage;
-    const uint32_t recv = base + (uint32_t)a.off_recv;
-    const uint32_t bar_mma = smem_u32(&s_bar[0]), bar_done = smem_u32(&s_bar[1]), bar_recv = smem_u32(&s_bar[2]);
-    const uint32_t bar_fin = smem_u32(&s_bar[3]);
+    const uint32_t xs = base, ws = base + (uint32_t)a.off_w;
+    const uint32_t bar_mma = smem_u32(&s_mma);
     const int kslice = (int)c * a.kc;
     const uint32_t xstage = (uint32_t)rpc * 128u;
     MR_TRACE_STAMP(a.trace, 0);
@@ -112,12 +110,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
             mbar_init(smem_u32(&s_wfull[s]), 1);
         }
         mbar_init(bar_mma, 1);
-        mbar_init(bar_done, (unsigned)a.cs);
-        mbar_init(bar_recv, 1);
-        mbar_init(bar_fin, (unsigned)nown);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const unsigned stall = (a.flags & 2) ? 16u : 0u;
-        if (my_rows > 0) mbar_expect_tx(bar_recv, (unsigned)(my_rows * a.cs * N * 4) + stall);
         tma_prefetch_map(&a.tm_w);
         tma_prefetch_map(&a.tm_x);
         for (int s = 0; s < a.nstage; ++s) {
@@ -132,14 +125,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    cluster_arrive_relaxed();  // completed by cluster_wait() before the first remote access
     pdl_trigger();
-    pdl_wait();
+    pdl_wait();  // (also orders this launch's partial stores after the previous launch's reads)
     MR_TRACE_STAMP(a.trace, 8);
     if (tid == 0)
         for (int s = 0; s < a.nstage; ++s) {
             const uint32_t full = smem_u32(&s_full[s]);
-            mbar_expect_tx(full, (unsigned)(rpc * kTcStageK * 2));
+            const unsigned stall = ((a.flags & 2) && s == 0) ? 16u : 0u;
+            mbar_expect_tx(full, (unsigned)(rpc * kTcStageK * 2) + stall);
             tma_load_2d(xs + (uint32_t)s * xstage, &a.tm_x, kslice + s * kTcStageK, row0, full);
         }
     tc_fence_before();
@@ -155,7 +148,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
             // (after a wait that ran out, the later stages are still waited
             // for, bounded, so that no copy is left in flight)
             if (!tc_wait0(smem_u32(&s_wfull[s]), a.wait_ns)) fail = 1;
-            MR_TRACE_STAMP(a.trace, 22 + s);
             if (!tc_wait0(smem_u32(&s_full[s]), a.wait_ns)) fail = 1;
             MR_TRACE_STAMP(a.trace, 16 + s);
             if (fail) continue;
@@ -172,26 +164,23 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
                     : "memory");
             }
         }
-        s_ok[3] = fail;
+        s_ok[1] = fail;
         // arrives once every MMA issued above has completed
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_mma)
                      : "memory");
         MR_TRACE_STAMP(a.trace, 1);
     }
-    const bool mma_ok = tc_cta_wait0(bar_mma, a.wait_ns, &s_ok[0]) && s_ok[3] == 0;
+    const bool mma_ok = tc_cta_wait0(bar_mma, a.wait_ns, &s_ok[0]) && s_ok[1] == 0;
     MR_TRACE_STAMP(a.trace, 9);
-    // this CTA's tensor core is done with its x stages: tell every CTA of the
-    // cluster (their partials may land there from now on)
-    cluster_wait();  // every CTA of the cluster has initialised its barriers
-    if (tid < a.cs) mbar_arrive_remote(map_rank(bar_done, (unsigned)tid));
 
-    // ---- accumulator -> [token][expert] rows in the weight stages: warp w
-    //      reads lanes (experts) 32 (w % 4) .. + 31, column blocks of 16
-    //      tokens w / 4 and w / 4 + 4
+    // ---- accumulator -> this CTA's slice of the partials: warp w reads
+    //      lanes (experts) 32 (w % 4) .. + 31, column blocks of 16 tokens
+    //      w / 4 and w / 4 + 4; for each token a warp stores 32 consecutive
+    //      experts
     tc_fence_after();
     const int e = (warp & 3) * 32 + lane;
-    uint32_t v[2][16];
     if (mma_ok) {
+        uint32_t v[2][16];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int cb = (warp >> 2) + 4 * i;
@@ -206,17 +195,16 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
         }
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (e < N) {
-            float* st = reinterpret_cast<float*>(dsm + (stg - smem_u32(dsm)));
+            float* slice = a.part + ((int64_t)cl * a.cs + c) * rpc * N;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int cb = (warp >> 2) + 4 * i;
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (cb * 16 + j < Mq) st[(cb * 16 + j) * N + e] = __uint_as_float(v[i][j]);
+                    if (cb * 16 + j < Mq) slice[(cb * 16 + j) * N + e] = __uint_as_float(v[i][j]);
             }
         }
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the rows, visible to the bulk copies
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -224,41 +212,28 @@ __global__ void __launch_bounds__(kRouteThreads, 1) tc_gemv_kernel(const __grid_
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
     }
     MR_TRACE_STAMP(a.trace, 10);
-    const bool all_done = tc_cta_wait0(bar_done, a.wait_ns, &s_ok[1]);
-    MR_TRACE_STAMP(a.trace, 11);
+    // every slice of the cluster is in place (every CTA reaches this point)
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    MR_TRACE_STAMP(a.trace, 2);
 
-    // ---- owner o's rows of this K slice: one bulk copy into its slot c
-    if (mma_ok && all_done && tid < nown) {
-        const int rows = min(tok, Mq - tid * tok);
-        const unsigned bytes = (unsigned)(tok * N * 4);
-        bulk_copy_to_cta(map_rank(recv + (uint32_t)c * bytes, (unsigned)tid), stg + (uint32_t)tid * bytes,
-                         (unsigned)(rows * N * 4), map_rank(bar_recv, (unsigned)tid));
-    }
-
-    // ---- owner: split-K sum of each logit over the CS slices, in CTA order
-    if (my_rows > 0 && tc_cta_wait0(bar_recv, a.wait_ns, &s_ok[2])) {
-        MR_TRACE_STAMP(a.trace, 2);
-        // every CTA's copy into this one has landed: each may leave
-        if (tid < a.cs) mbar_arrive_remote(map_rank(bar_fin, (unsigned)tid));
-        const float* rv = reinterpret_cast<const float*>(dsm + (recv - smem_u32(dsm)));
-        const int plane = tok * N;  // floats between two slices' partials
-        const int n = tid & 127;    // expert n (N <= 128) of rows tid / 128, + 4, ...
-        for (int rl = tid >> 7; rl < my_rows && n < N; rl += kRouteThreads / 128) {
-            const float* pp = rv + rl * N + n;
-            float sum = 0.0f;
-            for (int sl = 0; sl < a.cs; sl += 8) {  // cs is 8 or 16: loads first, then the adds in order
-                float t8[8];
+    // ---- CTA c: split-K sum of the logits of its rows over the CS slices,
+    //      in CTA order
+    const float* rows = a.part + (int64_t)cl * a.cs * rpc * N + (int64_t)((int)c * tok) * N;
+    const int plane = rpc * N;  // floats between two slices
+    const int n = tid & 127;    // expert n (N <= 128) of rows tid / 128, + 4, ...
+    for (int rl = tid >> 7; rl < my_rows && n < N; rl += kRouteThreads / 128) {
+        const float* pp = rows + rl * N + n;
+        float sum = 0.0f;
+        for (int sl = 0; sl < a.cs; sl += 8) {  // cs is 8 or 16: loads first, then the adds in order
+            float t8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) t8[u] = pp[(sl + u) * plane];
+            for (int u = 0; u < 8; ++u) t8[u] = __ldcg(pp + (sl + u) * plane);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) sum = __fadd_rn(sum, t8[u]);
-            }
-            a.logits[(int64_t)(row0 + (int)c * tok + rl) * N + n] = sum;
+            for (int u = 0; u < 8; ++u) sum = __fadd_rn(sum, t8[u]);
         }
-        MR_TRACE_STAMP(a.trace, 3);
+        a.logits[(int64_t)(row0 + (int)c * tok + rl) * N + n] = sum;
     }
-    // this CTA's copies must have been read before it leaves
-    if (tid == 0) tc_wait0(bar_fin, a.wait_ns);
+    MR_TRACE_STAMP(a.trace, 3);
 }
 
 namespace {
@@ -302,13 +277,14 @@ int g_prepared[64];  // per device: kernel attributes set
 }  // namespace
 
 int launch_tc_gemv(const TcGemvPlan& p, const void* x, int64_t ldx, const void* w, float* logits, int M, int N,
-                   int K, cudaStream_t st, cudaError_t* err) {
+                   int K, void* part, cudaStream_t st, cudaError_t* err) {
     int dev = 0;
     if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return MR_ERR_CUDA;
     if (dev < 0 || dev >= 64) return MR_ERR_UNSUPPORTED;
     TcGemvArgs a{};
     if (!encode_rows(&a.tm_x, x, M, K, ldx, p.rpc) || !encode_rows(&a.tm_w, w, N, K, K, N)) return MR_ERR_UNSUPPORTED;
     a.logits = logits;
+    a.part = static_cast<float*>(part);
     a.trace = static_cast<unsigned long long*>(trace_buffer());
     a.wait_ns = wait_limit_ns();
     a.M = M;
@@ -318,12 +294,9 @@ int launch_tc_gemv(const TcGemvPlan& p, const void* x, int64_t ldx, const void* 
     a.nstage = p.nstage;
     a.rpc = p.rpc;
     a.tok = p.tok;
-    a.tok_shift = ilog2_exact(p.tok);
     a.cs = p.cs;
     a.tmem_cols = p.tmem_cols;
     a.off_w = p.off_w;
-    a.off_stage = p.off_stage;
-    a.off_recv = p.off_recv;
     a.flags = launch_flags();
     if (!g_prepared[dev]) {
         if ((*err = cudaFuncSetAttribute(tc_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemMax)) !=

@@ -199,20 +199,21 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
 // slice arrives in stages of kTcStageK k (one 128-byte swizzled row per
 // token or expert), all resident at once: per stage an rpc-row x tile (the
 // MMA's N side) and a 128-row weight tile (its M side; rows past N are never
-// written).  After the CTA's MMAs the weight stages hold the accumulator as
-// [token][expert] rows (when it fits there; else after), and the owners'
-// receive buffers take the x stages' place once every CTA of the cluster has
-// finished its MMAs (or follow the rest when the x stages are smaller).
-// Offsets are from a 1024-byte aligned base inside the dynamic shared memory
-// (1024 bytes of slack).
+// written).  Offsets are from a 1024-byte aligned base inside the dynamic
+// shared memory (1024 bytes of slack).  The split-K partials go through
+// scratch: part_bytes of fp32 [clusters][cs][rpc][N].
 constexpr int kTcStageK = 64;
 constexpr int kTcWStageBytes = 128 * 128;
 constexpr int kTcMaxStages = 8;
 constexpr int kTcSmemMax = 226 * 1024;  // dynamic (the per-block maximum is 227 KiB with the static part)
 
 struct TcGemvPlan {
-    int cs, kc, nq, nstage, rpc, tok, clusters, tmem_cols, off_w, off_stage, off_recv, smem;
+    int cs, kc, nq, nstage, rpc, tok, clusters, tmem_cols, off_w, smem, part_bytes;
 };
+
+// Scratch bytes of the partials for any plan of M rows (any count of
+// resident clusters): clusters * rpc < M + rpc <= M + 128 rows, cs <= 16.
+inline int64_t tc_gemv_part_bound(int M, int N) { return (int64_t)(M + 127) * N * 16 * 4; }
 
 // fit: clusters resident at once.  Rows per cluster: M spread over fit
 // clusters, rounded up to a multiple of 16 (the MMA's N), 16 to 128: the
@@ -233,19 +234,13 @@ inline bool tc_gemv_plan(int M, int N, int K, int cs, int fit, TcGemvPlan* p) {
     if (q.rpc < 16) q.rpc = 16;
     if (q.rpc > 128) q.rpc = 128;
     q.clusters = (M + q.rpc - 1) / q.rpc;
-    q.tok = 1;
-    while (q.tok * cs < q.rpc) q.tok *= 2;
+    q.tok = (q.rpc + cs - 1) / cs;  // rows whose logits each CTA sums (every CTA takes a share)
     q.tmem_cols = 32;  // fp32 accumulator: 128 lanes (experts) x rpc columns (tokens)
     while (q.tmem_cols < q.rpc) q.tmem_cols *= 2;
     const int xbytes = q.nstage * q.rpc * 128, wbytes = q.nstage * kTcWStageBytes;
-    const int sbytes = q.rpc * N * 4, rbytes = cs * q.tok * N * 4;
     q.off_w = xbytes;
-    int end = xbytes + wbytes;
-    q.off_stage = sbytes <= wbytes ? q.off_w : end;
-    if (sbytes > wbytes) end += sbytes;
-    q.off_recv = rbytes <= xbytes ? 0 : end;
-    if (rbytes > xbytes) end += rbytes;
-    q.smem = 1024 + end;
+    q.smem = 1024 + xbytes + wbytes;
+    q.part_bytes = q.clusters * q.rpc * N * cs * 4;
     if (q.smem > kTcSmemMax) return false;
     *p = q;
     return true;

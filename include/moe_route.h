@@ -170,8 +170,9 @@ int mr_router_gemv_supported(int M, int N, int K, int64_t ldx);
 
 /*
  * Scratch bytes sufficient for every call of this library with M <= M_max
- * tokens, N experts, hidden K and top-k (router GEMV split-K partials, the
- * fused route, the multi-CTA sort of large batches).  The first
+ * tokens, N experts, hidden K and top-k (router GEMV split-K partials of
+ * either kernel above 64 rows, the fused route, the multi-CTA sort of large
+ * batches).  The first
  * MR_SCRATCH_COUNTER_BYTES hold counters.  Returns 0 for out-of-range
  * arguments.  Pure host function.
  */
@@ -188,12 +189,17 @@ int mr_scratch_reset(void *scratch, size_t scratch_bytes, void *stream);
  * One launch.  The K range is split over CTAs and the partials are summed in
  * split order (deterministic: the same inputs give the same bits on every
  * call):
- *  - whenever the cluster kernel's tiles fit (M <= 64; 64 < M <= 512 with
- *    N <= 128 on tcgen05): one thread-block cluster per 16 rows (64 above
- *    64 rows), each CTA a K slice, the partials summed by each row's owner
- *    CTA over distributed shared memory; no scratch.  N >= 512 splits the
- *    experts into groups of >= 128, one cluster each.  For M <= 64 these
- *    are the logits of mr_moe_route_sort_quant, bit for bit;
+ *  - M <= 64 when the cluster kernel's tiles fit: one thread-block cluster
+ *    per 16 rows, each CTA a K slice, the partials summed by each row's
+ *    owner CTA over distributed shared memory; no scratch.  The experts are
+ *    split into groups (one cluster each) as far as the co-resident
+ *    clusters allow.  These are the logits of mr_moe_route_sort_quant, bit
+ *    for bit;
+ *  - 64 < M <= 512 with N <= 128 (and K / cluster size a multiple of 16, at
+ *    most 8 stages of 64): the tensor-core GEMV (tcgen05, one cluster per
+ *    group of rows, each CTA a K slice); its partials pass through the
+ *    scratch work area (mr_scratch_bytes covers them), so it runs only
+ *    with a scratch of at least that size;
  *  - otherwise the split-K kernel: the last CTA to finish each (n-block,
  *    row-tile) sums the fp32 partials and re-zeroes its counter (scratch
  *    of mr_scratch_bytes bytes, else MR_ERR_INVALID_ARG / _SCRATCH_TOO_SMALL).

@@ -77,7 +77,10 @@ def test_sort_capacity(lib):
 def test_scratch_bytes(lib):
     b = mr.scratch_bytes(64, 128, 6144, 8)
     assert b >= 32768 and b % 256 == 0
-    # covers the largest split-K partial plane of any M up to M_max
+    # covers the largest split-K partial plane of any M up to M_max, and the
+    # tensor-core GEMV's partials ((M + 127) rows x N x 16 slices of fp32 at most)
+    assert mr.scratch_bytes(512, 128, 6144, 8) >= 32768 + (512 + 127) * 128 * 16 * 4
+    assert mr.scratch_bytes(65, 128, 6144, 8) >= 32768 + (65 + 127) * 128 * 16 * 4
     assert mr.scratch_bytes(512, 128, 6144, 8) >= b
     assert mr.scratch_bytes(4096, 128, 6144, 8) >= 32768 + 4 * 32768
     assert mr.scratch_bytes(0, 128, 6144, 8) == 0

@@ -175,8 +175,9 @@ int main() {
     for (int K : {512, 1024, 3584, 6144, 7168, 8192}) {
         mr::TcGemvPlan p;
         if (!mr::tc_gemv_plan(M, N, K, cs, fit, &p)) { printf("none %d %d %d %d %d\n", cs, fit, M, N, K); continue; }
-        printf("plan %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d\n", cs, fit, M, N, K, p.kc, p.nq, p.nstage,
-               p.rpc, p.tok, p.clusters, p.tmem_cols, p.off_w, p.off_stage, p.off_recv, p.smem, p.cs);
+        printf("plan %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %lld\n", cs, fit, M, N, K, p.kc, p.nq, p.nstage,
+               p.rpc, p.tok, p.clusters, p.tmem_cols, p.off_w, p.smem, p.part_bytes,
+               (long long)mr::tc_gemv_part_bound(M, N));
     }
 }
 """
@@ -187,9 +188,8 @@ def test_tc_gemv_plan_invariants(tmp_path):
     what the kernel relies on: whole 16-wide k-steps per CTA, at most 8
     resident 64-wide stages, 1024-byte aligned swizzled stage tiles, rows per
     cluster a multiple of 16 spreading M over the resident clusters (one
-    wave), the owners' token rows, the accumulator's columns, and the
-    transposed rows and receive buffers inside the dead stages or after them,
-    disjoint."""
+    wave), the owners' token rows, the accumulator's columns, and partials
+    within the scratch bound the library sizes scratch by."""
     src = tmp_path / "probe.cpp"
     src.write_text(TC_PROBE)
     exe = tmp_path / "probe"
@@ -207,32 +207,17 @@ def test_tc_gemv_plan_invariants(tmp_path):
             assert (M <= 64 or M > 512 or N > 128 or N % 8 or K % cs or kc % 16
                     or -(-kc // 64) > 8 or 1024 + (rpc * 128 + 16384) * -(-kc // 64) > 226 * 1024)
             continue
-        kc, nq, nstage, rpc, tok, clusters, tcols, off_w, off_stage, off_recv, smem, pcs = (int(v) for v in f[6:])
+        kc, nq, nstage, rpc, tok, clusters, tcols, off_w, smem, part, bound = (int(v) for v in f[6:])
         have[(cs, fit, M, N, K)] = dict(rpc=rpc, clusters=clusters, smem=smem)
-        assert 64 < M <= 512 and N <= 128 and N % 8 == 0 and pcs == cs
+        assert 64 < M <= 512 and N <= 128 and N % 8 == 0
         assert kc * cs == K and kc % 16 == 0 and nq == kc // 16 and nstage == -(-kc // 64) <= 8
         assert rpc == min(128, max(16, -(-(-(-M // fit)) // 16) * 16)) and clusters == -(-M // rpc)
         assert clusters <= fit or rpc == 128                       # one wave whenever 128-row clusters allow it
-        assert pow2(tok) and tok * cs >= rpc and (tok == 1 or tok * cs < 2 * rpc)
+        assert tok == -(-rpc // cs)                                # every CTA sums a share of the rows
         assert pow2(tcols) and tcols >= max(32, rpc) and tcols < 2 * max(32, rpc)
-        xbytes, wbytes = nstage * rpc * 128, nstage * 16384
-        assert off_w == xbytes and off_w % 1024 == 0 and (rpc * 128) % 1024 == 0
-        regions = [(0, xbytes), (off_w, off_w + wbytes)]
-        sbytes, rbytes = rpc * N * 4, cs * tok * N * 4
-        if sbytes <= wbytes:
-            assert off_stage == off_w
-        else:
-            assert off_stage >= off_w + wbytes
-            regions.append((off_stage, off_stage + sbytes))
-        if rbytes <= xbytes:
-            assert off_recv == 0
-        else:
-            assert off_recv >= off_w + wbytes
-            regions.append((off_recv, off_recv + rbytes))
-        regions.sort()
-        assert all(a[1] <= b[0] for a, b in zip(regions, regions[1:]))
-        assert off_stage % 16 == 0 and off_recv % 16 == 0
-        assert smem == 1024 + regions[-1][1] and smem <= 226 * 1024
+        assert off_w == nstage * rpc * 128 and off_w % 1024 == 0 and (rpc * 128) % 1024 == 0
+        assert smem == 1024 + off_w + nstage * 16384 and smem <= 226 * 1024
+        assert part == clusters * rpc * N * cs * 4 and part <= bound
     big = have[(16, 7, 512, 128, 6144)]
     assert big["rpc"] == 80 and big["clusters"] == 7           # one wave where 64-row clusters would need 8
     assert have[(16, 7, 448, 128, 6144)]["rpc"] == 64 and have[(16, 7, 128, 128, 6144)]["clusters"] == 4
