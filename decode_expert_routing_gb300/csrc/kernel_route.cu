@@ -101,16 +101,17 @@ __device__ __forceinline__ unsigned long long composite(unsigned key, int id) {
 }
 
 // Weight of slot r = lane (lane < k holds (val) of slot r: its logit, or
-// for the sigmoid gate its exact score): the same arithmetic as the
+// for the sigmoid gate (SIG) its exact score): the same arithmetic as the
 // standalone gate kernel.  row: the token's n_row logits (only the
 // full-softmax denominator reads it), in shared memory, or in global memory
 // written by other CTAs (read through L2).
+template <bool SIG>
 __device__ __forceinline__ float gate_weight(const RouteArgs& a, const float* row, int n_row, bool global_row,
                                              float my_val) {
     const int lane = threadIdx.x & 31;
     const bool live = lane < a.topk;
     float num, den;
-    if (a.scoring == 1) {
+    if constexpr (SIG) {
         num = live ? my_val : 0.0f;
         den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
         return a.renormalize ? __fdiv_rn(num, den) : num;
@@ -193,13 +194,14 @@ __device__ __forceinline__ void fill_sort_padding(const RouteArgs& a, int MK) {
 }
 
 // Gate weights of the CTA's owned rows: warp 15 - rl handles row rl.
+template <bool SIG>
 __device__ __forceinline__ void row_weights(const RouteArgs& a, const float* rowbuf, const float* oval, int my_rows,
                                             int grow) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, k = a.topk;
     if (warp >= kRouteWarps - my_rows) {
         const int rl = kRouteWarps - 1 - warp;
         const bool live = lane < k;
-        const float wgt = gate_weight(a, rowbuf + rl * a.N, a.N, false, live ? oval[rl * k + lane] : 0.0f);
+        const float wgt = gate_weight<SIG>(a, rowbuf + rl * a.N, a.N, false, live ? oval[rl * k + lane] : 0.0f);
         if (live) a.weights[(int64_t)(grow + rl) * k + lane] = wgt;
     }
 }
@@ -374,7 +376,11 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
 
 // HALF: at most 8 token rows (half of the m16 tile live).
 // GROUPS: the experts are split into a.ng groups, one cluster per group.
-template <bool HALF, bool GROUPS>
+// SIG: the sigmoid gate (scoring 1).  A separate instantiation: its exact
+// scoring is a third of the kernel's code, and carried unexecuted by the
+// softmax kernel it made every cold launch ~3 us slower (a warm one
+// ~0.15 us).
+template <bool HALF, bool GROUPS, bool SIG>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) unsigned long long s_bar[3];  // [0] partial logits in, [1] ids in, [2] MMAs done
@@ -657,7 +663,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         }
         if (a.mode == 0) continue;
         float sel0 = sum0, sel1 = sum1;
-        if (a.scoring == 1) {  // approximate keys: they only pick the candidates
+        if constexpr (SIG) {  // approximate keys: they only pick the candidates
             sel0 = __fadd_rn(sigmoid_approx(sum0), bpre0);
             sel1 = __fadd_rn(sigmoid_approx(sum1), bpre1);
         }
@@ -675,7 +681,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         // sigmoid gate: every expert of the exact top-k has an approximate
         // key within the margin of the k-th largest (>= T), so the
         // candidates reach that far down
-        if (a.scoring == 1) T = sigmoid_candidate_floor(T);
+        if constexpr (SIG) T = sigmoid_candidate_floor(T);
         MR_TRACE_CLK(a.trace, 4);
         const bool p0 = h0 && k0 >= T, p1 = h1 && k1 >= T;
         const unsigned b0 = __ballot_sync(kFull, p0), b1 = __ballot_sync(kFull, p1);
@@ -691,7 +697,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         // PR adjacent lanes per candidate, each counting the beaters among
         // candidates part, part + PR, ...; a segmented reduction adds them
         const int C = s_ccount;
-        if (a.scoring == 1) {  // the candidates' exact scores and keys (correctly rounded sigmoid + bias)
+        if constexpr (SIG) {  // the candidates' exact scores and keys (correctly rounded sigmoid + bias)
             for (int i = tid; i < C; i += kRouteThreads) {
                 const int id = 0x7FFFFFFF - (int)(unsigned)(ccand[i] & 0xFFFFFFFFull);
                 const float b = a.bias != nullptr ? __ldg(a.bias + id) : 0.0f;
@@ -718,7 +724,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                     const uint32_t cb = smem_u32(sm + a.off_merge), sbar = map_rank(bar1, (unsigned)sorter);
                     st_async_f2(map_rank(cb + (uint32_t)((ml * k + r) * 8), (unsigned)sorter),
                                 __uint_as_float((unsigned)cn), __uint_as_float((unsigned)(cn >> 32)), sbar);
-                    const float v = a.scoring == 1 ? cscore[ci] : rowbuf[rl * N + id - e_off];
+                    const float v = SIG ? cscore[ci] : rowbuf[rl * N + id - e_off];
                     st_async_s32(map_rank(cb + (uint32_t)(Mq * k * 8 + (ml * k + r) * 4), (unsigned)sorter),
                                  __float_as_int(v), sbar);
                 } else if (part == 0 && r < k) {
@@ -726,7 +732,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                     st_async_s32(map_rank(smem_u32(sm + a.off_ids) + (uint32_t)((ml * k + r) * 4), (unsigned)sorter),
                                  id, map_rank(bar1, (unsigned)sorter));
                     a.ids[(int64_t)m * k + r] = id;
-                    oval[rl * k + r] = a.scoring == 1 ? cscore[ci] : rowbuf[rl * N + id];
+                    oval[rl * k + r] = SIG ? cscore[ci] : rowbuf[rl * N + id];
                 }
             }
         }
@@ -828,18 +834,18 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
             MR_TRACE_CLK(a.trace, 7);
             const bool live = lane < k;
-            const float wgt = gate_weight(a, a.logits + (int64_t)m * NS, NS, true, live ? myval : 0.0f);
+            const float wgt = gate_weight<SIG>(a, a.logits + (int64_t)m * NS, NS, true, live ? myval : 0.0f);
             if (live) a.weights[(int64_t)m * k + lane] = wgt;
         }
         __syncthreads();  // every token's ids; the masks zeroed
         MR_TRACE_CLK(a.trace, 8);
     } else {
     if (!sorts) {  // the weights and the quantisation finish this CTA
-        row_weights(a, rowbuf, oval, my_rows, grow);
+        row_weights<SIG>(a, rowbuf, oval, my_rows, grow);
         quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
-    row_weights(a, rowbuf, oval, my_rows, grow);
+    row_weights<SIG>(a, rowbuf, oval, my_rows, grow);
     if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
     MR_TRACE_STAMP(a.trace, 5);
     MR_TRACE_WARP(a.trace, 9);
@@ -951,13 +957,13 @@ int route_device_error(int clear) {
 }
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
-static int g_attr_done[64][4];  // per device and instantiation
+static int g_attr_done[64][8];  // per device and instantiation
 
-template <bool HALF, bool GROUPS>
+template <bool HALF, bool GROUPS, bool SIG>
 static cudaError_t prepare(int dev) {
-    const int slot = (HALF ? 1 : 0) + (GROUPS ? 2 : 0);
+    const int slot = (HALF ? 1 : 0) + (GROUPS ? 2 : 0) + (SIG ? 4 : 0);
     if (g_attr_done[dev][slot]) return cudaSuccess;
-    auto k = route_cluster_kernel<HALF, GROUPS>;
+    auto k = route_cluster_kernel<HALF, GROUPS, SIG>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) g_attr_done[dev][slot] = 1;
@@ -968,7 +974,7 @@ int route_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (g_cluster16[dev] == 0) {
-        cudaError_t e = prepare<false, false>(dev);
+        cudaError_t e = prepare<false, false, false>(dev);
         int n = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -982,7 +988,7 @@ int route_cluster_size() {
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
         }
         g_cluster16[dev] = (e == cudaSuccess && n >= 1) ? 1 : -1;
         cudaGetLastError();  // a refused query leaves no sticky error
@@ -1009,7 +1015,7 @@ int route_max_clusters() {
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false>, &cfg);
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
         g_max_clusters[dev] = (e == cudaSuccess && n >= 1) ? n : 1;
         cudaGetLastError();
     }
@@ -1022,19 +1028,22 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     void (*kernel)(RouteArgs) = nullptr;
+    const bool sig = a.mode == 1 && a.scoring == 1;
+#define MR_PICK(H, G, S)                            \
+    do {                                            \
+        e = prepare<H, G, S>(dev);                  \
+        kernel = route_cluster_kernel<H, G, S>;     \
+    } while (0)
     if (p.ng > 1 && p.half) {
-        e = prepare<true, true>(dev);
-        kernel = route_cluster_kernel<true, true>;
+        if (sig) MR_PICK(true, true, true); else MR_PICK(true, true, false);
     } else if (p.ng > 1) {
-        e = prepare<false, true>(dev);
-        kernel = route_cluster_kernel<false, true>;
+        if (sig) MR_PICK(false, true, true); else MR_PICK(false, true, false);
     } else if (p.half) {
-        e = prepare<true, false>(dev);
-        kernel = route_cluster_kernel<true, false>;
+        if (sig) MR_PICK(true, false, true); else MR_PICK(true, false, false);
     } else {
-        e = prepare<false, false>(dev);
-        kernel = route_cluster_kernel<false, false>;
+        if (sig) MR_PICK(false, false, true); else MR_PICK(false, false, false);
     }
+#undef MR_PICK
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.cs * (p.clusters + p.sh_clusters));
