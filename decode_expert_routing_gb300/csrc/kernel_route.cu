@@ -853,8 +853,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // ---- sort.  One cluster: CTA 0 holds every id.  Several clusters: each
     //      CTA 0 publishes its rows' ids and takes a ticket; the last one
     //      gathers all ids and sorts (with several clusters its first phase
-    //      also fills the sentinels and the -1 block ids).
-    if (a.clusters > 1) {
+    //      also fills the sentinels and the -1 block ids).  HALF launches
+    //      (at most 8 rows) without expert groups are one cluster: their
+    //      instantiation carries none of this (about 10 KB of code).
+    if (!HALF && a.clusters > 1) {
         for (int f = tid; f < Mq * k; f += kRouteThreads) a.ids_scratch[row0 * k + f] = ids_all[f];
         const unsigned ticket = cta_ticket(a.counter, &s_ticket);
         if (ticket != (unsigned)(a.clusters - 1)) return;
@@ -875,7 +877,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         const int m = fdiv(f, a.mag_k);
         atomicOr(m < 32 ? &mlo[ids_all[f]] : &mhi[ids_all[f]], 1u << (m & 31));
     }
-    if (a.clusters > 1) fill_sort_padding(a, MK);
+    if ((GROUPS || !HALF) && a.clusters > 1) fill_sort_padding(a, MK);
     __syncthreads();
     MR_TRACE_CLK(a.trace, 14);
     MR_TRACE_WARP(a.trace, 10);
