@@ -100,6 +100,9 @@ __device__ __forceinline__ unsigned long long composite(unsigned key, int id) {
     return ((unsigned long long)key << 32) | (unsigned)(0x7FFFFFFF - id);
 }
 
+// Instantiations of the route kernel by what a launch computes.
+constexpr int kKindGemv = 0, kKindSoftmax = 1, kKindSigmoid = 2;
+
 // Weight of slot r = lane (lane < k holds (val) of slot r: its logit, or
 // for the sigmoid gate (SIG) its exact score): the same arithmetic as the
 // standalone gate kernel.  row: the token's n_row logits (only the
@@ -376,12 +379,15 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
 
 // HALF: at most 8 token rows (half of the m16 tile live).
 // GROUPS: the experts are split into a.ng groups, one cluster per group.
-// SIG: the sigmoid gate (scoring 1).  A separate instantiation: its exact
-// scoring is a third of the kernel's code, and carried unexecuted by the
-// softmax kernel it made every cold launch ~3 us slower (a warm one
-// ~0.15 us).
-template <bool HALF, bool GROUPS, bool SIG>
+// KIND: kKindGemv (mode 0, the GEMV alone), kKindSoftmax or kKindSigmoid
+// (mode 1 with that gate).  Each its own instantiation, carrying only its
+// code: the sigmoid gate's exact scoring is a third of the route's code,
+// and carried unexecuted by the softmax kernel it made every cold launch
+// ~3 us slower (a warm one ~0.15 us); the GEMV alone needs half the code of
+// the route.
+template <bool HALF, bool GROUPS, int KIND>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
+    constexpr bool SIG = KIND == kKindSigmoid, GEMV = KIND == kKindGemv;
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) unsigned long long s_bar[3];  // [0] partial logits in, [1] ids in, [2] MMAs done
     __shared__ int s_ok[3];
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int sorter = Mq <= (a.cs - 1) * tok ? a.cs - 1 : 0;
     // (with expert groups it collects the cluster's group candidates, and
     // the last cluster's collector merges and sorts)
-    const bool sorts = a.mode == 1 && c == sorter;
+    const bool sorts = !GEMV && c == sorter;
     const bool quants = nc == 0;  // one expert group per token group quantises x
     const int e_off = GROUPS ? nc * N : 0;
     const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]), bar2 = smem_u32(&s_bar[2]);
@@ -580,10 +586,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // done once its slice is quantised: nothing is ever sent to it.  Owners
     // quantise later, off the path of the gate.
     if (sorts) {
-        if (quants) quant_slice(a, xs, Mq, row0, kslice);
+        if (!GEMV && quants) quant_slice(a, xs, Mq, row0, kslice);
         if (a.clusters == 1) fill_sort_padding(a, a.M * k);
     } else if (my_rows == 0) {
-        if (quants) quant_slice(a, xs, Mq, row0, kslice);
+        if (!GEMV && quants) quant_slice(a, xs, Mq, row0, kslice);
         return;
     }
     if (my_rows > 0 && !cta_wait_bytes(bar0, a.wait_ns, &s_ok[0])) return;
@@ -613,7 +619,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int gl = 1 << a.gs_shift;
     const unsigned gmask = gl == 32 ? kFull : ((1u << gl) - 1u) << (lane & ~(gl - 1));
     const bool group_has = (tid & ~(gl - 1)) < N;  // the lane group's first expert exists
-    if (a.mode == 0) {  // GEMV alone: every (owned row, expert) in parallel
+    if constexpr (GEMV) {  // GEMV alone: every (owned row, expert) in parallel
         for (int idx = tid; idx < my_rows * N; idx += kRouteThreads) {
             const int rl = fdiv(idx, a.mag_n), n = idx - rl * N;
             const float* pp = recv + rl * N + n;
@@ -661,7 +667,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             rowbuf[rl * N + n1] = sum1;
             a.logits[lrow + n1] = sum1;
         }
-        if (a.mode == 0) continue;
         float sel0 = sum0, sel1 = sum1;
         if constexpr (SIG) {  // approximate keys: they only pick the candidates
             sel0 = __fadd_rn(sigmoid_approx(sum0), bpre0);
@@ -740,7 +745,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         if (tid == 0) s_ccount = 0;  // before the next row's second barrier
     }
     MR_TRACE_WARP(a.trace, 3);
-    if (a.mode == 0) return;  // nothing else reads this CTA's shared memory
     MR_TRACE_STAMP(a.trace, 4);
     MR_TRACE_CLK(a.trace, 9);
     MR_TRACE_CLK(a.trace, 11);
@@ -757,7 +761,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         //      candidates that beat it (a binary search: each list is
         //      descending; the composites are unique).
         if (!sorts) {
-            if (quants) quant_slice(a, xs, Mq, row0, kslice);
+            if (!GEMV && quants) quant_slice(a, xs, Mq, row0, kslice);
             return;
         }
         if (!cta_wait_bytes(bar1, a.wait_ns, &s_ok[1])) return;
@@ -959,13 +963,13 @@ int route_device_error(int clear) {
 }
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
-static int g_attr_done[64][8];  // per device and instantiation
+static int g_attr_done[64][12];  // per device and instantiation
 
-template <bool HALF, bool GROUPS, bool SIG>
+template <bool HALF, bool GROUPS, int KIND>
 static cudaError_t prepare(int dev) {
-    const int slot = (HALF ? 1 : 0) + (GROUPS ? 2 : 0) + (SIG ? 4 : 0);
+    const int slot = (HALF ? 1 : 0) + (GROUPS ? 2 : 0) + 4 * KIND;
     if (g_attr_done[dev][slot]) return cudaSuccess;
-    auto k = route_cluster_kernel<HALF, GROUPS, SIG>;
+    auto k = route_cluster_kernel<HALF, GROUPS, KIND>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) g_attr_done[dev][slot] = 1;
@@ -976,7 +980,7 @@ int route_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (g_cluster16[dev] == 0) {
-        cudaError_t e = prepare<false, false, false>(dev);
+        cudaError_t e = prepare<false, false, kKindSoftmax>(dev);
         int n = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -990,7 +994,7 @@ int route_cluster_size() {
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, kKindSoftmax>, &cfg);
         }
         g_cluster16[dev] = (e == cudaSuccess && n >= 1) ? 1 : -1;
         cudaGetLastError();  // a refused query leaves no sticky error
@@ -1017,7 +1021,7 @@ int route_max_clusters() {
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, false>, &cfg);
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, kKindSoftmax>, &cfg);
         g_max_clusters[dev] = (e == cudaSuccess && n >= 1) ? n : 1;
         cudaGetLastError();
     }
@@ -1030,20 +1034,28 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     void (*kernel)(RouteArgs) = nullptr;
-    const bool sig = a.mode == 1 && a.scoring == 1;
-#define MR_PICK(H, G, S)                            \
-    do {                                            \
-        e = prepare<H, G, S>(dev);                  \
-        kernel = route_cluster_kernel<H, G, S>;     \
+    const int kind = a.mode == 0 ? kKindGemv : (a.scoring == 1 ? kKindSigmoid : kKindSoftmax);
+#define MR_PICK(H, G)                                                      \
+    do {                                                                   \
+        if (kind == kKindGemv) {                                           \
+            e = prepare<H, G, kKindGemv>(dev);                             \
+            kernel = route_cluster_kernel<H, G, kKindGemv>;                \
+        } else if (kind == kKindSigmoid) {                                 \
+            e = prepare<H, G, kKindSigmoid>(dev);                          \
+            kernel = route_cluster_kernel<H, G, kKindSigmoid>;             \
+        } else {                                                           \
+            e = prepare<H, G, kKindSoftmax>(dev);                          \
+            kernel = route_cluster_kernel<H, G, kKindSoftmax>;             \
+        }                                                                  \
     } while (0)
     if (p.ng > 1 && p.half) {
-        if (sig) MR_PICK(true, true, true); else MR_PICK(true, true, false);
+        MR_PICK(true, true);
     } else if (p.ng > 1) {
-        if (sig) MR_PICK(false, true, true); else MR_PICK(false, true, false);
+        MR_PICK(false, true);
     } else if (p.half) {
-        if (sig) MR_PICK(true, false, true); else MR_PICK(true, false, false);
+        MR_PICK(true, false);
     } else {
-        if (sig) MR_PICK(false, false, true); else MR_PICK(false, false, false);
+        MR_PICK(false, false);
     }
 #undef MR_PICK
     if (e != cudaSuccess) return e;
