@@ -9,12 +9,12 @@ namespace mr {
 
 constexpr int kTopkWarps = 4;
 
-template <int NPL>
+template <int NPL, bool SIG>
 __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(TopkArgs a) {
     pdl_trigger();
     pdl_wait();
     const int m = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
-    if (m < a.M) warp_topk_row<NPL>(a, m, nullptr);
+    if (m < a.M) warp_topk_row<NPL, SIG>(a, m, nullptr);
 }
 
 int topk_npl(int N) { return N <= 128 ? 4 : N <= 256 ? 8 : N <= 512 ? 16 : 32; }
@@ -26,11 +26,16 @@ cudaError_t launch_topk(const float* logits, int M, int N, int topk, int scoring
                (launch_flags() & 8) ? 1 : 0};
     dim3 grid((M + kTopkWarps - 1) / kTopkWarps);
     const dim3 block(32 * kTopkWarps);
+    const bool sig = scoring == 1;
     switch (topk_npl(N)) {
-        case 4: return launch_kernel(topk_kernel<4>, grid, block, 0, st, a);
-        case 8: return launch_kernel(topk_kernel<8>, grid, block, 0, st, a);
-        case 16: return launch_kernel(topk_kernel<16>, grid, block, 0, st, a);
-        default: return launch_kernel(topk_kernel<32>, grid, block, 0, st, a);
+        case 4: return sig ? launch_kernel(topk_kernel<4, true>, grid, block, 0, st, a)
+                           : launch_kernel(topk_kernel<4, false>, grid, block, 0, st, a);
+        case 8: return sig ? launch_kernel(topk_kernel<8, true>, grid, block, 0, st, a)
+                           : launch_kernel(topk_kernel<8, false>, grid, block, 0, st, a);
+        case 16: return sig ? launch_kernel(topk_kernel<16, true>, grid, block, 0, st, a)
+                            : launch_kernel(topk_kernel<16, false>, grid, block, 0, st, a);
+        default: return sig ? launch_kernel(topk_kernel<32, true>, grid, block, 0, st, a)
+                            : launch_kernel(topk_kernel<32, false>, grid, block, 0, st, a);
     }
 }
 

@@ -71,7 +71,14 @@ __device__ __forceinline__ unsigned warp_select(unsigned (&key)[NPL], const floa
 // Gate of one token (row m) by one warp.  If ids_smem != nullptr the chosen
 // ids are also written there (slot order).  Reads the logits through L2 so
 // that rows written by other CTAs of the same launch are seen.
-template <int NPL>
+// The exact sigmoid score, out of line: the candidate loop below is unrolled
+// over a lane's NPL keys, and inlined it put NPL copies of the evaluation
+// into the kernel (324 KB of code at NPL = 32).
+__device__ __noinline__ float sigmoid_exact_call(float l, bool slow) { return sigmoid_exact(l, slow); }
+
+// SIG: the sigmoid gate (scoring 1), else softmax; a separate
+// instantiation, so the softmax gate carries none of the sigmoid's code.
+template <int NPL, bool SIG>
 __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids_smem) {
     const int lane = threadIdx.x & 31;
     const float* row = a.logits + (int64_t)m * a.N;
@@ -89,14 +96,14 @@ __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids
         unsigned kv = 0u;  // below every real key: never selected while real keys remain
         if (id < a.N) {
             float sel = val[j];
-            if (a.scoring == 1) sel = __fadd_rn(sigmoid_approx(val[j]), a.bias ? __ldg(a.bias + id) : 0.0f);
+            if constexpr (SIG) sel = __fadd_rn(sigmoid_approx(val[j]), a.bias ? __ldg(a.bias + id) : 0.0f);
             kv = ordered_key(sel);
         }
         key[j] = kv;
     }
     int my_id = 0;
     float my_val = 0.0f;  // slot lane's logit, or for the sigmoid gate its exact score
-    if (a.scoring == 1) {
+    if constexpr (SIG) {
         // the k-th largest approximate key bounds the candidates; they are
         // re-scored exactly, the others drop out, and the selection runs again
         unsigned probe[NPL];
@@ -108,7 +115,7 @@ __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids
         for (int j = 0; j < NPL; ++j) {
             const int id = lane + 32 * j;
             const bool cand = id < a.N && key[j] >= floor_key;
-            score[j] = cand ? sigmoid_exact(val[j], a.slow_sigmoid != 0) : 0.0f;
+            score[j] = cand ? sigmoid_exact_call(val[j], a.slow_sigmoid != 0) : 0.0f;
             key[j] = cand ? ordered_key(__fadd_rn(score[j], a.bias ? __ldg(a.bias + id) : 0.0f)) : 0u;
         }
         warp_select<NPL>(key, score, a.k, &my_id, &my_val);
@@ -119,7 +126,7 @@ __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids
     // weights: lane r < k owns slot r
     const bool live = lane < a.k;
     float num = 0.0f, den;
-    if (a.scoring == 1) {
+    if constexpr (SIG) {
         num = live ? my_val : 0.0f;
         den = a.renormalize ? warp_sum_fixed(num) : 1.0f;
     } else {
@@ -137,16 +144,16 @@ __device__ __forceinline__ void warp_topk_row(const TopkArgs& a, int m, int* ids
     }
     if (live) {
         a.ids[(int64_t)m * a.k + lane] = my_id;
-        a.weights[(int64_t)m * a.k + lane] = (a.scoring == 1 && !a.renormalize) ? num : __fdiv_rn(num, den);
+        a.weights[(int64_t)m * a.k + lane] = (SIG && !a.renormalize) ? num : __fdiv_rn(num, den);
         if (ids_smem) ids_smem[m * a.k + lane] = my_id;
     }
 }
 
-template <int NPL>
+template <int NPL, bool SIG>
 __device__ __forceinline__ void cta_topk_rows(const TopkArgs& a, int row_begin, int row_end,
                                               int* ids_smem) {
     const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    for (int m = row_begin + warp; m < row_end; m += nwarps) warp_topk_row<NPL>(a, m, ids_smem);
+    for (int m = row_begin + warp; m < row_end; m += nwarps) warp_topk_row<NPL, SIG>(a, m, ids_smem);
 }
 
 }  // namespace mr
