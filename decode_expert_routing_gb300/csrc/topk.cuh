@@ -71,11 +71,9 @@ __device__ __forceinline__ unsigned warp_select(unsigned (&key)[NPL], const floa
 // Gate of one token (row m) by one warp.  If ids_smem != nullptr the chosen
 // ids are also written there (slot order).  Reads the logits through L2 so
 // that rows written by other CTAs of the same launch are seen.
-// The exact sigmoid score, out of line: the candidate loop below is unrolled
-// over a lane's NPL keys, and inlined it put NPL copies of the evaluation
-// into the kernel (324 KB of code at NPL = 32).
-__device__ __noinline__ float sigmoid_exact_call(float l, bool slow) { return sigmoid_exact(l, slow); }
-
+// (The exact sigmoid score goes through sigmoid_exact_call: the candidate
+// loop below is unrolled over a lane's NPL keys, and inlined it put NPL
+// copies of the evaluation into the kernel, 324 KB of code at NPL = 32.)
 // SIG: the sigmoid gate (scoring 1), else softmax; a separate
 // instantiation, so the softmax gate carries none of the sigmoid's code.
 template <int NPL, bool SIG>
