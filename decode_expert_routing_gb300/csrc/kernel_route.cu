@@ -385,7 +385,10 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
 // and carried unexecuted by the softmax kernel it made every cold launch
 // ~3 us slower (a warm one ~0.15 us); the GEMV alone needs half the code of
 // the route.
-template <bool HALF, bool GROUPS, int KIND>
+// SH: the launch carries the shared expert's clusters (after the route's, or
+// alone).  Their CTA code is ~22 KB, a quarter of the softmax route's code
+// and half of the GEMV alone's, so only these instantiations carry it.
+template <bool HALF, bool GROUPS, int KIND, bool SH>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteArgs a) {
     constexpr bool SIG = KIND == kKindSigmoid, GEMV = KIND == kKindGemv;
     extern __shared__ __align__(16) unsigned char sm[];
@@ -395,9 +398,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     __shared__ __align__(16) unsigned s_wmin[kRouteWarps];  // gate: per warp, smallest group maximum
     __shared__ int s_ccount;                                  // gate: candidates so far
     __shared__ __align__(16) int s_wtot[2 * kRouteWarps];     // sort: blocks per warp (experts t, t + 512)
-    if ((int)(blockIdx.x >> a.cs_shift) >= a.clusters) {  // the shared expert's clusters
-        shared_gate_up_cta(a, (int)(blockIdx.x >> a.cs_shift) - a.clusters);
-        return;
+    if constexpr (SH) {
+        if ((int)(blockIdx.x >> a.cs_shift) >= a.clusters) {  // the shared expert's clusters
+            shared_gate_up_cta(a, (int)(blockIdx.x >> a.cs_shift) - a.clusters);
+            return;
+        }
     }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -963,13 +968,13 @@ int route_device_error(int clear) {
 }
 
 static int g_cluster16[64];     // per device: 0 unknown, 1 usable, -1 not
-static int g_attr_done[64][12];  // per device and instantiation
+static int g_attr_done[64][24];  // per device and instantiation
 
-template <bool HALF, bool GROUPS, int KIND>
+template <bool HALF, bool GROUPS, int KIND, bool SH>
 static cudaError_t prepare(int dev) {
-    const int slot = (HALF ? 1 : 0) + (GROUPS ? 2 : 0) + 4 * KIND;
+    const int slot = (HALF ? 1 : 0) + (GROUPS ? 2 : 0) + 4 * KIND + (SH ? 12 : 0);
     if (g_attr_done[dev][slot]) return cudaSuccess;
-    auto k = route_cluster_kernel<HALF, GROUPS, KIND>;
+    auto k = route_cluster_kernel<HALF, GROUPS, KIND, SH>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) g_attr_done[dev][slot] = 1;
@@ -980,7 +985,7 @@ int route_cluster_size() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (g_cluster16[dev] == 0) {
-        cudaError_t e = prepare<false, false, kKindSoftmax>(dev);
+        cudaError_t e = prepare<false, false, kKindSoftmax, false>(dev);
         int n = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -994,7 +999,7 @@ int route_cluster_size() {
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, kKindSoftmax>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, kKindSoftmax, false>, &cfg);
         }
         g_cluster16[dev] = (e == cudaSuccess && n >= 1) ? 1 : -1;
         cudaGetLastError();  // a refused query leaves no sticky error
@@ -1021,7 +1026,7 @@ int route_max_clusters() {
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, kKindSoftmax>, &cfg);
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<false, false, kKindSoftmax, false>, &cfg);
         g_max_clusters[dev] = (e == cudaSuccess && n >= 1) ? n : 1;
         cudaGetLastError();
     }
@@ -1035,29 +1040,39 @@ cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStr
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     void (*kernel)(RouteArgs) = nullptr;
     const int kind = a.mode == 0 ? kKindGemv : (a.scoring == 1 ? kKindSigmoid : kKindSoftmax);
-#define MR_PICK(H, G)                                                      \
-    do {                                                                   \
-        if (kind == kKindGemv) {                                           \
-            e = prepare<H, G, kKindGemv>(dev);                             \
-            kernel = route_cluster_kernel<H, G, kKindGemv>;                \
-        } else if (kind == kKindSigmoid) {                                 \
-            e = prepare<H, G, kKindSigmoid>(dev);                          \
-            kernel = route_cluster_kernel<H, G, kKindSigmoid>;             \
-        } else {                                                           \
-            e = prepare<H, G, kKindSoftmax>(dev);                          \
-            kernel = route_cluster_kernel<H, G, kKindSoftmax>;             \
-        }                                                                  \
+    const bool sh = p.sh_clusters > 0;
+#define MR_ONE(H, G, K, S)                                \
+    do {                                                  \
+        e = prepare<H, G, K, S>(dev);                     \
+        kernel = route_cluster_kernel<H, G, K, S>;        \
     } while (0)
-    if (p.ng > 1 && p.half) {
-        MR_PICK(true, true);
+#define MR_ROUTE(H, G)                                                        \
+    do {                                                                      \
+        if (kind == kKindSigmoid) {                                           \
+            if (sh) MR_ONE(H, G, kKindSigmoid, true); else MR_ONE(H, G, kKindSigmoid, false); \
+        } else {                                                              \
+            if (sh) MR_ONE(H, G, kKindSoftmax, true); else MR_ONE(H, G, kKindSoftmax, false); \
+        }                                                                     \
+    } while (0)
+    if (kind == kKindGemv) {
+        // (the GEMV alone never carries the shared expert: with shared
+        // clusters and no route clusters this is mr_shared_gate_up)
+        if (sh) MR_ONE(false, false, kKindGemv, true);
+        else if (p.ng > 1 && p.half) MR_ONE(true, true, kKindGemv, false);
+        else if (p.ng > 1) MR_ONE(false, true, kKindGemv, false);
+        else if (p.half) MR_ONE(true, false, kKindGemv, false);
+        else MR_ONE(false, false, kKindGemv, false);
+    } else if (p.ng > 1 && p.half) {
+        MR_ROUTE(true, true);
     } else if (p.ng > 1) {
-        MR_PICK(false, true);
+        MR_ROUTE(false, true);
     } else if (p.half) {
-        MR_PICK(true, false);
+        MR_ROUTE(true, false);
     } else {
-        MR_PICK(false, false);
+        MR_ROUTE(false, false);
     }
-#undef MR_PICK
+#undef MR_ROUTE
+#undef MR_ONE
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.cs * (p.clusters + p.sh_clusters));
