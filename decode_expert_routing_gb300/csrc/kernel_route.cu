@@ -893,9 +893,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     MR_TRACE_CLK(a.trace, 15);
     // blocks per expert nb = ceil(count / B); thread t: experts t and t + 512.
     // Exclusive scan over the experts: inside a warp from the ballots of the
-    // bits of nb (nb <= ceil(M / B) < 2^nbits), across warps from the warp
-    // totals; then the block starts and the expert id of every real block
-    // (padding blocks already hold -1).
+    // bits of nb (nb <= ceil(M / B) < 2^nbits), kept in start[]; across warps
+    // from the warp totals after one barrier.  Then, with no further barrier,
+    // each expert's thread writes its real blocks' expert id (padding blocks
+    // already hold -1) and each assignment's thread its slot of sorted ids:
+    // the first block of its expert is that expert's in-warp prefix plus the
+    // totals of the warps below it, which every thread reads alike.
     const int e0 = tid, e1 = tid + kRouteThreads;
     const int nb0 = e0 < NS ? fdiv(__popc(mlo[e0]) + __popc(mhi[e0]) + B - 1, a.mag_block) : 0;
     const int nb1 = e1 < NS ? fdiv(__popc(mlo[e1]) + __popc(mhi[e1]) + B - 1, a.mag_block) : 0;
@@ -909,43 +912,53 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         wt0 += __popc(q0) << bit;
         wt1 += __popc(q1) << bit;
     }
+    if (e0 < NS) start[e0] = pre0;
+    if (e1 < NS) start[e1] = pre1;
     if (lane == 0) {
         s_wtot[warp] = wt0;
         s_wtot[kRouteWarps + warp] = wt1;
     }
     MR_TRACE_CLK(a.trace, 16);
-    __syncthreads();
-    int before0 = 0, tot0 = 0, before1 = 0, tot1 = 0;
+    __syncthreads();  // start[] (in-warp prefixes) and the warp totals
+    int4 u[kRouteWarps / 4], v[kRouteWarps / 4];
+    int tot0 = 0, tot1 = 0;
 #pragma unroll
     for (int q = 0; q < kRouteWarps / 4; ++q) {
-        const int4 u = reinterpret_cast<const int4*>(s_wtot)[q];
-        const int4 v = reinterpret_cast<const int4*>(s_wtot + kRouteWarps)[q];
-        const int w0 = 4 * q;
-        before0 += (w0 < warp ? u.x : 0) + (w0 + 1 < warp ? u.y : 0) + (w0 + 2 < warp ? u.z : 0) + (w0 + 3 < warp ? u.w : 0);
-        before1 += (w0 < warp ? v.x : 0) + (w0 + 1 < warp ? v.y : 0) + (w0 + 2 < warp ? v.z : 0) + (w0 + 3 < warp ? v.w : 0);
-        tot0 += (u.x + u.y) + (u.z + u.w);
-        tot1 += (v.x + v.y) + (v.z + v.w);
+        u[q] = reinterpret_cast<const int4*>(s_wtot)[q];
+        v[q] = reinterpret_cast<const int4*>(s_wtot + kRouteWarps)[q];
+        tot0 += (u[q].x + u[q].y) + (u[q].z + u[q].w);
+        tot1 += (v[q].x + v[q].y) + (v[q].z + v[q].w);
     }
+    // blocks of the warps below warp w (of experts 0..511, or of 512.. after tot0)
+    auto below_warp = [&](int w, bool hi) {
+        int s = hi ? tot0 : 0;
+#pragma unroll
+        for (int q = 0; q < kRouteWarps / 4; ++q) {
+            const int4 x = hi ? v[q] : u[q];
+            const int w0 = 4 * q;
+            s += (w0 < w ? x.x : 0) + (w0 + 1 < w ? x.y : 0) + (w0 + 2 < w ? x.z : 0) + (w0 + 3 < w ? x.w : 0);
+        }
+        return s;
+    };
     MR_TRACE_CLK(a.trace, 17);
-    const int sb0 = before0 + pre0, sb1 = tot0 + before1 + pre1;  // first block of e0 / e1
     if (e0 < NS) {
-        start[e0] = sb0 * B;
+        const int sb0 = below_warp(warp, false) + pre0;  // first block of e0
         for (int i = 0; i < nb0; ++i) a.expert_ids[sb0 + i] = e0;
     }
     if (e1 < NS) {
-        start[e1] = sb1 * B;
+        const int sb1 = below_warp(warp, true) + pre1;
         for (int i = 0; i < nb1; ++i) a.expert_ids[sb1 + i] = e1;
     }
     if (tid == 0) *a.ntpp = (tot0 + tot1) * B;
     MR_TRACE_CLK(a.trace, 19);
     MR_TRACE_WARP(a.trace, 12);
-    __syncthreads();  // start[] complete
     MR_TRACE_CLK(a.trace, 22);
     for (int f = tid; f < MK; f += kRouteThreads) {
         const int e = ids_all[f], m = fdiv(f, a.mag_k);
         const unsigned below = m < 32 ? __popc(mlo[e] & ((1u << m) - 1u))
                                       : __popc(mlo[e]) + __popc(mhi[e] & ((1u << (m - 32)) - 1u));
-        a.sorted[start[e] + (int)below] = f;
+        const int sb = below_warp((e & (kRouteThreads - 1)) >> 5, e >= kRouteThreads) + start[e];
+        a.sorted[sb * B + (int)below] = f;
     }
     MR_TRACE_CLK(a.trace, 23);
     MR_TRACE_WARP(a.trace, 13);
