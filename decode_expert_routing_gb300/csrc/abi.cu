@@ -221,6 +221,7 @@ static mr::RouteArgs route_args(const mr::RoutePlan& p, const void* x, int64_t l
     a.off_ids = p.off_ids;
     a.off_mask = p.off_mask;
     a.off_start = p.off_start;
+    a.off_kred = p.off_kred;
     a.tok_shift = mr::ilog2_exact(p.tok);
     a.wpt_shift = mr::ilog2_exact(p.wpt);
     a.mag_n = mr::div_magic(p.nl);

@@ -14,10 +14,12 @@
 //      memory with 16-byte loads issued before the kernel waits on its
 //      predecessor (programmatic dependent launch), x fragments from the
 //      CTA's x slice in shared memory.
-//   2. Split-K reduction: every unit's partial tile goes by st.async to the
-//      CTA that owns the tile's token rows (token m belongs to CTA m / TOK),
-//      counted on that CTA's mbarrier; the owner waits for the bytes it
-//      expects and sums the CS*WPT partials of each logit in a fixed order.
+//   2. Split-K reduction: the WPT k-parts of a tile are added inside the
+//      CTA (through shared memory, in part order), and the CTA's partial tile
+//      goes by st.async to the CTA that owns the tile's token rows (token m
+//      belongs to CTA m / TOK), counted on that CTA's mbarrier; the owner
+//      waits for the bytes it expects and sums the CS partials of each logit
+//      in CTA order.
 //   3. Gate, the owner's whole CTA per row: a threshold below the k-th
 //      largest key from group maxima, then a parallel ranking of the few
 //      candidates; the chosen ids go at once to the sorting CTA (st.async).
@@ -69,6 +71,10 @@ __device__ __forceinline__ bool cta_wait_bytes(uint32_t bar, unsigned long long 
     }
     __syncthreads();
     return *s_ok != 0;
+}
+// Barrier of the nthreads threads (whole warps) that use barrier id (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 __device__ __forceinline__ uint4 lds128(const void* p) {
     return *reinterpret_cast<const uint4*>(p);
@@ -502,7 +508,13 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     const int j0 = warp >> a.wpt_shift;
     const int my_tiles = j0 < NT ? (NT - j0 + tiles_per_pass - 1) >> (4 - a.wpt_shift) : 0;
     const int nb = (my_tiles + kRouteBatch - 1) / kRouteBatch;
-    const int slot = c * wpt + p;
+    // The warps of one tile group (its wpt k-parts) add their partial tiles
+    // before sending: parts p >= 1 leave theirs in shared memory (one buffer
+    // per batch parity), and after the group's barrier part 0 adds them in
+    // part order and sends one partial per CTA and logit (slot c).
+    float* const kred = reinterpret_cast<float*>(sm + a.off_kred);
+    const int kbar = 1 + j0, kthreads = 32 * wpt;
+    const int slot = c;
     const int r0 = g, r1 = g + 8;  // one m16 tile: at most 16 token rows per cluster here
     uint32_t tok_bar[2] = {0u, 0u};  // at most 8 rows: mbarrier of the owner of tokens 2t and 2t + 1
 #pragma unroll
@@ -529,6 +541,22 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
             MR_TRACE_WARP(a.trace, 4);
             // acc[2 uu + h]: the expert of row g of unit uu's tile, token 2t + h
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __fadd_rn(acc[i], acc2[i]);
+            if (wpt > 1) {
+                float* kb = kred + (b & 1) * (kRouteWarps * 4 * 32);
+                if (p != 0) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) kb[(warp * 4 + i) * 32 + lane] = v[i];
+                }
+                named_bar_sync(kbar, kthreads);
+                if (p != 0) continue;
+                for (int q = 1; q < wpt; ++q) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = __fadd_rn(v[i], kb[((warp + q) * 4 + i) * 32 + lane]);
+                }
+            }
 #pragma unroll
             for (int uu = 0; uu < 2; ++uu) {
                 const int j = j0 + tiles_per_pass * (b * 2 + uu);
@@ -539,8 +567,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
                     if (r < Mq) {
                         const int own = r >> a.tok_shift, rl = r & (tok - 1);
                         const uint32_t la = recv_local + (uint32_t)(((slot * tok + rl) * N + j * 8 + g) * 4);
-                        st_async_s32(map_rank(la, (unsigned)own),
-                                     __float_as_int(__fadd_rn(acc[2 * uu + h], acc2[2 * uu + h])), tok_bar[h]);
+                        st_async_s32(map_rank(la, (unsigned)own), __float_as_int(v[2 * uu + h]), tok_bar[h]);
                     }
                 }
             }
@@ -566,6 +593,24 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
             }
         }
         MR_TRACE_WARP(a.trace, 4);
+        if (wpt > 1) {
+            float* kb = kred + (b & 1) * (kRouteWarps * 8 * 32);
+            if (p != 0) {
+#pragma unroll
+                for (int uu = 0; uu < kRouteBatch; ++uu)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) kb[(warp * 8 + uu * 4 + i) * 32 + lane] = acc[uu][i];
+            }
+            named_bar_sync(kbar, kthreads);
+            if (p != 0) continue;
+            for (int q = 1; q < wpt; ++q) {
+#pragma unroll
+                for (int uu = 0; uu < kRouteBatch; ++uu)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        acc[uu][i] = __fadd_rn(acc[uu][i], kb[((warp + q) * 8 + uu * 4 + i) * 32 + lane]);
+            }
+        }
 #pragma unroll
         for (int uu = 0; uu < kRouteBatch; ++uu) {
             const int j = j0 + tiles_per_pass * (b * kRouteBatch + uu);

@@ -52,6 +52,7 @@ struct RouteArgs {
     int tok;         // token rows owned per CTA
     int xpitch;      // bytes per x row in shared memory
     int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
+    int off_kred;    // wpt > 1: the k-parts' partial tiles handed to part 0 (two buffers)
     int tok_shift, wpt_shift;  // log2 of tok and wpt (both powers of two)
     int gs_shift;    // gate threshold: log2 of the lane-group size (<= 32 threads)
     int nslots;      // split-K partials per logit at the owner
@@ -103,7 +104,7 @@ struct RoutePlan {
     int nslots;
     bool half;
     int smem;
-    int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start;
+    int off_x, off_recv, off_row, off_key, off_cand, off_ids, off_mask, off_start, off_kred;
 };
 
 inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -149,7 +150,7 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     if (w == 0) return false;
     const int NTall = Ntot / 8;
     while (NTall * w < kRouteWarps && 2 * w <= kRouteWarps && S % (2 * w) == 0) w *= 2;
-    if ((cs * w) % 8 != 0) return false;  // the owner sums split-K slots in groups of 8
+    if (cs % 8 != 0) return false;  // the owner sums split-K slots in groups of 8
     q.wpt = w;
     q.spw = S / w;
     q.units = NT * w;
@@ -167,7 +168,8 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     // (tcgen05 at 16 rows: a chain of K/16 dependent MMAs issued by one
     // thread plus the accumulator read-back measured slower than 16 warps of
     // mma.sync, so the decode route keeps mma.sync)
-    q.nslots = cs * w;
+    // the CTA adds its k-parts before sending: one partial per CTA and logit
+    q.nslots = cs;
 
     int off = 0;
     q.off_x = off;  // row-major x slice (MMA operand of mma.sync; quantiser input)
@@ -188,6 +190,8 @@ inline bool route_plan(int M, int N, int K, int topk, int mode, int cs, RoutePla
     q.off_merge = off;  // ng > 1: the cluster's candidates as received (keys, then logits); in the
                         // merging CTA all candidates [M][ng][k] (8 B keys, then logits)
     if (mode == 1 && q.ng > 1) off = align_up(off + M * q.ng * topk * 12, 16);
+    q.off_kred = off;  // [batch parity][warp][value][lane] floats, values: 4 (half) or 8 per lane
+    if (w > 1) off = align_up(off + 2 * kRouteWarps * (q.half ? 4 : 8) * 32 * 4, 16);
     q.smem = off;
     if (q.smem > kRouteSmemMax) return false;
     *p = q;
