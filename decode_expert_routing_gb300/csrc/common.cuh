@@ -72,16 +72,18 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Last-arriver ticket: returns the counter value before this CTA's increment.
-// The whole CTA calls it after writing what it publishes.  Each thread's
-// release fence orders its own writes before the barrier; thread 0's
-// acq_rel atomic publishes them at gpu scope and, in the CTA that draws the
-// last ticket, acquires every other CTA's; the barrier passes that on to the
-// CTA's threads, which then read the published data through L2 (ld.cg).
+// The whole CTA calls it after writing what it publishes.  The barrier
+// orders every thread's writes before thread 0's fence and acq_rel atomic,
+// which publish them at gpu scope (release is cumulative: one thread's
+// fence covers what the barrier ordered before it) and, in the CTA that
+// draws the last ticket, acquire every other CTA's; the second barrier
+// passes that on to the CTA's threads, which then read the published data
+// through L2 (ld.cg).  (A fence in every thread measured slower.)
 __device__ __forceinline__ unsigned cta_ticket(unsigned* counter, unsigned* s_slot) {
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     __syncthreads();
     if (threadIdx.x == 0) {
         unsigned old;
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
         *s_slot = old;
     }
