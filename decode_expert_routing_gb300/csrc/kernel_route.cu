@@ -939,11 +939,13 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // blocks per expert nb = ceil(count / B); thread t: experts t and t + 512.
     // Exclusive scan over the experts: inside a warp from the ballots of the
     // bits of nb (nb <= ceil(M / B) < 2^nbits), kept in start[]; across warps
-    // from the warp totals after one barrier.  Then, with no further barrier,
-    // each expert's thread writes its real blocks' expert id (padding blocks
-    // already hold -1) and each assignment's thread its slot of sorted ids:
-    // the first block of its expert is that expert's in-warp prefix plus the
-    // totals of the warps below it, which every thread reads alike.
+    // from the 32 warp totals (experts 0..511 by warp, then 512..1023), which
+    // every warp scans with shuffles after one barrier: lane i then holds the
+    // blocks before the experts of total i, i = e / 32.  With no further
+    // barrier, each expert's thread writes its real blocks' expert id (padding
+    // blocks already hold -1) and each assignment's thread its slot of sorted
+    // ids (the first block of its expert plus the expert's tokens before it).
+    static_assert(2 * kRouteWarps == 32, "one warp total per lane");
     const int e0 = tid, e1 = tid + kRouteThreads;
     const int nb0 = e0 < NS ? fdiv(__popc(mlo[e0]) + __popc(mhi[e0]) + B - 1, a.mag_block) : 0;
     const int nb1 = e1 < NS ? fdiv(__popc(mlo[e1]) + __popc(mhi[e1]) + B - 1, a.mag_block) : 0;
@@ -965,45 +967,39 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     }
     MR_TRACE_CLK(a.trace, 16);
     __syncthreads();  // start[] (in-warp prefixes) and the warp totals
-    int4 u[kRouteWarps / 4], v[kRouteWarps / 4];
-    int tot0 = 0, tot1 = 0;
+    int wexc;         // lane i: blocks of the warp totals before total i
+    {
+        const int wv = s_wtot[lane];
+        int inc = wv;
 #pragma unroll
-    for (int q = 0; q < kRouteWarps / 4; ++q) {
-        u[q] = reinterpret_cast<const int4*>(s_wtot)[q];
-        v[q] = reinterpret_cast<const int4*>(s_wtot + kRouteWarps)[q];
-        tot0 += (u[q].x + u[q].y) + (u[q].z + u[q].w);
-        tot1 += (v[q].x + v[q].y) + (v[q].z + v[q].w);
-    }
-    // blocks of the warps below warp w (of experts 0..511, or of 512.. after tot0)
-    auto below_warp = [&](int w, bool hi) {
-        int s = hi ? tot0 : 0;
-#pragma unroll
-        for (int q = 0; q < kRouteWarps / 4; ++q) {
-            const int4 x = hi ? v[q] : u[q];
-            const int w0 = 4 * q;
-            s += (w0 < w ? x.x : 0) + (w0 + 1 < w ? x.y : 0) + (w0 + 2 < w ? x.z : 0) + (w0 + 3 < w ? x.w : 0);
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(kFull, inc, d);
+            if (lane >= d) inc += o;
         }
-        return s;
-    };
+        wexc = inc - wv;
+        if (tid == 31) *a.ntpp = inc * B;
+    }
     MR_TRACE_CLK(a.trace, 17);
-    if (e0 < NS) {
-        const int sb0 = below_warp(warp, false) + pre0;  // first block of e0
-        for (int i = 0; i < nb0; ++i) a.expert_ids[sb0 + i] = e0;
+    {
+        const int sb0 = __shfl_sync(kFull, wexc, warp) + pre0;  // first block of e0
+        if (e0 < NS)
+            for (int i = 0; i < nb0; ++i) a.expert_ids[sb0 + i] = e0;
+        const int sb1 = __shfl_sync(kFull, wexc, kRouteWarps + warp) + pre1;
+        if (e1 < NS)
+            for (int i = 0; i < nb1; ++i) a.expert_ids[sb1 + i] = e1;
     }
-    if (e1 < NS) {
-        const int sb1 = below_warp(warp, true) + pre1;
-        for (int i = 0; i < nb1; ++i) a.expert_ids[sb1 + i] = e1;
-    }
-    if (tid == 0) *a.ntpp = (tot0 + tot1) * B;
     MR_TRACE_CLK(a.trace, 19);
     MR_TRACE_WARP(a.trace, 12);
     MR_TRACE_CLK(a.trace, 22);
-    for (int f = tid; f < MK; f += kRouteThreads) {
-        const int e = ids_all[f], m = fdiv(f, a.mag_k);
-        const unsigned below = m < 32 ? __popc(mlo[e] & ((1u << m) - 1u))
-                                      : __popc(mlo[e]) + __popc(mhi[e] & ((1u << (m - 32)) - 1u));
-        const int sb = below_warp((e & (kRouteThreads - 1)) >> 5, e >= kRouteThreads) + start[e];
-        a.sorted[sb * B + (int)below] = f;
+    for (int base = warp * 32; base < MK; base += kRouteThreads) {  // whole warps (shuffles)
+        const int f = base + lane;
+        const int e = f < MK ? ids_all[f] : 0, m = fdiv(f, a.mag_k);
+        const int sb = __shfl_sync(kFull, wexc, e >> 5);
+        if (f < MK) {
+            const unsigned below = m < 32 ? __popc(mlo[e] & ((1u << m) - 1u))
+                                          : __popc(mlo[e]) + __popc(mhi[e] & ((1u << (m - 32)) - 1u));
+            a.sorted[(sb + start[e]) * B + (int)below] = f;
+        }
     }
     MR_TRACE_CLK(a.trace, 23);
     MR_TRACE_WARP(a.trace, 13);
