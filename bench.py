@@ -777,9 +777,6 @@ def run_ours(args):
     ev_in = [torch.cuda.Event() for _ in range(2)]     # input copy of set b done
     ev_comp = [torch.cuda.Event() for _ in range(2)]   # kernels on set b done
     ev_out = [torch.cuda.Event() for _ in range(2)]    # output copy of set b done
-    for b in range(2):
-        ev_comp[b].record(stream)
-        ev_out[b].record(stream)
 
     def e2e_step(i):
         b, s = i & 1, i % SLOTS
@@ -797,24 +794,39 @@ def run_ours(args):
             harena[b].copy_(arena[b], non_blocking=True)
         ev_out[b].record(s_out)
 
-    for i in range(4):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    s_in.wait_event(e0)
-    for b in range(2):  # the timed steps start after e0
-        ev_comp[b].record(stream)
-        ev_out[b].record(stream)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    stream.wait_event(ev_out[0])
-    stream.wait_event(ev_out[1])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_value = job_gbs(STEP_BYTES, e2e_steps, world, reduce_max_ms(e0.elapsed_time(e1), world, dev))
+    def e2e_run(n):  # n pipelined steps, joined back into the compute stream
+        for b in range(2):
+            ev_comp[b].record(stream)
+            ev_out[b].record(stream)
+        for i in range(n):
+            e2e_step(i)
+        stream.wait_event(ev_out[0])
+        stream.wait_event(ev_out[1])
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return job_gbs(STEP_BYTES, e2e_steps, world, reduce_max_ms(t0.elapsed_time(t1), world, dev))
+
+    # eager: every copy and launch issued from Python in the timed region
+    with torch.cuda.stream(stream):
+        e2e_run(4)
+        e2e_eager = timed(lambda: e2e_run(e2e_steps))
+    # the same pipelined steps captured once as a CUDA graph (the serving
+    # pattern: the copies from and to pinned host memory and every launch
+    # replayed, one graph launch from the host)
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph, stream=stream):
+        e2e_run(e2e_steps)
+    with torch.cuda.stream(stream):  # replays go to the capture stream, between the timing events
+        e2e_graph.replay()
+        e2e_value = timed(lambda: e2e_graph.replay())
 
     cpu = cpu_baseline_leg() if (rank == 0 and world == 1) else None
 
@@ -838,9 +850,12 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "eager_launches_value": round(e2e_eager, 3),
                     "path": "every M's x from one pinned host buffer to the device, one prepared route "
                             "call (PreparedRoute) per M, every output in one arena copied to pinned host; "
-                            "two buffer sets, the copies on their own streams overlapping the kernels"},
+                            "two buffer sets, the copies on their own streams overlapping the kernels; "
+                            "value: the timed steps captured as one CUDA graph and replayed, "
+                            "eager_launches_value: the same steps issued from Python"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "gpu": props.name, "sms": props.multi_processor_count,

@@ -690,12 +690,20 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
         float sum0 = 0.0f, sum1 = 0.0f;
         if (h0) {
             const float* pp = recv + rl * N + n0;
-            for (int sl = 0; sl < nslots; sl += 8) {  // nslots % 8 == 0; loads first, then the adds in order
-                float v[8];
+            if (nslots == 16) {  // every load in flight, then the adds in order
+                float v[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) v[u] = pp[(sl + u) * plane];
+                for (int u = 0; u < 16; ++u) v[u] = pp[u * plane];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) sum0 = __fadd_rn(sum0, v[u]);
+                for (int u = 0; u < 16; ++u) sum0 = __fadd_rn(sum0, v[u]);
+            } else {
+                for (int sl = 0; sl < nslots; sl += 8) {  // nslots % 8 == 0; loads first, then the adds in order
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = pp[(sl + u) * plane];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) sum0 = __fadd_rn(sum0, v[u]);
+                }
             }
         }
         if (h1) {
