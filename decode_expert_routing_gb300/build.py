@@ -19,7 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_route.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["abi.cu", "kernels_gemv.cu", "kernels_aux.cu", "kernel_route.cu", "kernel_tc_gemv.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "kernels_gemv.cu", "kernels_aux.cu", "kernel_route.cu", "kernel_route_spw6.cu",
+           "kernel_route_spw7.cu", "kernel_tc_gemv.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No --use_fast_math: the quantiser and the sigmoid recipe need IEEE rounding
 # and subnormals (no flush to zero).

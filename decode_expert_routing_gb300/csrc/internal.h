@@ -71,6 +71,12 @@ int route_max_clusters();  // clusters of route_cluster_size() CTAs that fit on 
 int route_device_error(int clear);
 unsigned long long wait_limit_ns();
 cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStream_t st);
+// the instantiations for 6 and 7 k steps per k-part (kernel_route_spw6.cu,
+// kernel_route_spw7.cu) and their bounded-wait flags
+cudaError_t launch_route_cluster_spw6(const RoutePlan& p, const RouteArgs& a, cudaStream_t st);
+cudaError_t launch_route_cluster_spw7(const RoutePlan& p, const RouteArgs& a, cudaStream_t st);
+int route_timeout_flag_spw6(int clear);
+int route_timeout_flag_spw7(int clear);
 // Router GEMV alone above 64 rows on tcgen05 (tensor maps encoded here),
 // its split-K partials in part (p.part_bytes, 16-byte aligned); returns an
 // mr_status, with the CUDA error in *err on MR_ERR_CUDA.
