@@ -68,8 +68,12 @@ int route_max_clusters() {
 }
 
 cudaError_t launch_route_cluster(const RoutePlan& p, const RouteArgs& a, cudaStream_t st) {
-    if (p.clusters > 0 && a.spw == 6) return launch_route_cluster_spw6(p, a, st);
-    if (p.clusters > 0 && a.spw == 7) return launch_route_cluster_spw7(p, a, st);
+    // the step count of the route's clusters and of the shared expert's, when
+    // the launch has both they must agree to take a fixed-count instantiation
+    const int rs = p.clusters > 0 ? a.spw : 0, ss = p.sh_clusters > 0 ? a.sh_spw : 0;
+    const int spw = rs == 0 ? ss : (ss == 0 || ss == rs ? rs : 0);
+    if (spw == 6) return launch_route_cluster_spw6(p, a, st);
+    if (spw == 7) return launch_route_cluster_spw7(p, a, st);
     return launch_route_spw<0>(p, a, st);
 }
 

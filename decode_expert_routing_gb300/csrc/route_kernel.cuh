@@ -277,6 +277,7 @@ __device__ __forceinline__ void row_weights(const RouteArgs& a, const float* row
 // split-K partials in a fixed order and writes bf16(silu(gate) * up).
 // Out of line (inlined, it made every cold launch of the route ~2 us
 // slower); it reads each launch value it needs once, on entry.
+template <int SPW>  // 32-wide k steps per k-part, as the route's (0: a.sh_spw at run time)
 static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int sc) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) unsigned long long s_shbar;
@@ -286,7 +287,7 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
     // every launch value this function uses, read once here (through the
     // reference the compiler would read some again after every store)
     const int Mq = a.M, K = a.K, kc = a.kc, P = a.sh_pairs, R = 2 * P, I = a.sh_I;
-    const int tok = a.tok, wpt = a.sh_wpt, spw = a.sh_spw, nslots = a.sh_nslots;
+    const int tok = a.tok, wpt = a.sh_wpt, spw = SPW ? SPW : a.sh_spw, nslots = a.sh_nslots;
     const int xpitch = a.xpitch, units = a.sh_units, tok_shift = a.tok_shift, spitch = a.sh_spitch;
     const int flags = a.flags;
     const unsigned long long wait_ns = a.wait_ns;
@@ -373,8 +374,8 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
         const unsigned char* srow0 = ss + (j * 8 + 2 * t) * spitch + p * spw;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int s = 0; s < kRouteSpwMax; ++s) {
-            if (s < spw) {
+        for (int s = 0; s < (SPW ? SPW : kRouteSpwMax); ++s) {
+            if (SPW || s < spw) {
                 const int kk = (p * spw + s) * 32 + 8 * t;
                 const uint4 xa = g < Mq ? lds128(xs + g * xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
                 const uint4 xb = g + 8 < Mq ? lds128(xs + (g + 8) * xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     __shared__ __align__(16) int s_wtot[2 * kRouteWarps];     // sort: blocks per warp (experts t, t + 512)
     if constexpr (SH) {
         if ((int)(blockIdx.x >> a.cs_shift) >= a.clusters) {  // the shared expert's clusters
-            shared_gate_up_cta(a, (int)(blockIdx.x >> a.cs_shift) - a.clusters);
+            shared_gate_up_cta<SPW>(a, (int)(blockIdx.x >> a.cs_shift) - a.clusters);
             return;
         }
     }
