@@ -40,6 +40,37 @@ __device__ __forceinline__ void mma_bf16_m16n8k16(float (&c)[4], uint32_t a0, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A * B for one m16n8k16 f16 tile with fp32 accumulation.
+__device__ __forceinline__ void mma_f16_m16n8k16(float (&c)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two bf16 (one 32-bit pair) -> two f16.  *exact is cleared unless both
+// convert exactly: zero, or a biased exponent in [110, 142] (2^-17 <= |v| <
+// 2^16: f16 covers that bf16 range to the last bit, its subnormal spacing
+// 2^-24 down to 2^-17; larger values overflow and smaller ones lose bits).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t two, bool* exact) {
+    const uint32_t e_lo = (two >> 7) & 0xFFu, e_hi = (two >> 23) & 0xFFu;
+    const bool ok_lo = (two & 0x7FFFu) == 0u || (e_lo >= 110u && e_lo <= 142u);
+    const bool ok_hi = (two & 0x7FFF0000u) == 0u || (e_hi >= 110u && e_hi <= 142u);
+    if (!(ok_lo && ok_hi)) *exact = false;
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(two & 0xFFFF0000u)), "f"(__uint_as_float(two << 16)));
+    return r;
+}
+
+// Two E4M3 codes (the low 16 bits) -> two f16 (exact: every E4M3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    return (uint32_t)hr.x | ((uint32_t)hr.y << 16);
+}
+
 // Router input on the norm's scale: two bf16 residual values (one 32-bit
 // pair) -> bf16((x * rstd) * s) with s = g or, for a Gemma RMSNorm, 1 + g;
 // each fp32 step rounds to nearest even (no contraction), and the bf16

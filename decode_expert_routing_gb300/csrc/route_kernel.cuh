@@ -47,6 +47,7 @@
 // flag when it runs out.  One cluster leaves nothing in scratch; several
 // clusters leave their ticket counter at zero again.
 #pragma once
+#include <type_traits>
 #include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -352,27 +353,45 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
         }
     }
     pdl_wait();
-    // the x slice -> shared memory (on the norm's scale when rstd is given)
+    // the x slice -> shared memory (on the norm's scale when rstd is given),
+    // as f16 when every value of the CTA's slice converts exactly: then the
+    // E4M3 weights go to the MMAs by one conversion per pair (f16 holds every
+    // E4M3 value) instead of the longer exact E4M3 -> bf16 one, and the
+    // products and their fp32 sums are those of the bf16 MMAs.  Otherwise
+    // (a value at or above 2^16 or below 2^-17) the slice is staged again as
+    // bf16 and the bf16 MMAs run.
     const int vpr = kc / 8;
+    bool exact = true;
     for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
         const int r = v / vpr, cv = v - r * vpr;
         uint4 d = ld_ro_v4(xg + (int64_t)r * ldx + kslice + cv * 8);
         if (rstd != nullptr) d = norm_chunk(d, ld_ro_v4(norm_w + kslice + cv * 8), __ldg(rstd + r), gemma);
+        d = make_uint4(bf16x2_to_f16x2(d.x, &exact), bf16x2_to_f16x2(d.y, &exact), bf16x2_to_f16x2(d.z, &exact),
+                       bf16x2_to_f16x2(d.w, &exact));
         *reinterpret_cast<uint4*>(xs + r * xpitch + cv * 16) = d;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
+    const bool use_f16 = __syncthreads_and(exact) != 0;
+    if (!use_f16) {
+        for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
+            const int r = v / vpr, cv = v - r * vpr;
+            uint4 d = ld_ro_v4(xg + (int64_t)r * ldx + kslice + cv * 8);
+            if (rstd != nullptr) d = norm_chunk(d, ld_ro_v4(norm_w + kslice + cv * 8), __ldg(rstd + r), gemma);
+            *reinterpret_cast<uint4*>(xs + r * xpitch + cv * 16) = d;
+        }
+        __syncthreads();
+    }
     cluster_wait();  // every CTA of the cluster is running: DSMEM is live
     uint32_t owner_bar[2] = {0u, 0u};
 #pragma unroll
     for (int h = 0; h < 2; ++h)
         if (g + 8 * h < Mq) owner_bar[h] = map_rank(bar, (unsigned)((g + 8 * h) >> tok_shift));
-#pragma unroll 1
-    for (int u = warp; u < units; u += kRouteWarps) {
-        const int j = u / wpt, p = u - j * wpt;
+    // one (tile, k-part) unit: each 32-wide k step (one MX block) is two MMAs
+    // into a fresh block sum, added to the accumulator times its E8M0 scale
+    auto unit_steps = [&](auto f16, int j, int p, float (&acc)[4]) {
+        constexpr bool F16 = decltype(f16)::value;
         const unsigned char* wrow = ws + (j * 8 + g) * wpitch + p * spw * 32 + 8 * t;
         const unsigned char* srow0 = ss + (j * 8 + 2 * t) * spitch + p * spw;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int s = 0; s < (SPW ? SPW : kRouteSpwMax); ++s) {
             if (SPW || s < spw) {
@@ -380,11 +399,18 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
                 const uint4 xa = g < Mq ? lds128(xs + g * xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
                 const uint4 xb = g + 8 < Mq ? lds128(xs + (g + 8) * xpitch + kk * 2) : make_uint4(0u, 0u, 0u, 0u);
                 const uint2 w8 = *reinterpret_cast<const uint2*>(wrow + s * 32);
-                const uint32_t b0 = e4m3x2_to_bf16x2(w8.x), b1 = e4m3x2_to_bf16x2(w8.x >> 16);
-                const uint32_t b2 = e4m3x2_to_bf16x2(w8.y), b3 = e4m3x2_to_bf16x2(w8.y >> 16);
                 float blk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_bf16_m16n8k16(blk, xa.x, xb.x, xa.y, xb.y, b0, b1);
-                mma_bf16_m16n8k16(blk, xa.z, xb.z, xa.w, xb.w, b2, b3);
+                if constexpr (F16) {
+                    const uint32_t b0 = e4m3x2_to_f16x2(w8.x), b1 = e4m3x2_to_f16x2(w8.x >> 16);
+                    const uint32_t b2 = e4m3x2_to_f16x2(w8.y), b3 = e4m3x2_to_f16x2(w8.y >> 16);
+                    mma_f16_m16n8k16(blk, xa.x, xb.x, xa.y, xb.y, b0, b1);
+                    mma_f16_m16n8k16(blk, xa.z, xb.z, xa.w, xb.w, b2, b3);
+                } else {
+                    const uint32_t b0 = e4m3x2_to_bf16x2(w8.x), b1 = e4m3x2_to_bf16x2(w8.x >> 16);
+                    const uint32_t b2 = e4m3x2_to_bf16x2(w8.y), b3 = e4m3x2_to_bf16x2(w8.y >> 16);
+                    mma_bf16_m16n8k16(blk, xa.x, xb.x, xa.y, xb.y, b0, b1);
+                    mma_bf16_m16n8k16(blk, xa.z, xb.z, xa.w, xb.w, b2, b3);
+                }
                 const float s0 = e8m0_value(srow0[s]), s1 = e8m0_value(srow0[spitch + s]);
                 acc[0] = __fmaf_rn(blk[0], s0, acc[0]);
                 acc[1] = __fmaf_rn(blk[1], s1, acc[1]);
@@ -392,6 +418,15 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
                 acc[3] = __fmaf_rn(blk[3], s1, acc[3]);
             }
         }
+    };
+#pragma unroll 1
+    for (int u = warp; u < units; u += kRouteWarps) {
+        const int j = u / wpt, p = u - j * wpt;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (use_f16)
+            unit_steps(std::true_type{}, j, p, acc);
+        else
+            unit_steps(std::false_type{}, j, p, acc);
         const int col = j * 8 + 2 * t, slot = c * wpt + p;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

@@ -45,7 +45,8 @@ def assert_act_close(gpu_bits, x, codes, scale):
     mag = np.abs(_bf16_vals(x)) @ absw.T          # sum_k |x W| per (m, r)
     dh = mag * 2.0 ** -16
     g, u = h[:, :I], h[:, I:]
-    silu = g / (1 + np.exp(-g))
+    with np.errstate(over="ignore"):  # exp(-g) = inf for very negative g: silu -> -0
+        silu = g / (1 + np.exp(-g))
     ref, got = _bf16_vals(ref_bits), _bf16_vals(gpu_bits)
     ulp = np.maximum(np.abs(ref), np.abs(got)) * 2.0 ** -7
     bound = 1.1 * np.abs(u) * dh[:, :I] + np.abs(silu) * dh[:, I:] + 1e-6 * np.abs(ref) + ulp + 1e-30
@@ -74,6 +75,27 @@ def test_shared_gate_up_is_deterministic_and_strided(mr):
     assert np.array_equal(a, b)
     assert_act_close(a.view(np.uint16), np.ascontiguousarray(xw[:, 128:128 + K]), codes, scale)
 
+
+@pytest.mark.parametrize("case", ["some slices", "every slice"])
+def test_shared_gate_up_values_outside_f16(mr, case):
+    """A CTA whose x slice holds a value that f16 does not carry exactly
+    (at or above 2^16, or below 2^-17 and not zero) runs the bf16 MMAs; the
+    others the f16 ones.  Both against the oracle: one large and one tiny
+    value in two K slices, or x scaled by 2^17 so that every slice holds
+    values past f16's range."""
+    M, K, I = 4, 6144, 768
+    x, _ = inputs.router_inputs(M, K, 8, 7)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    if case == "some slices":
+        xf[0, 5] = 3.0e5       # slice 0 (K / 16 = 384 columns a slice)
+        xf[1, 3000] = 1.0e-6   # slice 7
+        xf[2, 3001] = -2.0e-6
+    else:
+        xf *= 2.0 ** 17
+    xb = inputs.f64_to_bf16_bits(xf)
+    codes, scale = inputs.shared_expert_weights(I, K)
+    out = mr.shared_gate_up(to_dev_bf16(xb), to_dev(codes), to_dev(scale))
+    assert_act_close(host(out.view(torch_mod().int16)).view(np.uint16), xb, codes, scale)
 
 def _route_outputs_equal(a, b):
     for name in ("logits", "topk_ids", "topk_weights", "sorted_token_ids", "expert_ids",
