@@ -1,4 +1,4 @@
-// Plan and arguments of the cluster route kernel (kernel_route.cu).
+// Plan and arguments of the cluster route kernel (route_kernel.cuh).
 #pragma once
 
 #include <stddef.h>
