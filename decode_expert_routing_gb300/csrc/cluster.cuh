@@ -102,6 +102,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x
 // that CTA's mbarrier (dst and bar from map_rank).  Nothing tells the source
 // CTA when its bytes have been read: it must stay alive until the receiver
 // says so.
+// size bytes (a multiple of 16, both addresses 16-byte aligned) of global
+// memory into this CTA's shared memory, counted on its mbarrier bar
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, unsigned bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, uint32_t src, unsigned bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "r"(src), "r"(bytes), "r"(bar)

@@ -281,7 +281,7 @@ __device__ __forceinline__ void row_weights(const RouteArgs& a, const float* row
 template <int SPW>  // 32-wide k steps per k-part, as the route's (0: a.sh_spw at run time)
 static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int sc) {
     extern __shared__ __align__(16) unsigned char sm[];
-    __shared__ __align__(8) unsigned long long s_shbar;
+    __shared__ __align__(8) unsigned long long s_shbar, s_shwbar;  // partials in; weight rows in
     __shared__ int s_shok;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c = (int)cluster_rank();
@@ -306,40 +306,33 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
     const uint32_t recv_local = smem_u32(sm + a.sh_off_recv);
     const int my_rows = max(0, min(tok, Mq - c * tok));
     const int pair0 = sc * P;
-    const uint32_t bar = smem_u32(&s_shbar);
+    const uint32_t bar = smem_u32(&s_shbar), wbar = smem_u32(&s_shwbar);
+    const int wpitch = kc + 16, spr = kc / 32;
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(wbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         const unsigned stall = (flags & 2) ? 16u : 0u;  // test hook: bytes that never come
         if (my_rows > 0) mbar_expect_tx(bar, (unsigned)(my_rows * nslots * R * 4) + stall);
+        mbar_expect_tx(wbar, (unsigned)(R * kc));
     }
     cluster_arrive_relaxed();
     pdl_trigger();
     const int64_t kslice = (int64_t)c * kc;
     const int K32 = K / 32;
     // The CTA's weight slice (R rows x kc E4M3 bytes, rows padded by 16 B
-    // against bank conflicts) and its scale bytes go to shared memory by
-    // cp.async, all issued before the dependency wait (they are parameters);
-    // then units u = warp, warp + 16, ... (tile j = u / wpt, k-part p =
-    // u % wpt) read them from there in a rolled loop (a CTA runs it once, from
-    // a cold instruction cache).
-    const int wpitch = kc + 16, cpr = kc / 16, spr = kc / 32;
-    // 16-byte chunk cc of local row lr: thread tid takes chunk tid % cpr of
-    // rows tid / cpr, + 512 / cpr, ... when cpr divides 512 (kc = 384:
-    // cpr = 24 does not, so the (row, chunk) pair advances with a carry)
-    {
-        const int dr = kRouteThreads / cpr, dc = kRouteThreads - dr * cpr;
-        int lr = tid / cpr, cc = tid - lr * cpr;
-        for (; lr < R; lr += dr, cc += dc) {
-            if (cc >= cpr) {
-                cc -= cpr;
-                if (++lr >= R) break;
-            }
-            const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
-            cp_async16(smem_u32(ws + lr * wpitch + cc * 16), wg8 + gr * K + kslice + cc * 16);
-        }
+    // against bank conflicts) goes to shared memory by bulk copies, a row
+    // each (kc bytes, a multiple of 32; K a multiple of 512 and the base
+    // 16-byte aligned, so every row starts on a 16-byte boundary), counted on
+    // wbar; its scale bytes by plain loads; all issued before the dependency
+    // wait (they are parameters).  Then units u = warp, warp + 16, ... (tile
+    // j = u / wpt, k-part p = u % wpt) read them from there in a rolled loop
+    // (a CTA runs it once, from a cold instruction cache).
+    __syncthreads();  // wbar initialised before any copy counts on it
+    for (int lr = tid; lr < R; lr += kRouteThreads) {
+        const int64_t gr = lr < P ? pair0 + lr : I + pair0 + (lr - P);
+        bulk_load(smem_u32(ws + lr * wpitch), wg8 + gr * K + kslice, (unsigned)kc, wbar);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid < R) {  // a thread per row: its kc / 32 scale bytes, 8 loads in flight at a time
         const int64_t gr = tid < P ? pair0 + tid : I + pair0 + (tid - P);
         const uint8_t* src = sg8 + gr * K32 + kslice / 32;
@@ -370,7 +363,24 @@ static __device__ __noinline__ void shared_gate_up_cta(const RouteArgs& a, int s
                        bf16x2_to_f16x2(d.w, &exact));
         *reinterpret_cast<uint4*>(xs + r * xpitch + cv * 16) = d;
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // thread 0 waits for the weight rows (bounded: after a wait that ran out
+    // it sets the flag and waits once more, so that no copy is left in
+    // flight; the CTA then goes on, its partials not valid, so that its
+    // owners' waits and its own still end)
+    if (tid == 0) {
+        bool ok = mbar_try_wait0(wbar);
+        if (!ok) {
+            unsigned long long t0 = global_ns();
+            while (!(ok = mbar_try_wait0(wbar)) && global_ns() - t0 < wait_ns) {
+            }
+            if (!ok) {
+                atomicExch(&g_route_timeout, 1);
+                t0 = global_ns();
+                while (!mbar_try_wait0(wbar) && global_ns() - t0 < wait_ns) {
+                }
+            }
+        }
+    }
     const bool use_f16 = __syncthreads_and(exact) != 0;
     if (!use_f16) {
         for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
