@@ -63,6 +63,28 @@ def test_fused_equals_chain_and_oracle(mr, cid, M):
     check_quant(x, host(fused["q"]), host(fused["scale"]))
 
 
+@pytest.mark.parametrize("K,N", [(512, 64), (2048, 128), (3072, 128), (4096, 128), (7168, 128), (6144, 256)])
+@pytest.mark.parametrize("M", [1, 8, 16, 40])
+def test_every_k_step_count(mr, K, N, M):
+    """The route kernel is compiled for 6 and 7 k steps per k-part (K =
+    3072 / 6144 and 7168 on 16 CTAs) and for a run-time count otherwise (K =
+    512: 1, 2048: 4, 4096: 8): each against the oracle, and the GEMV alone
+    bitwise equal to the route's logits."""
+    x, w = inputs.router_inputs(M, K, N, 2)
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    scratch = mr.Scratch(M, N, K, 8)
+    fused = mr.moe_route_sort_quant(xd, wd, 8, 16, scratch=scratch)
+    alone = mr.router_gemv(xd, wd, scratch=scratch)
+    lh = host(fused["logits"])
+    assert np.array_equal(lh.view(np.uint32), host(alone).view(np.uint32))
+    assert_logits_close(lh, oracle.router_gemv(x, w))
+    ids, _ = check_gate(lh, host(fused["topk_ids"]), host(fused["topk_weights"]), 8, "softmax")
+    check_sort(ids, N, 16, host(fused["sorted_token_ids"]), host(fused["expert_ids"]),
+               host(fused["num_tokens_post_padded"]))
+    check_quant(x, host(fused["q"]), host(fused["scale"]))
+    assert int(scratch.counters().abs().sum()) == 0
+
+
 def test_fused_without_quant(mr):
     x, w = inputs.router_inputs(4, 6144, 128, 2)
     xd, wd = to_dev_bf16(x), to_dev_bf16(w)
