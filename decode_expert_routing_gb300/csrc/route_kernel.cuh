@@ -579,12 +579,20 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      the norm would store them)
     unsigned char* xs = sm + a.off_x;
     const bool norm = a.rstd != nullptr;
-    for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
-        const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
-        uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
-        if (norm)
+    if (norm) {
+        for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
+            const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
+            uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
             d = norm_chunk(d, ld_ro_v4(a.norm_w + kslice + cv * 8), __ldg(a.rstd + row0 + r), a.norm_gemma != 0);
-        *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
+            *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
+        }
+    } else {  // straight to shared memory: every chunk in flight at once, no register round trip
+        for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
+            const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
+            cp_async16(smem_u32(xs + r * a.xpitch + cv * 16), xq + (int64_t)r * a.ldx + kslice + cv * 8);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     MR_TRACE_WARP(a.trace, 0);
     __syncthreads();
