@@ -458,8 +458,11 @@ int mr_norm_apply(const void *sres, int64_t ldx, const float *rstd, const void *
  * fused multiply-add; the K range is split over the CTAs of a cluster as in
  * the router GEMV and the partial sums are added in a fixed order, so the
  * result is deterministic.  Each CTA stages its K slice of the weights in
- * shared memory (cp.async, issued before it waits on the previous kernel);
- * the number of clusters is the most that run beside the route's at once.
+ * shared memory (bulk async copies, issued before it waits on the previous
+ * kernel); the number of clusters is the most that run beside the route's
+ * at once.  A CTA whose slice of x converts to f16 exactly (zero, or
+ * 2^-17 <= |x| < 2^16) runs f16 MMAs on the codes converted to f16, else
+ * bf16 MMAs: the products are exact either way.
  * The output keeps finite values when the
  * weights' scale bytes are at most 246 (|W| below 2^128).  1 <= M <= 16,
  * K % 512 == 0, I % 8 == 0, and I up to 1536 at K = 6144 (at most 48 row
