@@ -97,6 +97,23 @@ def test_shared_gate_up_values_outside_f16(mr, case):
     out = mr.shared_gate_up(to_dev_bf16(xb), to_dev(codes), to_dev(scale))
     assert_act_close(host(out.view(torch_mod().int16)).view(np.uint16), xb, codes, scale)
 
+@pytest.mark.parametrize("v", [2.0 ** -17, -(2.0 ** -17) * 1.5, 65280.0, -65280.0, 2.0 ** -18, 65536.0])
+def test_shared_gate_up_f16_range_edges(mr, v):
+    """Values at the edges of f16's exact range in one slice: 2^-17 (f16
+    subnormal spacing 2^-24 still carries the bf16's last bit), 65280 (the
+    largest bf16 below 2^16) stay on the f16 MMAs; 2^-18 (a bit lost) and
+    2^16 (past f16's largest value) send the slice to the bf16 MMAs.  Either
+    way the result matches the oracle."""
+    M, K, I = 2, 6144, 768
+    x, _ = inputs.router_inputs(M, K, 8, 7)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    xf[1, 4000] = v
+    xb = inputs.f64_to_bf16_bits(xf)
+    assert inputs.bf16_bits_to_f32(xb)[1, 4000] == np.float32(v)
+    codes, scale = inputs.shared_expert_weights(I, K)
+    out = mr.shared_gate_up(to_dev_bf16(xb), to_dev(codes), to_dev(scale))
+    assert_act_close(host(out.view(torch_mod().int16)).view(np.uint16), xb, codes, scale)
+
 def _route_outputs_equal(a, b):
     for name in ("logits", "topk_ids", "topk_weights", "sorted_token_ids", "expert_ids",
                  "num_tokens_post_padded", "q", "scale"):
