@@ -88,11 +88,9 @@ __device__ __forceinline__ int fdiv(int x, unsigned long long mag) {
     return (int)(((unsigned long long)(unsigned)x * mag) >> 32);
 }
 
-// Gate-weight fragments of batch b of this warp's units (SPW: the k steps
-// per k-part when fixed at compile time, else 0).  A warp keeps one
+// Gate-weight fragments of batch b of this warp's units.  A warp keeps one
 // k-part p = warp % wpt for all its units, so the x fragments it loads serve
 // every unit of a batch; unit i of the warp is tile (warp / wpt) + i * (16 / wpt).
-template <int SPW>
 __device__ __forceinline__ void load_w_batch(const RouteArgs& a, const uint16_t* wg, int64_t kslice, int warp,
                                              int g, int t, int b, uint4 (&wv)[kRouteBatch][kRouteSpwMax]) {
     const int p = warp & (a.wpt - 1), tiles_per_pass = kRouteWarps >> a.wpt_shift;
@@ -100,11 +98,10 @@ __device__ __forceinline__ void load_w_batch(const RouteArgs& a, const uint16_t*
     for (int uu = 0; uu < kRouteBatch; ++uu) {
         const int j = (warp >> a.wpt_shift) + tiles_per_pass * (b * kRouteBatch + uu);
         const bool ok = j < (a.N >> 3);
-        const int spw = SPW ? SPW : a.spw;
-        const uint16_t* wp = wg + (int64_t)(j * 8 + g) * a.K + kslice + (int64_t)p * spw * 32 + 8 * t;
+        const uint16_t* wp = wg + (int64_t)(j * 8 + g) * a.K + kslice + (int64_t)p * a.spw * 32 + 8 * t;
 #pragma unroll
-        for (int s = 0; s < (SPW ? SPW : kRouteSpwMax); ++s)
-            wv[uu][s] = (ok && (SPW || s < spw)) ? ld_stream_v4(wp + s * 32) : make_uint4(0u, 0u, 0u, 0u);
+        for (int s = 0; s < kRouteSpwMax; ++s)
+            wv[uu][s] = (ok && s < a.spw) ? ld_stream_v4(wp + s * 32) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -566,7 +563,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      precede the wait
     uint4 wv[kRouteBatch][kRouteSpwMax];
     const int vpr = a.kc / 8;  // 16-byte chunks per row of the CTA's K slice
-    load_w_batch<SPW>(a, wg, kslice, warp, g, t, 0, wv);
+    load_w_batch(a, wg, kslice, warp, g, t, 0, wv);
     float bpre0 = 0.0f, bpre1 = 0.0f;  // selection bias of this thread's experts t and t + 512
     if (a.bias != nullptr) {
         if (tid < N) bpre0 = __ldg(a.bias + e_off + tid);
@@ -630,7 +627,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     for (int h = 0; h < 2; ++h)
         if (2 * t + h < Mq) tok_bar[h] = map_rank(bar0, (unsigned)((2 * t + h) >> a.tok_shift));
     for (int b = 0; b < nb; ++b) {
-        if (b > 0) load_w_batch<SPW>(a, wg, kslice, warp, g, t, b, wv);
+        if (b > 0) load_w_batch(a, wg, kslice, warp, g, t, b, wv);
         if constexpr (HALF) {
             // At most 8 token rows: the experts take the MMA's 16-row side
             // (the batch's two 8-expert tiles, rows 0-7 and 8-15) and the
