@@ -579,25 +579,21 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     //      the norm would store them)
     unsigned char* xs = sm + a.off_x;
     const bool norm = a.rstd != nullptr;
-    // the x slice of K columns [ks, ks + kc) -> xs (the caller synchronises)
-    auto stage_x = [&](int64_t ks) {
-        if (norm) {
-            for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
-                const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
-                uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + ks + cv * 8);
-                d = norm_chunk(d, ld_ro_v4(a.norm_w + ks + cv * 8), __ldg(a.rstd + row0 + r), a.norm_gemma != 0);
-                *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
-            }
-        } else {  // straight to shared memory: every chunk in flight at once, no register round trip
-            for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
-                const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
-                cp_async16(smem_u32(xs + r * a.xpitch + cv * 16), xq + (int64_t)r * a.ldx + ks + cv * 8);
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (norm) {
+        for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
+            const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
+            uint4 d = ld_ro_v4(xq + (int64_t)r * a.ldx + kslice + cv * 8);
+            d = norm_chunk(d, ld_ro_v4(a.norm_w + kslice + cv * 8), __ldg(a.rstd + row0 + r), a.norm_gemma != 0);
+            *reinterpret_cast<uint4*>(xs + r * a.xpitch + cv * 16) = d;
         }
-    };
-    stage_x(kslice);
+    } else {  // straight to shared memory: every chunk in flight at once, no register round trip
+        for (int v = tid; v < Mq * vpr; v += kRouteThreads) {
+            const int r = fdiv(v, a.mag_vpr), cv = v - r * vpr;
+            cp_async16(smem_u32(xs + r * a.xpitch + cv * 16), xq + (int64_t)r * a.ldx + kslice + cv * 8);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
     MR_TRACE_WARP(a.trace, 0);
     __syncthreads();
     MR_TRACE_STAMP(a.trace, 1);
@@ -722,11 +718,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     // barriers of this CTA).  A CTA that owns no rows and does not sort is
     // done once its slice is quantised: nothing is ever sent to it.  Owners
     // quantise later, off the path of the gate.
-    // above 8 rows the sorting CTA is CTA 0, which owns a row: the last CTA
-    // quantises its slice instead, after its own (off the sort's path)
-    const bool q0_moved = !HALF && !GROUPS && !GEMV && sorter == 0;
     if (sorts) {
-        if (!GEMV && quants && !q0_moved) quant_slice(a, xs, Mq, row0, kslice);
+        if (!GEMV && quants) quant_slice(a, xs, Mq, row0, kslice);
         if (a.clusters == 1) fill_sort_padding(a, a.M * k);
     } else if (my_rows == 0) {
         if (!GEMV && quants) quant_slice(a, xs, Mq, row0, kslice);
@@ -995,12 +988,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_cluster_kernel(RouteAr
     if (!sorts) {  // the weights and the quantisation finish this CTA
         row_weights<SIG>(a, rowbuf, oval, my_rows, grow);
         quant_slice(a, xs, Mq, row0, kslice);
-        if (q0_moved && c == a.cs - 1) {  // and the sorting CTA's slice
-            __syncthreads();
-            stage_x(0);
-            __syncthreads();
-            quant_slice(a, xs, Mq, row0, 0);
-        }
         return;
     }
     row_weights<SIG>(a, rowbuf, oval, my_rows, grow);
